@@ -1,0 +1,423 @@
+"""Benchmark of the KDA hot path (libkda) on GB300.
+
+One step = one kda_chunk_fwd prefill over the packed variable-length
+workload (64 sequences, lengths U{256..8192}, H=32, dk=dv=128, bf16 q/k/v,
+fp32 z/beta/state, nonzero initial state, final state returned).  `value` is
+prefill throughput in Mtokens/s (tokens, not head-tokens).  The decode step
+(256 requests x 32 heads, 1000 steps, state updated in place) is measured in
+the same run and reported under "decode" as state-update HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
+
+For N > 1 launch one rank per GPU with torch.distributed.run; each rank runs
+its own workload (seed = rank), no data-path collective: weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill Mtokens/s (H=32,d=128) & decode state-update HBM GB/s vs peak"
+UNIT = "Mtokens/s"
+PREFILL_BYTES_PER_HEAD_TOKEN = 3 * 256 + 512 + 4 + 256  # q,k,v bf16 + z fp32 + beta + o bf16
+STATE_BYTES = 128 * 128 * 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------- distributed --
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, world, seconds):
+    """Whole-job throughput: tokens all ranks processed / max-over-ranks time."""
+    return tokens_per_rank * world / seconds / 1e6
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc = None
+        self.lines = []
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_oracle_sample(budget_s=12.0, seed=0, max_seqs=64):
+    """Time the fp64 oracle (as it stands) on whole sequences of the varlen
+    workload, all 32 heads each, until `budget_s` of wall time is used.
+    Returns (tokens/s, head_tokens, threads, description)."""
+    import oracle
+    import workloads
+    lens = workloads.varlen_lengths(seed=seed)
+    done_tok, elapsed, used = 0, 0.0, 1
+    n = 0
+    while elapsed < budget_s and n < min(max_seqs, len(lens)):
+        p = workloads.random_problem([lens[n]], 32, 128, 128, init_std=0.1, seed=seed + n,
+                                     name="varlen-sample")
+        t0 = time.perf_counter()
+        _, _, used = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host,
+                                      p.initial_state)
+        elapsed += time.perf_counter() - t0
+        done_tok += lens[n]
+        n += 1
+    desc = (f"{n} whole sequence(s) of the varlen workload ({done_tok} tokens x 32 heads, "
+            f"dk=dv=128), fp64 per-token recurrence, {elapsed:.1f} s")
+    return done_tok / elapsed, done_tok * 32, used, desc
+
+
+def reference_arm(args):
+    """The oracle as it stands on the host cores: `--impl reference`."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+    lens = workloads.varlen_lengths(seed=0)
+    # one step = one whole sequence x 32 heads (about a second of CPU work)
+    per_step = []
+    used = 1
+    for i in range(args.warmup + args.steps):
+        L = lens[i % len(lens)]
+        p = workloads.random_problem([L], 32, 128, 128, init_std=0.1, seed=i,
+                                     name="varlen-sample")
+        t0 = time.perf_counter()
+        _, _, used = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host,
+                                      p.initial_state)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            per_step.append((L, dt))
+    tok = sum(L for L, _ in per_step)
+    sec = sum(dt for _, dt in per_step)
+    value = tok / sec / 1e6
+    sample = (f"each step one whole sequence of the varlen workload (lengths "
+              f"{[L for L, _ in per_step]}), all 32 heads, dk=dv=128")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / len(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "varlen", "description": "64 seqs U{256..8192}, H=32, "
+                   "dk=dv=128, bf16 inputs widened to fp64, initial state N(0,0.1)",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU ---
+
+def event_time_ms(fn, stream):
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    return a, b
+
+
+def bench_prefill(kda, p, steps, warmup, dist, device):
+    import torch
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(p.v)
+    fin = torch.empty_like(p.initial_state)
+
+    def step():
+        kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, out=out,
+                      final_state=fin, cu_seqlens_host=p.cu_seqlens_host)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    evs = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(steps):
+        evs.append(event_time_ms(step, stream))
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [a.elapsed_time(b) for a, b in evs]
+    err = kda.get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err} after the timed prefill")
+    return total_ms, per_launch
+
+
+def bench_decode(kda, d, steps, device):
+    import torch
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(d.v[0])
+    warm = 3
+    for t in range(warm):
+        kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=out)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for t in range(steps):
+        kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=out)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def bench_e2e(kda, p, steps, device):
+    """Host buffers in pinned memory; each step copies the inputs in, runs
+    kda_chunk_fwd and copies out and final_state back, all inside the timed
+    region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    host = {n: getattr(p, n).cpu().pin_memory() for n in ("q", "k", "v", "z", "beta",
+                                                          "cu_seqlens", "initial_state")}
+    dev = {n: torch.empty_like(getattr(p, n)) for n in host}
+    out_h = torch.empty(p.v.shape, dtype=p.v.dtype).pin_memory()
+    fin_h = torch.empty(p.initial_state.shape, dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(p.v)
+    fin_d = torch.empty_like(p.initial_state)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * 4
+
+    def step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["z"], dev["beta"], dev["cu_seqlens"],
+                      dev["initial_state"], out=out_d, final_state=fin_d,
+                      cu_seqlens_host=p.cu_seqlens_host)
+        out_h.copy_(out_d, non_blocking=True)
+        fin_h.copy_(fin_d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu")
+    ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import linear_attention_layer_gb300 as kda
+    import workloads
+
+    rank, world, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libkda has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    kda.load()
+    skip = set(filter(None, args.skip.split(",")))
+    peaks, peak_src = load_peaks()
+
+    # ---- prefill (the step) ----
+    p = workloads.prefill_workload(args.workload, device=device, seed=rank)
+    torch.cuda.synchronize()
+    H = p.meta["num_heads"]
+    T = p.total_tokens
+    N = p.num_seqs
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(device).uuid)
+        if gpu_uuid and not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = None
+    with ClockSampler(gpu_uuid) as clk:
+        total_ms, per_launch = bench_prefill(kda, p, args.steps, args.warmup, dist, device)
+    total_ms = max_over_ranks(total_ms, dist, device)
+    ms_per_step = total_ms / args.steps
+    value = weak_scaling_value(T, world, total_ms / 1e3 / args.steps)
+    launch_ms = statistics.mean(per_launch)
+    state_io = (2 if p.initial_state is not None else 1) * N * H * STATE_BYTES
+    alg_bytes = T * H * PREFILL_BYTES_PER_HEAD_TOKEN + 4 * (N + 1) + state_io
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    hbm_peak = peaks["hbm_gbs"]
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "kernel": "kda_chunk_fwd", "algorithmic_bytes_per_launch": alg_bytes,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "description": workloads.DESCRIPTIONS[args.workload],
+                   "num_seqs": N, "total_tokens": T, "num_heads": H, "dk": 128, "dv": 128,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+
+    # ---- decode ----
+    if "decode" not in skip:
+        del p
+        torch.cuda.empty_cache()
+        p = None
+        d = workloads.decode_workload(device=device, seed=rank, steps=args.decode_steps + 3)
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_uuid) as dclk:
+            dec_ms = bench_decode(kda, d, args.decode_steps, device)
+        per_step_ms = dec_ms / args.decode_steps
+        Nq, Hq = d.meta["num_requests"], d.meta["num_heads"]
+        dec_bytes = Nq * Hq * (2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256)
+        gbs = dec_bytes / (per_step_ms * 1e-3) / 1e9
+        line["decode"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(per_step_ms, 5),
+            "steps": args.decode_steps, "workload": workloads.DESCRIPTIONS["decode"],
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "kernel": "kda_decode_step", "algorithmic_bytes_per_launch": dec_bytes,
+                         "peak_source": f"{peak_src} hbm_gbs"},
+            "clocks": dclk.summary(), "gpu_launches": args.decode_steps}
+        del d
+        torch.cuda.empty_cache()
+
+    # ---- end to end through host buffers ----
+    if "e2e" not in skip:
+        if p is None:
+            p = workloads.prefill_workload(args.workload, device=device, seed=rank)
+        ms, h2d, d2h = bench_e2e(kda, p, args.e2e_steps, device)
+        ms = max_over_ranks(ms, dist, device)
+        line["e2e"] = {"value": round(weak_scaling_value(T, world, ms / 1e3), 3), "unit": UNIT,
+                       "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+        line["gpu_launches"] += args.e2e_steps
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----
+    if "cpu" not in skip and rank == 0 and world == 1:
+        tps, htok, used, desc = cpu_oracle_sample(args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(tps / 1e6, 6), "unit": UNIT, "cores": used,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * kda.h -- C ABI of libkda: Kimi Delta Attention (KDA) on one GB300 GPU.
+ *
+ * The operation (mhpq.cn/news/56770, section "KDA 到底在算什么"): per head, a
+ * dk x dv state S is decayed, corrected and written once per token,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,
+ *
+ * alpha_t being a dk-vector (one retention per key channel, i.e. per row of
+ * S) and beta_t a scalar.  The retention comes from the lower-bounded gate
+ * (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构", section
+ * "下界衰减：一个纯粹为硬件让步的算法改动"):
+ *
+ *     log alpha = gmin * sigmoid(z),   gmin = -5,
+ *
+ * with the per-head scale e^A of that section already folded into z by the
+ * caller.  q and k are L2-normalised inside the library as
+ * x / sqrt(sum x^2 + 1e-6) (mhpq.cn/news/56770, the Q/K preprocessing
+ * paragraph; the page gives no epsilon, 1e-6 is this library's choice).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, contiguous, packed over a variable-length batch):
+ *     q, k        [T_tot, H, dk]   io dtype (fp32 or bf16)
+ *     v, out      [T_tot, H, dv]   io dtype
+ *     z           [T_tot, H, dk]   fp32 gate logits
+ *     beta        [T_tot, H]       fp32 write strength, used as given
+ *     state       [N, H, dk, dv]   fp32, row = key channel
+ *     cu_seqlens  [N + 1]          int32 offsets, cu_seqlens[0] = 0,
+ *                                  non-decreasing, cu_seqlens[N] = T_tot
+ * Pointers marked "device" must point to device memory of the current
+ * device; every such buffer is owned by the caller.  The library allocates
+ * no memory of its own besides one static device error word, never frees,
+ * and never synchronises except in kda_get_device_error().
+ *
+ * Execution: work is enqueued asynchronously on `stream` (NULL = legacy
+ * default stream).  Calls are thread-safe when they use distinct streams
+ * and do not share output buffers.
+ *
+ * Errors: argument problems the host can see (NULL required pointer,
+ * unsupported size or dtype, a host copy of cu_seqlens that is not
+ * monotone or disagrees with total_tokens) return KDA_ERR_INVALID_ARGUMENT
+ * and enqueue nothing.  A failed launch returns KDA_ERR_CUDA.  Problems only
+ * the device can see (device cu_seqlens out of range or non-monotone) skip
+ * the offending work item and set the device error word, which
+ * kda_get_device_error() reports.
+ *
+ * Supported sizes: dk, dv in {32, 64, 128}; H >= 1; N >= 1; T_tot >= 0.
+ * Zero-length sequences are legal: their final state equals their initial
+ * state.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream, declared here so that this header
+ * does not need the CUDA headers. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARGUMENT = 1, /* rejected on the host, nothing enqueued   */
+  KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (size/dtype)   */
+  KDA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed     */
+  KDA_ERR_TIMEOUT = 4,          /* a bounded device-side wait expired       */
+  KDA_ERR_DEVICE_CHECK = 5      /* a device-side argument check failed      */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Shapes and options of one call. */
+typedef struct {
+  int32_t num_seqs;     /* N: sequences (prefill) or live requests (decode) */
+  int32_t total_tokens; /* T_tot: packed tokens; equals N for decode        */
+  int32_t num_heads;    /* H                                                */
+  int32_t dk;           /* key / query channels per head                    */
+  int32_t dv;           /* value channels per head                          */
+  int32_t io_dtype;     /* kda_dtype_t of q, k, v and out                   */
+  /* Optional HOST copy of cu_seqlens ([N + 1] int32), used only to plan
+   * the launch (longest-first order, splitting long sequences across SMs).
+   * May be NULL; then the plan assumes nothing about lengths.  When given
+   * it is checked and must equal the device copy. */
+  const int32_t* cu_seqlens_host;
+  /* Optional device scratch for splitting long sequences across SMs in
+   * kda_chunk_fwd (see kda_chunk_fwd_workspace_size).  NULL / 0 disables
+   * the split; results are the same either way. */
+  void* workspace;
+  size_t workspace_bytes;
+} kda_desc_t;
+
+/*
+ * kda_chunk_fwd -- prefill over a packed variable-length batch.
+ *
+ * Chunkwise evaluation of the recurrence above (mhpq.cn/news/56770, section
+ * "KDA 到底在算什么"; the chunked-with-reciprocal-decay form of
+ * blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构", section "下界衰减").
+ * For every sequence n and head h, the state starts at initial_state[n, h]
+ * (zeros when initial_state is NULL), runs over the tokens
+ * cu_seqlens[n] .. cu_seqlens[n+1]-1 writing out[t, h, :] = S_t^T q_t, and
+ * is stored to final_state[n, h] when final_state is not NULL.
+ *
+ *   q, k, v, z, beta   device, read-only, layouts above
+ *   initial_state      device, [N, H, dk, dv] fp32, or NULL for zeros
+ *   cu_seqlens         device, [N + 1] int32
+ *   out                device, [T_tot, H, dv] io dtype, written
+ *   final_state        device, [N, H, dk, dv] fp32, written, or NULL;
+ *                      may alias initial_state exactly (in-place prefix
+ *                      caching): each (n, h) state is read before it is
+ *                      written.  out must not alias any input.
+ *
+ * bf16 inputs run the tensor-core path (dk = dv = 128) or the CUDA-core
+ * path (other sizes); fp32 inputs always run the fp32 CUDA-core path.
+ */
+kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,
+                           const void* v, const float* z, const float* beta,
+                           const float* initial_state, const int32_t* cu_seqlens,
+                           void* out, float* final_state, kda_stream_t stream);
+
+/* Bytes of device scratch that let kda_chunk_fwd split long sequences
+ * across SMs for this descriptor (0 when no split would be planned).
+ * Needs desc->cu_seqlens_host.  Returns KDA_ERR_INVALID_ARGUMENT on a bad
+ * descriptor. */
+kda_status_t kda_chunk_fwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
+
+/*
+ * kda_recurrent_fwd -- the same operation and arguments as kda_chunk_fwd,
+ * evaluated token by token (the recurrence exactly as written on
+ * mhpq.cn/news/56770, section "KDA 到底在算什么") with the fp32 state held in
+ * registers.  It is the GPU reference the chunked path is compared with;
+ * it is slower on long sequences.  workspace fields are ignored.
+ */
+kda_status_t kda_recurrent_fwd(const kda_desc_t* desc, const void* q, const void* k,
+                               const void* v, const float* z, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens,
+                               void* out, float* final_state, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one new token for each of N live requests, updating
+ * their states in place (the decode regime: blog.higcp.com
+ * "猜想：K3 可能是最适合 TPU 的 MoE 架构", section "三条容易被忽略的代价" (3),
+ * where state traffic dominates at large batch).
+ *
+ *   desc               num_seqs = total_tokens = N (requests)
+ *   q, k               device, [N, H, dk] io dtype
+ *   v                  device, [N, H, dv] io dtype
+ *   z                  device, [N, H, dk] fp32
+ *   beta               device, [N, H] fp32
+ *   state              device, [N, H, dk, dv] fp32, read and overwritten
+ *                      with S_t
+ *   out                device, [N, H, dv] io dtype, written with S_t^T q_t
+ * desc->cu_seqlens_host and workspace are ignored.
+ */
+kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* k,
+                             const void* v, const float* z, const float* beta,
+                             float* state, void* out, kda_stream_t stream);
+
+/* Static, human-readable name of a status. */
+const char* kda_status_string(kda_status_t status);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device: KDA_OK, KDA_ERR_DEVICE_CHECK or KDA_ERR_TIMEOUT.  Returns
+ * KDA_ERR_CUDA if the synchronisation itself fails. */
+kda_status_t kda_get_device_error(kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

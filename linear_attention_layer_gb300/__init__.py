@@ -1,0 +1,224 @@
+"""Python binding of libkda (Kimi Delta Attention on GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_lib/libkda.so``, reached through its C ABI (``include/kda.h``)
+with ctypes.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: if the library is missing or a call fails, these functions raise.
+
+Entry points (same names as the C ABI, without the ``kda_`` prefix):
+    chunk_fwd      -- chunked prefill over a packed variable-length batch
+    recurrent_fwd  -- token-by-token prefill (the GPU reference path)
+    decode_step    -- one token for each live request, state updated in place
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["chunk_fwd", "recurrent_fwd", "decode_step", "chunk_fwd_workspace_size",
+           "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
+           "EXPORTED_SYMBOLS"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
+
+KDA_OK = 0
+KDA_F32, KDA_BF16 = 0, 1
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
+           3: "KDA_ERR_CUDA", 4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_DEVICE_CHECK"}
+
+#: Every function include/kda.h declares.
+EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
+                    "kda_decode_step", "kda_status_string", "kda_get_device_error")
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed: {_STATUS.get(status, status)}")
+
+
+class KdaDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("io_dtype", ctypes.c_int32), ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libkda.so not found at {LIB_PATH}; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, dp = ctypes.c_void_p, ctypes.POINTER(KdaDesc)
+        for name in ("kda_chunk_fwd", "kda_recurrent_fwd"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_get_device_error.restype = ctypes.c_int
+        lib.kda_get_device_error.argtypes = [vp]
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(name, t, dtype, shape, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.device != device or not t.is_cuda:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _io_code(dtype):
+    if dtype == torch.float32:
+        return KDA_F32
+    if dtype == torch.bfloat16:
+        return KDA_BF16
+    raise ValueError(f"q/k/v must be float32 or bfloat16, got {dtype}")
+
+
+def make_desc(num_seqs, total_tokens, num_heads, dk, dv, io_dtype, cu_seqlens_host=None,
+              workspace=None):
+    """Build the C descriptor.  Returns (desc, keepalive) -- keep both alive
+    for the duration of the call."""
+    d = KdaDesc()
+    d.num_seqs, d.total_tokens, d.num_heads = int(num_seqs), int(total_tokens), int(num_heads)
+    d.dk, d.dv, d.io_dtype = int(dk), int(dv), int(io_dtype)
+    keep = None
+    if cu_seqlens_host is not None:
+        keep = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+        d.cu_seqlens_host = ctypes.cast(keep, ctypes.POINTER(ctypes.c_int32))
+    if workspace is not None:
+        d.workspace = ctypes.c_void_p(workspace.data_ptr())
+        d.workspace_bytes = workspace.numel() * workspace.element_size()
+    return d, keep
+
+
+def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state,
+             output_final_state, cu_seqlens_host, workspace, stream):
+    lib = load()
+    if q.dim() != 3:
+        raise ValueError("q must be [T_tot, H, dk]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (T, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (T, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (T, H, dv), dev)
+    _check_tensor("z", z, torch.float32, (T, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (T, H), dev)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check_tensor("out", out, q.dtype, (T, H, dv), dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check_tensor("final_state", final_state, torch.float32, (N, H, dk, dv), dev)
+    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace)
+    with torch.cuda.device(dev):
+        st = getattr(lib, name)(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                _ptr(final_state), _stream_handle(stream))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, name)
+    return out, final_state
+
+
+def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, final_state=None,
+              output_final_state=True, cu_seqlens_host=None, workspace=None, stream=None):
+    """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state)."""
+    return _prefill("kda_chunk_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
+                    final_state, output_final_state, cu_seqlens_host, workspace, stream)
+
+
+def recurrent_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
+                  final_state=None, output_final_state=True, cu_seqlens_host=None, stream=None):
+    """Token-by-token KDA prefill (``kda_recurrent_fwd``).  Returns (out, final_state)."""
+    return _prefill("kda_recurrent_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
+                    final_state, output_final_state, cu_seqlens_host, None, stream)
+
+
+def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, cu_seqlens_host):
+    """Bytes of device scratch that let ``chunk_fwd`` split long sequences."""
+    desc, keep = make_desc(num_seqs, total_tokens, num_heads, dk, dv, _io_code(dtype),
+                           cu_seqlens_host)
+    n = ctypes.c_size_t(0)
+    st = load().kda_chunk_fwd_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_workspace_size")
+    return int(n.value)
+
+
+def decode_step(q, k, v, z, beta, state, *, out=None, stream=None):
+    """One decode step (``kda_decode_step``); ``state`` is updated in place.
+    q, k: [N, H, dk]; v: [N, H, dv]; z: [N, H, dk] fp32; beta: [N, H] fp32;
+    state: [N, H, dk, dv] fp32.  Returns out [N, H, dv]."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (N, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (N, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (N, H, dv), dev)
+    _check_tensor("z", z, torch.float32, (N, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (N, H), dev)
+    _check_tensor("state", state, torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    _check_tensor("out", out, q.dtype, (N, H, dv), dev)
+    desc, _ = make_desc(N, N, H, dk, dv, _io_code(q.dtype))
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                 _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise and read/clear the device error word (a kda_status_t)."""
+    lib = load()
+    return int(lib.kda_get_device_error(_stream_handle(stream)))

@@ -1,0 +1,174 @@
+// kda_api.cu -- the C ABI of libkda: argument validation, planning and
+// dispatch to the kernels.  The declarations and their contract are in
+// include/kda.h.
+#include <cuda_runtime.h>
+
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/kda.h"
+#include "kda_launch.h"
+
+namespace {
+
+// The device error word: first device-detected problem since the last
+// kda_get_device_error() on this device.
+__device__ int g_kda_device_error = 0;
+
+int* device_error_word() {
+  // One address per device; cudaGetSymbolAddress resolves it for the
+  // current device.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<int*>(p);
+}
+
+bool supported_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+kda_status_t check_desc(const kda_desc_t* d, bool decode) {
+  if (!d) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads <= 0)
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (!supported_dim(d->dk) || !supported_dim(d->dv)) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->io_dtype != KDA_F32 && d->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+  if (decode) {
+    if (d->total_tokens != d->num_seqs) return KDA_ERR_INVALID_ARGUMENT;
+    return KDA_OK;
+  }
+  if (d->num_seqs == 0 && d->total_tokens != 0) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->cu_seqlens_host) {
+    const int32_t* cu = d->cu_seqlens_host;
+    if (cu[0] != 0) return KDA_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < d->num_seqs; ++i)
+      if (cu[i + 1] < cu[i]) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu[d->num_seqs] != d->total_tokens) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  return KDA_OK;
+}
+
+kda::Problem to_problem(const kda_desc_t* d) {
+  kda::Problem p;
+  p.num_seqs = d->num_seqs;
+  p.total_tokens = d->total_tokens;
+  p.num_heads = d->num_heads;
+  p.dk = d->dk;
+  p.dv = d->dv;
+  p.io_bf16 = d->io_dtype == KDA_BF16;
+  return p;
+}
+
+kda_status_t prefill_common(const kda_desc_t* desc, const void* q, const void* k,
+                            const void* v, const float* z, const float* beta,
+                            const float* initial_state, const int32_t* cu_seqlens, void* out,
+                            float* final_state, kda::Args& a) {
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (!cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->total_tokens > 0 && (!q || !k || !v || !z || !beta || !out))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (out && (out == q || out == k || out == v || out == (const void*)z ||
+              out == (const void*)beta))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (final_state && final_state != initial_state &&
+      ((const void*)final_state == q || (const void*)final_state == k ||
+       (const void*)final_state == v))
+    return KDA_ERR_INVALID_ARGUMENT;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.z = z;
+  a.beta = beta;
+  a.initial_state = initial_state;
+  a.cu_seqlens = cu_seqlens;
+  a.out = out;
+  a.final_state = final_state;
+  a.err = device_error_word();
+  if (!a.err) return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,
+                           const void* v, const float* z, const float* beta,
+                           const float* initial_state, const int32_t* cu_seqlens, void* out,
+                           float* final_state, kda_stream_t stream) {
+  kda::Args a;
+  kda_status_t s = prefill_common(desc, q, k, v, z, beta, initial_state, cu_seqlens, out,
+                                  final_state, a);
+  if (s != KDA_OK) return s;
+  const kda::Problem p = to_problem(desc);
+  cudaError_t e = kda::launch_chunk_simt(p, a, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_chunk_fwd_workspace_size(const kda_desc_t* desc, size_t* bytes) {
+  if (!bytes) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  *bytes = 0;
+  return KDA_OK;
+}
+
+kda_status_t kda_recurrent_fwd(const kda_desc_t* desc, const void* q, const void* k,
+                               const void* v, const float* z, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens,
+                               void* out, float* final_state, kda_stream_t stream) {
+  kda::Args a;
+  kda_status_t s = prefill_common(desc, q, k, v, z, beta, initial_state, cu_seqlens, out,
+                                  final_state, a);
+  if (s != KDA_OK) return s;
+  cudaError_t e = kda::launch_recurrent(to_problem(desc), a, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* k,
+                             const void* v, const float* z, const float* beta, float* state,
+                             void* out, kda_stream_t stream) {
+  kda_status_t s = check_desc(desc, true);
+  if (s != KDA_OK) return s;
+  if (desc->num_seqs > 0 && (!q || !k || !v || !z || !beta || !state || !out))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (out && (out == q || out == k || out == v || out == (const void*)state))
+    return KDA_ERR_INVALID_ARGUMENT;
+  const kda::Problem p = to_problem(desc);
+  cudaError_t e = kda::launch_decode(p, q, k, v, z, beta, state, out, nullptr,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+const char* kda_status_string(kda_status_t status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+kda_status_t kda_get_device_error(kda_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_kda_device_error, sizeof(int)) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(int)) != cudaSuccess)
+      return KDA_ERR_CUDA;
+  }
+  switch (h) {
+    case 0: return KDA_OK;
+    case KDA_ERR_TIMEOUT: return KDA_ERR_TIMEOUT;
+    default: return KDA_ERR_DEVICE_CHECK;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// kda_launch.h -- internal launchers behind the C ABI (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+struct Problem {
+  int num_seqs;
+  int total_tokens;
+  int num_heads;
+  int dk;
+  int dv;
+  int io_bf16;  // 0 = fp32 q/k/v/out, 1 = bf16
+};
+
+struct Args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* z;
+  const float* beta;
+  const float* initial_state;  // may be null (zeros)
+  const int32_t* cu_seqlens;   // device
+  void* out;
+  float* final_state;  // may be null
+  int* err;            // device error word
+};
+
+// One work item of a chunked launch: a (sequence, head) pair, processed
+// over tokens [tok_begin, tok_end) of that sequence (relative to its start).
+// A negative tok_end means "to the end of the sequence".
+struct WorkItem {
+  int32_t seq;
+  int32_t head;
+};
+
+// Decode: one token per (request, head), state updated in place.
+cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
+                          const float* z, const float* beta, float* state, void* out,
+                          int* err, cudaStream_t stream);
+
+// Token-by-token prefill over a packed batch.
+cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);
+
+// Chunked prefill on CUDA cores in fp32 (any supported size, fp32 or bf16 io).
+cudaError_t launch_chunk_simt(const Problem& p, const Args& a, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,233 @@
+// kda_recurrent.cu -- token-by-token KDA kernels: the decode step and the
+// recurrent prefill.
+//
+// Both evaluate, for one (sequence, head), the state update and read-out of
+// mhpq.cn/news/56770, section "KDA 到底在算什么", one token at a time:
+//     Sbar = Diag(alpha_t) S_{t-1}
+//     e    = v_t - Sbar^T k_t            (erase: what the key currently reads)
+//     S_t  = Sbar + beta_t k_t e^T       (= (I - b k k^T) Sbar + b k v^T)
+//     o_t  = S_t^T q_t = Sbar^T q_t + beta_t (k_t . q_t) e
+// so one pass over S gives both reductions (Sbar^T k and Sbar^T q) and the
+// write-back.  The decode step is the regime where that pass dominates: the
+// fp32 state streams HBM -> registers -> HBM once per token with 128-bit
+// coalesced accesses (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构",
+// section "三条容易被忽略的代价" (3), decode as its own regime).
+//
+// Thread layout: one CTA of 256 threads per (sequence, head).  A state row
+// (dv floats) is covered by dv/4 threads holding one float4 each; the 1024/dv
+// row groups of a CTA stride over the dk rows, so every thread holds
+// R = dk*dv/1024 float4 of S (16 at dk = dv = 128) in registers.
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+namespace {
+
+constexpr int kNT = 256;
+
+template <int DK, int DV>
+struct RecShape {
+  static constexpr int TPR = DV / 4;    // threads per row
+  static constexpr int RG = kNT / TPR;  // row groups
+  static constexpr int R = DK / RG;     // rows (float4) per thread
+  static_assert(DK % RG == 0 && R >= 1, "unsupported shape");
+};
+
+template <int DK, int DV>
+struct RecSmem {
+  float qs[DK], ks[DK], as[DK];
+  float vs[DV], es[DV];
+  float red[2][RecShape<DK, DV>::RG][DV];
+  float part[3][kNT / 32];
+};
+
+// Stage one token's q, k, alpha = exp(g), v into shared memory and the
+// partial sums |q|^2, |k|^2, q.k per warp.
+template <int DK, int DV, typename T>
+__device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, const T* kp,
+                                            const T* vp, const float* zp) {
+  const int tid = threadIdx.x;
+  float qq = 0.f, kk = 0.f, kq = 0.f;
+  if (tid < DK) {
+    const float a = IO<T>::ld(qp + tid);
+    const float b = IO<T>::ld(kp + tid);
+    sm.qs[tid] = a;
+    sm.ks[tid] = b;
+    sm.as[tid] = __expf(log_decay(__ldg(zp + tid)));
+    qq = a * a;
+    kk = b * b;
+    kq = a * b;
+  }
+  if (tid < DV) sm.vs[tid] = IO<T>::ld(vp + tid);
+  if (tid < ((DK + 31) & ~31)) {
+    qq = warp_sum(qq);
+    kk = warp_sum(kk);
+    kq = warp_sum(kq);
+    if ((tid & 31) == 0) {
+      sm.part[0][tid >> 5] = qq;
+      sm.part[1][tid >> 5] = kk;
+      sm.part[2][tid >> 5] = kq;
+    }
+  }
+}
+
+// Apply one token to the register-resident state s.  Requires stage_token
+// followed by __syncthreads().  Writes o_t (when op != nullptr).
+template <int DK, int DV, typename T>
+__device__ __forceinline__ void apply_token(RecSmem<DK, DV>& sm, float4 (&s)[RecShape<DK, DV>::R],
+                                            float b, T* op) {
+  using SH = RecShape<DK, DV>;
+  const int tid = threadIdx.x;
+  const int c4 = tid % SH::TPR, rg = tid / SH::TPR;
+  constexpr int NW = (DK + 31) / 32;
+  float qq = 0.f, kk = 0.f, kq = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    qq += sm.part[0][w];
+    kk += sm.part[1][w];
+    kq += sm.part[2][w];
+  }
+  const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
+  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) {
+    const int r = rg + i * SH::RG;
+    const float a = sm.as[r], kr = sm.ks[r] * rk, qr = sm.qs[r] * rq;
+    s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+    pk.x += kr * s[i].x; pk.y += kr * s[i].y; pk.z += kr * s[i].z; pk.w += kr * s[i].w;
+    pq.x += qr * s[i].x; pq.y += qr * s[i].y; pq.z += qr * s[i].z; pq.w += qr * s[i].w;
+  }
+  reinterpret_cast<float4*>(sm.red[0][rg])[c4] = pk;
+  reinterpret_cast<float4*>(sm.red[1][rg])[c4] = pq;
+  __syncthreads();
+  if (tid < DV) {
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int g = 0; g < SH::RG; ++g) {
+      sk += sm.red[0][g][tid];
+      sq += sm.red[1][g][tid];
+    }
+    const float e = sm.vs[tid] - sk;
+    if (op) IO<T>::st(op + tid, sq + b * (kq * rk * rq) * e);
+    sm.es[tid] = b * e;
+  }
+  __syncthreads();
+  const float4 e4 = reinterpret_cast<const float4*>(sm.es)[c4];
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) {
+    const float kr = sm.ks[rg + i * SH::RG] * rk;
+    s[i].x += kr * e4.x; s[i].y += kr * e4.y; s[i].z += kr * e4.z; s[i].w += kr * e4.w;
+  }
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kNT, 2)
+decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+              const float* __restrict__ z, const float* __restrict__ beta,
+              float* __restrict__ state, T* __restrict__ out) {
+  using SH = RecShape<DK, DV>;
+  __shared__ __align__(16) RecSmem<DK, DV> sm;
+  const size_t unit = blockIdx.x;  // n * H + h
+  const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
+  float4* S = reinterpret_cast<float4*>(state + unit * DK * DV);
+  float4 s[SH::R];
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
+  stage_token<DK, DV, T>(sm, q + unit * DK, k + unit * DK, v + unit * DV, z + unit * DK);
+  __syncthreads();
+  apply_token<DK, DV, T>(sm, s, __ldg(beta + unit), out + unit * DV);
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kNT, 2)
+recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                 const float* __restrict__ z, const float* __restrict__ beta,
+                 const float* initial_state, const int32_t* __restrict__ cu, T* __restrict__ out,
+                 float* final_state, int H, int total, int* err) {
+  using SH = RecShape<DK, DV>;
+  __shared__ __align__(16) RecSmem<DK, DV> sm;
+  const int n = blockIdx.x / H, h = blockIdx.x % H;
+  int bos, eos;
+  if (!seq_range(cu, n, total, err, bos, eos)) return;
+  const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
+  const size_t sbase = (size_t)blockIdx.x * DK * DV;
+  float4 s[SH::R];
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) {
+    s[i] = initial_state
+               ? __ldg(reinterpret_cast<const float4*>(initial_state + sbase) +
+                       (size_t)(rg + i * SH::RG) * SH::TPR + c4)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t = bos; t < eos; ++t) {
+    const size_t th = (size_t)t * H + h;
+    __syncthreads();  // previous token finished reading shared memory
+    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK);
+    __syncthreads();
+    apply_token<DK, DV, T>(sm, s, __ldg(beta + th), out + th * DV);
+  }
+  if (final_state) {
+#pragma unroll
+    for (int i = 0; i < SH::R; ++i)
+      reinterpret_cast<float4*>(final_state + sbase)[(size_t)(rg + i * SH::RG) * SH::TPR + c4] = s[i];
+  }
+}
+
+template <int DK, int DV, typename T>
+cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, const void* v,
+                            const float* z, const float* beta, float* state, void* out,
+                            cudaStream_t st) {
+  const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  decode_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
+      (const T*)q, (const T*)k, (const T*)v, z, beta, state, (T*)out);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename T>
+cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
+  const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  recurrent_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
+      (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
+      (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err);
+  return cudaGetLastError();
+}
+
+#define KDA_SIZE_SWITCH(DKV, DVV, ...)                                         \
+  [&]() -> cudaError_t {                                                       \
+    switch ((DKV) * 1000 + (DVV)) {                                            \
+      case 32032: { constexpr int DK = 32, DV = 32; return __VA_ARGS__(); }    \
+      case 32064: { constexpr int DK = 32, DV = 64; return __VA_ARGS__(); }    \
+      case 32128: { constexpr int DK = 32, DV = 128; return __VA_ARGS__(); }   \
+      case 64032: { constexpr int DK = 64, DV = 32; return __VA_ARGS__(); }    \
+      case 64064: { constexpr int DK = 64, DV = 64; return __VA_ARGS__(); }    \
+      case 64128: { constexpr int DK = 64, DV = 128; return __VA_ARGS__(); }   \
+      case 128032: { constexpr int DK = 128, DV = 32; return __VA_ARGS__(); }  \
+      case 128064: { constexpr int DK = 128, DV = 64; return __VA_ARGS__(); }  \
+      case 128128: { constexpr int DK = 128, DV = 128; return __VA_ARGS__(); } \
+      default: return cudaErrorInvalidValue;                                   \
+    }                                                                          \
+  }()
+
+}  // namespace
+
+cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
+                          const float* z, const float* beta, float* state, void* out,
+                          int* /*err*/, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
+    return p.io_bf16 ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, state, out, st)
+                     : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, state, out, st);
+  });
+}
+
+cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
+    return p.io_bf16 ? recurrent_dispatch<DK, DV, __nv_bfloat16>(p, a, st)
+                     : recurrent_dispatch<DK, DV, float>(p, a, st);
+  });
+}
+
+}  // namespace kda

@@ -1,0 +1,72 @@
+"""Helpers for comparing the CUDA path with the fp64 oracle.
+
+Tolerances (what the hot path must meet against the fp64 recurrence):
+  * fp32 q/k/v: relative L2 error <= 1e-4 on the output and on the final state;
+  * bf16 q/k/v with fp32 state: relative L2 <= 1e-2 and max |err| <= 2e-2 * RMS
+    of the reference, on the output and on the final state.
+relative L2 = ||x - ref||_2 / ||ref||_2 over the whole compared tensor.
+"""
+import numpy as np
+import torch
+
+import oracle
+
+TOL_F32 = 1e-4
+TOL_BF16_REL = 1e-2
+TOL_BF16_MAX_RMS = 2e-2
+
+
+def as64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().float().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def rel_l2(x, ref):
+    x, ref = as64(x), as64(ref)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / den) if den > 0 else float(np.linalg.norm(x))
+
+
+def max_over_rms(x, ref):
+    x, ref = as64(x), as64(ref)
+    rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    return float(np.max(np.abs(x - ref)) / rms) if rms > 0 else float(np.max(np.abs(x), initial=0))
+
+
+def assert_close(x, ref, io_dtype, what=""):
+    """The tolerance rule above, by io dtype."""
+    e = rel_l2(x, ref)
+    if io_dtype == torch.float32:
+        assert e <= TOL_F32, f"{what}: rel-L2 {e:.3e} > {TOL_F32}"
+    else:
+        m = max_over_rms(x, ref)
+        assert e <= TOL_BF16_REL, f"{what}: rel-L2 {e:.3e} > {TOL_BF16_REL}"
+        assert m <= TOL_BF16_MAX_RMS, f"{what}: max|err|/RMS {m:.3e} > {TOL_BF16_MAX_RMS}"
+    return e
+
+
+def oracle_pairs(p, pairs, threads=0):
+    """Run the oracle on selected (sequence, head) pairs of Problem p.
+    Returns {(n, h): (out [L, dv], final [dk, dv])} in float64."""
+    cu = p.cu_seqlens_host
+    qs, ks, vs, zs, bs, s0s, lens = [], [], [], [], [], [], []
+    for n, h in pairs:
+        a, b = cu[n], cu[n + 1]
+        qs.append(p.q[a:b, h:h + 1].cpu())
+        ks.append(p.k[a:b, h:h + 1].cpu())
+        vs.append(p.v[a:b, h:h + 1].cpu())
+        zs.append(p.z[a:b, h:h + 1].cpu())
+        bs.append(p.beta[a:b, h:h + 1].cpu())
+        if p.initial_state is not None:
+            s0s.append(p.initial_state[n:n + 1, h:h + 1].cpu())
+        lens.append(b - a)
+    cat = lambda xs: torch.cat(xs, 0)
+    cu2 = np.concatenate([[0], np.cumsum(lens)])
+    s0 = cat(s0s).reshape(len(pairs), 1, *s0s[0].shape[2:]) if s0s else None
+    out, fin, _ = oracle.recurrent(cat(qs), cat(ks), cat(vs), cat(zs), cat(bs), cu2, s0,
+                                   threads=threads)
+    res = {}
+    for i, (n, h) in enumerate(pairs):
+        res[(n, h)] = (out[cu2[i]:cu2[i + 1], 0], fin[i, 0])
+    return res

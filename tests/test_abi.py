@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/kda.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_layer_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kda.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return kda.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(kda.EXPORTED_SYMBOLS), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_CUDA"), (4, "KDA_ERR_TIMEOUT"), (5, "KDA_ERR_DEVICE_CHECK")]:
+        assert kda.status_string(code) == name
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_descriptor_layout_matches_header():
+    # 6 x int32, then three pointer-sized fields (LP64)
+    assert ctypes.sizeof(kda.KdaDesc) == 48
+    assert kda.KdaDesc.cu_seqlens_host.offset == 24
+    assert kda.KdaDesc.workspace.offset == 32
+    assert kda.KdaDesc.workspace_bytes.offset == 40
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+def _call_chunk(lib, desc, cu=FAKE, q=FAKE, out=ctypes.c_void_p(0x2000), fn="kda_chunk_fwd"):
+    f = getattr(lib, fn)
+    return f(ctypes.byref(desc), q, FAKE, FAKE, FAKE, FAKE, None, cu, out, None, None)
+
+
+@pytest.mark.parametrize("fn", ["kda_chunk_fwd", "kda_recurrent_fwd"])
+@pytest.mark.parametrize("bad", [
+    dict(dk=48), dict(dv=256), dict(dk=0), dict(num_heads=0), dict(io_dtype=7),
+    dict(num_seqs=-1), dict(total_tokens=-5), dict(num_seqs=0, total_tokens=3),
+    dict(cu_host=[0, 5, 3]), dict(cu_host=[1, 5, 8]), dict(cu_host=[0, 4, 7]),
+])
+def test_prefill_rejects_bad_descriptor(lib, fn, bad):
+    p = dict(num_seqs=2, total_tokens=8, num_heads=2, dk=64, dv=64, io_dtype=kda.KDA_BF16)
+    bad = dict(bad)
+    cu_host = bad.pop("cu_host", None)
+    p.update(bad)
+    desc, keep = kda.make_desc(p["num_seqs"], p["total_tokens"], p["num_heads"], p["dk"], p["dv"],
+                               p["io_dtype"], cu_host)
+    assert _call_chunk(lib, desc, fn=fn) == 1
+
+
+def test_prefill_rejects_null_and_aliasing(lib):
+    desc, keep = kda.make_desc(2, 8, 2, 64, 64, kda.KDA_BF16, [0, 3, 8])
+    assert _call_chunk(lib, desc, cu=None) == 1          # cu_seqlens required
+    assert _call_chunk(lib, desc, q=None) == 1           # q required when T > 0
+    assert _call_chunk(lib, desc, out=None) == 1         # out required when T > 0
+    assert _call_chunk(lib, desc, out=FAKE) == 1         # out aliases q
+    assert lib.kda_chunk_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None,
+                             None) == 1
+
+
+def test_decode_rejects_bad_arguments(lib):
+    d, _ = kda.make_desc(4, 4, 2, 128, 128, kda.KDA_BF16)
+    f = lib.kda_decode_step
+    st = ctypes.c_void_p(0x3000)
+    out = ctypes.c_void_p(0x4000)
+    assert f(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, None, out, None) == 1  # no state
+    assert f(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, st, st, None) == 1     # out == state
+    d2, _ = kda.make_desc(4, 5, 2, 128, 128, kda.KDA_BF16)  # total_tokens != num_seqs
+    assert f(ctypes.byref(d2), FAKE, FAKE, FAKE, FAKE, FAKE, st, out, None) == 1
+    d3, _ = kda.make_desc(4, 4, 2, 96, 128, kda.KDA_BF16)
+    assert f(ctypes.byref(d3), FAKE, FAKE, FAKE, FAKE, FAKE, st, out, None) == 1
+
+
+def test_workspace_size_query(lib):
+    d, keep = kda.make_desc(1, 65536, 32, 128, 128, kda.KDA_BF16, [0, 65536])
+    n = ctypes.c_size_t(123)
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value % 256 == 0
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(d), None) == 1
+    bad, _ = kda.make_desc(1, 65536, 32, 100, 128, kda.KDA_BF16, [0, 65536])
+    assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1

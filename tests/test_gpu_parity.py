@@ -1,0 +1,235 @@
+"""GPU parity: the libkda kernels (through the C ABI) against the fp64 oracle
+on the same seeded inputs, element by element, with the tolerances of
+tests/parity.py.  Small cases compare every output; the full-size workloads
+compare every output of a sample of (sequence, head) pairs."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_layer_gb300 as kda
+import oracle
+import workloads
+from tests.parity import assert_close, oracle_pairs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.load()
+    torch.cuda.set_device(0)
+
+
+def _check_all(p, out, fin, io_dtype):
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state)
+    assert_close(out, ro, io_dtype, "out")
+    assert_close(fin, rf, io_dtype, "final_state")
+
+
+# ----------------------------------------------------------- small cases --
+
+RAGGED = [1, 15, 16, 17, 0, 63, 65, 130]
+
+
+@pytest.mark.parametrize("entry", ["chunk_fwd", "recurrent_fwd"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+def test_prefill_small_ragged(entry, dtype, dk, dv):
+    p = workloads.random_problem(RAGGED, 3, dk, dv, dtype, z_std=1.5, init_std=0.1, seed=5,
+                                 device=DEV)
+    fn = getattr(kda, entry)
+    out, fin = fn(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                  cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    _check_all(p, out, fin, dtype)
+    assert kda.get_device_error() == 0
+
+
+def test_tiny_workload_fp32():
+    """B=1, H=1, T=64, dk=dv=32 in fp32: relative L2 <= 1e-4."""
+    p = workloads.prefill_workload("tiny", device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, None,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    _check_all(p, out, fin, torch.float32)
+
+
+@pytest.mark.parametrize("z_mean", [-2.0, 2.0, 6.0])
+def test_prefill_decay_extremes(z_mean):
+    """Gate logits near saturation (16-token sums close to -80) and slow decay."""
+    p = workloads.random_problem([300, 77], 2, 128, 128, torch.bfloat16, z_mean=z_mean,
+                                 init_std=0.5, seed=7, device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    _check_all(p, out, fin, torch.bfloat16)
+
+
+def test_no_initial_state_no_final_state():
+    p = workloads.random_problem([40, 9], 2, 64, 64, torch.float32, seed=8, device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, None,
+                             output_final_state=False)
+    torch.cuda.synchronize()
+    assert fin is None
+    ro, _, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, None)
+    assert_close(out, ro, torch.float32, "out")
+
+
+def test_final_state_may_alias_initial_state():
+    p = workloads.random_problem([50, 33, 0], 2, 128, 128, torch.bfloat16, init_std=0.1, seed=9,
+                                 device=DEV)
+    s0 = p.initial_state.clone()
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, s0)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             final_state=p.initial_state)
+    torch.cuda.synchronize()
+    assert fin.data_ptr() == p.initial_state.data_ptr()
+    assert_close(out, ro, torch.bfloat16, "out")
+    assert_close(fin, rf, torch.bfloat16, "final_state")
+
+
+def test_prefix_split_matches_whole_run():
+    """final_state of tokens [0, t) fed back as initial_state of [t, T) equals
+    one pass over [0, T) (prefix reuse)."""
+    p = workloads.random_problem([500], 4, 128, 128, torch.bfloat16, init_std=0.1, seed=10,
+                                 device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    t = 203
+    cu_a = torch.tensor([0, t], dtype=torch.int32, device=DEV)
+    cu_b = torch.tensor([0, 500 - t], dtype=torch.int32, device=DEV)
+    sl = lambda x, a, b: x[a:b].contiguous()
+    oa, fa = kda.chunk_fwd(sl(p.q, 0, t), sl(p.k, 0, t), sl(p.v, 0, t), sl(p.z, 0, t),
+                           sl(p.beta, 0, t), cu_a, p.initial_state)
+    ob, fb = kda.chunk_fwd(sl(p.q, t, 500), sl(p.k, t, 500), sl(p.v, t, 500), sl(p.z, t, 500),
+                           sl(p.beta, t, 500), cu_b, fa)
+    torch.cuda.synchronize()
+    assert rel_l2(torch.cat([oa, ob]), out) <= 1e-2
+    assert rel_l2(fb, fin) <= 1e-2
+
+
+def test_chunked_and_recurrent_gpu_paths_agree():
+    p = workloads.random_problem([1000, 257, 3], 4, 128, 128, torch.bfloat16, init_std=0.1,
+                                 seed=11, device=DEV)
+    oc, fc = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                           cu_seqlens_host=p.cu_seqlens_host)
+    orr, fr = kda.recurrent_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    torch.cuda.synchronize()
+    assert_close(oc, orr, torch.bfloat16, "out chunk vs recurrent")
+    assert_close(fc, fr, torch.bfloat16, "final chunk vs recurrent")
+
+
+def test_zero_tokens_and_zero_length_sequences():
+    p = workloads.random_problem([0, 0], 2, 64, 64, torch.bfloat16, init_std=0.1, seed=12,
+                                 device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 2, 64)
+    assert torch.equal(fin, p.initial_state)
+
+
+def test_bad_device_cu_seqlens_sets_error_word():
+    """The host copy is absent, so only the kernel can see the out-of-range
+    offset: it skips that sequence, records KDA_ERR_DEVICE_CHECK, and the
+    context stays usable."""
+    p = workloads.random_problem([20, 20], 1, 64, 64, torch.bfloat16, seed=13, device=DEV)
+    bad = torch.tensor([0, 20, 999], dtype=torch.int32, device=DEV)
+    assert kda.get_device_error() == 0
+    kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, bad, None)
+    assert kda.get_device_error() == 5
+    assert kda.get_device_error() == 0  # cleared by the read
+    out, _ = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, None)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+
+
+# ---------------------------------------------------------------- decode --
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
+def test_decode_steps_small(dtype, dk, dv):
+    d = workloads.decode_workload(5, 3, dk, dv, steps=6, io_dtype=dtype, device=DEV, seed=3)
+    S = d.state.clone()
+    s_ref = d.state.cpu()
+    for t in range(6):
+        o = kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], S)
+        torch.cuda.synchronize()
+        ro, s_ref = oracle.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], s_ref)
+        assert_close(o, ro, dtype, f"decode out step {t}")
+    assert_close(S, s_ref, dtype, "decode state")
+
+
+def test_decode_chain_equals_prefill():
+    """T decode steps on one request equal a T-token prefill (GPU paths)."""
+    T = 48
+    p = workloads.random_problem([T], 2, 128, 128, torch.bfloat16, init_std=0.1, seed=14,
+                                 device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    S = p.initial_state.clone()
+    outs = []
+    for t in range(T):
+        sl = lambda x: x[t:t + 1].contiguous()
+        outs.append(kda.decode_step(sl(p.q), sl(p.k), sl(p.v), sl(p.z), sl(p.beta), S))
+    torch.cuda.synchronize()
+    assert_close(torch.cat(outs), out, torch.bfloat16, "decode chain vs chunk out")
+    assert_close(S, fin, torch.bfloat16, "decode chain vs chunk state")
+
+
+# ------------------------------------------------- full-size workloads -----
+
+def _sampled_prefill(name, pairs_fn, **kw):
+    p = workloads.prefill_workload(name, device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host, **kw)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    pairs = pairs_fn(p)
+    ref = oracle_pairs(p, pairs)
+    cu = p.cu_seqlens_host
+    for (n, h), (ro, rf) in ref.items():
+        assert_close(out[cu[n]:cu[n + 1], h], ro, torch.bfloat16, f"{name} out (n={n}, h={h})")
+        assert_close(fin[n, h], rf, torch.bfloat16, f"{name} final (n={n}, h={h})")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
+
+
+def test_full_prefill_workload_sampled():
+    _sampled_prefill("prefill", lambda p: [(0, 0), (1, 7), (2, 15), (3, 3)])
+
+
+@pytest.mark.parametrize("name", ["long", "long_slow"])
+def test_full_long_workload_sampled(name):
+    _sampled_prefill(name, lambda p: [(0, 0), (0, 13), (0, 31)])
+
+
+def test_full_varlen_workload_sampled():
+    def pairs(p):
+        lens = np.diff(p.cu_seqlens_host)
+        longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+        return [(longest, 0), (shortest, 31), (5, 17), (63, 9)]
+    _sampled_prefill("varlen", pairs)
+
+
+def test_full_decode_workload_sampled():
+    """256 requests x 32 heads, 1000 steps in place; every step's output and
+    the final state of sampled (request, head) pairs against the oracle's
+    1000-token recurrence."""
+    steps = 1000
+    d = workloads.decode_workload(256, 32, 128, 128, steps=steps, device=DEV)
+    pairs = [(0, 0), (77, 5), (255, 31)]
+    s0 = {pr: d.state[pr[0], pr[1]].cpu().clone() for pr in pairs}
+    outs = {pr: [] for pr in pairs}
+    for t in range(steps):
+        o = kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state)
+        for (n, h) in pairs:
+            outs[(n, h)].append(o[n, h].clone())
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    for (n, h) in pairs:
+        ro, rf, _ = oracle.recurrent(d.q[:, n, h:h + 1], d.k[:, n, h:h + 1], d.v[:, n, h:h + 1],
+                                     d.z[:, n, h:h + 1], d.beta[:, n, h:h + 1], [0, steps],
+                                     s0[(n, h)][None, None])
+        assert_close(torch.stack(outs[(n, h)]), ro[:, 0], torch.bfloat16, f"decode out {n},{h}")
+        assert_close(d.state[n, h], rf[0, 0], torch.bfloat16, f"decode state {n},{h}")
