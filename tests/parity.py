@@ -5,6 +5,13 @@ Tolerances (what the hot path must meet against the fp64 recurrence):
   * bf16 q/k/v with fp32 state: relative L2 <= 1e-2 and max |err| <= 2e-2 * RMS
     of the reference, on the output and on the final state.
 relative L2 = ||x - ref||_2 / ||ref||_2 over the whole compared tensor.
+
+The max-error bound measures the computation, not the storage type: a bf16
+output cannot hold the fp64 value closer than half a bf16 ulp of that value,
+so that representation error (|ref| * 2^-9 at most) is discounted element by
+element before the bound is applied.  Without the discount the rounding of
+the largest outputs alone (|o| up to ~12 RMS on these workloads) exceeds
+2e-2 * RMS even for an exact computation.
 """
 import numpy as np
 import torch
@@ -28,19 +35,34 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / den) if den > 0 else float(np.linalg.norm(x))
 
 
-def max_over_rms(x, ref):
+def half_ulp(ref, dtype):
+    """Half a unit in the last place of each value in `dtype` (bf16: 8
+    significant bits, so half an ulp of |r| in [2^(E-1), 2^E) is 2^(E-9))."""
+    ref = np.abs(as64(ref))
+    if dtype != torch.bfloat16:
+        return np.zeros_like(ref)
+    _, e = np.frexp(ref)
+    return np.where(ref > 0, np.ldexp(1.0, e - 9), 0.0)
+
+
+def max_over_rms(x, ref, storage=None):
     x, ref = as64(x), as64(ref)
     rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
-    return float(np.max(np.abs(x - ref)) / rms) if rms > 0 else float(np.max(np.abs(x), initial=0))
+    err = np.abs(x - ref)
+    if storage is not None:
+        err = np.maximum(err - half_ulp(ref, storage), 0.0)
+    return float(np.max(err, initial=0.0) / rms) if rms > 0 else float(np.max(err, initial=0.0))
 
 
 def assert_close(x, ref, io_dtype, what=""):
-    """The tolerance rule above, by io dtype."""
+    """The tolerance rule above, by io dtype (x's own dtype sets the storage
+    rounding that is discounted)."""
     e = rel_l2(x, ref)
     if io_dtype == torch.float32:
         assert e <= TOL_F32, f"{what}: rel-L2 {e:.3e} > {TOL_F32}"
     else:
-        m = max_over_rms(x, ref)
+        storage = x.dtype if isinstance(x, torch.Tensor) else None
+        m = max_over_rms(x, ref, storage)
         assert e <= TOL_BF16_REL, f"{what}: rel-L2 {e:.3e} > {TOL_BF16_REL}"
         assert m <= TOL_BF16_MAX_RMS, f"{what}: max|err|/RMS {m:.3e} > {TOL_BF16_MAX_RMS}"
     return e
