@@ -70,7 +70,7 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp,
-           "-Xlinker", f"-rpath={libdir}", "-lcuda"]
+           "-Xlinker", f"-rpath={libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libkda.so failed:\n{r.stdout}\n{r.stderr}")

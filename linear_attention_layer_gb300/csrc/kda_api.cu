@@ -103,7 +103,9 @@ kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,
                                   final_state, a);
   if (s != KDA_OK) return s;
   const kda::Problem p = to_problem(desc);
-  cudaError_t e = kda::launch_chunk_simt(p, a, (cudaStream_t)stream);
+  cudaError_t e = kda::chunk_tc_supported(p, a)
+                      ? kda::launch_chunk_tc(p, a, desc->cu_seqlens_host, (cudaStream_t)stream)
+                      : kda::launch_chunk_simt(p, a, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

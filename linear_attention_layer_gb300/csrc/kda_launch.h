@@ -48,4 +48,10 @@ cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t strea
 // Chunked prefill on CUDA cores in fp32 (any supported size, fp32 or bf16 io).
 cudaError_t launch_chunk_simt(const Problem& p, const Args& a, cudaStream_t stream);
 
+// Chunked prefill on the tensor cores (bf16 io, dk = dv = 128, 16-byte
+// aligned buffers).  cu_host (optional) orders the work longest-first.
+bool chunk_tc_supported(const Problem& p, const Args& a);
+cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host,
+                            cudaStream_t stream);
+
 }  // namespace kda

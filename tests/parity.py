@@ -45,24 +45,26 @@ def half_ulp(ref, dtype):
     return np.where(ref > 0, np.ldexp(1.0, e - 9), 0.0)
 
 
-def max_over_rms(x, ref, storage=None):
+def max_over_rms(x, ref, storage=None, roundings=1):
     x, ref = as64(x), as64(ref)
     rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
     err = np.abs(x - ref)
     if storage is not None:
-        err = np.maximum(err - half_ulp(ref, storage), 0.0)
+        err = np.maximum(err - roundings * half_ulp(ref, storage), 0.0)
     return float(np.max(err, initial=0.0) / rms) if rms > 0 else float(np.max(err, initial=0.0))
 
 
-def assert_close(x, ref, io_dtype, what=""):
+def assert_close(x, ref, io_dtype, what="", both_stored=False):
     """The tolerance rule above, by io dtype (x's own dtype sets the storage
-    rounding that is discounted)."""
+    rounding that is discounted).  both_stored: ref is itself a bf16 result
+    of the library (two GPU paths compared), so each side carries its own
+    half-ulp output rounding."""
     e = rel_l2(x, ref)
     if io_dtype == torch.float32:
         assert e <= TOL_F32, f"{what}: rel-L2 {e:.3e} > {TOL_F32}"
     else:
         storage = x.dtype if isinstance(x, torch.Tensor) else None
-        m = max_over_rms(x, ref, storage)
+        m = max_over_rms(x, ref, storage, 2 if both_stored else 1)
         assert e <= TOL_BF16_REL, f"{what}: rel-L2 {e:.3e} > {TOL_BF16_REL}"
         assert m <= TOL_BF16_MAX_RMS, f"{what}: max|err|/RMS {m:.3e} > {TOL_BF16_MAX_RMS}"
     return e
