@@ -216,7 +216,8 @@ def bench_prefill(kda, p, steps, warmup, dist, device):
     import torch
     stream = torch.cuda.current_stream()
     out = torch.empty_like(p.v)
-    fin = torch.empty_like(p.initial_state)
+    fin = torch.empty((p.num_seqs, p.meta["num_heads"], p.meta["dk"], p.meta["dv"]),
+                      dtype=torch.float32, device=p.v.device)
 
     def step():
         kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, out=out,
@@ -269,13 +270,16 @@ def bench_e2e(kda, p, steps, device):
     region."""
     import torch
     stream = torch.cuda.current_stream()
-    host = {n: getattr(p, n).cpu().pin_memory() for n in ("q", "k", "v", "z", "beta",
-                                                          "cu_seqlens", "initial_state")}
+    names = ["q", "k", "v", "z", "beta", "cu_seqlens"]
+    if p.initial_state is not None:
+        names.append("initial_state")
+    host = {n: getattr(p, n).cpu().pin_memory() for n in names}
     dev = {n: torch.empty_like(getattr(p, n)) for n in host}
+    fshape = (p.num_seqs, p.meta["num_heads"], p.meta["dk"], p.meta["dv"])
     out_h = torch.empty(p.v.shape, dtype=p.v.dtype).pin_memory()
-    fin_h = torch.empty(p.initial_state.shape, dtype=torch.float32).pin_memory()
+    fin_h = torch.empty(fshape, dtype=torch.float32).pin_memory()
     out_d = torch.empty_like(p.v)
-    fin_d = torch.empty_like(p.initial_state)
+    fin_d = torch.empty(fshape, dtype=torch.float32, device=p.v.device)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * 4
 
@@ -283,7 +287,7 @@ def bench_e2e(kda, p, steps, device):
         for n in host:
             dev[n].copy_(host[n], non_blocking=True)
         kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["z"], dev["beta"], dev["cu_seqlens"],
-                      dev["initial_state"], out=out_d, final_state=fin_d,
+                      dev.get("initial_state"), out=out_d, final_state=fin_d,
                       cu_seqlens_host=p.cu_seqlens_host)
         out_h.copy_(out_d, non_blocking=True)
         fin_h.copy_(fin_d, non_blocking=True)
