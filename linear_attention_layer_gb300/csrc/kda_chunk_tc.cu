@@ -64,7 +64,7 @@ using namespace kda::tc;
 
 constexpr int kC = 64;     // chunk length
 constexpr int kD = 128;    // dk = dv
-constexpr int kNT = 128;   // threads per CTA
+constexpr int kNT = 256;   // threads per CTA (8 warps; warps w and w+4 share a TMEM lane quadrant)
 constexpr int kMaxOrder = 6144;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) ----
@@ -76,18 +76,19 @@ constexpr uint32_t OFF_G = 81920;     // 80K: Gram operands, later A / T / P / T
 constexpr uint32_t G_QT = OFF_G;              // Q~  fp32 [64 t][128 c] (xor-swizzled)
 constexpr uint32_t G_KT = OFF_G + 32768;      // K~  fp32 [64 j][128 c] (xor-swizzled)
 constexpr uint32_t G_KPT = OFF_G + 65536;     // K~+ bf16 [64 t][128 c] (xor-swizzled)
-constexpr uint32_t G_AKK = OFF_G;             // A   fp32 [64][64]          (after the Gram)
-constexpr uint32_t G_T32 = OFF_G + 16384;     // T   fp32 [64][64]
-constexpr uint32_t G_P = OFF_G + 32768;       // P   fp16 [64 t][64 j] SW128: K-major B
-constexpr uint32_t G_TP = OFF_G + 40960;      // T'  fp16 [64 t][64 j] SW128: K-major B
-constexpr uint32_t G_WT = OFF_G + 49152;      // W^T fp16 [128 c][64 t] SW128: MN-major B
+constexpr int kLS = 68;                       // row stride (floats) of A and T: conflict-free
+constexpr uint32_t G_AKK = OFF_G;             // A   fp32 [64][kLS]         (after the Gram)
+constexpr uint32_t G_T32 = OFF_G + 17408;     // T   fp32 [64][kLS]
+constexpr uint32_t G_P = OFF_G + 34816;       // P   fp16 [64 t][64 j] SW128: K-major B
+constexpr uint32_t G_TP = OFF_G + 43008;      // T'  fp16 [64 t][64 j] SW128: K-major B
+constexpr uint32_t G_WT = OFF_G + 51200;      // W^T fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_QPT = 163840;  // Q+^T  fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major A
 constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-major B
 constexpr uint32_t OFF_MISC = 212992;
 // misc floats
 constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_ER = 320, M_EGR = 832,
-              M_DAB = 1344, M_END = 1344 + 6 * 128;
+              M_DAB = 1344, M_R = 2112, M_END = 2112 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 
@@ -122,13 +123,56 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, long lo
   return true;
 }
 
-// fp32 element (t, c) of a [64][128] tile, 32-bit word index xor (row % 8) * 4
+// fp32 element (t, c) of a [64][128] tile; the column index is xor-ed with
+// (row % 8) * 16 so that groups of 4 columns stay contiguous (vector loads)
+// and 8 consecutive rows fall on distinct banks.
 __device__ __forceinline__ uint32_t f32_off(int t, int c) {
-  return (uint32_t)t * 512u + ((uint32_t)(c ^ ((t & 7) << 2)) << 2);
+  return (uint32_t)t * 512u + ((uint32_t)(c ^ ((t & 7) << 4)) << 2);
 }
-// bf16 element (t, c) of a [64][128] tile, element index xor (row % 8) * 8
+// bf16 element (t, c) of a [64][128] tile, same column swizzle.
 __device__ __forceinline__ uint32_t b16_off(int t, int c) {
-  return (uint32_t)t * 256u + ((uint32_t)(c ^ ((t & 7) << 3)) << 1);
+  return (uint32_t)t * 256u + ((uint32_t)(c ^ ((t & 7) << 4)) << 1);
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// acc (16 x 16, two m16n8 tiles) += X (16 x K) * Y (K x 16) in three-pass tf32
+// (hi*hi + hi*lo + lo*hi, close to fp32).  X starts at (xr, xc) and Y at
+// (yr, yc) of fp32 matrices with row stride kLS.  One warp.
+__device__ __forceinline__ void warp_gemm16_3tf32(float (&acc)[2][4], const float* X, int xr,
+                                                  int xc, const float* Y, int yr, int yc, int K,
+                                                  int g, int q) {
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(X[(xr + g) * kLS + xc + k0 + q], ah[0], al[0]);
+    split_tf32(X[(xr + g + 8) * kLS + xc + k0 + q], ah[1], al[1]);
+    split_tf32(X[(xr + g) * kLS + xc + k0 + q + 4], ah[2], al[2]);
+    split_tf32(X[(xr + g + 8) * kLS + xc + k0 + q + 4], ah[3], al[3]);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(Y[(yr + k0 + q) * kLS + yc + 8 * n + g], bh0, bl0);
+      split_tf32(Y[(yr + k0 + q + 4) * kLS + yc + 8 * n + g], bh1, bl1);
+      mma_1688_tf32(acc[n], ah, bh0, bh1);
+      mma_1688_tf32(acc[n], ah, bl0, bl1);
+      mma_1688_tf32(acc[n], al, bh0, bh1);
+    }
+  }
+}
+
+// M[r0 + row][c0 + col] = s * acc (accumulator layout of warp_gemm16_3tf32)
+__device__ __forceinline__ void warp_store16(float* M, int r0, int c0, const float (&acc)[2][4],
+                                             float s, int g, int q) {
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    M[(r0 + g) * kLS + c0 + 8 * n + 2 * q] = s * acc[n][0];
+    M[(r0 + g) * kLS + c0 + 8 * n + 2 * q + 1] = s * acc[n][1];
+    M[(r0 + g + 8) * kLS + c0 + 8 * n + 2 * q] = s * acc[n][2];
+    M[(r0 + g + 8) * kLS + c0 + 8 * n + 2 * q + 1] = s * acc[n][3];
+  }
 }
 
 // Store 16 consecutive values of row `row`, starting at column `col` (a
@@ -195,8 +239,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   sync_tc();
   const uint32_t tmem = *s_tmem;
-  // this thread's TMEM lane (row): warp w owns lanes 32w .. 32w+31
-  const uint32_t my_lane = tmem + ((uint32_t)(warp * 32) << 16);
+  // this thread's TMEM lane (row): warps w and w+4 own lanes 32(w%4) .. +31
+  // and split the columns of every TMEM pass between them (half wh)
+  const uint32_t my_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const int row = tid & 127, wh = warp >> 2;
   uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0;
   bool pend_qkz = false, pend_v = false;  // TMA copies in flight (uniform)
   bool aborted = false;
@@ -223,14 +269,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, bos, bar_v);
     }
     pend_qkz = pend_v = nchunks > 0;
+    // beta of the first chunk (later chunks are prefetched one chunk ahead)
+    float beta_pf = 0.f;
+    if (tid < min(kC, eos - bos)) beta_pf = __ldg(P.beta + (size_t)(bos + tid) * H + h);
 
     // ---- entry state S^T: lane n holds column n of S (fp32 and fp16) ----
     {
-      const int n = tid;
+      const int n = row;
       const float* src = P.initial_state ? P.initial_state + ((size_t)seq * H + h) * kD * kD + n
                                          : nullptr;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 16) {
+      for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = src ? __ldg(src + (size_t)(c0 + i) * kD) : 0.f;
@@ -258,12 +307,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- B: token norms and beta ----------------
       {
-        const int t = tid >> 1, hh = tid & 1;
-        const unsigned char* qrow = sm + OFF_Q + hh * 8192 + t * 128;
-        const unsigned char* krow = sm + OFF_K + hh * 8192 + t * 128;
+        const int t = tid >> 2, qq = tid & 3;
+        const unsigned char* qrow = sm + OFF_Q + (qq >> 1) * 8192 + t * 128 + (qq & 1) * 64;
+        const unsigned char* krow = sm + OFF_K + (qq >> 1) * 8192 + t * 128 + (qq & 1) * 64;
         float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           const uint4 a = *reinterpret_cast<const uint4*>(qrow + (j << 4));
           const uint4 b = *reinterpret_cast<const uint4*>(krow + (j << 4));
           const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
@@ -277,83 +326,123 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         sq += __shfl_xor_sync(0xffffffffu, sq, 1);
         sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        if (hh == 0) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        if (qq == 0) {
           misc[M_RQ + t] = t < len ? rsqrtf(sq + kNormEps) : 0.f;
           misc[M_RK + t] = t < len ? rsqrtf(sk + kNormEps) : 0.f;
         }
-        if (tid < kC) misc[M_BETA + tid] = tid < len ? __ldg(P.beta + (size_t)(t0 + tid) * H + h) : 0.f;
+        if (tid < kC) {
+          misc[M_BETA + tid] = beta_pf;
+          beta_pf = 0.f;
+          if (tid < min(kC, eos - t0 - kC)) beta_pf = __ldg(P.beta + (size_t)(t0 + kC + tid) * H + h);
+        }
       }
       __syncthreads();
 
       // ---------------- C: gate, cumulative decay, per-channel tables ----------------
-      const int c = tid;
-      float r[4];
       float* Z = reinterpret_cast<float*>(sm + OFF_Z);
       {
-        float G = 0.f;
+        // two threads per key channel (adjacent lanes), 32 tokens each
+        const int c = tid >> 1, hf = tid & 1;
+        float zz[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zz[i] = Z[(32 * hf + i) * kD + c];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zz[i] = (32 * hf + i < len) ? log_decay(zz[i]) : 0.f;
+        float run = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          run += zz[i];
+          zz[i] = run;
+        }
+        const float first = __shfl_sync(0xffffffffu, run, lane & ~1);  // sum over tokens 0..31
+        const float off = hf ? first : 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          zz[i] += off;
+          Z[(32 * hf + i) * kD + c] = zz[i];
+        }
+        const float mid = zz[15], end = zz[31];
+        const float pmid = __shfl_xor_sync(0xffffffffu, mid, 1);
+        const float pend = __shfl_xor_sync(0xffffffffu, end, 1);
+        float r[4];
         r[0] = 0.f;
+        r[1] = hf ? pmid : mid;
+        r[2] = hf ? pend : end;
+        r[3] = hf ? mid : pmid;
+        const float G = hf ? end : pend;
+        if (hf == 0) {
+          misc[M_DECAY + c] = __expf(G);
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-          if ((t & 15) == 0 && t > 0) r[t >> 4] = G;
-          const float g = t < len ? log_decay(Z[t * kD + c]) : 0.f;
-          G += g;
-          Z[t * kD + c] = G;
+          for (int a = 0; a < 4; ++a) {
+            misc[M_ER + a * kD + c] = __expf(r[a]);
+            misc[M_EGR + a * kD + c] = __expf(G - r[a]);
+            misc[M_R + a * kD + c] = r[a];
+          }
+        } else {
+          misc[M_DAB + 0 * kD + c] = __expf(r[1] - r[0]);
+          misc[M_DAB + 1 * kD + c] = __expf(r[2] - r[0]);
+          misc[M_DAB + 2 * kD + c] = __expf(r[2] - r[1]);
+          misc[M_DAB + 3 * kD + c] = __expf(r[3] - r[0]);
+          misc[M_DAB + 4 * kD + c] = __expf(r[3] - r[1]);
+          misc[M_DAB + 5 * kD + c] = __expf(r[3] - r[2]);
         }
-        misc[M_DECAY + c] = __expf(G);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          misc[M_ER + a * kD + c] = __expf(r[a]);
-          misc[M_EGR + a * kD + c] = __expf(G - r[a]);
-        }
-        misc[M_DAB + 0 * kD + c] = __expf(r[1] - r[0]);
-        misc[M_DAB + 1 * kD + c] = __expf(r[2] - r[0]);
-        misc[M_DAB + 2 * kD + c] = __expf(r[2] - r[1]);
-        misc[M_DAB + 3 * kD + c] = __expf(r[3] - r[0]);
-        misc[M_DAB + 4 * kD + c] = __expf(r[3] - r[1]);
-        misc[M_DAB + 5 * kD + c] = __expf(r[3] - r[2]);
       }
+      __syncthreads();  // G and the per-channel tables of every channel are ready
 
-      // ---------------- D: decayed operands (thread = key channel c) ----------------
+      // ---------------- D: decayed operands (thread = 2 key channels x 32 tokens) ----------------
       {
-        const float* er = misc + M_ER;
-        const float* egr = misc + M_EGR;
-        const unsigned char* qs = sm + OFF_Q;
-        const unsigned char* ks = sm + OFF_K;
-        const uint32_t sw = (uint32_t)(c & 7);
+        const int c = 2 * (tid & 63), a = tid >> 6;
+        const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
+        const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
+        const uint32_t sw0 = (uint32_t)(c & 7), sw1 = (uint32_t)((c + 1) & 7);
+        {
+          const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
+          const float er0 = misc[M_ER + a * kD + c], er1 = misc[M_ER + a * kD + c + 1];
+          const float eg0 = misc[M_EGR + a * kD + c], eg1 = misc[M_EGR + a * kD + c + 1];
 #pragma unroll
-        for (int t8 = 0; t8 < kC; t8 += 8) {
-          uint32_t qp_pack[4], kp_pack[4], kh_pack[4];
+          for (int t8 = 0; t8 < 16; t8 += 8) {
+            float qpv[2][8], kpv[2][8], khv[2][8];
 #pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            float qpv[2], kpv[2], khv[2];
+            for (int i = 0; i < 8; ++i) {
+              const int t = 16 * a + t8 + i;
+              const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
+              const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
+              const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
+              const uint32_t off = sw128_offset(t, c & 63);
+              const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
+              const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
+              const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
+              const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
+              const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
+              const float qt0 = q0 * F0, qt1 = q1 * F1;
+              const float kp0 = k0 * F0, kp1 = k1 * F1;
+              const float kt0 = k0 * E0, kt1 = k1 * E1;
+              *reinterpret_cast<float2*>(sm + G_QT + f32_off(t, c)) = make_float2(qt0, qt1);
+              *reinterpret_cast<float2*>(sm + G_KT + f32_off(t, c)) =
+                  make_float2(__uint_as_float(to_tf32(kt0)), __uint_as_float(to_tf32(kt1)));
+              *reinterpret_cast<uint32_t*>(sm + G_KPT + b16_off(t, c)) = pack_bf16(kp0, kp1);
+              qpv[0][i] = qt0 * er0; qpv[1][i] = qt1 * er1;
+              kpv[0][i] = kp0 * er0; kpv[1][i] = kp1 * er1;
+              khv[0][i] = kt0 * eg0; khv[1][i] = kt1 * eg1;
+            }
+            const uint32_t tc8 = (uint32_t)(16 * a + t8) >> 3;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int t = t8 + i + e, a = t >> 4;
-              const float Gt = Z[t * kD + c];
-              const float F = __expf(Gt - r[a]);
-              const float E = __fdividef(1.0f, F);
-              const uint32_t off = (uint32_t)(c >> 6) * 8192u + sw128_offset(t, c & 63);
-              const float qh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qs + off)) * misc[M_RQ + t];
-              const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ks + off)) * misc[M_RK + t];
-              const float qt = qh * F, kpt = kh * F, kt = kh * E;
-              *reinterpret_cast<float*>(sm + G_QT + f32_off(t, c)) = qt;
-              *reinterpret_cast<float*>(sm + G_KT + f32_off(t, c)) = kt;
-              *reinterpret_cast<__nv_bfloat16*>(sm + G_KPT + b16_off(t, c)) = __float2bfloat16_rn(kpt);
-              qpv[e] = qt * er[a * kD + c];
-              kpv[e] = kpt * er[a * kD + c];
-              khv[e] = kt * egr[a * kD + c];
+              const uint32_t row = (uint32_t)(c + e);
+              const uint32_t off = row * 128u + ((tc8 ^ (e ? sw1 : sw0)) << 4);
+              *reinterpret_cast<uint4*>(sm + OFF_QPT + off) =
+                  make_uint4(pack_f16(qpv[e][0], qpv[e][1]), pack_f16(qpv[e][2], qpv[e][3]),
+                             pack_f16(qpv[e][4], qpv[e][5]), pack_f16(qpv[e][6], qpv[e][7]));
+              *reinterpret_cast<uint4*>(sm + OFF_KPT + off) =
+                  make_uint4(pack_f16(kpv[e][0], kpv[e][1]), pack_f16(kpv[e][2], kpv[e][3]),
+                             pack_f16(kpv[e][4], kpv[e][5]), pack_f16(kpv[e][6], kpv[e][7]));
+              *reinterpret_cast<uint4*>(sm + OFF_KH + off) =
+                  make_uint4(pack_f16(khv[e][0], khv[e][1]), pack_f16(khv[e][2], khv[e][3]),
+                             pack_f16(khv[e][4], khv[e][5]), pack_f16(khv[e][6], khv[e][7]));
             }
-            qp_pack[i >> 1] = pack_f16(qpv[0], qpv[1]);
-            kp_pack[i >> 1] = pack_f16(kpv[0], kpv[1]);
-            kh_pack[i >> 1] = pack_f16(khv[0], khv[1]);
           }
-          const uint32_t chunk_off = (uint32_t)c * 128u + ((((uint32_t)t8 >> 3) ^ sw) << 4);
-          *reinterpret_cast<uint4*>(sm + OFF_QPT + chunk_off) =
-              make_uint4(qp_pack[0], qp_pack[1], qp_pack[2], qp_pack[3]);
-          *reinterpret_cast<uint4*>(sm + OFF_KPT + chunk_off) =
-              make_uint4(kp_pack[0], kp_pack[1], kp_pack[2], kp_pack[3]);
-          *reinterpret_cast<uint4*>(sm + OFF_KH + chunk_off) =
-              make_uint4(kh_pack[0], kh_pack[1], kh_pack[2], kh_pack[3]);
         }
       }
       fence_proxy_async_smem();
@@ -380,60 +469,62 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_qkz = (ci + 1 < nchunks);
 
       // ---------------- E: Gram blocks, tf32 mma.sync ----------------
-      float accP[3][2][4], accA[3][2][4];
+      // warps 0-3 build P, warps 4-7 build A, three blocks each at most
+      float acc[3][2][4];
       {
-        const int g = lane >> 2, q4 = lane & 3;
-        const float* Qt = reinterpret_cast<const float*>(sm + G_QT);
-        const float* Kt = reinterpret_cast<const float*>(sm + G_KT);
+        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 2;
         const unsigned char* Kpt = sm + G_KPT;
 #pragma unroll
         for (int bi = 0; bi < 3; ++bi) {
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) accP[bi][n][i] = accA[bi][n][i] = 0.f;
-          const int blk = warp + 4 * bi;
+            for (int i = 0; i < 4; ++i) acc[bi][n][i] = 0.f;
+          const int blk = (warp & 3) + 4 * bi;
           if (blk >= 10) continue;
           const int a = c_blk_a[blk], b = c_blk_b[blk];
           const float* dab = misc + M_DAB + (a > b ? dab_index(a, b) : 0) * kD;
           const int ta = 16 * a + g, jb = 16 * b + g;
-#pragma unroll 4
-          for (int c0 = 0; c0 < kD; c0 += 8) {
-            const int ca = c0 + q4, cb = c0 + q4 + 4;
-            float s0 = 1.f, s1 = 1.f;
-            if (a != b) { s0 = dab[ca]; s1 = dab[cb]; }
-            uint32_t fq[4], fk[4];
-            fq[0] = to_tf32(Qt[f32_off(ta, ca) >> 2] * s0);
-            fq[1] = to_tf32(Qt[f32_off(ta + 8, ca) >> 2] * s0);
-            fq[2] = to_tf32(Qt[f32_off(ta, cb) >> 2] * s1);
-            fq[3] = to_tf32(Qt[f32_off(ta + 8, cb) >> 2] * s1);
-            const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kpt + b16_off(ta, ca)));
-            const float k1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kpt + b16_off(ta + 8, ca)));
-            const float k2 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kpt + b16_off(ta, cb)));
-            const float k3 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(Kpt + b16_off(ta + 8, cb)));
-            fk[0] = to_tf32(k0 * s0);
-            fk[1] = to_tf32(k1 * s0);
-            fk[2] = to_tf32(k2 * s1);
-            fk[3] = to_tf32(k3 * s1);
-            const uint32_t b00 = to_tf32(Kt[f32_off(jb, ca) >> 2]);
-            const uint32_t b01 = to_tf32(Kt[f32_off(jb, cb) >> 2]);
-            const uint32_t b10 = to_tf32(Kt[f32_off(jb + 8, ca) >> 2]);
-            const uint32_t b11 = to_tf32(Kt[f32_off(jb + 8, cb) >> 2]);
-            mma_1688_tf32(accP[bi][0], fq, b00, b01);
-            mma_1688_tf32(accP[bi][1], fq, b10, b11);
-            mma_1688_tf32(accA[bi][0], fk, b00, b01);
-            mma_1688_tf32(accA[bi][1], fk, b10, b11);
+#pragma unroll 2
+          for (int c0 = 0; c0 < kD; c0 += 16) {
+            // 16 channels as two k-steps of 8; thread q covers channels
+            // c0+4q .. c0+4q+3 (logical k = q / q+4 -> channel c0+4q / +1 in
+            // the first step, +2 / +3 in the second; A and B agree).
+            const int cc = c0 + 4 * q4;
+            const float4 s4 = (a != b) ? *reinterpret_cast<const float4*>(dab + cc)
+                                       : make_float4(1.f, 1.f, 1.f, 1.f);
+            float4 x0, x1;
+            if (prod == 0) {
+              x0 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta, cc));
+              x1 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta + 8, cc));
+            } else {
+              const uint2 y0 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta, cc));
+              const uint2 y1 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta + 8, cc));
+              x0 = make_float4(bf16_lo(y0.x), bf16_hi(y0.x), bf16_lo(y0.y), bf16_hi(y0.y));
+              x1 = make_float4(bf16_lo(y1.x), bf16_hi(y1.x), bf16_lo(y1.y), bf16_hi(y1.y));
+            }
+            const float4 kb0 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb, cc));
+            const float4 kb1 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb + 8, cc));
+            uint32_t fa[4];
+            fa[0] = to_tf32(x0.x * s4.x); fa[1] = to_tf32(x1.x * s4.x);
+            fa[2] = to_tf32(x0.y * s4.y); fa[3] = to_tf32(x1.y * s4.y);
+            mma_1688_tf32(acc[bi][0], fa, __float_as_uint(kb0.x), __float_as_uint(kb0.y));
+            mma_1688_tf32(acc[bi][1], fa, __float_as_uint(kb1.x), __float_as_uint(kb1.y));
+            fa[0] = to_tf32(x0.z * s4.z); fa[1] = to_tf32(x1.z * s4.z);
+            fa[2] = to_tf32(x0.w * s4.w); fa[3] = to_tf32(x1.w * s4.w);
+            mma_1688_tf32(acc[bi][0], fa, __float_as_uint(kb0.z), __float_as_uint(kb0.w));
+            mma_1688_tf32(acc[bi][1], fa, __float_as_uint(kb1.z), __float_as_uint(kb1.w));
           }
         }
       }
       __syncthreads();  // Gram operands no longer read
       {
-        const int g = lane >> 2, q4 = lane & 3;
+        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 2;
         float* Akk = reinterpret_cast<float*>(sm + G_AKK);
         unsigned char* Pm = sm + G_P;
 #pragma unroll
         for (int bi = 0; bi < 3; ++bi) {
-          const int blk = warp + 4 * bi;
+          const int blk = (warp & 3) + 4 * bi;
           if (blk >= 10) continue;
           const int a = c_blk_a[blk], b = c_blk_b[blk];
 #pragma unroll
@@ -441,22 +532,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
               const int t = 16 * a + g + 8 * hr, j = 16 * b + 8 * n + 2 * q4;
-              const float p0 = j <= t ? accP[bi][n][2 * hr] : 0.f;
-              const float p1 = j + 1 <= t ? accP[bi][n][2 * hr + 1] : 0.f;
-              *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = pack_f16(p0, p1);
-              const float bt = misc[M_BETA + t];
-              Akk[t * kC + j] = j < t ? bt * accA[bi][n][2 * hr] : 0.f;
-              Akk[t * kC + j + 1] = j + 1 < t ? bt * accA[bi][n][2 * hr + 1] : 0.f;
+              if (prod == 0) {
+                const float p0 = j <= t ? acc[bi][n][2 * hr] : 0.f;
+                const float p1 = j + 1 <= t ? acc[bi][n][2 * hr + 1] : 0.f;
+                *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = pack_f16(p0, p1);
+              } else {
+                const float bt = misc[M_BETA + t];
+                Akk[t * kLS + j] = j < t ? bt * acc[bi][n][2 * hr] : 0.f;
+                Akk[t * kLS + j + 1] = j + 1 < t ? bt * acc[bi][n][2 * hr + 1] : 0.f;
+              }
             }
         }
-        for (int zb = warp; zb < 6; zb += 4) {
-          const int a = c_zero_a[zb], b = c_zero_b[zb];
+        if (prod == 0) {
+          for (int zb = warp & 3; zb < 6; zb += 4) {
+            const int a = c_zero_a[zb], b = c_zero_b[zb];
 #pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const int e = lane * 8 + i, t = 16 * a + (e >> 4), j = 16 * b + (e & 15);
-            *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
-            Akk[t * kC + j] = 0.f;
-            Akk[t * kC + j + 1] = 0.f;
+            for (int i = 0; i < 8; i += 2) {
+              const int e = lane * 8 + i, t = 16 * a + (e >> 4), j = 16 * b + (e & 15);
+              *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
+            }
           }
         }
       }
@@ -466,51 +560,51 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       {
         const float* Akk = reinterpret_cast<const float*>(sm + G_AKK);
         float* T = reinterpret_cast<float*>(sm + G_T32);
-        if (lane < 16) {  // diagonal block `warp`, column `lane`, forward substitution
+        if (warp < 4 && lane < 16) {  // diagonal block `warp`, column `lane`, forward substitution
           const int base = 16 * warp, cc = lane;
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float s = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) s -= Akk[(base + i) * kC + base + j] * x[j];
+            for (int j = 0; j < i; ++j) s -= Akk[(base + i) * kLS + base + j] * x[j];
             x[i] = s;
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) T[(base + i) * kC + base + cc] = x[i];
+          for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
         }
         __syncthreads();
+        // off-diagonal blocks by block forward substitution, one level (a - b = d)
+        // at a time, one block per warp:
+        //   Y = sum_{k=b}^{a-1} A_ak T_kb  (kept in the unused block (b, a)),
+        //   T_ab = -T_aa Y
+        {
+          const int g = lane >> 2, q4 = lane & 3;
 #pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-          const int nelem = (4 - d) * 256;
-          // Y_ab = sum_{j in blocks b..a-1} A[a rows][j] T[j][b cols], kept in block (b, a)
-          for (int e = tid; e < nelem; e += kNT) {
-            const int b = e >> 8, a = b + d, rr = (e >> 4) & 15, cc = e & 15;
-            float y = 0.f;
-            for (int j = 16 * b; j < 16 * a; ++j) y += Akk[(16 * a + rr) * kC + j] * T[j * kC + 16 * b + cc];
-            T[(16 * b + rr) * kC + 16 * a + cc] = y;
+          for (int d = 1; d < 4; ++d) {
+            if (warp < 4 - d) {
+              const int b = warp, a = b + d;
+              float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+              warp_gemm16_3tf32(acc, Akk, 16 * a, 16 * b, T, 16 * b, 16 * b, 16 * d, g, q4);
+              warp_store16(T, 16 * b, 16 * a, acc, 1.f, g, q4);
+              __syncwarp();
+              float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+              warp_gemm16_3tf32(acc2, T, 16 * a, 16 * a, T, 16 * b, 16 * a, 16, g, q4);
+              warp_store16(T, 16 * a, 16 * b, acc2, -1.f, g, q4);
+            }
+            __syncthreads();
           }
-          __syncthreads();
-          // T_ab = -T_aa Y_ab
-          for (int e = tid; e < nelem; e += kNT) {
-            const int b = e >> 8, a = b + d, rr = (e >> 4) & 15, cc = e & 15;
-            float s = 0.f;
-            for (int m = 0; m <= rr; ++m)
-              s -= T[(16 * a + rr) * kC + 16 * a + m] * T[(16 * b + m) * kC + 16 * a + cc];
-            T[(16 * a + rr) * kC + 16 * b + cc] = s;
-          }
-          __syncthreads();
         }
         // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal
         {
-          const int t = tid >> 1, j0 = (tid & 1) * 32;
+          const int t = tid >> 2, j0 = (tid & 3) * 16;
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 16) {
+          for (int jj = 0; jj < 16; jj += 16) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int j = j0 + jj + i;
-              v[i] = ((j >> 4) <= (t >> 4)) ? T[t * kC + j] * misc[M_BETA + j] : 0.f;
+              v[i] = ((j >> 4) <= (t >> 4)) ? T[t * kLS + j] * misc[M_BETA + j] : 0.f;
             }
             st_row16_f16(sm + G_TP, t, j0 + jj, v);
           }
@@ -521,9 +615,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_v = false;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       {  // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
-        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 8;
+        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 4;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
           uint4 x = vv[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -567,11 +661,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- H: W^T -> fp16 (MN-major B, row c) ----------------
 #pragma unroll
-      for (int col = 0; col < kC; col += 16) {
+      for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
         float v[16];
         tmem_ld16(my_lane + TW + col, v);
         tmem_ld_wait();
-        st_row16_f16(sm + G_WT, tid, col, v);
+        st_row16_f16(sm + G_WT, row, col, v);
       }
       fence_proxy_async_smem();
       sync_tc();
@@ -594,7 +688,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // ---------------- J: U^T -> fp16 in TMEM; S^T <- S^T Diag(e^{G_C}) ----------------
       {
 #pragma unroll
-        for (int col = 0; col < kC; col += 16) {
+        for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
           float v[16];
           tmem_ld16(my_lane + TU + col, v);
           tmem_ld_wait();
@@ -608,7 +702,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         const float* dec = misc + M_DECAY;
 #pragma unroll 1
-        for (int col = 0; col < kD; col += 16) {
+        for (int col = 64 * wh; col < 64 * wh + 64; col += 16) {
           float v[16];
           tmem_ld16(my_lane + TS32 + col, v);
           tmem_ld_wait();
@@ -640,9 +734,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- L: write O; S^T -> fp16 for the next chunk ----------------
       {
-        __nv_bfloat16* ocol = P.out + ((size_t)t0 * H + h) * kD + tid;
+        __nv_bfloat16* ocol = P.out + ((size_t)t0 * H + h) * kD + row;
 #pragma unroll
-        for (int col = 0; col < kC; col += 16) {
+        for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
           float v[16];
           tmem_ld16(my_lane + TO + col, v);
           tmem_ld_wait();
@@ -651,7 +745,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
         }
 #pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
+        for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
           float v[16];
           tmem_ld16(my_lane + TS32 + c0, v);
           tmem_ld_wait();
@@ -671,9 +765,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     // ---- final state: lane n holds column n ----
     if (P.final_state) {
-      float* dst = P.final_state + ((size_t)seq * H + h) * kD * kD + tid;
+      float* dst = P.final_state + ((size_t)seq * H + h) * kD * kD + row;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 16) {
+      for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
         float v[16];
         tmem_ld16(my_lane + TS32 + c0, v);
         tmem_ld_wait();

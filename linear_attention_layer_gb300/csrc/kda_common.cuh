@@ -40,7 +40,7 @@ struct IO<__nv_bfloat16> {
 
 // log-decay g = kGateMin * sigmoid(z).
 __device__ __forceinline__ float log_decay(float z) {
-  return kGateMin / (1.0f + __expf(-z));
+  return __fdividef(kGateMin, 1.0f + __expf(-z));
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
