@@ -408,8 +408,8 @@ def main():
         ms = max_over_ranks(ms, dist, device)
         line["e2e"] = {"value": round(weak_scaling_value(T, world, ms / 1e3), 3), "unit": UNIT,
                        "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
-        line["gpu_launches"] += args.e2e_steps
+                       "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                       "gpu_launches": args.e2e_steps}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     if "cpu" not in skip and rank == 0 and world == 1:

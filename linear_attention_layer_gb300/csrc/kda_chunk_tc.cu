@@ -246,7 +246,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0;
   bool pend_qkz = false, pend_v = false;  // TMA copies in flight (uniform)
   bool aborted = false;
-  bool range_ok = true;  // fp16 operand range held (this thread)
+  float absmax = 0.f;  // largest |value| this thread converted to fp16
 
   for (int u = blockIdx.x; u < P.num_units && !aborted; u += gridDim.x) {
     const int si = u / H, h = u % H;
@@ -288,7 +288,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-          range_ok &= f16_ok(v[2 * i]) & f16_ok(v[2 * i + 1]);
+          absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
         }
         tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
       }
@@ -313,8 +313,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float sq = 0.f, sk = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 a = *reinterpret_cast<const uint4*>(qrow + (j << 4));
-          const uint4 b = *reinterpret_cast<const uint4*>(krow + (j << 4));
+          const int jj = (j + qq + t) & 3;  // any order covers the row; this one is conflict-free
+          const uint4 a = *reinterpret_cast<const uint4*>(qrow + (jj << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(krow + (jj << 4));
           const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -623,7 +624,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-            range_ok &= f16_ok(lo) & f16_ok(hi);
+            absmax = fmaxf(absmax, fmaxf(fabsf(lo), fabsf(hi)));
             w[j] = pack_f16(lo, hi);
           }
           vv[i] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -696,7 +697,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-            range_ok &= f16_ok(v[2 * i]) & f16_ok(v[2 * i + 1]);
+            absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
           }
           tmem_st8(my_lane + TU16 + (col >> 1), hp);
         }
@@ -707,7 +708,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld16(my_lane + TS32 + col, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= dec[col + i];
+          for (int i = 0; i < 16; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
+            v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
+          }
           tmem_st16(my_lane + TS32 + col, v);
         }
         tmem_st_wait();
@@ -753,7 +757,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-            range_ok &= f16_ok(v[2 * i]) & f16_ok(v[2 * i + 1]);
+            absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
           }
           tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
         }
@@ -778,7 +782,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     sync_tc();
   }
 
-  if (!range_ok) report_error(P.err, kErrDeviceCheck);
+  if (!(absmax < kF16Max)) report_error(P.err, kErrDeviceCheck);
   if (aborted) {
     if (tid == 0) {
       report_error(P.err, kErrTimeout);
