@@ -64,7 +64,7 @@ using namespace kda::tc;
 
 constexpr int kC = 64;     // chunk length
 constexpr int kD = 128;    // dk = dv
-constexpr int kNT = 256;   // threads per CTA (8 warps; warps w and w+4 share a TMEM lane quadrant)
+constexpr int kNT = 512;   // threads per CTA (16 warps; warps w, w+4, w+8, w+12 share a TMEM lane quadrant)
 constexpr int kMaxOrder = 6144;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) ----
@@ -88,7 +88,7 @@ constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-majo
 constexpr uint32_t OFF_MISC = 212992;
 // misc floats
 constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_ER = 320, M_EGR = 832,
-              M_DAB = 1344, M_R = 2112, M_END = 2112 + 4 * 128;
+              M_DAB = 1344, M_R = 2112, M_TOT = 2624, M_END = 2624 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 
@@ -239,10 +239,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   sync_tc();
   const uint32_t tmem = *s_tmem;
-  // this thread's TMEM lane (row): warps w and w+4 own lanes 32(w%4) .. +31
-  // and split the columns of every TMEM pass between them (half wh)
+  // TMEM lane quadrant w % 4 (row = tid % 128); the kWQ warps sharing a
+  // quadrant split the columns of every TMEM pass (part cq)
   const uint32_t my_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  const int row = tid & 127, wh = warp >> 2;
+  const int row = tid & 127, cq = warp >> 2;
   uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0;
   bool pend_qkz = false, pend_v = false;  // TMA copies in flight (uniform)
   bool aborted = false;
@@ -278,8 +278,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int n = row;
       const float* src = P.initial_state ? P.initial_state + ((size_t)seq * H + h) * kD * kD + n
                                          : nullptr;
-#pragma unroll 1
-      for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
+#pragma unroll
+      for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = src ? __ldg(src + (size_t)(c0 + i) * kD) : 0.f;
@@ -307,15 +307,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- B: token norms and beta ----------------
       {
-        const int t = tid >> 2, qq = tid & 3;
-        const unsigned char* qrow = sm + OFF_Q + (qq >> 1) * 8192 + t * 128 + (qq & 1) * 64;
-        const unsigned char* krow = sm + OFF_K + (qq >> 1) * 8192 + t * 128 + (qq & 1) * 64;
+        // eight threads per token, 16 channels each (two 16-byte chunks)
+        const int t = tid >> 3, e = tid & 7;
+        const int boff = (e >> 2) * 8192 + t * 128 + (e & 3) * 32;
         float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int jj = (j + qq + t) & 3;  // any order covers the row; this one is conflict-free
-          const uint4 a = *reinterpret_cast<const uint4*>(qrow + (jj << 4));
-          const uint4 b = *reinterpret_cast<const uint4*>(krow + (jj << 4));
+        for (int j = 0; j < 2; ++j) {
+          const int jj = j ^ (e >> 2);  // either order covers both chunks; this one is conflict-free
+          const uint4 a = *reinterpret_cast<const uint4*>(sm + OFF_Q + boff + (jj << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(sm + OFF_K + boff + (jj << 4));
           const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -325,11 +325,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             sk += x * x + y * y;
           }
         }
-        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-        if (qq == 0) {
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        }
+        if (e == 0) {
           misc[M_RQ + t] = t < len ? rsqrtf(sq + kNormEps) : 0.f;
           misc[M_RK + t] = t < len ? rsqrtf(sk + kNormEps) : 0.f;
         }
@@ -339,111 +340,95 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (tid < min(kC, eos - t0 - kC)) beta_pf = __ldg(P.beta + (size_t)(t0 + kC + tid) * H + h);
         }
       }
-      __syncthreads();
 
       // ---------------- C: gate, cumulative decay, per-channel tables ----------------
       float* Z = reinterpret_cast<float*>(sm + OFF_Z);
       {
-        // two threads per key channel (adjacent lanes), 32 tokens each
-        const int c = tid >> 1, hf = tid & 1;
-        float zz[32];
+        // thread = (subtile a, key channel c); a warp covers 32 channels of one subtile
+        const int c = tid & 127, a = tid >> 7;
+        float zz[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) zz[i] = Z[(32 * hf + i) * kD + c];
+        for (int i = 0; i < 16; ++i) zz[i] = Z[(16 * a + i) * kD + c];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) zz[i] = (32 * hf + i < len) ? log_decay(zz[i]) : 0.f;
-        float run = 0.f;
+        for (int i = 0; i < 16; ++i) zz[i] = (16 * a + i < len) ? log_decay(zz[i]) : 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          run += zz[i];
-          zz[i] = run;
-        }
-        const float first = __shfl_sync(0xffffffffu, run, lane & ~1);  // sum over tokens 0..31
-        const float off = hf ? first : 0.f;
+        for (int i = 1; i < 16; ++i) zz[i] += zz[i - 1];
+        misc[M_TOT + a * kD + c] = zz[15];
+        __syncthreads();
+        float tot[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          zz[i] += off;
-          Z[(32 * hf + i) * kD + c] = zz[i];
-        }
-        const float mid = zz[15], end = zz[31];
-        const float pmid = __shfl_xor_sync(0xffffffffu, mid, 1);
-        const float pend = __shfl_xor_sync(0xffffffffu, end, 1);
-        float r[4];
-        r[0] = 0.f;
-        r[1] = hf ? pmid : mid;
-        r[2] = hf ? pend : end;
-        r[3] = hf ? mid : pmid;
-        const float G = hf ? end : pend;
-        if (hf == 0) {
-          misc[M_DECAY + c] = __expf(G);
+        for (int b = 0; b < 4; ++b) tot[b] = misc[M_TOT + b * kD + c];
+        float rr[4];  // cumulative log-decay before each subtile
+        rr[0] = 0.f;
+        rr[1] = tot[0];
+        rr[2] = tot[0] + tot[1];
+        rr[3] = rr[2] + tot[2];
+        const float GC = rr[3] + tot[3];
+        const float r = a == 0 ? rr[0] : (a == 1 ? rr[1] : (a == 2 ? rr[2] : rr[3]));
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            misc[M_ER + a * kD + c] = __expf(r[a]);
-            misc[M_EGR + a * kD + c] = __expf(G - r[a]);
-            misc[M_R + a * kD + c] = r[a];
-          }
+        for (int i = 0; i < 16; ++i) Z[(16 * a + i) * kD + c] = zz[i] + r;
+        misc[M_R + a * kD + c] = r;
+        misc[M_ER + a * kD + c] = __expf(r);
+        misc[M_EGR + a * kD + c] = __expf(GC - r);
+        if (a == 0) {
+          misc[M_DECAY + c] = __expf(GC);
         } else {
-          misc[M_DAB + 0 * kD + c] = __expf(r[1] - r[0]);
-          misc[M_DAB + 1 * kD + c] = __expf(r[2] - r[0]);
-          misc[M_DAB + 2 * kD + c] = __expf(r[2] - r[1]);
-          misc[M_DAB + 3 * kD + c] = __expf(r[3] - r[0]);
-          misc[M_DAB + 4 * kD + c] = __expf(r[3] - r[1]);
-          misc[M_DAB + 5 * kD + c] = __expf(r[3] - r[2]);
+          // D_ab = e^{r_a - r_b}, b < a; slots (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+          const int base = a == 1 ? 0 : (a == 2 ? 1 : 3);
+#pragma unroll
+          for (int b = 0; b < 3; ++b)
+            if (b < a) misc[M_DAB + (base + b) * kD + c] = __expf(r - rr[b]);
         }
       }
       __syncthreads();  // G and the per-channel tables of every channel are ready
 
-      // ---------------- D: decayed operands (thread = 2 key channels x 32 tokens) ----------------
+      // ---------------- D: decayed operands (thread = 2 key channels x 8 tokens) ----------------
       {
-        const int c = 2 * (tid & 63), a = tid >> 6;
+        const int c = 2 * (tid & 63), a = (tid >> 6) & 3, tb = 16 * a + 8 * (tid >> 8);
         const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
         const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
         const uint32_t sw0 = (uint32_t)(c & 7), sw1 = (uint32_t)((c + 1) & 7);
-        {
-          const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
-          const float er0 = misc[M_ER + a * kD + c], er1 = misc[M_ER + a * kD + c + 1];
-          const float eg0 = misc[M_EGR + a * kD + c], eg1 = misc[M_EGR + a * kD + c + 1];
+        const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
+        const float er0 = misc[M_ER + a * kD + c], er1 = misc[M_ER + a * kD + c + 1];
+        const float eg0 = misc[M_EGR + a * kD + c], eg1 = misc[M_EGR + a * kD + c + 1];
+        float qpv[2][8], kpv[2][8], khv[2][8];
 #pragma unroll
-          for (int t8 = 0; t8 < 16; t8 += 8) {
-            float qpv[2][8], kpv[2][8], khv[2][8];
+        for (int i = 0; i < 8; ++i) {
+          const int t = tb + i;
+          const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
+          const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
+          const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
+          const uint32_t off = sw128_offset(t, c & 63);
+          const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
+          const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
+          const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
+          const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
+          const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
+          const float qt0 = q0 * F0, qt1 = q1 * F1;
+          const float kp0 = k0 * F0, kp1 = k1 * F1;
+          const float kt0 = k0 * E0, kt1 = k1 * E1;
+          *reinterpret_cast<float2*>(sm + G_QT + f32_off(t, c)) = make_float2(qt0, qt1);
+          *reinterpret_cast<float2*>(sm + G_KT + f32_off(t, c)) =
+              make_float2(__uint_as_float(to_tf32(kt0)), __uint_as_float(to_tf32(kt1)));
+          *reinterpret_cast<uint32_t*>(sm + G_KPT + b16_off(t, c)) = pack_bf16(kp0, kp1);
+          qpv[0][i] = qt0 * er0; qpv[1][i] = qt1 * er1;
+          kpv[0][i] = kp0 * er0; kpv[1][i] = kp1 * er1;
+          khv[0][i] = kt0 * eg0; khv[1][i] = kt1 * eg1;
+        }
+        const uint32_t tc8 = (uint32_t)tb >> 3;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int t = 16 * a + t8 + i;
-              const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
-              const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
-              const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
-              const uint32_t off = sw128_offset(t, c & 63);
-              const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
-              const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
-              const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
-              const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
-              const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
-              const float qt0 = q0 * F0, qt1 = q1 * F1;
-              const float kp0 = k0 * F0, kp1 = k1 * F1;
-              const float kt0 = k0 * E0, kt1 = k1 * E1;
-              *reinterpret_cast<float2*>(sm + G_QT + f32_off(t, c)) = make_float2(qt0, qt1);
-              *reinterpret_cast<float2*>(sm + G_KT + f32_off(t, c)) =
-                  make_float2(__uint_as_float(to_tf32(kt0)), __uint_as_float(to_tf32(kt1)));
-              *reinterpret_cast<uint32_t*>(sm + G_KPT + b16_off(t, c)) = pack_bf16(kp0, kp1);
-              qpv[0][i] = qt0 * er0; qpv[1][i] = qt1 * er1;
-              kpv[0][i] = kp0 * er0; kpv[1][i] = kp1 * er1;
-              khv[0][i] = kt0 * eg0; khv[1][i] = kt1 * eg1;
-            }
-            const uint32_t tc8 = (uint32_t)(16 * a + t8) >> 3;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const uint32_t row = (uint32_t)(c + e);
-              const uint32_t off = row * 128u + ((tc8 ^ (e ? sw1 : sw0)) << 4);
-              *reinterpret_cast<uint4*>(sm + OFF_QPT + off) =
-                  make_uint4(pack_f16(qpv[e][0], qpv[e][1]), pack_f16(qpv[e][2], qpv[e][3]),
-                             pack_f16(qpv[e][4], qpv[e][5]), pack_f16(qpv[e][6], qpv[e][7]));
-              *reinterpret_cast<uint4*>(sm + OFF_KPT + off) =
-                  make_uint4(pack_f16(kpv[e][0], kpv[e][1]), pack_f16(kpv[e][2], kpv[e][3]),
-                             pack_f16(kpv[e][4], kpv[e][5]), pack_f16(kpv[e][6], kpv[e][7]));
-              *reinterpret_cast<uint4*>(sm + OFF_KH + off) =
-                  make_uint4(pack_f16(khv[e][0], khv[e][1]), pack_f16(khv[e][2], khv[e][3]),
-                             pack_f16(khv[e][4], khv[e][5]), pack_f16(khv[e][6], khv[e][7]));
-            }
-          }
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t rw = (uint32_t)(c + e);
+          const uint32_t off = rw * 128u + ((tc8 ^ (e ? sw1 : sw0)) << 4);
+          *reinterpret_cast<uint4*>(sm + OFF_QPT + off) =
+              make_uint4(pack_f16(qpv[e][0], qpv[e][1]), pack_f16(qpv[e][2], qpv[e][3]),
+                         pack_f16(qpv[e][4], qpv[e][5]), pack_f16(qpv[e][6], qpv[e][7]));
+          *reinterpret_cast<uint4*>(sm + OFF_KPT + off) =
+              make_uint4(pack_f16(kpv[e][0], kpv[e][1]), pack_f16(kpv[e][2], kpv[e][3]),
+                         pack_f16(kpv[e][4], kpv[e][5]), pack_f16(kpv[e][6], kpv[e][7]));
+          *reinterpret_cast<uint4*>(sm + OFF_KH + off) =
+              make_uint4(pack_f16(khv[e][0], khv[e][1]), pack_f16(khv[e][2], khv[e][3]),
+                         pack_f16(khv[e][4], khv[e][5]), pack_f16(khv[e][6], khv[e][7]));
         }
       }
       fence_proxy_async_smem();
@@ -470,18 +455,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_qkz = (ci + 1 < nchunks);
 
       // ---------------- E: Gram blocks, tf32 mma.sync ----------------
-      // warps 0-3 build P, warps 4-7 build A, three blocks each at most
-      float acc[3][2][4];
+      // warps 0-7 build P, warps 8-15 build A; warp w&7 takes blocks w&7 and (w&7)+8
+      float acc[2][2][4];
       {
-        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 2;
+        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 3;
         const unsigned char* Kpt = sm + G_KPT;
 #pragma unroll
-        for (int bi = 0; bi < 3; ++bi) {
+        for (int bi = 0; bi < 2; ++bi) {
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[bi][n][i] = 0.f;
-          const int blk = (warp & 3) + 4 * bi;
+          const int blk = (warp & 7) + 8 * bi;
           if (blk >= 10) continue;
           const int a = c_blk_a[blk], b = c_blk_b[blk];
           const float* dab = misc + M_DAB + (a > b ? dab_index(a, b) : 0) * kD;
@@ -520,12 +505,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       __syncthreads();  // Gram operands no longer read
       {
-        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 2;
+        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 3;
         float* Akk = reinterpret_cast<float*>(sm + G_AKK);
         unsigned char* Pm = sm + G_P;
 #pragma unroll
-        for (int bi = 0; bi < 3; ++bi) {
-          const int blk = (warp & 3) + 4 * bi;
+        for (int bi = 0; bi < 2; ++bi) {
+          const int blk = (warp & 7) + 8 * bi;
           if (blk >= 10) continue;
           const int a = c_blk_a[blk], b = c_blk_b[blk];
 #pragma unroll
@@ -544,14 +529,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               }
             }
         }
-        if (prod == 0) {
-          for (int zb = warp & 3; zb < 6; zb += 4) {
-            const int a = c_zero_a[zb], b = c_zero_b[zb];
+        if (prod == 0 && (warp & 7) < 6) {
+          const int zb = warp & 7;
+          const int a = c_zero_a[zb], b = c_zero_b[zb];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const int e = lane * 8 + i, t = 16 * a + (e >> 4), j = 16 * b + (e & 15);
-              *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
-            }
+          for (int i = 0; i < 8; i += 2) {
+            const int e = lane * 8 + i, t = 16 * a + (e >> 4), j = 16 * b + (e & 15);
+            *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
           }
         }
       }
@@ -585,9 +569,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int d = 1; d < 4; ++d) {
             if (warp < 4 - d) {
               const int b = warp, a = b + d;
-              float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-              warp_gemm16_3tf32(acc, Akk, 16 * a, 16 * b, T, 16 * b, 16 * b, 16 * d, g, q4);
-              warp_store16(T, 16 * b, 16 * a, acc, 1.f, g, q4);
+              float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+              warp_gemm16_3tf32(acc1, Akk, 16 * a, 16 * b, T, 16 * b, 16 * b, 16 * d, g, q4);
+              warp_store16(T, 16 * b, 16 * a, acc1, 1.f, g, q4);
               __syncwarp();
               float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
               warp_gemm16_3tf32(acc2, T, 16 * a, 16 * a, T, 16 * b, 16 * a, 16, g, q4);
@@ -598,17 +582,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal
         {
-          const int t = tid >> 2, j0 = (tid & 3) * 16;
+          const int t = tid >> 3, j0 = (tid & 7) * 8;
+          float v[8];
 #pragma unroll
-          for (int jj = 0; jj < 16; jj += 16) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int j = j0 + jj + i;
-              v[i] = ((j >> 4) <= (t >> 4)) ? T[t * kLS + j] * misc[M_BETA + j] : 0.f;
-            }
-            st_row16_f16(sm + G_TP, t, j0 + jj, v);
+          for (int i = 0; i < 8; ++i) {
+            const int j = j0 + i;
+            v[i] = ((j >> 4) <= (t >> 4)) ? T[t * kLS + j] * misc[M_BETA + j] : 0.f;
           }
+          *reinterpret_cast<uint4*>(sm + G_TP + t * 128 + ((((uint32_t)j0 >> 3) ^ (t & 7)) << 4)) =
+              make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
+                         pack_f16(v[6], v[7]));
         }
       }
       ok = wait_bar(bar_v, ph_v, P.spin_cycles);
@@ -616,9 +599,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_v = false;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       {  // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
-        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 4;
+        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
           uint4 x = vv[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -661,12 +644,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_v = (ci + 1 < nchunks);
 
       // ---------------- H: W^T -> fp16 (MN-major B, row c) ----------------
-#pragma unroll
-      for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
+      {
         float v[16];
-        tmem_ld16(my_lane + TW + col, v);
+        tmem_ld16(my_lane + TW + 16 * cq, v);
         tmem_ld_wait();
-        st_row16_f16(sm + G_WT, row, col, v);
+        st_row16_f16(sm + G_WT, row, 16 * cq, v);
       }
       fence_proxy_async_smem();
       sync_tc();
@@ -688,10 +670,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- J: U^T -> fp16 in TMEM; S^T <- S^T Diag(e^{G_C}) ----------------
       {
-#pragma unroll
-        for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
+        {
           float v[16];
-          tmem_ld16(my_lane + TU + col, v);
+          tmem_ld16(my_lane + TU + 16 * cq, v);
           tmem_ld_wait();
           uint32_t hp[8];
 #pragma unroll
@@ -699,11 +680,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
             absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
           }
-          tmem_st8(my_lane + TU16 + (col >> 1), hp);
+          tmem_st8(my_lane + TU16 + 8 * cq, hp);
         }
         const float* dec = misc + M_DECAY;
-#pragma unroll 1
-        for (int col = 64 * wh; col < 64 * wh + 64; col += 16) {
+#pragma unroll
+        for (int col = 32 * cq; col < 32 * cq + 32; col += 16) {
           float v[16];
           tmem_ld16(my_lane + TS32 + col, v);
           tmem_ld_wait();
@@ -739,8 +720,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // ---------------- L: write O; S^T -> fp16 for the next chunk ----------------
       {
         __nv_bfloat16* ocol = P.out + ((size_t)t0 * H + h) * kD + row;
-#pragma unroll
-        for (int col = 32 * wh; col < 32 * wh + 32; col += 16) {
+        {
+          const int col = 16 * cq;
           float v[16];
           tmem_ld16(my_lane + TO + col, v);
           tmem_ld_wait();
@@ -748,8 +729,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i = 0; i < 16; ++i)
             if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
         }
-#pragma unroll 1
-        for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
+#pragma unroll
+        for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
           float v[16];
           tmem_ld16(my_lane + TS32 + c0, v);
           tmem_ld_wait();
@@ -770,8 +751,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- final state: lane n holds column n ----
     if (P.final_state) {
       float* dst = P.final_state + ((size_t)seq * H + h) * kD * kD + row;
-#pragma unroll 1
-      for (int c0 = 64 * wh; c0 < 64 * wh + 64; c0 += 16) {
+#pragma unroll
+      for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
         float v[16];
         tmem_ld16(my_lane + TS32 + c0, v);
         tmem_ld_wait();
