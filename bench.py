@@ -212,16 +212,23 @@ def event_time_ms(fn, stream):
     return a, b
 
 
-def bench_prefill(kda, p, steps, warmup, dist, device):
+def bench_prefill(kda, p, steps, warmup, dist, device, split=False):
     import torch
     stream = torch.cuda.current_stream()
     out = torch.empty_like(p.v)
     fin = torch.empty((p.num_seqs, p.meta["num_heads"], p.meta["dk"], p.meta["dv"]),
                       dtype=torch.float32, device=p.v.device)
+    ws = None
+    if split:  # scratch that lets few long sequences split across SMs (allocated once)
+        nbytes = kda.chunk_fwd_workspace_size(p.num_seqs, p.total_tokens, p.meta["num_heads"],
+                                              p.meta["dk"], p.meta["dv"], p.q.dtype,
+                                              p.cu_seqlens_host)
+        if nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
     def step():
         kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, out=out,
-                      final_state=fin, cu_seqlens_host=p.cu_seqlens_host)
+                      final_state=fin, cu_seqlens_host=p.cu_seqlens_host, workspace=ws)
 
     for _ in range(warmup):
         step()
@@ -316,6 +323,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu")
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
+    ap.add_argument("--split", action="store_true",
+                    help="pass scratch so that few long sequences are split across SMs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -350,7 +359,8 @@ def main():
     except Exception:
         gpu_uuid = None
     with ClockSampler(gpu_uuid) as clk:
-        total_ms, per_launch = bench_prefill(kda, p, args.steps, args.warmup, dist, device)
+        total_ms, per_launch = bench_prefill(kda, p, args.steps, args.warmup, dist, device,
+                                             split=args.split)
     total_ms = max_over_ranks(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
     value = weak_scaling_value(T, world, total_ms / 1e3 / args.steps)
@@ -370,7 +380,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "description": workloads.DESCRIPTIONS[args.workload],
                    "num_seqs": N, "total_tokens": T, "num_heads": H, "dk": 128, "dv": 128,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                   "split_long_sequences": bool(args.split)},
         "roofline": roofline,
         "clocks": clk.summary(),
         "gpu_launches": args.steps,

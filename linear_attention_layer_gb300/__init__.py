@@ -168,7 +168,21 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
 
 def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, final_state=None,
               output_final_state=True, cu_seqlens_host=None, workspace=None, stream=None):
-    """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state)."""
+    """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state).
+
+    ``workspace``: a device tensor of scratch (at least
+    ``chunk_fwd_workspace_size`` bytes, 256-byte aligned) that lets long
+    sequences be split across SMs, ``"auto"`` to allocate it here with torch,
+    or None (no split).  Results agree either way within the tolerances."""
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be a tensor, 'auto' or None")
+        workspace = None
+        if cu_seqlens_host is not None:
+            nbytes = chunk_fwd_workspace_size(len(cu_seqlens_host) - 1, q.shape[0], q.shape[1],
+                                              q.shape[2], v.shape[-1], q.dtype, cu_seqlens_host)
+            if nbytes:
+                workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     return _prefill("kda_chunk_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
                     final_state, output_final_state, cu_seqlens_host, workspace, stream)
 

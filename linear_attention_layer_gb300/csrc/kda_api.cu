@@ -104,7 +104,8 @@ kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,
   if (s != KDA_OK) return s;
   const kda::Problem p = to_problem(desc);
   cudaError_t e = kda::chunk_tc_supported(p, a)
-                      ? kda::launch_chunk_tc(p, a, desc->cu_seqlens_host, (cudaStream_t)stream)
+                      ? kda::launch_chunk_tc(p, a, desc->cu_seqlens_host, desc->workspace,
+                                             desc->workspace_bytes, (cudaStream_t)stream)
                       : kda::launch_chunk_simt(p, a, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -113,7 +114,7 @@ kda_status_t kda_chunk_fwd_workspace_size(const kda_desc_t* desc, size_t* bytes)
   if (!bytes) return KDA_ERR_INVALID_ARGUMENT;
   kda_status_t s = check_desc(desc, false);
   if (s != KDA_OK) return s;
-  *bytes = 0;
+  *bytes = kda::chunk_tc_workspace_bytes(to_problem(desc), desc->cu_seqlens_host);
   return KDA_OK;
 }
 

@@ -49,6 +49,8 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <array>
+#include <cmath>
 #include <mutex>
 #include <numeric>
 #include <vector>
@@ -103,16 +105,28 @@ constexpr uint32_t TO = 384;    // O^T fp32   [n][t]    64 cols
 // largest magnitude an fp16 operand may take
 constexpr float kF16Max = 65504.0f;
 
+// Work list.  mode 0: units are (sequence, head) pairs, list[i] = the i-th
+// sequence to process (longest first) when use_order, token ranges from the
+// device cu_seqlens.  mode 1 (splitting long sequences): list holds entries
+// of kEnt ints {seq, token begin, token end, in, out, flags}; in / out are
+// state slots of `ws` (>= 0), or kSlotZero / kSlotIdentity / kSlotUser (the
+// caller's initial / final state of `seq`), kSlotNone for no output state;
+// flags & kFlagZeroV treats v as zero.
+constexpr int kEnt = 6;
+constexpr int kSlotNone = -1, kSlotZero = -1, kSlotIdentity = -2, kSlotUser = -3;
+constexpr int kFlagZeroV = 1;
+
 struct Params {
   const float* beta;
   const float* initial_state;
   const int32_t* cu;
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;   // may be null (no output written)
   float* final_state;
+  float* ws;            // state slots [slot][H][dk][dv] (mode 1)
   int* err;
-  int H, total, num_seqs, num_units, use_order;
+  int H, total, num_seqs, num_units, use_order, mode;
   long long spin_cycles;
-  int order[kMaxOrder];
+  int list[kMaxOrder];
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, long long limit) {
@@ -250,8 +264,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   for (int u = blockIdx.x; u < P.num_units && !aborted; u += gridDim.x) {
     const int si = u / H, h = u % H;
-    const int seq = P.use_order ? P.order[si] : si;
-    const int bos = P.cu[seq], eos = P.cu[seq + 1];
+    int seq, bos, eos, in_slot = kSlotUser, out_slot = kSlotUser, flags = 0;
+    if (P.mode == 0) {
+      seq = P.use_order ? P.list[si] : si;
+      bos = P.cu[seq];
+      eos = P.cu[seq + 1];
+    } else {
+      const int* e = P.list + kEnt * si;
+      seq = e[0]; bos = e[1]; eos = e[2]; in_slot = e[3]; out_slot = e[4]; flags = e[5];
+    }
+    const bool zero_v = (flags & kFlagZeroV) != 0;
     if (bos < 0 || eos < bos || eos > P.total) {
       if (tid == 0) report_error(P.err, kErrDeviceCheck);
       continue;
@@ -264,11 +286,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_load_3d(sm + OFF_K, &tm_k, 0, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_Z, &tm_z, 0, h, bos, bar_qkz);
-      mbar_arrive_expect_tx(bar_v, 16384u);
-      tma_load_3d(sm + OFF_V, &tm_v, 0, h, bos, bar_v);
-      tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, bos, bar_v);
+      if (!zero_v) {
+        mbar_arrive_expect_tx(bar_v, 16384u);
+        tma_load_3d(sm + OFF_V, &tm_v, 0, h, bos, bar_v);
+        tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, bos, bar_v);
+      }
     }
-    pend_qkz = pend_v = nchunks > 0;
+    pend_qkz = nchunks > 0;
+    pend_v = nchunks > 0 && !zero_v;
     // beta of the first chunk (later chunks are prefetched one chunk ahead)
     float beta_pf = 0.f;
     if (tid < min(kC, eos - bos)) beta_pf = __ldg(P.beta + (size_t)(bos + tid) * H + h);
@@ -276,13 +301,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- entry state S^T: lane n holds column n of S (fp32 and fp16) ----
     {
       const int n = row;
-      const float* src = P.initial_state ? P.initial_state + ((size_t)seq * H + h) * kD * kD + n
-                                         : nullptr;
+      const float* src = nullptr;
+      if (in_slot == kSlotUser) {
+        if (P.initial_state) src = P.initial_state + ((size_t)seq * H + h) * kD * kD + n;
+      } else if (in_slot >= 0) {
+        src = P.ws + ((size_t)in_slot * H + h) * kD * kD + n;
+      }
+      const float diag = in_slot == kSlotIdentity ? 1.f : 0.f;
 #pragma unroll
       for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = src ? __ldg(src + (size_t)(c0 + i) * kD) : 0.f;
+        for (int i = 0; i < 16; ++i)
+          v[i] = src ? __ldg(src + (size_t)(c0 + i) * kD) : (c0 + i == n ? diag : 0.f);
         tmem_st16(my_lane + TS32 + c0, v);
         uint32_t hp[8];
 #pragma unroll
@@ -594,15 +625,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                          pack_f16(v[6], v[7]));
         }
       }
-      ok = wait_bar(bar_v, ph_v, P.spin_cycles);
-      ph_v ^= 1;
-      pend_v = false;
+      if (!zero_v) {
+        ok = wait_bar(bar_v, ph_v, P.spin_cycles);
+        ph_v ^= 1;
+        pend_v = false;
+      }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       {  // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
         uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          uint4 x = vv[i];
+          uint4 x = zero_v ? make_uint4(0u, 0u, 0u, 0u) : vv[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -635,13 +668,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ph_mma ^= 1;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
-      if (tid == 0 && ci + 1 < nchunks) {  // v stage consumed
+      if (tid == 0 && ci + 1 < nchunks && !zero_v) {  // v stage consumed
         const int tn = t0 + kC;
         mbar_arrive_expect_tx(bar_v, 16384u);
         tma_load_3d(sm + OFF_V, &tm_v, 0, h, tn, bar_v);
         tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, tn, bar_v);
       }
-      pend_v = (ci + 1 < nchunks);
+      pend_v = (ci + 1 < nchunks) && !zero_v;
 
       // ---------------- H: W^T -> fp16 (MN-major B, row c) ----------------
       {
@@ -720,7 +753,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // ---------------- L: write O; S^T -> fp16 for the next chunk ----------------
       {
         __nv_bfloat16* ocol = P.out + ((size_t)t0 * H + h) * kD + row;
-        {
+        if (P.out) {
           const int col = 16 * cq;
           float v[16];
           tmem_ld16(my_lane + TO + col, v);
@@ -749,8 +782,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (aborted) break;
 
     // ---- final state: lane n holds column n ----
-    if (P.final_state) {
-      float* dst = P.final_state + ((size_t)seq * H + h) * kD * kD + row;
+    float* dst = nullptr;
+    if (out_slot == kSlotUser) {
+      if (P.final_state) dst = P.final_state + ((size_t)seq * H + h) * kD * kD + row;
+    } else if (out_slot >= 0) {
+      dst = P.ws + ((size_t)out_slot * H + h) * kD * kD + row;
+    }
+    if (dst) {
 #pragma unroll
       for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
         float v[16];
@@ -813,6 +851,171 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------- splitting long sequences --
+//
+// When there are fewer (sequence, head) units than SMs, a long sequence is cut
+// into segments that run in parallel (the intra-device counterpart of the
+// context-parallel scheme of blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE
+// 架构", section "第二层"): the state after a segment is affine in the state
+// before it, S_out = M S_in + S~, with M the product of the segment's
+// per-token transitions (the final state of the segment run from S_in = I
+// with v = 0) and S~ the final state run from S_in = 0.  Pass 1 computes
+// (S~, M) for the inner segments (the first segment runs from the true
+// initial state), a prefix scan S_in(p+1) = M_p S_in(p) + S~_p yields every
+// segment's entry state, and pass 2 reruns each segment from its entry state,
+// writing the outputs and, for the last segment, the final state.
+
+constexpr int kScanThreads = 256;
+constexpr int kMaxScanSeqs = 512;
+constexpr int kScanLd = 132;  // padded row (floats) of the scan's shared tiles
+
+struct ScanSeq {
+  int seq, base, nseg;
+};
+struct ScanParams {
+  const float* initial_state;  // caller's, may be null
+  float* ws;
+  int H, E;
+  ScanSeq s[kMaxScanSeqs];
+};
+
+// One CTA per (sequence, head), fp32: entry state of segment 0 (a copy of
+// the initial state, so that the final state may alias it), then
+// S_in(p+1) = M_p S_in(p) + S~_p for the inner segments.  Thread (ty, tx)
+// owns rows 8ty.. and columns 8tx.. of the 128 x 128 state.
+__global__ void __launch_bounds__(kScanThreads)
+state_scan_kernel(const __grid_constant__ ScanParams Q) {
+  extern __shared__ __align__(16) float scan_smem[];
+  float* Mt = scan_smem;                 // M transposed: Mt[k][c]
+  float* Ss = scan_smem + kD * kScanLd;  // current state: Ss[k][j]
+  const ScanSeq sq = Q.s[blockIdx.x / Q.H];
+  const int h = blockIdx.x % Q.H, tid = threadIdx.x;
+  const int r0 = (tid >> 4) * 8, c0 = (tid & 15) * 8;
+  const size_t st = (size_t)kD * kD;
+  auto slot = [&](int s) { return Q.ws + ((size_t)s * Q.H + h) * st; };
+  {
+    float* dst = slot(sq.base);
+    const float* src = Q.initial_state ? Q.initial_state + ((size_t)sq.seq * Q.H + h) * st : nullptr;
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; j += 4) {
+        const size_t o = (size_t)(r0 + i) * kD + c0 + j;
+        *reinterpret_cast<float4*>(dst + o) =
+            src ? *reinterpret_cast<const float4*>(src + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+  }
+  if (sq.nseg < 3) return;
+  float s[8][8];
+  {
+    const float* src = slot(sq.base + 1);
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; ++j) s[i][j] = src[(size_t)(r0 + i) * kD + c0 + j];
+  }
+  for (int p = 1; p + 1 < sq.nseg; ++p) {
+    const float* M = slot(2 * Q.E + sq.base + p);
+    const float* St = slot(Q.E + sq.base + p);
+    __syncthreads();
+    for (int idx = tid; idx < kD * kD; idx += kScanThreads) {
+      const int c = idx >> 7, k = idx & 127;
+      Mt[k * kScanLd + c] = M[idx];
+    }
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; ++j) Ss[(r0 + i) * kScanLd + c0 + j] = s[i][j];
+    __syncthreads();
+    float acc[8][8];
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; ++j) acc[i][j] = St[(size_t)(r0 + i) * kD + c0 + j];
+#pragma unroll 4
+    for (int k = 0; k < kD; ++k) {
+      const float4 m0 = *reinterpret_cast<const float4*>(Mt + k * kScanLd + r0);
+      const float4 m1 = *reinterpret_cast<const float4*>(Mt + k * kScanLd + r0 + 4);
+      const float4 s0 = *reinterpret_cast<const float4*>(Ss + k * kScanLd + c0);
+      const float4 s1 = *reinterpret_cast<const float4*>(Ss + k * kScanLd + c0 + 4);
+      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(mv[i], sv[j], acc[i][j]);
+    }
+    float* dst = slot(sq.base + p + 1);
+    for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; ++j) {
+        s[i][j] = acc[i][j];
+        dst[(size_t)(r0 + i) * kD + c0 + j] = acc[i][j];
+      }
+  }
+}
+
+struct SplitPlan {
+  bool use = false;
+  int seg_len = 0, E = 0;
+  std::vector<int> nseg, base;
+  size_t bytes = 0;
+};
+
+constexpr int kMaxEntries = kMaxOrder / kEnt;
+
+// Choose a segment length by a waves-of-SMs cost model; split only when it
+// beats the unsplit launch by a clear margin.
+SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms) {
+  SplitPlan best;
+  if (!cu || p.num_seqs == 0 || p.num_seqs > kMaxScanSeqs) return best;
+  const long units = (long)p.num_seqs * p.num_heads;
+  if (units >= 2L * sms) return best;
+  long maxc = 0, sumc = 0;
+  for (int n = 0; n < p.num_seqs; ++n) {
+    const long c = (cu[n + 1] - cu[n] + kC - 1) / kC;
+    maxc = std::max(maxc, c);
+    sumc += c;
+  }
+  const double unsplit = std::max<double>(maxc, std::ceil((double)sumc * p.num_heads / sms));
+  double best_cost = 0.85 * unsplit;
+  for (int target = 2; target <= 64; ++target) {
+    const long segc = (maxc + target - 1) / target;  // chunks per segment
+    if (segc < 4) break;
+    long e = 0, u1 = 0, u3 = 0, steps = 0;
+    std::vector<int> ns(p.num_seqs);
+    for (int n = 0; n < p.num_seqs; ++n) {
+      const long c = (cu[n + 1] - cu[n] + kC - 1) / kC;
+      const int k = (int)std::max<long>(1, (c + segc - 1) / segc);
+      ns[n] = k;
+      e += k;
+      u3 += k;
+      if (k >= 2) u1 += 1 + 2 * (k - 2);
+      steps = std::max<long>(steps, k - 2);
+    }
+    if (e > kMaxEntries || u1 > kMaxEntries) continue;
+    u1 *= p.num_heads;
+    u3 *= p.num_heads;
+    const double cost = std::ceil((double)u1 / sms) * segc + std::ceil((double)u3 / sms) * segc +
+                        (double)steps;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best.use = true;
+      best.seg_len = (int)(segc * kC);
+      best.E = (int)e;
+      best.nseg = ns;
+    }
+  }
+  if (best.use) {
+    best.base.resize(p.num_seqs);
+    int b = 0;
+    for (int n = 0; n < p.num_seqs; ++n) {
+      best.base[n] = b;
+      b += best.nseg[n];
+    }
+    best.bytes = 3 * (size_t)best.E * p.num_heads * kD * kD * sizeof(float);
+  }
+  return best;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
 }  // namespace tcp
 
 bool chunk_tc_supported(const Problem& p, const Args& a) {
@@ -822,21 +1025,29 @@ bool chunk_tc_supported(const Problem& p, const Args& a) {
          (!a.initial_state || al(a.initial_state)) && (!a.final_state || al(a.final_state));
 }
 
-cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host,
-                            cudaStream_t st) {
+size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host) {
+  if (!p.io_bf16 || p.dk != 128 || p.dv != 128) return 0;
+  const int sms = tcp::sm_count();
+  if (sms <= 0) return 0;
+  const tcp::SplitPlan plan = tcp::plan_split(p, cu_host, sms);
+  return plan.use ? (plan.bytes + 255) / 256 * 256 : 0;
+}
+
+cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,
+                            size_t ws_bytes, cudaStream_t st) {
   using namespace tcp;
   if (p.num_seqs == 0) return cudaSuccess;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(state_scan_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(2 * kD * kScanLd * sizeof(float)));
   });
   if (attr_err != cudaSuccess) return attr_err;
 
@@ -858,24 +1069,100 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.cu = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.final_state = a.final_state;
+  prm.ws = nullptr;
   prm.err = a.err;
   prm.H = p.num_heads;
   prm.total = p.total_tokens;
   prm.num_seqs = p.num_seqs;
-  prm.num_units = p.num_seqs * p.num_heads;
   prm.spin_cycles = 4000000000LL;  // ~2 s at 2 GHz
   prm.use_order = 0;
-  if (cu_host && p.num_seqs <= kMaxOrder) {
-    std::vector<int> idx(p.num_seqs);
-    std::iota(idx.begin(), idx.end(), 0);
-    std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
-      return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
-    });
-    for (int i = 0; i < p.num_seqs; ++i) prm.order[i] = idx[i];
-    prm.use_order = 1;
+  prm.mode = 0;
+
+  SplitPlan plan;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0) {
+    plan = plan_split(p, cu_host, sms);
+    if (plan.use && ws_bytes < plan.bytes) plan.use = false;
   }
-  const int grid = std::min(prm.num_units, sms);
-  chunk_tc_kernel<<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+  if (!plan.use) {
+    prm.num_units = p.num_seqs * p.num_heads;
+    if (cu_host && p.num_seqs <= kMaxOrder) {
+      std::vector<int> idx(p.num_seqs);
+      std::iota(idx.begin(), idx.end(), 0);
+      std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
+        return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
+      });
+      for (int i = 0; i < p.num_seqs; ++i) prm.list[i] = idx[i];
+      prm.use_order = 1;
+    }
+    chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    return cudaGetLastError();
+  }
+
+  // ---- split: pass 1 (inner segments' S~ and M, segment 0 from the true state) ----
+  const int E = plan.E;
+  prm.ws = static_cast<float*>(ws);
+  prm.mode = 1;
+  auto seg = [&](int n, int q, int& tb, int& te) {
+    tb = cu_host[n] + q * plan.seg_len;
+    te = std::min(cu_host[n + 1], tb + plan.seg_len);
+  };
+  int ne = 0;
+  auto put = [&](int n, int tb, int te, int in, int out, int flags) {
+    int* e = prm.list + kEnt * ne++;
+    e[0] = n; e[1] = tb; e[2] = te; e[3] = in; e[4] = out; e[5] = flags;
+  };
+  for (int n = 0; n < p.num_seqs; ++n) {
+    const int k = plan.nseg[n], b = plan.base[n];
+    int tb, te;
+    if (k >= 2) {
+      seg(n, 0, tb, te);
+      put(n, tb, te, kSlotUser, b + 1, 0);
+    }
+    for (int q = 1; q + 1 < k; ++q) {
+      seg(n, q, tb, te);
+      put(n, tb, te, kSlotZero, E + b + q, 0);
+      put(n, tb, te, kSlotIdentity, 2 * E + b + q, kFlagZeroV);
+    }
+  }
+  prm.out = nullptr;
+  if (ne > 0) {
+    prm.num_units = ne * p.num_heads;
+    chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // ---- scan ----
+  {
+    static thread_local ScanParams sp;
+    sp.initial_state = a.initial_state;
+    sp.ws = static_cast<float*>(ws);
+    sp.H = p.num_heads;
+    sp.E = E;
+    for (int n = 0; n < p.num_seqs; ++n) sp.s[n] = ScanSeq{n, plan.base[n], plan.nseg[n]};
+    state_scan_kernel<<<p.num_seqs * p.num_heads, kScanThreads,
+                        2 * kD * kScanLd * sizeof(float), st>>>(sp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // ---- pass 2: every segment from its entry state, longest first ----
+  std::vector<std::array<int, 4>> segs;  // {len, n, q, k}
+  for (int n = 0; n < p.num_seqs; ++n)
+    for (int q = 0; q < plan.nseg[n]; ++q) {
+      int tb, te;
+      seg(n, q, tb, te);
+      segs.push_back({te - tb, n, q, plan.nseg[n]});
+    }
+  std::stable_sort(segs.begin(), segs.end(),
+                   [](const std::array<int, 4>& x, const std::array<int, 4>& y) { return x[0] > y[0]; });
+  ne = 0;
+  for (const auto& sgi : segs) {
+    int tb, te;
+    seg(sgi[1], sgi[2], tb, te);
+    put(sgi[1], tb, te, plan.base[sgi[1]] + sgi[2], sgi[2] + 1 == sgi[3] ? kSlotUser : kSlotNone, 0);
+  }
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.num_units = ne * p.num_heads;
+  chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
   return cudaGetLastError();
 }
 

@@ -49,9 +49,12 @@ cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t strea
 cudaError_t launch_chunk_simt(const Problem& p, const Args& a, cudaStream_t stream);
 
 // Chunked prefill on the tensor cores (bf16 io, dk = dv = 128, 16-byte
-// aligned buffers).  cu_host (optional) orders the work longest-first.
+// aligned buffers).  cu_host (optional) orders the work longest-first and,
+// with enough workspace (256-byte aligned), lets long sequences be split
+// across SMs.
 bool chunk_tc_supported(const Problem& p, const Args& a);
-cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host,
-                            cudaStream_t stream);
+size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host);
+cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace kda

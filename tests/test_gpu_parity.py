@@ -234,3 +234,51 @@ def test_full_decode_workload_sampled():
                                      s0[(n, h)][None, None])
         assert_close(torch.stack(outs[(n, h)]), ro[:, 0], torch.bfloat16, f"decode out {n},{h}")
         assert_close(d.state[n, h], rf[0, 0], torch.bfloat16, f"decode state {n},{h}")
+
+
+# ------------------------------------------- long sequences split across SMs --
+
+def _ws_bytes(p):
+    return kda.chunk_fwd_workspace_size(p.num_seqs, p.total_tokens, p.meta["num_heads"],
+                                        p.meta["dk"], p.meta["dv"], p.q.dtype, p.cu_seqlens_host)
+
+
+@pytest.mark.parametrize("lens,H,init", [([3000], 4, None), ([5000, 1200, 64, 0, 700], 2, 0.1)])
+def test_split_matches_unsplit_and_oracle(lens, H, init):
+    """With workspace, few long sequences are cut into segments (transition M
+    and zero-start state per segment, a prefix scan, then a second pass); the
+    result must match the unsplit kernel and the oracle."""
+    p = workloads.random_problem(lens, H, 128, 128, torch.bfloat16, init_std=init, seed=21,
+                                 device=DEV)
+    assert _ws_bytes(p) > 0  # a split is planned for this shape
+    o1, f1 = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                           cu_seqlens_host=p.cu_seqlens_host)
+    o2, f2 = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                           cu_seqlens_host=p.cu_seqlens_host, workspace="auto")
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    assert_close(o2, o1, torch.bfloat16, "split vs unsplit out", both_stored=True)
+    assert_close(f2, f1, torch.bfloat16, "split vs unsplit final")
+    _check_all(p, o2, f2, torch.bfloat16)
+
+
+def test_split_final_state_may_alias_initial_state():
+    p = workloads.random_problem([4000, 900], 3, 128, 128, torch.bfloat16, init_std=0.1, seed=22,
+                                 device=DEV)
+    s0 = p.initial_state.clone()
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, s0)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             final_state=p.initial_state, cu_seqlens_host=p.cu_seqlens_host,
+                             workspace="auto")
+    torch.cuda.synchronize()
+    assert_close(out, ro, torch.bfloat16, "out")
+    assert_close(fin, rf, torch.bfloat16, "final_state")
+
+
+@pytest.mark.parametrize("name", ["long", "long_slow"])
+def test_full_long_workload_split_sampled(name):
+    """The long-context workload (one 65536-token sequence, 32 heads) through
+    the split path."""
+    p = workloads.prefill_workload(name, device=DEV)
+    assert _ws_bytes(p) > 0
+    _sampled_prefill(name, lambda p: [(0, 0), (0, 19)], workspace="auto")
