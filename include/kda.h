@@ -161,6 +161,39 @@ kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* 
                              const void* v, const float* z, const float* beta,
                              float* state, void* out, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
+ * device memory.  The pages describe no counterpart of this entry point.
+ *
+ * kda_chunk_fwd splits a few long sequences across SMs only when the caller
+ * passes scratch in desc->workspace.  Callers whose device memory is owned
+ * by a host framework that reserved all of HBM up front, plugins that are
+ * not allowed to allocate, and latency-critical loops that cannot afford
+ * cudaMalloc's implicit synchronisation may have no way to provide it.
+ * This variant takes the same arguments (inputs and outputs still come from
+ * the caller; desc->workspace is ignored) and uses instead a scratch array
+ * of KDA_NOALLOC_SCRATCH_BYTES that is part of the library: every GPU that
+ * loads libkda holds it until the process exits.  It calls no cudaMalloc,
+ * no cudaFree and no allocating library routine.
+ *
+ *   - The first call on a device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress, with the device current); make that
+ *     first call before any stream capture on the device.
+ *   - A split that would need more scratch than KDA_NOALLOC_SCRATCH_BYTES
+ *     (see kda_chunk_fwd_workspace_size) is rejected with
+ *     KDA_ERR_INVALID_ARGUMENT and nothing is enqueued.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     every byte a call reads is written earlier in that same call, so
+ *     nothing needs clearing.  Calls whose work overlaps on the GPU (for
+ *     example on two streams) race on the array: serialise them.
+ * Results are those of kda_chunk_fwd with a sufficient workspace.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+kda_status_t kda_chunk_fwd_noalloc(const kda_desc_t* desc, const void* q, const void* k,
+                                   const void* v, const float* z, const float* beta,
+                                   const float* initial_state, const int32_t* cu_seqlens,
+                                   void* out, float* final_state, kda_stream_t stream);
+
 /* Static, human-readable name of a status. */
 const char* kda_status_string(kda_status_t status);
 

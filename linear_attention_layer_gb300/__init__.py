@@ -18,7 +18,8 @@ import threading
 
 import torch
 
-__all__ = ["chunk_fwd", "recurrent_fwd", "decode_step", "chunk_fwd_workspace_size",
+__all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
+           "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
 
@@ -31,7 +32,12 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
 
 #: Every function include/kda.h declares.
 EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
-                    "kda_decode_step", "kda_status_string", "kda_get_device_error")
+                    "kda_decode_step", "kda_status_string", "kda_get_device_error",
+                    "kda_chunk_fwd_noalloc")
+
+#: Size of the library's own scratch array used by chunk_fwd_noalloc
+#: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class KDAError(RuntimeError):
@@ -63,7 +69,7 @@ def load() -> ctypes.CDLL:
                 "`python -c 'import __graft_entry__ as g; g.build()'`")
         lib = ctypes.CDLL(LIB_PATH)
         vp, dp = ctypes.c_void_p, ctypes.POINTER(KdaDesc)
-        for name in ("kda_chunk_fwd", "kda_recurrent_fwd"):
+        for name in ("kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_noalloc"):
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -191,6 +197,18 @@ def recurrent_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
                   final_state=None, output_final_state=True, cu_seqlens_host=None, stream=None):
     """Token-by-token KDA prefill (``kda_recurrent_fwd``).  Returns (out, final_state)."""
     return _prefill("kda_recurrent_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
+                    final_state, output_final_state, cu_seqlens_host, None, stream)
+
+
+def chunk_fwd_noalloc(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
+                      final_state=None, output_final_state=True, cu_seqlens_host=None,
+                      stream=None):
+    """``kda_chunk_fwd_noalloc``: the chunked prefill for callers that cannot
+    allocate device memory; its scratch for splitting long sequences is an
+    array inside the library (NOALLOC_SCRATCH_BYTES).  Pass ``out`` and
+    ``final_state`` to keep this wrapper from allocating them with torch.
+    Returns (out, final_state)."""
+    return _prefill("kda_chunk_fwd_noalloc", q, k, v, z, beta, cu_seqlens, initial_state, out,
                     final_state, output_final_state, cu_seqlens_host, None, stream)
 
 

@@ -92,6 +92,19 @@ kda_status_t prefill_common(const kda_desc_t* desc, const void* q, const void* k
 
 }  // namespace
 
+namespace kda {
+// Host-side validation shared with kda_chunk_fwd_noalloc (kda_noalloc.cu).
+kda_status_t validate_prefill(const kda_desc_t* desc, const void* q, const void* k,
+                              const void* v, const float* z, const float* beta,
+                              const float* initial_state, const int32_t* cu_seqlens, void* out,
+                              float* final_state, Args& a, Problem& p) {
+  const kda_status_t s = prefill_common(desc, q, k, v, z, beta, initial_state, cu_seqlens, out,
+                                        final_state, a);
+  if (s == KDA_OK) p = to_problem(desc);
+  return s;
+}
+}  // namespace kda
+
 extern "C" {
 
 kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,

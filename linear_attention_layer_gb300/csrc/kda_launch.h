@@ -58,3 +58,13 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
                             size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace kda
+
+#include "../../include/kda.h"
+
+namespace kda {
+// Host validation of a prefill call (the checks of kda_chunk_fwd); fills a and p.
+kda_status_t validate_prefill(const kda_desc_t* desc, const void* q, const void* k,
+                              const void* v, const float* z, const float* beta,
+                              const float* initial_state, const int32_t* cu_seqlens, void* out,
+                              float* final_state, Args& a, Problem& p);
+}  // namespace kda
