@@ -194,6 +194,18 @@ kda_status_t kda_chunk_fwd_noalloc(const kda_desc_t* desc, const void* q, const 
                                    const float* initial_state, const int32_t* cu_seqlens,
                                    void* out, float* final_state, kda_stream_t stream);
 
+/*
+ * kda_testing_inject_wait_timeout -- testing aid for the failure path (the
+ * device-side waits are bounded; this makes one of them run out).  The next
+ * `launches` tensor-core prefill launches issued from the calling host thread
+ * arm their first input barrier with 16 bytes that no copy delivers and cut
+ * the wait budget to ~10 ms: the wait expires, the kernel records
+ * KDA_ERR_TIMEOUT in the device error word, cancels the phantom bytes, lets
+ * its real copies land, frees its Tensor Memory and returns.  Outputs of
+ * such a launch are undefined.  0 disarms.
+ */
+void kda_testing_inject_wait_timeout(int launches);
+
 /* Static, human-readable name of a status. */
 const char* kda_status_string(kda_status_t status);
 

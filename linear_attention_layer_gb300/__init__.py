@@ -33,7 +33,7 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
 #: Every function include/kda.h declares.
 EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
                     "kda_decode_step", "kda_status_string", "kda_get_device_error",
-                    "kda_chunk_fwd_noalloc")
+                    "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_testing_inject_wait_timeout.restype = None
+        lib.kda_testing_inject_wait_timeout.argtypes = [ctypes.c_int]
         lib.kda_get_device_error.restype = ctypes.c_int
         lib.kda_get_device_error.argtypes = [vp]
         _lib = lib
@@ -254,3 +256,9 @@ def get_device_error(stream=None) -> int:
     """Synchronise and read/clear the device error word (a kda_status_t)."""
     lib = load()
     return int(lib.kda_get_device_error(_stream_handle(stream)))
+
+
+def testing_inject_wait_timeout(launches: int = 1) -> None:
+    """Make the next `launches` tensor-core prefill launches of this thread hit
+    an expired device wait (``kda_testing_inject_wait_timeout``)."""
+    load().kda_testing_inject_wait_timeout(int(launches))

@@ -126,6 +126,7 @@ struct Params {
   int* err;
   int H, total, num_seqs, num_units, use_order, mode;
   long long spin_cycles;
+  int inject_timeout;   // testing: make the first input wait of each unit unsatisfiable
   int list[kMaxOrder];
 };
 
@@ -259,6 +260,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int row = tid & 127, cq = warp >> 2;
   uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0;
   bool pend_qkz = false, pend_v = false;  // TMA copies in flight (uniform)
+  bool pend_mma = false;                  // an MMA commit not yet observed
   bool aborted = false;
   float absmax = 0.f;  // largest |value| this thread converted to fp16
 
@@ -280,7 +282,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     const int nchunks = (eos - bos + kC - 1) / kC;
     if (tid == 0 && nchunks > 0) {
-      mbar_arrive_expect_tx(bar_qkz, 65536u);
+      // (testing) 16 expected bytes that no copy delivers: the wait below expires
+      mbar_arrive_expect_tx(bar_qkz, 65536u + (P.inject_timeout ? 16u : 0u));
       tma_load_3d(sm + OFF_Q, &tm_q, 0, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_K, &tm_k, 0, h, bos, bar_qkz);
@@ -332,8 +335,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int len = min(kC, eos - t0);
       // ---------------- A: inputs ----------------
       bool ok = wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
-      ph_qkz ^= 1;
-      pend_qkz = false;
+      if (ok) {
+        ph_qkz ^= 1;
+        pend_qkz = false;
+      }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
 
       // ---------------- B: token norms and beta ----------------
@@ -627,8 +632,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (!zero_v) {
         ok = wait_bar(bar_v, ph_v, P.spin_cycles);
-        ph_v ^= 1;
-        pend_v = false;
+        if (ok) {
+          ph_v ^= 1;
+          pend_v = false;
+        }
       }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       {  // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
@@ -664,8 +671,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(bar_mma);
       }
+      pend_mma = true;
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-      ph_mma ^= 1;
+      if (ok) {
+        ph_mma ^= 1;
+        pend_mma = false;
+      }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
       if (tid == 0 && ci + 1 < nchunks && !zero_v) {  // v stage consumed
@@ -696,8 +707,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                  make_sdesc(bw + kk * 2048, 8192, 1024, kSwizzle128), idn, true);
         mma_commit(bar_mma);
       }
+      pend_mma = true;
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-      ph_mma ^= 1;
+      if (ok) {
+        ph_mma ^= 1;
+        pend_mma = false;
+      }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
 
@@ -745,8 +760,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(bar_mma);
       }
+      pend_mma = true;
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-      ph_mma ^= 1;
+      if (ok) {
+        ph_mma ^= 1;
+        pend_mma = false;
+      }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
 
@@ -806,8 +825,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
       report_error(P.err, kErrTimeout);
       // let copies already in flight land before the shared memory goes away
-      if (pend_qkz) wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
+      if (pend_qkz) {
+        if (P.inject_timeout) mbar_complete_tx(bar_qkz, 16u);  // cancel the injected bytes
+        wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
+      }
       if (pend_v) wait_bar(bar_v, ph_v, P.spin_cycles);
+      if (pend_mma) wait_bar(bar_mma, ph_mma, P.spin_cycles);
     }
   }
   sync_tc();
@@ -955,6 +978,9 @@ struct SplitPlan {
 
 constexpr int kMaxEntries = kMaxOrder / kEnt;
 
+// launches (from this host thread) that still get an unsatisfiable input wait
+thread_local int g_inject_wait_timeout = 0;
+
 // Choose a segment length by a waves-of-SMs cost model; split only when it
 // beats the unsplit launch by a clear margin.
 SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms) {
@@ -1075,6 +1101,12 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.total = p.total_tokens;
   prm.num_seqs = p.num_seqs;
   prm.spin_cycles = 4000000000LL;  // ~2 s at 2 GHz
+  prm.inject_timeout = 0;
+  if (g_inject_wait_timeout > 0) {  // testing aid, see kda_testing_inject_wait_timeout
+    --g_inject_wait_timeout;
+    prm.inject_timeout = 1;
+    prm.spin_cycles = 20000000LL;  // ~10 ms
+  }
   prm.use_order = 0;
   prm.mode = 0;
 
@@ -1167,3 +1199,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
 }
 
 }  // namespace kda
+
+extern "C" void kda_testing_inject_wait_timeout(int launches) {
+  kda::tcp::g_inject_wait_timeout = launches > 0 ? launches : 0;
+}

@@ -282,3 +282,21 @@ def test_full_long_workload_split_sampled(name):
     p = workloads.prefill_workload(name, device=DEV)
     assert _ws_bytes(p) > 0
     _sampled_prefill(name, lambda p: [(0, 0), (0, 19)], workspace="auto")
+
+
+def test_expired_device_wait_reports_timeout_and_recovers():
+    """A bounded device wait that runs out (made unsatisfiable on purpose by the
+    testing hook) ends the kernel with KDA_ERR_TIMEOUT in the error word, no
+    trap; the next call on the same context is correct."""
+    p = workloads.random_problem([200, 70], 2, 128, 128, torch.bfloat16, init_std=0.1, seed=23,
+                                 device=DEV)
+    assert kda.get_device_error() == 0
+    kda.testing_inject_wait_timeout(1)
+    kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                  cu_seqlens_host=p.cu_seqlens_host)
+    assert kda.get_device_error() == 4  # KDA_ERR_TIMEOUT
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    _check_all(p, out, fin, torch.bfloat16)
