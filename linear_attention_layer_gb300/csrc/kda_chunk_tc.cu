@@ -79,10 +79,11 @@ constexpr uint32_t G_QT = OFF_G;              // Q~  fp32 [64 t][128 c] (xor-swi
 constexpr uint32_t G_KT = OFF_G + 32768;      // K~  fp32 [64 j][128 c] (xor-swizzled)
 constexpr uint32_t G_KPT = OFF_G + 65536;     // K~+ bf16 [64 t][128 c] (xor-swizzled)
 constexpr int kLS = 68;                       // row stride (floats) of A and T: conflict-free
-constexpr uint32_t G_AKK = OFF_G;             // A   fp32 [64][kLS]         (after the Gram)
-constexpr uint32_t G_T32 = OFF_G + 17408;     // T   fp32 [64][kLS]
-constexpr uint32_t G_P = OFF_G + 34816;       // P   fp16 [64 t][64 j] SW128: K-major B
-constexpr uint32_t G_TP = OFF_G + 43008;      // T'  fp16 [64 t][64 j] SW128: K-major B
+constexpr uint32_t G_P = OFF_G;               // P   fp16 [64 t][64 j] SW128: K-major B (over Q~)
+// in the q/k/z stage, free between operand prep and the next chunk's prefetch:
+constexpr uint32_t S_AKK = OFF_Q;             // A   fp32 [64][kLS]
+constexpr uint32_t S_T32 = OFF_Q + 17408;     // T   fp32 [64][kLS]
+constexpr uint32_t S_TP = OFF_Q + 35840;      // T'  fp16 [64 t][64 j] SW128: K-major B
 constexpr uint32_t G_WT = OFF_G + 51200;      // W^T fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_QPT = 163840;  // Q+^T  fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major A
@@ -178,6 +179,35 @@ __device__ __forceinline__ void warp_gemm16_3tf32(float (&acc)[2][4], const floa
   }
 }
 
+// One 16 x 8 output tile (columns 8*nt .. of a 16-wide block) of X * Y in
+// three-pass tf32, stored as s * result at M[r0 + row][c0 + 8*nt + col].
+// X(row, k) is produced by `xf` (so it may combine several stored blocks);
+// Y starts at (yr, yc) of a row-stride-kLS matrix.  One warp.
+template <typename XF>
+__device__ __forceinline__ void warp_tile_3tf32(XF xf, const float* Y, int yr, int yc, int K,
+                                                int nt, float* M, int r0, int c0, float s,
+                                                int g, int q) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(xf(g, k0 + q), ah[0], al[0]);
+    split_tf32(xf(g + 8, k0 + q), ah[1], al[1]);
+    split_tf32(xf(g, k0 + q + 4), ah[2], al[2]);
+    split_tf32(xf(g + 8, k0 + q + 4), ah[3], al[3]);
+    uint32_t bh0, bl0, bh1, bl1;
+    split_tf32(Y[(yr + k0 + q) * kLS + yc + 8 * nt + g], bh0, bl0);
+    split_tf32(Y[(yr + k0 + q + 4) * kLS + yc + 8 * nt + g], bh1, bl1);
+    mma_1688_tf32(acc, ah, bh0, bh1);
+    mma_1688_tf32(acc, ah, bl0, bl1);
+    mma_1688_tf32(acc, al, bh0, bh1);
+  }
+  float* m = M + (r0 + g) * kLS + c0 + 8 * nt + 2 * q;
+  m[0] = s * acc[0];
+  m[1] = s * acc[1];
+  m[8 * kLS] = s * acc[2];
+  m[8 * kLS + 1] = s * acc[3];
+}
+
 // M[r0 + row][c0 + col] = s * acc (accumulator layout of warp_gemm16_3tf32)
 __device__ __forceinline__ void warp_store16(float* M, int r0, int c0, const float (&acc)[2][4],
                                              float s, int g, int q) {
@@ -202,6 +232,11 @@ __device__ __forceinline__ void st_row16_f16(unsigned char* tile, int row, int c
   const uint32_t c0 = (uint32_t)(col >> 3);
   *reinterpret_cast<uint4*>(tile + row * 128 + (((c0) ^ (row & 7)) << 4)) = a;
   *reinterpret_cast<uint4*>(tile + row * 128 + (((c0 + 1) ^ (row & 7)) << 4)) = b;
+}
+
+// Barrier of one 256-thread warp group (ids 1, 2; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -470,16 +505,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       fence_proxy_async_smem();
       sync_tc();
       if (tid == 0) {
-        // q/k/z stage consumed: prefetch the next chunk
-        if (ci + 1 < nchunks) {
-          const int tn = t0 + kC;
-          mbar_arrive_expect_tx(bar_qkz, 65536u);
-          tma_load_3d(sm + OFF_Q, &tm_q, 0, h, tn, bar_qkz);
-          tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, tn, bar_qkz);
-          tma_load_3d(sm + OFF_K, &tm_k, 0, h, tn, bar_qkz);
-          tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, tn, bar_qkz);
-          tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
-        }
         // O^T = S^T Q+^T  (M=128 value channels, N=64 tokens, K=128 key channels)
         const uint32_t id_o = make_idesc_f16(128, kC, false, true);
         const uint32_t bq = smem_u32(sm + OFF_QPT);
@@ -488,45 +513,57 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mma_ts(tmem + TO, tmem + TS16 + kk * 8,
                  make_sdesc(bq + kk * 2048, 8192, 1024, kSwizzle128), id_o, kk > 0);
       }
-      pend_qkz = (ci + 1 < nchunks);
 
       // ---------------- E: Gram blocks, tf32 mma.sync ----------------
-      // warps 0-7 build P, warps 8-15 build A; warp w&7 takes blocks w&7 and (w&7)+8
+      // Two warp groups from here to the first MMA: warps 0-7 build P and
+      // convert v; warps 8-15 build A and invert I + A.  Neither group touches
+      // the other's buffers.  Warp w&7 takes blocks w&7 and (w&7)+8.
+      const int grp = warp >> 3;
       float acc[2][2][4];
       {
-        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 3;
+        const int g = lane >> 2, q4 = lane & 3, prod = grp;
         const unsigned char* Kpt = sm + G_KPT;
+        const int nb = (warp & 7) + 8 < 10 ? 2 : 1;  // blocks of this warp
+        int ta[2], jb[2];
+        bool scaled[2];
+        const float* dab[2];
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
+          const int blk = min((warp & 7) + 8 * bi, 9);
+          const int a = c_blk_a[blk], b = c_blk_b[blk];
+          ta[bi] = 16 * a + g;
+          jb[bi] = 16 * b + g;
+          scaled[bi] = a != b;
+          dab[bi] = misc + M_DAB + (a > b ? dab_index(a, b) : 0) * kD;
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[bi][n][i] = 0.f;
-          const int blk = (warp & 7) + 8 * bi;
-          if (blk >= 10) continue;
-          const int a = c_blk_a[blk], b = c_blk_b[blk];
-          const float* dab = misc + M_DAB + (a > b ? dab_index(a, b) : 0) * kD;
-          const int ta = 16 * a + g, jb = 16 * b + g;
+        }
 #pragma unroll 2
-          for (int c0 = 0; c0 < kD; c0 += 16) {
-            // 16 channels as two k-steps of 8; thread q covers channels
-            // c0+4q .. c0+4q+3 (logical k = q / q+4 -> channel c0+4q / +1 in
-            // the first step, +2 / +3 in the second; A and B agree).
-            const int cc = c0 + 4 * q4;
-            const float4 s4 = (a != b) ? *reinterpret_cast<const float4*>(dab + cc)
-                                       : make_float4(1.f, 1.f, 1.f, 1.f);
+        for (int c0 = 0; c0 < kD; c0 += 16) {
+          // 16 channels as two k-steps of 8; thread q covers channels
+          // c0+4q .. c0+4q+3 (logical k = q / q+4 -> channel c0+4q / +1 in
+          // the first step, +2 / +3 in the second; A and B agree).  The two
+          // blocks of a warp are interleaved for independent MMA chains.
+          const int cc = c0 + 4 * q4;
+#pragma unroll
+          for (int bi = 0; bi < 2; ++bi) {
+            if (bi == 1 && nb < 2) continue;
+            const float4 s4 = scaled[bi] ? *reinterpret_cast<const float4*>(dab[bi] + cc)
+                                         : make_float4(1.f, 1.f, 1.f, 1.f);
             float4 x0, x1;
             if (prod == 0) {
-              x0 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta, cc));
-              x1 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta + 8, cc));
+              x0 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta[bi], cc));
+              x1 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta[bi] + 8, cc));
             } else {
-              const uint2 y0 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta, cc));
-              const uint2 y1 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta + 8, cc));
+              const uint2 y0 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta[bi], cc));
+              const uint2 y1 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta[bi] + 8, cc));
               x0 = make_float4(bf16_lo(y0.x), bf16_hi(y0.x), bf16_lo(y0.y), bf16_hi(y0.y));
               x1 = make_float4(bf16_lo(y1.x), bf16_hi(y1.x), bf16_lo(y1.y), bf16_hi(y1.y));
             }
-            const float4 kb0 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb, cc));
-            const float4 kb1 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb + 8, cc));
+            const float4 kb0 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb[bi], cc));
+            const float4 kb1 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb[bi] + 8, cc));
             uint32_t fa[4];
             fa[0] = to_tf32(x0.x * s4.x); fa[1] = to_tf32(x1.x * s4.x);
             fa[2] = to_tf32(x0.y * s4.y); fa[3] = to_tf32(x1.y * s4.y);
@@ -539,10 +576,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
-      __syncthreads();  // Gram operands no longer read
-      {
-        const int g = lane >> 2, q4 = lane & 3, prod = warp >> 3;
-        float* Akk = reinterpret_cast<float*>(sm + G_AKK);
+      if (grp == 0) {
+        // ---- P group: P (over Q~, so after every P warp is done with it), v ----
+        const int g = lane >> 2, q4 = lane & 3;
+        group_sync(2);
         unsigned char* Pm = sm + G_P;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
@@ -554,18 +591,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
               const int t = 16 * a + g + 8 * hr, j = 16 * b + 8 * n + 2 * q4;
-              if (prod == 0) {
-                const float p0 = j <= t ? acc[bi][n][2 * hr] : 0.f;
-                const float p1 = j + 1 <= t ? acc[bi][n][2 * hr + 1] : 0.f;
-                *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = pack_f16(p0, p1);
-              } else {
-                const float bt = misc[M_BETA + t];
-                Akk[t * kLS + j] = j < t ? bt * acc[bi][n][2 * hr] : 0.f;
-                Akk[t * kLS + j + 1] = j + 1 < t ? bt * acc[bi][n][2 * hr + 1] : 0.f;
-              }
+              const float p0 = j <= t ? acc[bi][n][2 * hr] : 0.f;
+              const float p1 = j + 1 <= t ? acc[bi][n][2 * hr + 1] : 0.f;
+              *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = pack_f16(p0, p1);
             }
         }
-        if (prod == 0 && (warp & 7) < 6) {
+        if ((warp & 7) < 6) {
           const int zb = warp & 7;
           const int a = c_zero_a[zb], b = c_zero_b[zb];
 #pragma unroll
@@ -574,75 +605,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
           }
         }
-      }
-      __syncthreads();
-
-      // ---------------- F: T = (I + A)^{-1}, T' = T diag(beta); V -> fp16 ----------------
-      {
-        const float* Akk = reinterpret_cast<const float*>(sm + G_AKK);
-        float* T = reinterpret_cast<float*>(sm + G_T32);
-        if (warp < 4 && lane < 16) {  // diagonal block `warp`, column `lane`, forward substitution
-          const int base = 16 * warp, cc = lane;
-          float x[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float s = (i == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < i; ++j) s -= Akk[(base + i) * kLS + base + j] * x[j];
-            x[i] = s;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
-        }
-        __syncthreads();
-        // off-diagonal blocks by block forward substitution, one level (a - b = d)
-        // at a time, one block per warp:
-        //   Y = sum_{k=b}^{a-1} A_ak T_kb  (kept in the unused block (b, a)),
-        //   T_ab = -T_aa Y
-        {
-          const int g = lane >> 2, q4 = lane & 3;
-#pragma unroll 1
-          for (int d = 1; d < 4; ++d) {
-            if (warp < 4 - d) {
-              const int b = warp, a = b + d;
-              float acc1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-              warp_gemm16_3tf32(acc1, Akk, 16 * a, 16 * b, T, 16 * b, 16 * b, 16 * d, g, q4);
-              warp_store16(T, 16 * b, 16 * a, acc1, 1.f, g, q4);
-              __syncwarp();
-              float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-              warp_gemm16_3tf32(acc2, T, 16 * a, 16 * a, T, 16 * b, 16 * a, 16, g, q4);
-              warp_store16(T, 16 * a, 16 * b, acc2, -1.f, g, q4);
-            }
-            __syncthreads();
+        if (!zero_v) {
+          ok = wait_bar(bar_v, ph_v, P.spin_cycles);
+          if (ok) {
+            ph_v ^= 1;
+            pend_v = false;
           }
         }
-        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal
-        {
-          const int t = tid >> 3, j0 = (tid & 7) * 8;
-          float v[8];
+        // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
+        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 4;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int j = j0 + i;
-            v[i] = ((j >> 4) <= (t >> 4)) ? T[t * kLS + j] * misc[M_BETA + j] : 0.f;
-          }
-          *reinterpret_cast<uint4*>(sm + G_TP + t * 128 + ((((uint32_t)j0 >> 3) ^ (t & 7)) << 4)) =
-              make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
-                         pack_f16(v[6], v[7]));
-        }
-      }
-      if (!zero_v) {
-        ok = wait_bar(bar_v, ph_v, P.spin_cycles);
-        if (ok) {
-          ph_v ^= 1;
-          pend_v = false;
-        }
-      }
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-      {  // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
-        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint4 x = zero_v ? make_uint4(0u, 0u, 0u, 0u) : vv[i];
+        for (int i = 0; i < 4; ++i) {
+          uint4 x = zero_v || !ok ? make_uint4(0u, 0u, 0u, 0u) : vv[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -652,14 +626,123 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           vv[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+      } else {
+        // ---- A group: A, T = (I + A)^{-1}, T' = T diag(beta) ----
+        const int g = lane >> 2, q4 = lane & 3, wg = warp & 7;
+        float* Akk = reinterpret_cast<float*>(sm + S_AKK);
+        float* T = reinterpret_cast<float*>(sm + S_T32);
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi) {
+          const int blk = wg + 8 * bi;
+          if (blk >= 10) continue;
+          const int a = c_blk_a[blk], b = c_blk_b[blk];
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int t = 16 * a + g + 8 * hr, j = 16 * b + 8 * n + 2 * q4;
+              const float bt = misc[M_BETA + t];
+              Akk[t * kLS + j] = j < t ? bt * acc[bi][n][2 * hr] : 0.f;
+              Akk[t * kLS + j + 1] = j + 1 < t ? bt * acc[bi][n][2 * hr + 1] : 0.f;
+            }
+        }
+        group_sync(1);
+        if (wg < 4 && lane < 16) {  // diagonal block wg, column `lane`, forward substitution
+          const int base = 16 * wg, cc = lane;
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float sacc = (i == cc) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < i; ++j) sacc -= Akk[(base + i) * kLS + base + j] * x[j];
+            x[i] = sacc;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
+        }
+        group_sync(1);
+        // Off-diagonal blocks.  With D = blockdiag(I + A_aa) (inverses T_aa above)
+        // and L the blocks below it, I + A = D (I + N), N = D^{-1} L, N^4 = 0, so
+        //   T = (I - N + N^2 - N^3) D^{-1},   T_ab = X_ab T_bb.
+        // Four levels of 16x16 products in 16x8 tiles.  N lives in T's lower
+        // blocks, N^2 / N^3 in T's unused upper blocks, and the final
+        // off-diagonal T_ab overwrite A's lower blocks.
+        {
+          float* Afin = Akk;
+          auto blk = [&](const float* M, int r0, int c0) {
+            return [M, r0, c0](int r, int k) { return M[(r0 + r) * kLS + c0 + k]; };
+          };
+          // level A: N_ab = T_aa A_ab for the six blocks a > b
+          for (int task = wg; task < 12; task += 8) {
+            const int bi = task >> 1, nt = task & 1;
+            const int a = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+            const int b = bi < 3 ? bi : (bi < 5 ? bi - 3 : 0);
+            warp_tile_3tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
+                            1.f, g, q4);
+          }
+          group_sync(1);
+          // level B: N^2_20, N^2_31, N^2_30 (upper blocks 02, 13, 03) and T_10, T_21, T_32
+          for (int task = wg; task < 12; task += 8) {
+            const int nt = task & 1;
+            switch (task >> 1) {
+              case 0: warp_tile_3tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
+              case 1: warp_tile_3tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
+              case 2: warp_tile_3tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
+              case 3: warp_tile_3tf32(blk(T, 16, 0), T, 0, 0, 16, nt, Afin, 16, 0, -1.f, g, q4); break;
+              case 4: warp_tile_3tf32(blk(T, 32, 16), T, 16, 16, 16, nt, Afin, 32, 16, -1.f, g, q4); break;
+              default: warp_tile_3tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
+            }
+          }
+          group_sync(1);
+          // level C: N^3_30 = N_32 N^2_20 (upper block 23); T_20 = (N^2_20 - N_20) T_00;
+          // T_31 = (N^2_31 - N_31) T_11
+          if (wg < 6) {
+            const int task = wg >> 1, nt = wg & 1;
+            if (task == 0) {
+              warp_tile_3tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
+            } else if (task == 1) {
+              auto xf = [T](int r, int k) { return T[r * kLS + 32 + k] - T[(32 + r) * kLS + k]; };
+              warp_tile_3tf32(xf, T, 0, 0, 16, nt, Afin, 32, 0, 1.f, g, q4);
+            } else {
+              auto xf = [T](int r, int k) {
+                return T[(16 + r) * kLS + 48 + k] - T[(48 + r) * kLS + 16 + k];
+              };
+              warp_tile_3tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
+            }
+          }
+          group_sync(1);
+          // level D: T_30 = (N^2_30 - N_30 - N^3_30) T_00
+          if (wg < 2) {
+            auto xf = [T](int r, int k) {
+              return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
+            };
+            warp_tile_3tf32(xf, T, 0, 0, 16, wg, Afin, 48, 0, 1.f, g, q4);
+          }
+          group_sync(1);
+        }
+        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal
+        {
+          const int gt = tid & 255, t = gt >> 2, j0 = (gt & 3) * 16;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = j0 + i;
+            const int bt = t >> 4, bj = j >> 4;
+            const float tv = bj == bt ? T[t * kLS + j] : (bj < bt ? Akk[t * kLS + j] : 0.f);
+            v[i] = tv * misc[M_BETA + j];
+          }
+          st_row16_f16(sm + S_TP, t, j0, v);
+        }
       }
       fence_proxy_async_smem();
-      sync_tc();
+      tc_fence_before();
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
+      tc_fence_after();
 
       // ---------------- G: W^T = K+^T T'^T,  U~^T = V^T T'^T ----------------
       if (tid == 0) {
         const uint32_t ak = smem_u32(sm + OFF_KPT), av = smem_u32(sm + OFF_V),
-                       bt = smem_u32(sm + G_TP);
+                       bt = smem_u32(sm + S_TP);
         const uint32_t id_w = make_idesc_f16(128, kC, false, false);
         const uint32_t id_u = make_idesc_f16(128, kC, true, false);
 #pragma unroll
@@ -679,12 +762,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
-      if (tid == 0 && ci + 1 < nchunks && !zero_v) {  // v stage consumed
+      if (tid == 0 && ci + 1 < nchunks) {  // stages consumed: prefetch the next chunk
         const int tn = t0 + kC;
-        mbar_arrive_expect_tx(bar_v, 16384u);
-        tma_load_3d(sm + OFF_V, &tm_v, 0, h, tn, bar_v);
-        tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, tn, bar_v);
+        mbar_arrive_expect_tx(bar_qkz, 65536u);
+        tma_load_3d(sm + OFF_Q, &tm_q, 0, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_K, &tm_k, 0, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
+        if (!zero_v) {
+          mbar_arrive_expect_tx(bar_v, 16384u);
+          tma_load_3d(sm + OFF_V, &tm_v, 0, h, tn, bar_v);
+          tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, tn, bar_v);
+        }
       }
+      pend_qkz = ci + 1 < nchunks;
       pend_v = (ci + 1 < nchunks) && !zero_v;
 
       // ---------------- H: W^T -> fp16 (MN-major B, row c) ----------------
