@@ -13,38 +13,43 @@
 //   O = Q+ S + P U,  S <- Diag(e^{G_C}) S + Khat^T U
 //
 // with Q+ = q^ e^{G}, K+ = k^ e^{G}, Khat = k^ e^{G_C - G}.  The factors
-// e^{G_t - G_j} span e^{+-320} across a 64-token chunk, beyond fp32/bf16, so
-// the pairwise (Gram) products use one reference per 16-token subtile: with
-// r_a the cumulative log-decay before subtile a, Q~ = q^ e^{G - r_a} <= 1,
-// K~ = k^ e^{r_a - G} <= e^80 and D_ab = e^{r_a - r_b}, a block (a, b) of P
-// is (Q~_a D_ab) K~_b^T.  The e^80 bound is what the lower-bounded gate buys
-// (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构", section "下界衰减":
-// log alpha >= -5, so a 16-token tile decays by less than e^-80 and its
-// reciprocal stays finite), and it lets the diagonal blocks go through the
-// tensor cores like the others.
+// e^{G_t - G_j} span e^{+-320} across a 64-token chunk, beyond fp32, so the
+// pairwise (Gram) products use one reference per 16-token query subtile:
+// with r_a the cumulative log-decay before subtile a,
+//   Q~_t = q^_t e^{G_t - r_a} <= 1,  K~q_t = k^_t e^{G_t - r_a} <= 1   (t in a)
+//   K^(a)_j = k^_j e^{r_a - G_j}: <= e^80 for j in a, <= 1 for earlier j,
+// so P[t, j] = Q~_t . K^(a)_j and A[t, j] = b_t K~q_t . K^(a)_j for every
+// j <= t, and no product ever leaves the fp32 range.  The e^80 bound is what
+// the lower-bounded gate buys (blog.higcp.com "猜想：K3 可能是最适合 TPU 的
+// MoE 架构", section "下界衰减": log alpha >= -5, so a 16-token tile decays by
+// less than e^-80 and its reciprocal stays finite).  K^(a) is formed from
+// K^(a-1) by the per-channel factor e^{r_a - r_{a-1}} (>= e^-80), so only
+// values that are negligible in fact underflow.
 //
-// Everything else is kept in the transposed orientation so that every
-// tcgen05 GEMM has M = 128 and the state and U can feed the tensor core
+// Everything else is kept in the transposed orientation so that the dense
+// tcgen05 GEMMs have M = 128 and the state and U can feed the tensor core
 // straight from Tensor Memory:
 //   W^T = K+^T T'^T,  U~^T = V^T T'^T,  U^T = U~^T - S^T W^T,
 //   O^T = S^T Q+^T + U^T P^T,  S^T <- S^T Diag(e^{G_C}) + U^T Khat.
 // S^T (fp32, 128 lanes = value channel) stays resident in TMEM across
 // chunks; its fp16 copy and U^T's are A operands read from TMEM.
 //
-// Precision: the Gram products run as tf32 warp MMAs on fp32 operands (the
-// e^80 range rules out fp16 there); the dense products use fp16 operands
-// (11-bit significand; all of them are bounded by 1 or by the data) with
-// fp32 accumulation.  bf16 operands there would leave ~0.2% relative error
-// on the largest outputs.
+// Precision: the Gram products run as tcgen05 kind::tf32 on operands rounded
+// to tf32 once (the e^80 range rules out fp16 there); the dense products
+// use fp16 operands (11-bit significand; all of them are bounded by 1 or by
+// the data) with fp32 accumulation.  bf16 operands there would leave ~0.2%
+// relative error on the largest outputs.  The inverse runs in three-pass
+// tf32 warp MMAs (close to fp32).
 //
-// One CTA (4 warps) per SM walks (sequence, head) work units, longest
+// One CTA (16 warps) per SM walks (sequence, head) work units, longest
 // sequence first.  Per chunk:
 //   TMA   q, k, v (bf16, 128B swizzle) and z (fp32) tiles into shared memory;
 //   CUDA  gate g = -5 sigmoid(z), per-channel cumulative sums, L2 norms, and
 //         the decayed operands written in tensor-core layouts;
-//   mma.sync (tf32)  the ten 16x16 Gram blocks of P and A;
-//   CUDA  T = (I + A)^{-1} by block forward substitution (fp32);
-//   tcgen05   the five dense products above, accumulators in TMEM.
+//   tcgen05 (tf32)  the Gram products: four M = 64 (keys) x N = 32 blocks,
+//         one per query subtile, giving P^T and A^T in TMEM;
+//   CUDA  T = (I + A)^{-1}: 16x16 diagonal inverses, then a four-level series;
+//   tcgen05 (f16)   the five dense products above, accumulators in TMEM.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -74,34 +79,43 @@ constexpr uint32_t OFF_Q = 0;         // q stage: [2 c-blk][64 t][64 c] bf16, SW
 constexpr uint32_t OFF_K = 16384;     // k stage, same
 constexpr uint32_t OFF_Z = 32768;     // z stage: [64 t][128 c] fp32 (TMA); then G in place
 constexpr uint32_t OFF_V = 65536;     // v stage: [2 n-blk][64 j][64 n] SW128; fp16 in place = MN-major A
-constexpr uint32_t OFF_G = 81920;     // 80K: Gram operands, later A / T / P / T' / W^T
-constexpr uint32_t G_QT = OFF_G;              // Q~  fp32 [64 t][128 c] (xor-swizzled)
-constexpr uint32_t G_KT = OFF_G + 32768;      // K~  fp32 [64 j][128 c] (xor-swizzled)
-constexpr uint32_t G_KPT = OFF_G + 65536;     // K~+ bf16 [64 t][128 c] (xor-swizzled)
+constexpr uint32_t OFF_G = 81920;     // 80K: Gram A operand, later A / T / T' / P / W^T
+// Gram operands (tf32, K-major, 128-byte swizzle; one region per 32-channel atom):
+//   G_M (A operand, M = 128) over the q / k / z stages: [4 atoms][128 rows][32 c],
+//       row t = Q~_t, row 64 + t = K~q_t;
+//   G_N (B operand, N = 160) in the Gram region: [4 atoms][160 rows][32 c], K^(a)
+//       (keys of subtiles 0..a, reference r_a) at rows ka_row(a) .. ka_row(a) + 16(a+1) - 1.
+constexpr uint32_t G_M = OFF_Q;
+constexpr uint32_t kGMAtom = 128 * 128;
+constexpr uint32_t G_N = OFF_G;
+constexpr uint32_t kGNAtom = 160 * 128;
+constexpr int kGN = 160;
+__host__ __device__ constexpr int ka_row(int a) { return 8 * a * (a + 1); }  // 0, 16, 48, 96
 constexpr int kLS = 68;                       // row stride (floats) of A and T: conflict-free
-constexpr uint32_t G_P = OFF_G;               // P   fp16 [64 t][64 j] SW128: K-major B (over Q~)
-// in the q/k/z stage, free between operand prep and the next chunk's prefetch:
-constexpr uint32_t S_AKK = OFF_Q;             // A   fp32 [64][kLS]
-constexpr uint32_t S_T32 = OFF_Q + 17408;     // T   fp32 [64][kLS]
-constexpr uint32_t S_TP = OFF_Q + 35840;      // T'  fp16 [64 t][64 j] SW128: K-major B
-constexpr uint32_t G_WT = OFF_G + 51200;      // W^T fp16 [128 c][64 t] SW128: MN-major B
+// in the Gram A region once the Gram products are done:
+constexpr uint32_t S_AKK = OFF_G;             // A   fp32 [64][kLS]
+constexpr uint32_t S_T32 = OFF_G + 17408;     // T   fp32 [64][kLS]
+constexpr uint32_t S_TP = OFF_G + 34816;      // T'  fp16 [64 t][64 j] SW128: K-major B
+constexpr uint32_t G_P = OFF_G + 43008;       // P   fp16 [64 t][64 j] SW128: K-major B
 constexpr uint32_t OFF_QPT = 163840;  // Q+^T  fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major A
 constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-major B
 constexpr uint32_t OFF_MISC = 212992;
 // misc floats
-constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_ER = 320, M_EGR = 832,
-              M_DAB = 1344, M_R = 2112, M_TOT = 2624, M_END = 2624 + 4 * 128;
+constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_ER = 320, M_ED = 832,
+              M_R = 1344, M_TOT = 1856, M_END = 1856 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 
 // ---- Tensor Memory columns (all 128 lanes) ----
 constexpr uint32_t TS32 = 0;    // S^T fp32   [n][c]   128 cols
 constexpr uint32_t TS16 = 128;  // S^T fp16   [n][c/2]  64 cols (A operand)
-constexpr uint32_t TW = 192;    // W^T fp32   [c][t]    64 cols
+constexpr uint32_t TG = 192;    // Gram [Q~; K~q] K^(a)^T  [t][key row] 160 cols, until read back
+constexpr uint32_t TY16 = 192;  // Y^T fp16   [n][t/2]  32 cols (A operand), after the Gram
 constexpr uint32_t TU = 256;    // U~^T / U^T [n][t]    64 cols
 constexpr uint32_t TU16 = 320;  // U^T fp16   [n][t/2]  32 cols (A operand)
 constexpr uint32_t TO = 384;    // O^T fp32   [n][t]    64 cols
+constexpr uint32_t TY = 448;    // Y^T = S^T K+^T fp32 [n][t] 64 cols
 
 // largest magnitude an fp16 operand may take
 constexpr float kF16Max = 65504.0f;
@@ -139,44 +153,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, long lo
   return true;
 }
 
-// fp32 element (t, c) of a [64][128] tile; the column index is xor-ed with
-// (row % 8) * 16 so that groups of 4 columns stay contiguous (vector loads)
-// and 8 consecutive rows fall on distinct banks.
-__device__ __forceinline__ uint32_t f32_off(int t, int c) {
-  return (uint32_t)t * 512u + ((uint32_t)(c ^ ((t & 7) << 4)) << 2);
-}
-// bf16 element (t, c) of a [64][128] tile, same column swizzle.
-__device__ __forceinline__ uint32_t b16_off(int t, int c) {
-  return (uint32_t)t * 256u + ((uint32_t)(c ^ ((t & 7) << 4)) << 1);
-}
-
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
   hi = to_tf32(x);
   lo = to_tf32(x - __uint_as_float(hi));
-}
-
-// acc (16 x 16, two m16n8 tiles) += X (16 x K) * Y (K x 16) in three-pass tf32
-// (hi*hi + hi*lo + lo*hi, close to fp32).  X starts at (xr, xc) and Y at
-// (yr, yc) of fp32 matrices with row stride kLS.  One warp.
-__device__ __forceinline__ void warp_gemm16_3tf32(float (&acc)[2][4], const float* X, int xr,
-                                                  int xc, const float* Y, int yr, int yc, int K,
-                                                  int g, int q) {
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t ah[4], al[4];
-    split_tf32(X[(xr + g) * kLS + xc + k0 + q], ah[0], al[0]);
-    split_tf32(X[(xr + g + 8) * kLS + xc + k0 + q], ah[1], al[1]);
-    split_tf32(X[(xr + g) * kLS + xc + k0 + q + 4], ah[2], al[2]);
-    split_tf32(X[(xr + g + 8) * kLS + xc + k0 + q + 4], ah[3], al[3]);
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      uint32_t bh0, bl0, bh1, bl1;
-      split_tf32(Y[(yr + k0 + q) * kLS + yc + 8 * n + g], bh0, bl0);
-      split_tf32(Y[(yr + k0 + q + 4) * kLS + yc + 8 * n + g], bh1, bl1);
-      mma_1688_tf32(acc[n], ah, bh0, bh1);
-      mma_1688_tf32(acc[n], ah, bl0, bl1);
-      mma_1688_tf32(acc[n], al, bh0, bh1);
-    }
-  }
 }
 
 // One 16 x 8 output tile (columns 8*nt .. of a 16-wide block) of X * Y in
@@ -208,18 +187,6 @@ __device__ __forceinline__ void warp_tile_3tf32(XF xf, const float* Y, int yr, i
   m[8 * kLS + 1] = s * acc[3];
 }
 
-// M[r0 + row][c0 + col] = s * acc (accumulator layout of warp_gemm16_3tf32)
-__device__ __forceinline__ void warp_store16(float* M, int r0, int c0, const float (&acc)[2][4],
-                                             float s, int g, int q) {
-#pragma unroll
-  for (int n = 0; n < 2; ++n) {
-    M[(r0 + g) * kLS + c0 + 8 * n + 2 * q] = s * acc[n][0];
-    M[(r0 + g) * kLS + c0 + 8 * n + 2 * q + 1] = s * acc[n][1];
-    M[(r0 + g + 8) * kLS + c0 + 8 * n + 2 * q] = s * acc[n][2];
-    M[(r0 + g + 8) * kLS + c0 + 8 * n + 2 * q + 1] = s * acc[n][3];
-  }
-}
-
 // Store 16 consecutive values of row `row`, starting at column `col` (a
 // multiple of 16, < 64), as fp16 into a 128-byte-row SW128 tile.
 __device__ __forceinline__ void st_row16_f16(unsigned char* tile, int row, int col,
@@ -234,25 +201,41 @@ __device__ __forceinline__ void st_row16_f16(unsigned char* tile, int row, int c
   *reinterpret_cast<uint4*>(tile + row * 128 + (((c0 + 1) ^ (row & 7)) << 4)) = b;
 }
 
-// Barrier of one 256-thread warp group (ids 1, 2; 0 is __syncthreads).
-__device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+// Store 8 consecutive values of row `row`, starting at column `col` (a
+// multiple of 8, < 64), as fp16 into a 128-byte-row SW128 tile.
+__device__ __forceinline__ void st_row8_f16(unsigned char* tile, int row, int col,
+                                            const float (&v)[8]) {
+  const uint4 a = make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
+                             pack_f16(v[6], v[7]));
+  *reinterpret_cast<uint4*>(tile + row * 128 + ((((uint32_t)col >> 3) ^ (row & 7)) << 4)) = a;
 }
+
+// Byte offset of fp32 element (row, c) of a K-major tf32 operand with the
+// 128-byte swizzle: 32 channels per 128-byte row, one region of `atom`
+// bytes per 32-channel group, 16-byte chunk index XOR (row % 8).
+__device__ __forceinline__ uint32_t tf32_off(int row, int c, uint32_t atom) {
+  return (uint32_t)(c >> 5) * atom + (uint32_t)row * 128u +
+         ((((uint32_t)(c & 31) >> 2) ^ ((uint32_t)row & 7)) << 4) + ((uint32_t)(c & 3) << 2);
+}
+
+// Descriptors of 128-byte-swizzled operands at byte offset `off` from the
+// base described by `base` (a 1024-byte aligned, K-major descriptor):
+// K-major (8-row groups 1024 bytes apart) or MN-major (64-element atoms
+// 8192 bytes apart, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t desc_k(uint64_t base, uint32_t off) {
+  return base + (uint64_t)(off >> 4);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint64_t base, uint32_t off) {
+  return base + (uint64_t)(off >> 4) + ((uint64_t)(8192 >> 4) << 16);
+}
+
+// x rounded to tf32 (nearest, ties away), kept as an fp32 bit pattern
+__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
 
 __device__ __forceinline__ void sync_tc() {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-}
-
-// Gram blocks (query subtile a, key subtile b), a >= b, and zero blocks a < b.
-__constant__ int8_t c_blk_a[10] = {0, 1, 1, 2, 2, 2, 3, 3, 3, 3};
-__constant__ int8_t c_blk_b[10] = {0, 0, 1, 0, 1, 2, 0, 1, 2, 3};
-__constant__ int8_t c_zero_a[6] = {0, 0, 0, 1, 1, 2};
-__constant__ int8_t c_zero_b[6] = {1, 2, 3, 2, 3, 3};
-
-__device__ __forceinline__ int dab_index(int a, int b) {  // a > b
-  return a == 1 ? 0 : (a == 2 ? 1 + b : 3 + b);
 }
 
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < kF16Max; }
@@ -269,6 +252,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* bar_v = bar_qkz + 1;
   uint64_t* bar_mma = bar_qkz + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_qkz + 3);
+  uint64_t* bar_mma2 = bar_qkz + 4;  // the state products issued with the Gram
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = P.H;
@@ -281,6 +265,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_qkz, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_mma2, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -289,13 +274,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   sync_tc();
   const uint32_t tmem = *s_tmem;
+  // descriptor of the shared-memory base; per-operand descriptors add offsets
+  const uint64_t dbase = make_sdesc(smem_u32(sm), 0, 1024, kSwizzle128);
   // TMEM lane quadrant w % 4 (row = tid % 128); the kWQ warps sharing a
   // quadrant split the columns of every TMEM pass (part cq)
   const uint32_t my_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const int row = tid & 127, cq = warp >> 2;
-  uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0;
+  uint32_t ph_qkz = 0, ph_v = 0, ph_mma = 0, ph_mma2 = 0;
   bool pend_qkz = false, pend_v = false;  // TMA copies in flight (uniform)
-  bool pend_mma = false;                  // an MMA commit not yet observed
+  bool pend_mma = false, pend_mma2 = false;  // MMA commits not yet observed
   bool aborted = false;
   float absmax = 0.f;  // largest |value| this thread converted to fp16
 
@@ -440,171 +427,124 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int i = 0; i < 16; ++i) Z[(16 * a + i) * kD + c] = zz[i] + r;
         misc[M_R + a * kD + c] = r;
         misc[M_ER + a * kD + c] = __expf(r);
-        misc[M_EGR + a * kD + c] = __expf(GC - r);
-        if (a == 0) {
-          misc[M_DECAY + c] = __expf(GC);
-        } else {
-          // D_ab = e^{r_a - r_b}, b < a; slots (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-          const int base = a == 1 ? 0 : (a == 2 ? 1 : 3);
-#pragma unroll
-          for (int b = 0; b < 3; ++b)
-            if (b < a) misc[M_DAB + (base + b) * kD + c] = __expf(r - rr[b]);
-        }
+        misc[M_ED + a * kD + c] = __expf(zz[15]);  // e^{r_{a+1} - r_a}, r_4 = G_C
+        if (a == 0) misc[M_DECAY + c] = __expf(GC);
       }
       __syncthreads();  // G and the per-channel tables of every channel are ready
 
       // ---------------- D: decayed operands (thread = 2 key channels x 8 tokens) ----------------
+      // Pass 1 reads q, k and G (all in the input stages) into registers;
+      // pass 2, after a barrier, writes the Gram operands over those stages
+      // and the fp16 operands of the dense products.
       {
         const int c = 2 * (tid & 63), a = (tid >> 6) & 3, tb = 16 * a + 8 * (tid >> 8);
-        const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
-        const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
-        const uint32_t sw0 = (uint32_t)(c & 7), sw1 = (uint32_t)((c + 1) & 7);
-        const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
-        const float er0 = misc[M_ER + a * kD + c], er1 = misc[M_ER + a * kD + c + 1];
-        const float eg0 = misc[M_EGR + a * kD + c], eg1 = misc[M_EGR + a * kD + c + 1];
-        float qpv[2][8], kpv[2][8], khv[2][8];
+        float qt[2][8], kq[2][8], kt[2][8];  // Q~ and K~q (<= 1), K~ = K^(a) (<= e^80)
+        {
+          const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
+          const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
+          const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int t = tb + i;
+            const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
+            const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
+            const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
+            const uint32_t off = sw128_offset(t, c & 63);
+            const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
+            const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
+            const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
+            const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
+            const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
+            qt[0][i] = q0 * F0; qt[1][i] = q1 * F1;
+            kq[0][i] = k0 * F0; kq[1][i] = k1 * F1;
+            kt[0][i] = k0 * E0; kt[1][i] = k1 * E1;
+          }
+        }
+        __syncthreads();  // every thread is done with the q / k / G stages
+        // adjacent-subtile factors e^{r_{b+1} - r_b} (r_4 = G_C), each >= e^-80
+        float ed[2][4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          ed[0][b] = misc[M_ED + b * kD + c];
+          ed[1][b] = misc[M_ED + b * kD + c + 1];
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int t = tb + i;
-          const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
-          const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
-          const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
-          const uint32_t off = sw128_offset(t, c & 63);
-          const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
-          const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
-          const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
-          const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
-          const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
-          const float qt0 = q0 * F0, qt1 = q1 * F1;
-          const float kp0 = k0 * F0, kp1 = k1 * F1;
-          const float kt0 = k0 * E0, kt1 = k1 * E1;
-          *reinterpret_cast<float2*>(sm + G_QT + f32_off(t, c)) = make_float2(qt0, qt1);
-          *reinterpret_cast<float2*>(sm + G_KT + f32_off(t, c)) =
-              make_float2(__uint_as_float(to_tf32(kt0)), __uint_as_float(to_tf32(kt1)));
-          *reinterpret_cast<uint32_t*>(sm + G_KPT + b16_off(t, c)) = pack_bf16(kp0, kp1);
-          qpv[0][i] = qt0 * er0; qpv[1][i] = qt1 * er1;
-          kpv[0][i] = kp0 * er0; kpv[1][i] = kp1 * er1;
-          khv[0][i] = kt0 * eg0; khv[1][i] = kt1 * eg1;
+          // M-side rows: Q~ at t, K~q at 64 + t
+          *reinterpret_cast<float2*>(sm + G_M + tf32_off(t, c, kGMAtom)) =
+              make_float2(tf32f(qt[0][i]), tf32f(qt[1][i]));
+          *reinterpret_cast<float2*>(sm + G_M + tf32_off(64 + t, c, kGMAtom)) =
+              make_float2(tf32f(kq[0][i]), tf32f(kq[1][i]));
+          // A operand: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, by the chain
+          // K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80 is formed)
+          float x0 = kt[0][i], x1 = kt[1][i];
+#pragma unroll
+          for (int ap = 0; ap < 4; ++ap) {
+            if (ap < a) continue;
+            if (ap > a) {
+              x0 *= ed[0][ap - 1];
+              x1 *= ed[1][ap - 1];
+            }
+            *reinterpret_cast<float2*>(sm + G_N + tf32_off(ka_row(ap) + t, c, kGNAtom)) =
+                make_float2(tf32f(x0), tf32f(x1));
+          }
         }
+        // fp16 dense operands, [c][t] rows of 64 tokens: Q+ = Q~ e^{r_a},
+        // K+ = K~q e^{r_a}, Khat = K^(3) e^{G_C - r_3}
         const uint32_t tc8 = (uint32_t)tb >> 3;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
+          const float er = misc[M_ER + a * kD + c + e];
+          float kh[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x = kt[e][i];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              if (b >= a) x *= ed[e][b];
+            kh[i] = x;
+          }
           const uint32_t rw = (uint32_t)(c + e);
-          const uint32_t off = rw * 128u + ((tc8 ^ (e ? sw1 : sw0)) << 4);
+          const uint32_t off = rw * 128u + ((tc8 ^ (rw & 7)) << 4);
           *reinterpret_cast<uint4*>(sm + OFF_QPT + off) =
-              make_uint4(pack_f16(qpv[e][0], qpv[e][1]), pack_f16(qpv[e][2], qpv[e][3]),
-                         pack_f16(qpv[e][4], qpv[e][5]), pack_f16(qpv[e][6], qpv[e][7]));
+              make_uint4(pack_f16(qt[e][0] * er, qt[e][1] * er), pack_f16(qt[e][2] * er, qt[e][3] * er),
+                         pack_f16(qt[e][4] * er, qt[e][5] * er), pack_f16(qt[e][6] * er, qt[e][7] * er));
           *reinterpret_cast<uint4*>(sm + OFF_KPT + off) =
-              make_uint4(pack_f16(kpv[e][0], kpv[e][1]), pack_f16(kpv[e][2], kpv[e][3]),
-                         pack_f16(kpv[e][4], kpv[e][5]), pack_f16(kpv[e][6], kpv[e][7]));
+              make_uint4(pack_f16(kq[e][0] * er, kq[e][1] * er), pack_f16(kq[e][2] * er, kq[e][3] * er),
+                         pack_f16(kq[e][4] * er, kq[e][5] * er), pack_f16(kq[e][6] * er, kq[e][7] * er));
           *reinterpret_cast<uint4*>(sm + OFF_KH + off) =
-              make_uint4(pack_f16(khv[e][0], khv[e][1]), pack_f16(khv[e][2], khv[e][3]),
-                         pack_f16(khv[e][4], khv[e][5]), pack_f16(khv[e][6], khv[e][7]));
+              make_uint4(pack_f16(kh[0], kh[1]), pack_f16(kh[2], kh[3]), pack_f16(kh[4], kh[5]),
+                         pack_f16(kh[6], kh[7]));
         }
       }
       fence_proxy_async_smem();
       sync_tc();
       if (tid == 0) {
-        // O^T = S^T Q+^T  (M=128 value channels, N=64 tokens, K=128 key channels)
+        // Gram, tf32: D[r][p] = M_r . N_p over the 128 channels, M = [Q~; K~q]
+        // (128 rows), N = the packed K^(a) (160 rows)
+        const uint32_t id_g = make_idesc_tf32(128, kGN);
+#pragma unroll
+        for (int kb = 0; kb < kD / 32; ++kb)
+#pragma unroll
+          for (int k8 = 0; k8 < 4; ++k8)
+            mma_tf32_ss(tmem + TG, desc_k(dbase, G_M + kb * kGMAtom + k8 * 32),
+                        desc_k(dbase, G_N + kb * kGNAtom + k8 * 32), id_g, (kb | k8) != 0);
+        mma_commit(bar_mma);
+        // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
+        // K=128 key channels); they only need the entry state
         const uint32_t id_o = make_idesc_f16(128, kC, false, true);
-        const uint32_t bq = smem_u32(sm + OFF_QPT);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(tmem + TO, tmem + TS16 + kk * 8,
-                 make_sdesc(bq + kk * 2048, 8192, 1024, kSwizzle128), id_o, kk > 0);
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          mma_ts(tmem + TO, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_QPT + kk * 2048), id_o, kk > 0);
+          mma_ts(tmem + TY, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_KPT + kk * 2048), id_o, kk > 0);
+        }
+        mma_commit(bar_mma2);
       }
+      pend_mma2 = true;
 
-      // ---------------- E: Gram blocks, tf32 mma.sync ----------------
-      // Two warp groups from here to the first MMA: warps 0-7 build P and
-      // convert v; warps 8-15 build A and invert I + A.  Neither group touches
-      // the other's buffers.  Warp w&7 takes blocks w&7 and (w&7)+8.
-      const int grp = warp >> 3;
-      float acc[2][2][4];
+      // ---------------- E: v -> fp16 while the Gram runs; read back P and A ----------------
       {
-        const int g = lane >> 2, q4 = lane & 3, prod = grp;
-        const unsigned char* Kpt = sm + G_KPT;
-        const int nb = (warp & 7) + 8 < 10 ? 2 : 1;  // blocks of this warp
-        int ta[2], jb[2];
-        bool scaled[2];
-        const float* dab[2];
-#pragma unroll
-        for (int bi = 0; bi < 2; ++bi) {
-          const int blk = min((warp & 7) + 8 * bi, 9);
-          const int a = c_blk_a[blk], b = c_blk_b[blk];
-          ta[bi] = 16 * a + g;
-          jb[bi] = 16 * b + g;
-          scaled[bi] = a != b;
-          dab[bi] = misc + M_DAB + (a > b ? dab_index(a, b) : 0) * kD;
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[bi][n][i] = 0.f;
-        }
-#pragma unroll 2
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-          // 16 channels as two k-steps of 8; thread q covers channels
-          // c0+4q .. c0+4q+3 (logical k = q / q+4 -> channel c0+4q / +1 in
-          // the first step, +2 / +3 in the second; A and B agree).  The two
-          // blocks of a warp are interleaved for independent MMA chains.
-          const int cc = c0 + 4 * q4;
-#pragma unroll
-          for (int bi = 0; bi < 2; ++bi) {
-            if (bi == 1 && nb < 2) continue;
-            const float4 s4 = scaled[bi] ? *reinterpret_cast<const float4*>(dab[bi] + cc)
-                                         : make_float4(1.f, 1.f, 1.f, 1.f);
-            float4 x0, x1;
-            if (prod == 0) {
-              x0 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta[bi], cc));
-              x1 = *reinterpret_cast<const float4*>(sm + G_QT + f32_off(ta[bi] + 8, cc));
-            } else {
-              const uint2 y0 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta[bi], cc));
-              const uint2 y1 = *reinterpret_cast<const uint2*>(Kpt + b16_off(ta[bi] + 8, cc));
-              x0 = make_float4(bf16_lo(y0.x), bf16_hi(y0.x), bf16_lo(y0.y), bf16_hi(y0.y));
-              x1 = make_float4(bf16_lo(y1.x), bf16_hi(y1.x), bf16_lo(y1.y), bf16_hi(y1.y));
-            }
-            const float4 kb0 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb[bi], cc));
-            const float4 kb1 = *reinterpret_cast<const float4*>(sm + G_KT + f32_off(jb[bi] + 8, cc));
-            uint32_t fa[4];
-            fa[0] = to_tf32(x0.x * s4.x); fa[1] = to_tf32(x1.x * s4.x);
-            fa[2] = to_tf32(x0.y * s4.y); fa[3] = to_tf32(x1.y * s4.y);
-            mma_1688_tf32(acc[bi][0], fa, __float_as_uint(kb0.x), __float_as_uint(kb0.y));
-            mma_1688_tf32(acc[bi][1], fa, __float_as_uint(kb1.x), __float_as_uint(kb1.y));
-            fa[0] = to_tf32(x0.z * s4.z); fa[1] = to_tf32(x1.z * s4.z);
-            fa[2] = to_tf32(x0.w * s4.w); fa[3] = to_tf32(x1.w * s4.w);
-            mma_1688_tf32(acc[bi][0], fa, __float_as_uint(kb0.z), __float_as_uint(kb0.w));
-            mma_1688_tf32(acc[bi][1], fa, __float_as_uint(kb1.z), __float_as_uint(kb1.w));
-          }
-        }
-      }
-      if (grp == 0) {
-        // ---- P group: P (over Q~, so after every P warp is done with it), v ----
-        const int g = lane >> 2, q4 = lane & 3;
-        group_sync(2);
-        unsigned char* Pm = sm + G_P;
-#pragma unroll
-        for (int bi = 0; bi < 2; ++bi) {
-          const int blk = (warp & 7) + 8 * bi;
-          if (blk >= 10) continue;
-          const int a = c_blk_a[blk], b = c_blk_b[blk];
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int t = 16 * a + g + 8 * hr, j = 16 * b + 8 * n + 2 * q4;
-              const float p0 = j <= t ? acc[bi][n][2 * hr] : 0.f;
-              const float p1 = j + 1 <= t ? acc[bi][n][2 * hr + 1] : 0.f;
-              *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = pack_f16(p0, p1);
-            }
-        }
-        if ((warp & 7) < 6) {
-          const int zb = warp & 7;
-          const int a = c_zero_a[zb], b = c_zero_b[zb];
-#pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const int e = lane * 8 + i, t = 16 * a + (e >> 4), j = 16 * b + (e & 15);
-            *reinterpret_cast<uint32_t*>(Pm + sw128_offset(t, j)) = 0u;
-          }
-        }
         if (!zero_v) {
           ok = wait_bar(bar_v, ph_v, P.spin_cycles);
           if (ok) {
@@ -613,9 +553,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
-        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 4;
+        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
           uint4 x = zero_v || !ok ? make_uint4(0u, 0u, 0u, 0u) : vv[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -626,65 +566,147 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           vv[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-      } else {
-        // ---- A group: A, T = (I + A)^{-1}, T' = T diag(beta) ----
-        const int g = lane >> 2, q4 = lane & 3, wg = warp & 7;
+        const bool okg = wait_bar(bar_mma, ph_mma, P.spin_cycles);
+        if (okg) ph_mma ^= 1;
+        pend_mma = !okg;
+        ok = ok && okg;
+      }
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
+      tc_fence_after();
+      if (tid == 0 && ci + 1 < nchunks) {  // q / k / z stages are free: prefetch the next chunk
+        const int tn = t0 + kC;
+        mbar_arrive_expect_tx(bar_qkz, 65536u);
+        tma_load_3d(sm + OFF_Q, &tm_q, 0, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_K, &tm_k, 0, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, tn, bar_qkz);
+        tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
+      }
+      pend_qkz = ci + 1 < nchunks;
+      {
+        // TMEM row r = 32 (w % 4) + lane: P row t = r (r < 64) or A row t = r - 64.
+        // Warp w / 4 takes key subtile b; row t (query subtile a) finds key j =
+        // 16b + i of K^(a) at column ka_row(a) + j.  The two query subtiles of a
+        // warp read their columns in two loads.
+        const int s = warp & 3, b = warp >> 2;
+        const int r = 32 * s + lane, t = r & 63, a = t >> 4;
+        const int alo = 2 * (s & 1), ahi = alo + 1;  // subtiles of lanes 0-15 / 16-31
+        float v[16], w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { v[i] = 0.f; w[i] = 0.f; }
+        const uint32_t tl = tmem + ((uint32_t)(32 * s) << 16) + TG;
+        if (b <= alo) tmem_ld16(tl + ka_row(alo) + 16 * b, v);
+        if (b <= ahi) tmem_ld16(tl + ka_row(ahi) + 16 * b, w);
+        tmem_ld_wait();
+        if (a == ahi) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = w[i];
+        }
+        if (r < 64) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = (b <= a && 16 * b + i <= t) ? v[i] : 0.f;
+          st_row16_f16(sm + G_P, t, 16 * b, v);
+        } else if (b <= a) {
+          float* Akk = reinterpret_cast<float*>(sm + S_AKK) + t * kLS + 16 * b;
+          const float bt = misc[M_BETA + t];
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(Akk + i) =
+                make_float4(16 * b + i < t ? bt * v[i] : 0.f, 16 * b + i + 1 < t ? bt * v[i + 1] : 0.f,
+                            16 * b + i + 2 < t ? bt * v[i + 2] : 0.f,
+                            16 * b + i + 3 < t ? bt * v[i + 3] : 0.f);
+        }
+      }
+      __syncthreads();
+
+      // ---------------- F: T = (I + A)^{-1},  T' = T diag(beta) ----------------
+      {
+        const int g = lane >> 2, q4 = lane & 3;
         float* Akk = reinterpret_cast<float*>(sm + S_AKK);
         float* T = reinterpret_cast<float*>(sm + S_T32);
+        if (warp < 4) {
+          if (lane < 16) {
+            // diagonal block `warp`, column `lane` of its inverse: forward
+            // substitution, each solved entry swept into the rows below it
+            const int base = 16 * warp, cc = lane;
+            float x[16];
 #pragma unroll
-        for (int bi = 0; bi < 2; ++bi) {
-          const int blk = wg + 8 * bi;
-          if (blk >= 10) continue;
-          const int a = c_blk_a[blk], b = c_blk_b[blk];
+            for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
+            for (int i = 0; i < 15; ++i) {
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int t = 16 * a + g + 8 * hr, j = 16 * b + 8 * n + 2 * q4;
-              const float bt = misc[M_BETA + t];
-              Akk[t * kLS + j] = j < t ? bt * acc[bi][n][2 * hr] : 0.f;
-              Akk[t * kLS + j + 1] = j + 1 < t ? bt * acc[bi][n][2 * hr + 1] : 0.f;
+              for (int k = i + 1; k < 16; ++k) x[k] -= Akk[(base + k) * kLS + base + i] * x[i];
             }
-        }
-        group_sync(1);
-        if (wg < 4 && lane < 16) {  // diagonal block wg, column `lane`, forward substitution
-          const int base = 16 * wg, cc = lane;
-          float x[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float sacc = (i == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < i; ++j) sacc -= Akk[(base + i) * kLS + base + j] * x[j];
-            x[i] = sacc;
+            for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
           }
+        } else {
+          // meanwhile, on the state products: Y^T -> fp16, and the decay of
+          // S^T (fp32) by e^{G_C} ahead of this chunk's update.  Warp w works
+          // on its lane quadrant w % 4, part w / 4 - 1.
+          const bool okm = wait_bar(bar_mma2, ph_mma2, P.spin_cycles);
+          tc_fence_after();
+          if (okm) {
+            const int part = (warp >> 2) - 1;
+            if (part == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
+              for (int col = 0; col < kC; col += 16) {
+                float v[16];
+                tmem_ld16(my_lane + TY + col, v);
+                tmem_ld_wait();
+                uint32_t hp[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+                  absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+                }
+                tmem_st8(my_lane + TY16 + (col >> 1), hp);
+              }
+            } else {
+              const float* dec = misc + M_DECAY;
+#pragma unroll
+              for (int col = 64 * (part - 1); col < 64 * part; col += 16) {
+                float v[16];
+                tmem_ld16(my_lane + TS32 + col, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                  const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
+                  v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
+                }
+                tmem_st16(my_lane + TS32 + col, v);
+              }
+            }
+            tmem_st_wait();
+          }
+          ok = ok && okm;
         }
-        group_sync(1);
+        tc_fence_before();
+        __syncthreads();
         // Off-diagonal blocks.  With D = blockdiag(I + A_aa) (inverses T_aa above)
         // and L the blocks below it, I + A = D (I + N), N = D^{-1} L, N^4 = 0, so
         //   T = (I - N + N^2 - N^3) D^{-1},   T_ab = X_ab T_bb.
-        // Four levels of 16x16 products in 16x8 tiles.  N lives in T's lower
-        // blocks, N^2 / N^3 in T's unused upper blocks, and the final
-        // off-diagonal T_ab overwrite A's lower blocks.
+        // Four levels of 16x16 products in 16x8 tiles (one per warp).  N lives
+        // in T's lower blocks, N^2 / N^3 in T's unused upper blocks, and the
+        // final off-diagonal T_ab overwrite A's lower blocks.
         {
           float* Afin = Akk;
           auto blk = [&](const float* M, int r0, int c0) {
             return [M, r0, c0](int r, int k) { return M[(r0 + r) * kLS + c0 + k]; };
           };
           // level A: N_ab = T_aa A_ab for the six blocks a > b
-          for (int task = wg; task < 12; task += 8) {
-            const int bi = task >> 1, nt = task & 1;
+          if (warp < 12) {
+            const int bi = warp >> 1, nt = warp & 1;
             const int a = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
             const int b = bi < 3 ? bi : (bi < 5 ? bi - 3 : 0);
             warp_tile_3tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
                             1.f, g, q4);
           }
-          group_sync(1);
+          __syncthreads();
           // level B: N^2_20, N^2_31, N^2_30 (upper blocks 02, 13, 03) and T_10, T_21, T_32
-          for (int task = wg; task < 12; task += 8) {
-            const int nt = task & 1;
-            switch (task >> 1) {
+          if (warp < 12) {
+            const int nt = warp & 1;
+            switch (warp >> 1) {
               case 0: warp_tile_3tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
               case 1: warp_tile_3tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
               case 2: warp_tile_3tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
@@ -693,11 +715,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               default: warp_tile_3tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
             }
           }
-          group_sync(1);
+          __syncthreads();
           // level C: N^3_30 = N_32 N^2_20 (upper block 23); T_20 = (N^2_20 - N_20) T_00;
           // T_31 = (N^2_31 - N_31) T_11
-          if (wg < 6) {
-            const int task = wg >> 1, nt = wg & 1;
+          if (warp < 6) {
+            const int task = warp >> 1, nt = warp & 1;
             if (task == 0) {
               warp_tile_3tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
             } else if (task == 1) {
@@ -710,48 +732,52 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               warp_tile_3tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
             }
           }
-          group_sync(1);
+          __syncthreads();
           // level D: T_30 = (N^2_30 - N_30 - N^3_30) T_00
-          if (wg < 2) {
+          if (warp < 2) {
             auto xf = [T](int r, int k) {
               return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
             };
-            warp_tile_3tf32(xf, T, 0, 0, 16, wg, Afin, 48, 0, 1.f, g, q4);
+            warp_tile_3tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
           }
-          group_sync(1);
+          __syncthreads();
         }
-        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal
+        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal;
+        // thread = (row t, 8 columns j0..j0+7 of one 16-column block)
         {
-          const int gt = tid & 255, t = gt >> 2, j0 = (gt & 3) * 16;
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = j0 + i;
-            const int bt = t >> 4, bj = j >> 4;
-            const float tv = bj == bt ? T[t * kLS + j] : (bj < bt ? Akk[t * kLS + j] : 0.f);
-            v[i] = tv * misc[M_BETA + j];
+          const int t = tid >> 3, j0 = (tid & 7) * 8;
+          const int bt = t >> 4, bj = j0 >> 4;
+          const float* src = (bj == bt ? T : Akk) + t * kLS + j0;
+          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+          if (bj <= bt) {
+            x0 = *reinterpret_cast<const float4*>(src);
+            x1 = *reinterpret_cast<const float4*>(src + 4);
           }
-          st_row16_f16(sm + S_TP, t, j0, v);
+          const float4 b0 = *reinterpret_cast<const float4*>(misc + M_BETA + j0);
+          const float4 b1 = *reinterpret_cast<const float4*>(misc + M_BETA + j0 + 4);
+          const float v[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
+                              x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
+          st_row8_f16(sm + S_TP, t, j0, v);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
+      ph_mma2 ^= 1;
+      pend_mma2 = false;
 
-      // ---------------- G: W^T = K+^T T'^T,  U~^T = V^T T'^T ----------------
+      // ---------------- G: U^T = V^T T'^T - Y^T T'^T ----------------
       if (tid == 0) {
-        const uint32_t ak = smem_u32(sm + OFF_KPT), av = smem_u32(sm + OFF_V),
-                       bt = smem_u32(sm + S_TP);
-        const uint32_t id_w = make_idesc_f16(128, kC, false, false);
         const uint32_t id_u = make_idesc_f16(128, kC, true, false);
+        const uint32_t id_n = make_idesc_f16(128, kC, false, false, true);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t bd = make_sdesc(bt + kk * 32, 0, 1024, kSwizzle128);
-          mma_bf16_ss(tmem + TW, make_sdesc(ak + kk * 32, 0, 1024, kSwizzle128), bd, id_w, kk > 0);
-          mma_bf16_ss(tmem + TU, make_sdesc(av + kk * 2048, 8192, 1024, kSwizzle128), bd, id_u,
-                      kk > 0);
-        }
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16_ss(tmem + TU, desc_mn(dbase, OFF_V + kk * 2048), desc_k(dbase, S_TP + kk * 32),
+                      id_u, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_ts(tmem + TU, tmem + TY16 + kk * 8, desc_k(dbase, S_TP + kk * 32), id_n, true);
         mma_commit(bar_mma);
       }
       pend_mma = true;
@@ -762,93 +788,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (__syncthreads_or(!ok)) { aborted = true; break; }
       tc_fence_after();
-      if (tid == 0 && ci + 1 < nchunks) {  // stages consumed: prefetch the next chunk
+      if (tid == 0 && ci + 1 < nchunks && !zero_v) {  // v stage consumed: prefetch
         const int tn = t0 + kC;
-        mbar_arrive_expect_tx(bar_qkz, 65536u);
-        tma_load_3d(sm + OFF_Q, &tm_q, 0, h, tn, bar_qkz);
-        tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, tn, bar_qkz);
-        tma_load_3d(sm + OFF_K, &tm_k, 0, h, tn, bar_qkz);
-        tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, tn, bar_qkz);
-        tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
-        if (!zero_v) {
-          mbar_arrive_expect_tx(bar_v, 16384u);
-          tma_load_3d(sm + OFF_V, &tm_v, 0, h, tn, bar_v);
-          tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, tn, bar_v);
-        }
+        mbar_arrive_expect_tx(bar_v, 16384u);
+        tma_load_3d(sm + OFF_V, &tm_v, 0, h, tn, bar_v);
+        tma_load_3d(sm + OFF_V + 8192, &tm_v, 64, h, tn, bar_v);
       }
-      pend_qkz = ci + 1 < nchunks;
       pend_v = (ci + 1 < nchunks) && !zero_v;
 
-      // ---------------- H: W^T -> fp16 (MN-major B, row c) ----------------
+      // ---------------- J: U^T -> fp16 in TMEM ----------------
       {
         float v[16];
-        tmem_ld16(my_lane + TW + 16 * cq, v);
+        tmem_ld16(my_lane + TU + 16 * cq, v);
         tmem_ld_wait();
-        st_row16_f16(sm + G_WT, row, 16 * cq, v);
-      }
-      fence_proxy_async_smem();
-      sync_tc();
-
-      // ---------------- I: U^T = U~^T - S^T W^T ----------------
-      if (tid == 0) {
-        const uint32_t bw = smem_u32(sm + G_WT);
-        const uint32_t idn = make_idesc_f16(128, kC, false, true, true);
+        uint32_t hp[8];
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ts(tmem + TU, tmem + TS16 + kk * 8,
-                 make_sdesc(bw + kk * 2048, 8192, 1024, kSwizzle128), idn, true);
-        mma_commit(bar_mma);
-      }
-      pend_mma = true;
-      ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-      if (ok) {
-        ph_mma ^= 1;
-        pend_mma = false;
-      }
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-      tc_fence_after();
-
-      // ---------------- J: U^T -> fp16 in TMEM; S^T <- S^T Diag(e^{G_C}) ----------------
-      {
-        {
-          float v[16];
-          tmem_ld16(my_lane + TU + 16 * cq, v);
-          tmem_ld_wait();
-          uint32_t hp[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-            absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-          }
-          tmem_st8(my_lane + TU16 + 8 * cq, hp);
+        for (int i = 0; i < 8; ++i) {
+          hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+          absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
         }
-        const float* dec = misc + M_DECAY;
-#pragma unroll
-        for (int col = 32 * cq; col < 32 * cq + 32; col += 16) {
-          float v[16];
-          tmem_ld16(my_lane + TS32 + col, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
-            v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
-          }
-          tmem_st16(my_lane + TS32 + col, v);
-        }
+        tmem_st8(my_lane + TU16 + 8 * cq, hp);
         tmem_st_wait();
       }
       sync_tc();
 
       // ---------------- K: O^T += U^T P^T;  S^T += U^T Khat ----------------
       if (tid == 0) {
-        const uint32_t bp = smem_u32(sm + G_P), bk = smem_u32(sm + OFF_KH);
         const uint32_t id_o = make_idesc_f16(128, kC, false, false);
         const uint32_t id_s = make_idesc_f16(128, kD, false, false);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk) {
           const uint32_t au = tmem + TU16 + kk * 8;
-          mma_ts(tmem + TO, au, make_sdesc(bp + kk * 32, 0, 1024, kSwizzle128), id_o, true);
-          mma_ts(tmem + TS32, au, make_sdesc(bk + kk * 32, 0, 1024, kSwizzle128), id_s, true);
+          mma_ts(tmem + TO, au, desc_k(dbase, G_P + kk * 32), id_o, true);
+          mma_ts(tmem + TS32, au, desc_k(dbase, OFF_KH + kk * 32), id_s, true);
         }
         mma_commit(bar_mma);
       }
@@ -923,6 +895,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (pend_v) wait_bar(bar_v, ph_v, P.spin_cycles);
       if (pend_mma) wait_bar(bar_mma, ph_mma, P.spin_cycles);
+      if (pend_mma2) wait_bar(bar_mma2, ph_mma2, P.spin_cycles);
     }
   }
   sync_tc();

@@ -154,6 +154,28 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool a_mn_ma
          | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::tf32 (A, B format 2 = tf32), fp32 accumulate,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t make_idesc_tf32(int M, int N) {
+  return (1u << 4)                        // D format: f32
+         | (2u << 7)                      // A format: tf32
+         | (2u << 10)                     // B format: tf32
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32 (K = 8 per
+// instruction, 32-bit operands); issued by one thread.
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]: A is M lanes x K 16-bit values, two
 // per 32-bit column (even k in the low half); issued by one thread.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -277,10 +299,12 @@ __device__ __forceinline__ void mma_1688_tf32(float (&d)[4], const uint32_t (&a)
 }
 
 // fp32 -> tf32, round to nearest (ties away), as a 32-bit pattern.
+// x rounded to tf32 (10 fraction bits), to nearest with ties away from
+// zero, as an fp32 bit pattern: half a unit of the kept last place is added
+// to the magnitude bits (a carry moves into the exponent as it should) and
+// the 13 dropped bits are cleared.  Integer ALU work only; finite x.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+  return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
