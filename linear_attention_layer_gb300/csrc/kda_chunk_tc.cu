@@ -102,8 +102,8 @@ constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major
 constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-major B
 constexpr uint32_t OFF_MISC = 212992;
 // misc floats
-constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_ER = 320, M_ED = 832,
-              M_R = 1344, M_TOT = 1856, M_END = 1856 + 4 * 128;
+constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_TOT = 320,
+              M_END = 320 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
 
@@ -231,6 +231,9 @@ __device__ __forceinline__ uint64_t desc_mn(uint64_t base, uint32_t off) {
 
 // x rounded to tf32 (nearest, ties away), kept as an fp32 bit pattern
 __device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
+
+// Barrier of warps 0-11 (the ones inverting I + A), id 1.
+__device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 384;" ::: "memory"); }
 
 __device__ __forceinline__ void sync_tc() {
   tc_fence_before();
@@ -399,123 +402,99 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
 
-      // ---------------- C: gate, cumulative decay, per-channel tables ----------------
-      float* Z = reinterpret_cast<float*>(sm + OFF_Z);
+      // ---------------- C: gate and cumulative decay ----------------
+      // thread = (subtile a, key channel c) with its 16 tokens t = 16a + i; a
+      // warp covers 32 channels of one subtile.  G[i] is the cumulative
+      // log-decay from the start of the subtile through token t, i.e. G_t - r_a.
+      const int c = tid & 127, a = tid >> 7;
+      float G[16];
       {
-        // thread = (subtile a, key channel c); a warp covers 32 channels of one subtile
-        const int c = tid & 127, a = tid >> 7;
-        float zz[16];
+        const float* Z = reinterpret_cast<const float*>(sm + OFF_Z);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) zz[i] = Z[(16 * a + i) * kD + c];
+        for (int i = 0; i < 16; ++i) G[i] = Z[(16 * a + i) * kD + c];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) zz[i] = (16 * a + i < len) ? log_decay(zz[i]) : 0.f;
+        for (int i = 0; i < 16; ++i) G[i] = (16 * a + i < len) ? log_decay(G[i]) : 0.f;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) zz[i] += zz[i - 1];
-        misc[M_TOT + a * kD + c] = zz[15];
-        __syncthreads();
+        for (int i = 1; i < 16; ++i) G[i] += G[i - 1];
+        misc[M_TOT + a * kD + c] = G[15];
+      }
+      __syncthreads();  // subtile totals (and the token norms) are ready
+
+      // ---------------- D: decayed operands ----------------
+      // Pass 1 reads q and k (input stages) into registers; pass 2, after a
+      // barrier, writes the Gram operands over the stages and the fp16
+      // operands of the dense products.
+      {
         float tot[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) tot[b] = misc[M_TOT + b * kD + c];
-        float rr[4];  // cumulative log-decay before each subtile
-        rr[0] = 0.f;
-        rr[1] = tot[0];
-        rr[2] = tot[0] + tot[1];
-        rr[3] = rr[2] + tot[2];
-        const float GC = rr[3] + tot[3];
-        const float r = a == 0 ? rr[0] : (a == 1 ? rr[1] : (a == 2 ? rr[2] : rr[3]));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) Z[(16 * a + i) * kD + c] = zz[i] + r;
-        misc[M_R + a * kD + c] = r;
-        misc[M_ER + a * kD + c] = __expf(r);
-        misc[M_ED + a * kD + c] = __expf(zz[15]);  // e^{r_{a+1} - r_a}, r_4 = G_C
-        if (a == 0) misc[M_DECAY + c] = __expf(GC);
-      }
-      __syncthreads();  // G and the per-channel tables of every channel are ready
-
-      // ---------------- D: decayed operands (thread = 2 key channels x 8 tokens) ----------------
-      // Pass 1 reads q, k and G (all in the input stages) into registers;
-      // pass 2, after a barrier, writes the Gram operands over those stages
-      // and the fp16 operands of the dense products.
-      {
-        const int c = 2 * (tid & 63), a = (tid >> 6) & 3, tb = 16 * a + 8 * (tid >> 8);
-        float qt[2][8], kq[2][8], kt[2][8];  // Q~ and K~q (<= 1), K~ = K^(a) (<= e^80)
+        const float r = (a > 0 ? tot[0] : 0.f) + (a > 1 ? tot[1] : 0.f) + (a > 2 ? tot[2] : 0.f);
+        if (a == 0) misc[M_DECAY + c] = __expf(tot[0] + tot[1] + tot[2] + tot[3]);
+        float qt[16], kq[16], kt[16];  // Q~, K~q (<= 1) and K~ = K^(a) (<= e^80)
         {
           const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
           const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
-          const float r0 = misc[M_R + a * kD + c], r1 = misc[M_R + a * kD + c + 1];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int t = tb + i;
-            const float2 G2 = *reinterpret_cast<const float2*>(Z + t * kD + c);
-            const float F0 = __expf(G2.x - r0), F1 = __expf(G2.y - r1);
-            const float E0 = __fdividef(1.0f, F0), E1 = __fdividef(1.0f, F1);
+          for (int i = 0; i < 16; ++i) {
+            const int t = 16 * a + i;
+            const float F = __expf(G[i]), E = __fdividef(1.0f, F);
             const uint32_t off = sw128_offset(t, c & 63);
-            const uint32_t qq = *reinterpret_cast<const uint32_t*>(qs + off);
-            const uint32_t kw = *reinterpret_cast<const uint32_t*>(ks + off);
-            const float rq = misc[M_RQ + t], rk = misc[M_RK + t];
-            const float q0 = bf16_lo(qq) * rq, q1 = bf16_hi(qq) * rq;
-            const float k0 = bf16_lo(kw) * rk, k1 = bf16_hi(kw) * rk;
-            qt[0][i] = q0 * F0; qt[1][i] = q1 * F1;
-            kq[0][i] = k0 * F0; kq[1][i] = k1 * F1;
-            kt[0][i] = k0 * E0; kt[1][i] = k1 * E1;
+            const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qs + off)) *
+                            misc[M_RQ + t];
+            const float k = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ks + off)) *
+                            misc[M_RK + t];
+            qt[i] = q * F;
+            kq[i] = k * F;
+            kt[i] = k * E;
           }
         }
-        __syncthreads();  // every thread is done with the q / k / G stages
-        // adjacent-subtile factors e^{r_{b+1} - r_b} (r_4 = G_C), each >= e^-80
-        float ed[2][4];
+        __syncthreads();  // every thread is done with the q / k / z stages
+        // adjacent-subtile factors e^{r_{b+1} - r_b} = e^{tot_b} (r_4 = G_C), each >= e^-80
+        float ed[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          ed[0][b] = misc[M_ED + b * kD + c];
-          ed[1][b] = misc[M_ED + b * kD + c + 1];
-        }
+        for (int b = 0; b < 4; ++b) ed[b] = b >= a ? __expf(tot[b]) : 1.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = tb + i;
+        for (int i = 0; i < 16; ++i) {
+          const int t = 16 * a + i;
           // M-side rows: Q~ at t, K~q at 64 + t
-          *reinterpret_cast<float2*>(sm + G_M + tf32_off(t, c, kGMAtom)) =
-              make_float2(tf32f(qt[0][i]), tf32f(qt[1][i]));
-          *reinterpret_cast<float2*>(sm + G_M + tf32_off(64 + t, c, kGMAtom)) =
-              make_float2(tf32f(kq[0][i]), tf32f(kq[1][i]));
-          // A operand: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, by the chain
+          *reinterpret_cast<float*>(sm + G_M + tf32_off(t, c, kGMAtom)) = tf32f(qt[i]);
+          *reinterpret_cast<float*>(sm + G_M + tf32_off(64 + t, c, kGMAtom)) = tf32f(kq[i]);
+          // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, by the chain
           // K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80 is formed)
-          float x0 = kt[0][i], x1 = kt[1][i];
+          float x = kt[i];
 #pragma unroll
           for (int ap = 0; ap < 4; ++ap) {
             if (ap < a) continue;
-            if (ap > a) {
-              x0 *= ed[0][ap - 1];
-              x1 *= ed[1][ap - 1];
-            }
-            *reinterpret_cast<float2*>(sm + G_N + tf32_off(ka_row(ap) + t, c, kGNAtom)) =
-                make_float2(tf32f(x0), tf32f(x1));
+            if (ap > a) x *= ed[ap - 1];
+            *reinterpret_cast<float*>(sm + G_N + tf32_off(ka_row(ap) + t, c, kGNAtom)) = tf32f(x);
           }
         }
-        // fp16 dense operands, [c][t] rows of 64 tokens: Q+ = Q~ e^{r_a},
-        // K+ = K~q e^{r_a}, Khat = K^(3) e^{G_C - r_3}
-        const uint32_t tc8 = (uint32_t)tb >> 3;
+        // fp16 dense operands, row c of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a},
+        // K+ = K~q e^{r_a}, Khat
+        const float er = __expf(r);
+        const uint32_t rowoff = (uint32_t)c * 128u;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float er = misc[M_ER + a * kD + c + e];
-          float kh[8];
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const uint32_t off = rowoff + ((((uint32_t)(2 * a + h8)) ^ ((uint32_t)c & 7)) << 4);
+          const int i0 = 8 * h8;
+          float kh[8];  // Khat = K^(3) e^{G_C - r_3}, along the same chain
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            float x = kt[e][i];
+            float x = kt[i0 + i];
 #pragma unroll
             for (int b = 0; b < 4; ++b)
-              if (b >= a) x *= ed[e][b];
+              if (b >= a) x *= ed[b];
             kh[i] = x;
           }
-          const uint32_t rw = (uint32_t)(c + e);
-          const uint32_t off = rw * 128u + ((tc8 ^ (rw & 7)) << 4);
-          *reinterpret_cast<uint4*>(sm + OFF_QPT + off) =
-              make_uint4(pack_f16(qt[e][0] * er, qt[e][1] * er), pack_f16(qt[e][2] * er, qt[e][3] * er),
-                         pack_f16(qt[e][4] * er, qt[e][5] * er), pack_f16(qt[e][6] * er, qt[e][7] * er));
-          *reinterpret_cast<uint4*>(sm + OFF_KPT + off) =
-              make_uint4(pack_f16(kq[e][0] * er, kq[e][1] * er), pack_f16(kq[e][2] * er, kq[e][3] * er),
-                         pack_f16(kq[e][4] * er, kq[e][5] * er), pack_f16(kq[e][6] * er, kq[e][7] * er));
-          *reinterpret_cast<uint4*>(sm + OFF_KH + off) =
-              make_uint4(pack_f16(kh[0], kh[1]), pack_f16(kh[2], kh[3]), pack_f16(kh[4], kh[5]),
-                         pack_f16(kh[6], kh[7]));
+          *reinterpret_cast<uint4*>(sm + OFF_QPT + off) = make_uint4(
+              pack_f16(qt[i0] * er, qt[i0 + 1] * er), pack_f16(qt[i0 + 2] * er, qt[i0 + 3] * er),
+              pack_f16(qt[i0 + 4] * er, qt[i0 + 5] * er), pack_f16(qt[i0 + 6] * er, qt[i0 + 7] * er));
+          *reinterpret_cast<uint4*>(sm + OFF_KPT + off) = make_uint4(
+              pack_f16(kq[i0] * er, kq[i0 + 1] * er), pack_f16(kq[i0 + 2] * er, kq[i0 + 3] * er),
+              pack_f16(kq[i0 + 4] * er, kq[i0 + 5] * er), pack_f16(kq[i0 + 6] * er, kq[i0 + 7] * er));
+          *reinterpret_cast<uint4*>(sm + OFF_KH + off) = make_uint4(
+              pack_f16(kh[0], kh[1]), pack_f16(kh[2], kh[3]), pack_f16(kh[4], kh[5]),
+              pack_f16(kh[6], kh[7]));
         }
       }
       fence_proxy_async_smem();
@@ -531,17 +510,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mma_tf32_ss(tmem + TG, desc_k(dbase, G_M + kb * kGMAtom + k8 * 32),
                         desc_k(dbase, G_N + kb * kGNAtom + k8 * 32), id_g, (kb | k8) != 0);
         mma_commit(bar_mma);
-        // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
-        // K=128 key channels); they only need the entry state
-        const uint32_t id_o = make_idesc_f16(128, kC, false, true);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          mma_ts(tmem + TO, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_QPT + kk * 2048), id_o, kk > 0);
-          mma_ts(tmem + TY, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_KPT + kk * 2048), id_o, kk > 0);
-        }
-        mma_commit(bar_mma2);
       }
-      pend_mma2 = true;
 
       // ---------------- E: v -> fp16 while the Gram runs; read back P and A ----------------
       {
@@ -624,6 +593,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int g = lane >> 2, q4 = lane & 3;
         float* Akk = reinterpret_cast<float*>(sm + S_AKK);
         float* T = reinterpret_cast<float*>(sm + S_T32);
+        // Warps 0-11 invert; warps 12-15 meanwhile run the state products
+        // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
+        // K=128 key channels; they only need the entry state), convert Y^T to
+        // fp16 and decay S^T (fp32) by e^{G_C} ahead of this chunk's update.
+        pend_mma2 = true;
         if (warp < 4) {
           if (lane < 16) {
             // diagonal block `warp`, column `lane` of its inverse: forward
@@ -640,108 +614,114 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
           }
-        } else {
-          // meanwhile, on the state products: Y^T -> fp16, and the decay of
-          // S^T (fp32) by e^{G_C} ahead of this chunk's update.  Warp w works
-          // on its lane quadrant w % 4, part w / 4 - 1.
+        } else if (warp >= 12) {
+          if (warp == 12 && lane == 0) {
+            const uint32_t id_o = make_idesc_f16(128, kC, false, true);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              mma_ts(tmem + TO, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_QPT + kk * 2048), id_o,
+                     kk > 0);
+              mma_ts(tmem + TY, tmem + TS16 + kk * 8, desc_mn(dbase, OFF_KPT + kk * 2048), id_o,
+                     kk > 0);
+            }
+            mma_commit(bar_mma2);
+          }
+          __syncwarp();
           const bool okm = wait_bar(bar_mma2, ph_mma2, P.spin_cycles);
           tc_fence_after();
           if (okm) {
-            const int part = (warp >> 2) - 1;
-            if (part == 0) {
 #pragma unroll
-              for (int col = 0; col < kC; col += 16) {
-                float v[16];
-                tmem_ld16(my_lane + TY + col, v);
-                tmem_ld_wait();
-                uint32_t hp[8];
+            for (int col = 0; col < kC; col += 16) {
+              float v[16];
+              tmem_ld16(my_lane + TY + col, v);
+              tmem_ld_wait();
+              uint32_t hp[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-                  absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-                }
-                tmem_st8(my_lane + TY16 + (col >> 1), hp);
+              for (int i = 0; i < 8; ++i) {
+                hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+                absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
               }
-            } else {
-              const float* dec = misc + M_DECAY;
+              tmem_st8(my_lane + TY16 + (col >> 1), hp);
+            }
+            const float* dec = misc + M_DECAY;
+#pragma unroll 2
+            for (int col = 0; col < kD; col += 16) {
+              float v[16];
+              tmem_ld16(my_lane + TS32 + col, v);
+              tmem_ld_wait();
 #pragma unroll
-              for (int col = 64 * (part - 1); col < 64 * part; col += 16) {
-                float v[16];
-                tmem_ld16(my_lane + TS32 + col, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                  const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
-                  v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
-                }
-                tmem_st16(my_lane + TS32 + col, v);
+              for (int i = 0; i < 16; i += 4) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
+                v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
               }
+              tmem_st16(my_lane + TS32 + col, v);
             }
             tmem_st_wait();
           }
           ok = ok && okm;
         }
-        tc_fence_before();
-        __syncthreads();
-        // Off-diagonal blocks.  With D = blockdiag(I + A_aa) (inverses T_aa above)
-        // and L the blocks below it, I + A = D (I + N), N = D^{-1} L, N^4 = 0, so
-        //   T = (I - N + N^2 - N^3) D^{-1},   T_ab = X_ab T_bb.
-        // Four levels of 16x16 products in 16x8 tiles (one per warp).  N lives
-        // in T's lower blocks, N^2 / N^3 in T's unused upper blocks, and the
-        // final off-diagonal T_ab overwrite A's lower blocks.
-        {
-          float* Afin = Akk;
-          auto blk = [&](const float* M, int r0, int c0) {
-            return [M, r0, c0](int r, int k) { return M[(r0 + r) * kLS + c0 + k]; };
-          };
-          // level A: N_ab = T_aa A_ab for the six blocks a > b
-          if (warp < 12) {
-            const int bi = warp >> 1, nt = warp & 1;
-            const int a = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-            const int b = bi < 3 ? bi : (bi < 5 ? bi - 3 : 0);
-            warp_tile_3tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
-                            1.f, g, q4);
-          }
-          __syncthreads();
-          // level B: N^2_20, N^2_31, N^2_30 (upper blocks 02, 13, 03) and T_10, T_21, T_32
-          if (warp < 12) {
-            const int nt = warp & 1;
-            switch (warp >> 1) {
-              case 0: warp_tile_3tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
-              case 1: warp_tile_3tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
-              case 2: warp_tile_3tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
-              case 3: warp_tile_3tf32(blk(T, 16, 0), T, 0, 0, 16, nt, Afin, 16, 0, -1.f, g, q4); break;
-              case 4: warp_tile_3tf32(blk(T, 32, 16), T, 16, 16, 16, nt, Afin, 32, 16, -1.f, g, q4); break;
-              default: warp_tile_3tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
-            }
-          }
-          __syncthreads();
-          // level C: N^3_30 = N_32 N^2_20 (upper block 23); T_20 = (N^2_20 - N_20) T_00;
-          // T_31 = (N^2_31 - N_31) T_11
-          if (warp < 6) {
-            const int task = warp >> 1, nt = warp & 1;
-            if (task == 0) {
-              warp_tile_3tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
-            } else if (task == 1) {
-              auto xf = [T](int r, int k) { return T[r * kLS + 32 + k] - T[(32 + r) * kLS + k]; };
-              warp_tile_3tf32(xf, T, 0, 0, 16, nt, Afin, 32, 0, 1.f, g, q4);
-            } else {
-              auto xf = [T](int r, int k) {
-                return T[(16 + r) * kLS + 48 + k] - T[(48 + r) * kLS + 16 + k];
-              };
-              warp_tile_3tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
-            }
-          }
-          __syncthreads();
-          // level D: T_30 = (N^2_30 - N_30 - N^3_30) T_00
-          if (warp < 2) {
-            auto xf = [T](int r, int k) {
-              return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
+        if (warp < 12) {
+          inv_sync();
+          // Off-diagonal blocks.  With D = blockdiag(I + A_aa) (inverses T_aa above)
+          // and L the blocks below it, I + A = D (I + N), N = D^{-1} L, N^4 = 0, so
+          //   T = (I - N + N^2 - N^3) D^{-1},   T_ab = X_ab T_bb.
+          // Four levels of 16x16 products in 16x8 tiles (one per warp).  N lives
+          // in T's lower blocks, N^2 / N^3 in T's unused upper blocks, and the
+          // final off-diagonal T_ab overwrite A's lower blocks.
+          {
+            float* Afin = Akk;
+            auto blk = [&](const float* M, int r0, int c0) {
+              return [M, r0, c0](int r, int k) { return M[(r0 + r) * kLS + c0 + k]; };
             };
-            warp_tile_3tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
+            // level A: N_ab = T_aa A_ab for the six blocks a > b
+            if (warp < 12) {
+              const int bi = warp >> 1, nt = warp & 1;
+              const int a = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+              const int b = bi < 3 ? bi : (bi < 5 ? bi - 3 : 0);
+              warp_tile_3tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
+                              1.f, g, q4);
+            }
+            inv_sync();
+            // level B: N^2_20, N^2_31, N^2_30 (upper blocks 02, 13, 03) and T_10, T_21, T_32
+            if (warp < 12) {
+              const int nt = warp & 1;
+              switch (warp >> 1) {
+                case 0: warp_tile_3tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
+                case 1: warp_tile_3tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
+                case 2: warp_tile_3tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
+                case 3: warp_tile_3tf32(blk(T, 16, 0), T, 0, 0, 16, nt, Afin, 16, 0, -1.f, g, q4); break;
+                case 4: warp_tile_3tf32(blk(T, 32, 16), T, 16, 16, 16, nt, Afin, 32, 16, -1.f, g, q4); break;
+                default: warp_tile_3tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
+              }
+            }
+            inv_sync();
+            // level C: N^3_30 = N_32 N^2_20 (upper block 23); T_20 = (N^2_20 - N_20) T_00;
+            // T_31 = (N^2_31 - N_31) T_11
+            if (warp < 6) {
+              const int task = warp >> 1, nt = warp & 1;
+              if (task == 0) {
+                warp_tile_3tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
+              } else if (task == 1) {
+                auto xf = [T](int r, int k) { return T[r * kLS + 32 + k] - T[(32 + r) * kLS + k]; };
+                warp_tile_3tf32(xf, T, 0, 0, 16, nt, Afin, 32, 0, 1.f, g, q4);
+              } else {
+                auto xf = [T](int r, int k) {
+                  return T[(16 + r) * kLS + 48 + k] - T[(48 + r) * kLS + 16 + k];
+                };
+                warp_tile_3tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
+              }
+            }
+            inv_sync();
+            // level D: T_30 = (N^2_30 - N_30 - N^3_30) T_00
+            if (warp < 2) {
+              auto xf = [T](int r, int k) {
+                return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
+              };
+              warp_tile_3tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
+            }
           }
-          __syncthreads();
         }
+        __syncthreads();  // T, the final off-diagonal blocks and the side work are done
         // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal;
         // thread = (row t, 8 columns j0..j0+7 of one 16-column block)
         {
