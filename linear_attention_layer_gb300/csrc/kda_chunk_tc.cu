@@ -243,6 +243,41 @@ __device__ __forceinline__ void sync_tc() {
 
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < kF16Max; }
 
+// The end of a chunk, once its last products have landed in TMEM: O^T (lane
+// n = value channel, column t) to out[t0 + t][h][n] in bf16 for t < len, and
+// (conv_s) S^T fp32 -> fp16, the A operand of the next chunk's state products.
+// Warp part cq covers 16 columns of O^T and 32 of S^T.
+__device__ __forceinline__ void finish_chunk(__nv_bfloat16* out, int H, int h, int t0, int len,
+                                             uint32_t my_lane, uint32_t tmem, int row, int cq,
+                                             bool conv_s, float& absmax) {
+  if (out) {
+    __nv_bfloat16* ocol = out + ((size_t)t0 * H + h) * kD + row;
+    const int col = 16 * cq;
+    float v[16];
+    tmem_ld16(my_lane + TO + col, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
+  }
+  if (conv_s) {
+#pragma unroll
+    for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
+      float v[16];
+      tmem_ld16(my_lane + TS32 + c0, v);
+      tmem_ld_wait();
+      uint32_t hp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+        absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+      }
+      tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
+    }
+    tmem_st_wait();
+  }
+}
+
 __global__ void __launch_bounds__(kNT, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -355,6 +390,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     sync_tc();
 
+    bool pend_l = false;  // the previous chunk still has to write O and convert S^T
+    int l_t0 = 0, l_len = 0;
     for (int ci = 0; ci < nchunks; ++ci) {
       const int t0 = bos + ci * kC;
       const int len = min(kC, eos - t0);
@@ -402,6 +439,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
 
+      if (pend_l) {
+        // ---------------- L (previous chunk): write O; S^T -> fp16 ----------------
+        ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
+        if (ok) {
+          ph_mma ^= 1;
+          pend_mma = false;
+          tc_fence_after();
+          finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, true, absmax);
+        }
+        pend_l = false;
+      }
+
       // ---------------- C: gate and cumulative decay ----------------
       // thread = (subtile a, key channel c) with its 16 tokens t = 16a + i; a
       // warp covers 32 channels of one subtile.  G[i] is the cumulative
@@ -418,7 +467,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int i = 1; i < 16; ++i) G[i] += G[i - 1];
         misc[M_TOT + a * kD + c] = G[15];
       }
-      __syncthreads();  // subtile totals (and the token norms) are ready
+      tc_fence_before();
+      if (__syncthreads_or(!ok)) { aborted = true; break; }  // subtile totals, token norms
+      tc_fence_after();
 
       // ---------------- D: decayed operands ----------------
       // Pass 1 reads q and k (input stages) into registers; pass 2, after a
@@ -431,18 +482,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float r = (a > 0 ? tot[0] : 0.f) + (a > 1 ? tot[1] : 0.f) + (a > 2 ? tot[2] : 0.f);
         if (a == 0) misc[M_DECAY + c] = __expf(tot[0] + tot[1] + tot[2] + tot[3]);
         float qt[16], kq[16], kt[16];  // Q~, K~q (<= 1) and K~ = K^(a) (<= e^80)
+        // Row t = 16a + i of a 128-byte-swizzled tile holds this thread's element in
+        // 16-byte chunk (x ^ (i % 8)) with x its unswizzled chunk, so the address is
+        // a per-thread base for i % 8 plus 128 i.
         {
-          const unsigned char* qs = sm + OFF_Q + (c >> 6) * 8192;
-          const unsigned char* ks = sm + OFF_K + (c >> 6) * 8192;
+          const unsigned char* qk = sm + OFF_Q + (c >> 6) * 8192 + 2048 * a + (c & 7) * 2;
+          const uint32_t x = ((uint32_t)c & 63) >> 3;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int t = 16 * a + i;
             const float F = __expf(G[i]), E = __fdividef(1.0f, F);
-            const uint32_t off = sw128_offset(t, c & 63);
-            const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qs + off)) *
-                            misc[M_RQ + t];
-            const float k = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ks + off)) *
-                            misc[M_RK + t];
+            const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
+            const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qk + off)) *
+                            misc[M_RQ + 16 * a + i];
+            const float k = __bfloat162float(
+                                *reinterpret_cast<const __nv_bfloat16*>(qk + OFF_K - OFF_Q + off)) *
+                            misc[M_RK + 16 * a + i];
             qt[i] = q * F;
             kq[i] = k * F;
             kt[i] = k * E;
@@ -453,20 +507,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float ed[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) ed[b] = b >= a ? __expf(tot[b]) : 1.f;
+        {
+          const uint32_t x = ((uint32_t)c & 31) >> 2;
+          unsigned char* gm = sm + G_M + (c >> 5) * kGMAtom + 2048 * a + (c & 3) * 4;
+          unsigned char* gn = sm + G_N + (c >> 5) * kGNAtom + 2048 * a + (c & 3) * 4;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = 16 * a + i;
-          // M-side rows: Q~ at t, K~q at 64 + t
-          *reinterpret_cast<float*>(sm + G_M + tf32_off(t, c, kGMAtom)) = tf32f(qt[i]);
-          *reinterpret_cast<float*>(sm + G_M + tf32_off(64 + t, c, kGMAtom)) = tf32f(kq[i]);
-          // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, by the chain
-          // K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80 is formed)
-          float x = kt[i];
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
+            // M-side rows: Q~ at t, K~q at 64 + t
+            *reinterpret_cast<float*>(gm + off) = tf32f(qt[i]);
+            *reinterpret_cast<float*>(gm + 64 * 128 + off) = tf32f(kq[i]);
+            // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, rows ka_row(a') + t, by
+            // the chain K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80)
+            float v = kt[i];
 #pragma unroll
-          for (int ap = 0; ap < 4; ++ap) {
-            if (ap < a) continue;
-            if (ap > a) x *= ed[ap - 1];
-            *reinterpret_cast<float*>(sm + G_N + tf32_off(ka_row(ap) + t, c, kGNAtom)) = tf32f(x);
+            for (int ap = 0; ap < 4; ++ap) {
+              if (ap < a) continue;
+              if (ap > a) v *= ed[ap - 1];
+              *reinterpret_cast<float*>(gn + ka_row(ap) * 128 + off) = tf32f(v);
+            }
           }
         }
         // fp16 dense operands, row c of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a},
@@ -804,43 +863,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(bar_mma);
       }
+      // O and S^T are finished (L) while the next chunk computes its gates
       pend_mma = true;
-      ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-      if (ok) {
+      pend_l = true;
+      l_t0 = t0;
+      l_len = len;
+    }
+    if (aborted) break;
+    if (pend_l) {
+      // ---------------- L (last chunk): write O ----------------
+      const bool okl = wait_bar(bar_mma, ph_mma, P.spin_cycles);
+      if (okl) {
         ph_mma ^= 1;
         pend_mma = false;
+        tc_fence_after();
+        finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, false, absmax);
       }
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-      tc_fence_after();
-
-      // ---------------- L: write O; S^T -> fp16 for the next chunk ----------------
-      {
-        __nv_bfloat16* ocol = P.out + ((size_t)t0 * H + h) * kD + row;
-        if (P.out) {
-          const int col = 16 * cq;
-          float v[16];
-          tmem_ld16(my_lane + TO + col, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
-        }
-#pragma unroll
-        for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
-          float v[16];
-          tmem_ld16(my_lane + TS32 + c0, v);
-          tmem_ld_wait();
-          uint32_t hp[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-            absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-          }
-          tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
-        }
-        tmem_st_wait();
-      }
-      sync_tc();
+      pend_l = false;
+      tc_fence_before();
+      if (__syncthreads_or(!okl)) { aborted = true; break; }
     }
     if (aborted) break;
 
