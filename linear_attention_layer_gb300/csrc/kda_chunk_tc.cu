@@ -38,8 +38,9 @@
 // to tf32 once (the e^80 range rules out fp16 there); the dense products
 // use fp16 operands (11-bit significand; all of them are bounded by 1 or by
 // the data) with fp32 accumulation.  bf16 operands there would leave ~0.2%
-// relative error on the largest outputs.  The inverse runs in three-pass
-// tf32 warp MMAs (close to fp32).
+// relative error on the largest outputs.  The inverse's 16x16 diagonal
+// blocks are solved in fp32; its off-diagonal block products run as tf32
+// warp MMAs (its fp16 rounding for the tensor core bounds it anyway).
 //
 // One CTA (16 warps) per SM walks (sequence, head) work units, longest
 // sequence first.  Per chunk:
@@ -153,32 +154,22 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, long lo
   return true;
 }
 
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
-}
-
-// One 16 x 8 output tile (columns 8*nt .. of a 16-wide block) of X * Y in
-// three-pass tf32, stored as s * result at M[r0 + row][c0 + 8*nt + col].
-// X(row, k) is produced by `xf` (so it may combine several stored blocks);
-// Y starts at (yr, yc) of a row-stride-kLS matrix.  One warp.
+// One 16 x 8 output tile (columns 8*nt .. of a 16-wide block) of X * Y as
+// tf32 warp MMAs with fp32 accumulation, stored as s * result at
+// M[r0 + row][c0 + 8*nt + col].  X(row, k) is produced by `xf` (so it may
+// combine several stored blocks); Y starts at (yr, yc) of a row-stride-kLS
+// matrix.  One warp.  (The inverse these tiles build is rounded to fp16 for
+// its MMA right after, which bounds its precision more tightly than tf32
+// inputs do.)
 template <typename XF>
-__device__ __forceinline__ void warp_tile_3tf32(XF xf, const float* Y, int yr, int yc, int K,
-                                                int nt, float* M, int r0, int c0, float s,
-                                                int g, int q) {
+__device__ __forceinline__ void warp_tile_tf32(XF xf, const float* Y, int yr, int yc, int K, int nt,
+                                               float* M, int r0, int c0, float s, int g, int q) {
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t ah[4], al[4];
-    split_tf32(xf(g, k0 + q), ah[0], al[0]);
-    split_tf32(xf(g + 8, k0 + q), ah[1], al[1]);
-    split_tf32(xf(g, k0 + q + 4), ah[2], al[2]);
-    split_tf32(xf(g + 8, k0 + q + 4), ah[3], al[3]);
-    uint32_t bh0, bl0, bh1, bl1;
-    split_tf32(Y[(yr + k0 + q) * kLS + yc + 8 * nt + g], bh0, bl0);
-    split_tf32(Y[(yr + k0 + q + 4) * kLS + yc + 8 * nt + g], bh1, bl1);
-    mma_1688_tf32(acc, ah, bh0, bh1);
-    mma_1688_tf32(acc, ah, bl0, bl1);
-    mma_1688_tf32(acc, al, bh0, bh1);
+    const uint32_t a[4] = {to_tf32(xf(g, k0 + q)), to_tf32(xf(g + 8, k0 + q)),
+                           to_tf32(xf(g, k0 + q + 4)), to_tf32(xf(g + 8, k0 + q + 4))};
+    mma_1688_tf32(acc, a, to_tf32(Y[(yr + k0 + q) * kLS + yc + 8 * nt + g]),
+                  to_tf32(Y[(yr + k0 + q + 4) * kLS + yc + 8 * nt + g]));
   }
   float* m = M + (r0 + g) * kLS + c0 + 8 * nt + 2 * q;
   m[0] = s * acc[0];
@@ -502,34 +493,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             kt[i] = k * E;
           }
         }
-        __syncthreads();  // every thread is done with the q / k / z stages
         // adjacent-subtile factors e^{r_{b+1} - r_b} = e^{tot_b} (r_4 = G_C), each >= e^-80
         float ed[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) ed[b] = b >= a ? __expf(tot[b]) : 1.f;
-        {
-          const uint32_t x = ((uint32_t)c & 31) >> 2;
-          unsigned char* gm = sm + G_M + (c >> 5) * kGMAtom + 2048 * a + (c & 3) * 4;
-          unsigned char* gn = sm + G_N + (c >> 5) * kGNAtom + 2048 * a + (c & 3) * 4;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
-            // M-side rows: Q~ at t, K~q at 64 + t
-            *reinterpret_cast<float*>(gm + off) = tf32f(qt[i]);
-            *reinterpret_cast<float*>(gm + 64 * 128 + off) = tf32f(kq[i]);
-            // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, rows ka_row(a') + t, by
-            // the chain K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80)
-            float v = kt[i];
-#pragma unroll
-            for (int ap = 0; ap < 4; ++ap) {
-              if (ap < a) continue;
-              if (ap > a) v *= ed[ap - 1];
-              *reinterpret_cast<float*>(gn + ka_row(ap) * 128 + off) = tf32f(v);
-            }
-          }
-        }
-        // fp16 dense operands, row c of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a},
-        // K+ = K~q e^{r_a}, Khat
+        // fp16 dense operands (outside the input stages, so before the barrier), row c
+        // of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a}, K+ = K~q e^{r_a}, Khat
         const float er = __expf(r);
         const uint32_t rowoff = (uint32_t)c * 128u;
 #pragma unroll
@@ -554,6 +523,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           *reinterpret_cast<uint4*>(sm + OFF_KH + off) = make_uint4(
               pack_f16(kh[0], kh[1]), pack_f16(kh[2], kh[3]), pack_f16(kh[4], kh[5]),
               pack_f16(kh[6], kh[7]));
+        }
+        __syncthreads();  // every thread is done with the q / k / z stages
+        {
+          const uint32_t x = ((uint32_t)c & 31) >> 2;
+          unsigned char* gm = sm + G_M + (c >> 5) * kGMAtom + 2048 * a + (c & 3) * 4;
+          unsigned char* gn = sm + G_N + (c >> 5) * kGNAtom + 2048 * a + (c & 3) * 4;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
+            // M-side rows: Q~ at t, K~q at 64 + t
+            *reinterpret_cast<float*>(gm + off) = tf32f(qt[i]);
+            *reinterpret_cast<float*>(gm + 64 * 128 + off) = tf32f(kq[i]);
+            // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, rows ka_row(a') + t, by
+            // the chain K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80)
+            float v = kt[i];
+#pragma unroll
+            for (int ap = 0; ap < 4; ++ap) {
+              if (ap < a) continue;
+              if (ap > a) v *= ed[ap - 1];
+              *reinterpret_cast<float*>(gn + ka_row(ap) * 128 + off) = tf32f(v);
+            }
+          }
         }
       }
       fence_proxy_async_smem();
@@ -652,10 +643,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int g = lane >> 2, q4 = lane & 3;
         float* Akk = reinterpret_cast<float*>(sm + S_AKK);
         float* T = reinterpret_cast<float*>(sm + S_T32);
-        // Warps 0-11 invert; warps 12-15 meanwhile run the state products
+        // Warps 0-11 invert.  Meanwhile warps 12-15 run the state products
         // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
-        // K=128 key channels; they only need the entry state), convert Y^T to
-        // fp16 and decay S^T (fp32) by e^{G_C} ahead of this chunk's update.
+        // K=128 key channels; they only need the entry state) and convert Y^T to
+        // fp16, and warps 4-11, idle during the diagonal solves, decay S^T (fp32)
+        // by e^{G_C} ahead of this chunk's update.
         pend_mma2 = true;
         if (warp < 4) {
           if (lane < 16) {
@@ -673,7 +665,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
           }
-        } else if (warp >= 12) {
+        } else if (warp < 12) {
+          const float* dec = misc + M_DECAY;
+          const int c0 = 64 * ((warp - 4) >> 2);
+#pragma unroll 2
+          for (int col = c0; col < c0 + 64; col += 16) {
+            float v[16];
+            tmem_ld16(my_lane + TS32 + col, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
+              v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
+            }
+            tmem_st16(my_lane + TS32 + col, v);
+          }
+          tmem_st_wait();
+        } else {
           if (warp == 12 && lane == 0) {
             const uint32_t id_o = make_idesc_f16(128, kC, false, true);
 #pragma unroll
@@ -702,19 +710,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               }
               tmem_st8(my_lane + TY16 + (col >> 1), hp);
             }
-            const float* dec = misc + M_DECAY;
-#pragma unroll 2
-            for (int col = 0; col < kD; col += 16) {
-              float v[16];
-              tmem_ld16(my_lane + TS32 + col, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 16; i += 4) {
-                const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
-                v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
-              }
-              tmem_st16(my_lane + TS32 + col, v);
-            }
             tmem_st_wait();
           }
           ok = ok && okm;
@@ -737,7 +732,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const int bi = warp >> 1, nt = warp & 1;
               const int a = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
               const int b = bi < 3 ? bi : (bi < 5 ? bi - 3 : 0);
-              warp_tile_3tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
+              warp_tile_tf32(blk(T, 16 * a, 16 * a), Akk, 16 * a, 16 * b, 16, nt, T, 16 * a, 16 * b,
                               1.f, g, q4);
             }
             inv_sync();
@@ -745,12 +740,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (warp < 12) {
               const int nt = warp & 1;
               switch (warp >> 1) {
-                case 0: warp_tile_3tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
-                case 1: warp_tile_3tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
-                case 2: warp_tile_3tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
-                case 3: warp_tile_3tf32(blk(T, 16, 0), T, 0, 0, 16, nt, Afin, 16, 0, -1.f, g, q4); break;
-                case 4: warp_tile_3tf32(blk(T, 32, 16), T, 16, 16, 16, nt, Afin, 32, 16, -1.f, g, q4); break;
-                default: warp_tile_3tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
+                case 0: warp_tile_tf32(blk(T, 32, 16), T, 16, 0, 16, nt, T, 0, 32, 1.f, g, q4); break;
+                case 1: warp_tile_tf32(blk(T, 48, 32), T, 32, 16, 16, nt, T, 16, 48, 1.f, g, q4); break;
+                case 2: warp_tile_tf32(blk(T, 48, 16), T, 16, 0, 32, nt, T, 0, 48, 1.f, g, q4); break;
+                case 3: warp_tile_tf32(blk(T, 16, 0), T, 0, 0, 16, nt, Afin, 16, 0, -1.f, g, q4); break;
+                case 4: warp_tile_tf32(blk(T, 32, 16), T, 16, 16, 16, nt, Afin, 32, 16, -1.f, g, q4); break;
+                default: warp_tile_tf32(blk(T, 48, 32), T, 32, 32, 16, nt, Afin, 48, 32, -1.f, g, q4); break;
               }
             }
             inv_sync();
@@ -759,15 +754,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (warp < 6) {
               const int task = warp >> 1, nt = warp & 1;
               if (task == 0) {
-                warp_tile_3tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
+                warp_tile_tf32(blk(T, 48, 32), T, 0, 32, 16, nt, T, 32, 48, 1.f, g, q4);
               } else if (task == 1) {
                 auto xf = [T](int r, int k) { return T[r * kLS + 32 + k] - T[(32 + r) * kLS + k]; };
-                warp_tile_3tf32(xf, T, 0, 0, 16, nt, Afin, 32, 0, 1.f, g, q4);
+                warp_tile_tf32(xf, T, 0, 0, 16, nt, Afin, 32, 0, 1.f, g, q4);
               } else {
                 auto xf = [T](int r, int k) {
                   return T[(16 + r) * kLS + 48 + k] - T[(48 + r) * kLS + 16 + k];
                 };
-                warp_tile_3tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
+                warp_tile_tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
               }
             }
             inv_sync();
@@ -776,7 +771,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               auto xf = [T](int r, int k) {
                 return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
               };
-              warp_tile_3tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
+              warp_tile_tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
             }
           }
         }
