@@ -15,6 +15,7 @@ its own workload (seed = rank), no data-path collective: weak scaling.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -77,10 +78,128 @@ def weak_scaling_value(tokens_per_rank, world, seconds):
     return tokens_per_rank * world / seconds / 1e6
 
 
+# ------------------------------------------------------- measured traffic --
+
+# DRAM bytes of one prefill launch as counted by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), recorded under profiles/ together with a hash of
+# the sources the kernel is compiled from.  The record is used only while
+# those sources are unchanged, and only for the workload it was taken on.
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "kda_chunk_tc_dram_traffic_varlen.txt")
+KERNEL_SOURCES = ["linear_attention_layer_gb300/csrc/kda_chunk_tc.cu",
+                  "linear_attention_layer_gb300/csrc/tc_ptx.cuh",
+                  "linear_attention_layer_gb300/csrc/kda_common.cuh",
+                  "linear_attention_layer_gb300/csrc/kda_launch.h",
+                  "include/kda.h"]
+
+
+def kernel_sources_sha256():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """Bytes per launch from the record, or None if absent or stale."""
+    try:
+        rec = {}
+        with open(TRAFFIC_RECORD) as f:
+            for line in f:
+                line = line.strip()
+                if line and not line.startswith("#") and ":" in line:
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("workload") != workload or rec.get("sources_sha256") != kernel_sources_sha256():
+            return None
+        return int(rec["dram__bytes_read.sum"]) + int(rec["dram__bytes_write.sum"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- clocks --
 
+class NvmlClockSampler:
+    """SM clock, its maximum and the clock-event reasons, read through NVML
+    (read-only queries, libnvidia-ml from the driver) every `period` seconds
+    on a host thread while the timed region runs.  start() / stop() bracket
+    the region; summary() has the same keys as ClockSampler's."""
+    # nvmlClocksEventReason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_uuid, period=0.005):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.period = period
+        self.samples = []
+        self.thread = None
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.handle = ctypes.c_void_p()
+        if not gpu_uuid or lib.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(),
+                                                          ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle for this GPU")
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, 1, ctypes.byref(mx)) == 0 else None
+
+    def _read(self):
+        ct = self.ct
+        mhz, reasons = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(mhz)) != 0:
+            return None
+        bits = int(reasons.value) if self.reason_fn(self.handle, ct.byref(reasons)) == 0 else 0
+        return float(mhz.value), bits
+
+    def _loop(self):
+        import time
+        while not self.stop_flag.is_set():
+            v = self._read()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(self.period)
+
+    def start(self):
+        self.stop_flag = self.threading.Event()
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join()
+            self.thread = None
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml"}
+        reasons = set()
+        for _, bits in self.samples:
+            for bit, name in self.REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml"}
+
+
+def clock_sampler(gpu_uuid):
+    """NVML sampler when the driver's library answers, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(gpu_uuid)
+    except (OSError, AttributeError):
+        return ClockSampler(gpu_uuid)
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 50 ms while the timed region runs (fallback)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -90,9 +209,15 @@ class ClockSampler:
         self.lines = []
         self.gpu_id = gpu_id
 
+    def start(self):
+        self.__enter__()
+
+    def stop(self):
+        self.__exit__(None, None, None)
+
     def __enter__(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "50"]
         if self.gpu_id:
             cmd.insert(1, f"--id={self.gpu_id}")
         try:
@@ -128,9 +253,10 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvidia-smi"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -212,7 +338,7 @@ def event_time_ms(fn, stream):
     return a, b
 
 
-def bench_prefill(kda, p, steps, warmup, dist, device, split=False):
+def bench_prefill(kda, p, steps, warmup, dist, device, split=False, clk=None):
     import torch
     stream = torch.cuda.current_stream()
     out = torch.empty_like(p.v)
@@ -238,11 +364,15 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False):
     evs = []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
     t_start.record(stream)
     for _ in range(steps):
         evs.append(event_time_ms(step, stream))
     t_end.record(stream)
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
     barrier(dist)
     torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
@@ -253,7 +383,7 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False):
     return total_ms, per_launch
 
 
-def bench_decode(kda, d, steps, device):
+def bench_decode(kda, d, steps, device, clk=None):
     import torch
     stream = torch.cuda.current_stream()
     out = torch.empty_like(d.v[0])
@@ -263,11 +393,15 @@ def bench_decode(kda, d, steps, device):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
     a.record(stream)
     for t in range(steps):
         kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=out)
     b.record(stream)
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
     return a.elapsed_time(b)
 
 
@@ -358,9 +492,9 @@ def main():
             gpu_uuid = "GPU-" + gpu_uuid
     except Exception:
         gpu_uuid = None
-    with ClockSampler(gpu_uuid) as clk:
-        total_ms, per_launch = bench_prefill(kda, p, args.steps, args.warmup, dist, device,
-                                             split=args.split)
+    clk = clock_sampler(gpu_uuid)
+    total_ms, per_launch = bench_prefill(kda, p, args.steps, args.warmup, dist, device,
+                                         split=args.split, clk=clk)
     total_ms = max_over_ranks(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
     value = weak_scaling_value(T, world, total_ms / 1e3 / args.steps)
@@ -370,7 +504,8 @@ def main():
     achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
     hbm_peak = peaks["hbm_gbs"]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": None if args.split else measured_traffic(args.workload),
                 "kernel": "kda_chunk_fwd", "algorithmic_bytes_per_launch": alg_bytes,
                 "peak_source": f"{peak_src} hbm_gbs"}
     line = {
@@ -394,8 +529,8 @@ def main():
         p = None
         d = workloads.decode_workload(device=device, seed=rank, steps=args.decode_steps + 3)
         torch.cuda.synchronize()
-        with ClockSampler(gpu_uuid) as dclk:
-            dec_ms = bench_decode(kda, d, args.decode_steps, device)
+        dclk = clock_sampler(gpu_uuid)
+        dec_ms = bench_decode(kda, d, args.decode_steps, device, clk=dclk)
         per_step_ms = dec_ms / args.decode_steps
         Nq, Hq = d.meta["num_requests"], d.meta["num_heads"]
         dec_bytes = Nq * Hq * (2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256)
