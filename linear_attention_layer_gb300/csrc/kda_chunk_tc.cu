@@ -234,6 +234,26 @@ __device__ __forceinline__ void sync_tc() {
 
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < kF16Max; }
 
+// S^T (fp32 in TMEM, this warp's lane quadrant) <- S^T Diag(e^{G_C}) for
+// columns [c0, c0 + 16 * n16).
+__device__ __forceinline__ void decay_state_cols(uint32_t my_lane, const float* dec, int c0,
+                                                 int n16) {
+#pragma unroll 2
+  for (int k = 0; k < n16; ++k) {
+    const int col = c0 + 16 * k;
+    float v[16];
+    tmem_ld16(my_lane + TS32 + col, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
+      v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
+    }
+    tmem_st16(my_lane + TS32 + col, v);
+  }
+  tmem_st_wait();
+}
+
 // The end of a chunk, once its last products have landed in TMEM: O^T (lane
 // n = value channel, column t) to out[t0 + t][h][n] in bf16 for t < len, and
 // (conv_s) S^T fp32 -> fp16, the A operand of the next chunk's state products.
@@ -643,6 +663,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int g = lane >> 2, q4 = lane & 3;
         float* Akk = reinterpret_cast<float*>(sm + S_AKK);
         float* T = reinterpret_cast<float*>(sm + S_T32);
+        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal, for
+        // task k = (row 16 br + k / 8, columns 8 (k % 8) .. + 7) of block row br, once
+        // that block row of T is final
+        auto build_tp = [&](int br, int k) {
+          const int t = 16 * br + (k >> 3), j0 = (k & 7) * 8;
+          const int bj = j0 >> 4;
+          const float* src = (bj == br ? T : Akk) + t * kLS + j0;
+          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+          if (bj <= br) {
+            x0 = *reinterpret_cast<const float4*>(src);
+            x1 = *reinterpret_cast<const float4*>(src + 4);
+          }
+          const float4 b0 = *reinterpret_cast<const float4*>(misc + M_BETA + j0);
+          const float4 b1 = *reinterpret_cast<const float4*>(misc + M_BETA + j0 + 4);
+          const float v[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
+                              x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
+          st_row8_f16(sm + S_TP, t, j0, v);
+        };
         // Warps 0-11 invert.  Meanwhile warps 12-15 run the state products
         // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
         // K=128 key channels; they only need the entry state) and convert Y^T to
@@ -666,21 +704,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
           }
         } else if (warp < 12) {
-          const float* dec = misc + M_DECAY;
-          const int c0 = 64 * ((warp - 4) >> 2);
-#pragma unroll 2
-          for (int col = c0; col < c0 + 64; col += 16) {
-            float v[16];
-            tmem_ld16(my_lane + TS32 + col, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
-              v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
-            }
-            tmem_st16(my_lane + TS32 + col, v);
-          }
-          tmem_st_wait();
+          decay_state_cols(my_lane, misc + M_DECAY, 64 * ((warp - 4) >> 2), 4);
         } else {
           if (warp == 12 && lane == 0) {
             const uint32_t id_o = make_idesc_f16(128, kC, false, true);
@@ -764,6 +788,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 };
                 warp_tile_tf32(xf, T, 16, 16, 16, nt, Afin, 48, 16, 1.f, g, q4);
               }
+            } else if (warp >= 8) {
+              build_tp(0, tid - 256);  // T' block row 0 (T_00 is final)
             }
             inv_sync();
             // level D: T_30 = (N^2_30 - N_30 - N^3_30) T_00
@@ -772,27 +798,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 return T[r * kLS + 48 + k] - T[(48 + r) * kLS + k] - T[(32 + r) * kLS + 48 + k];
               };
               warp_tile_tf32(xf, T, 0, 0, 16, warp, Afin, 48, 0, 1.f, g, q4);
+            } else if (tid >= 64 && tid < 320) {
+              build_tp(1 + ((tid - 64) >> 7), (tid - 64) & 127);  // T' block rows 1, 2
             }
           }
         }
         __syncthreads();  // T, the final off-diagonal blocks and the side work are done
-        // T' (fp16, [t][j] rows) = T diag(beta), zero above the block diagonal;
-        // thread = (row t, 8 columns j0..j0+7 of one 16-column block)
-        {
-          const int t = tid >> 3, j0 = (tid & 7) * 8;
-          const int bt = t >> 4, bj = j0 >> 4;
-          const float* src = (bj == bt ? T : Akk) + t * kLS + j0;
-          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-          if (bj <= bt) {
-            x0 = *reinterpret_cast<const float4*>(src);
-            x1 = *reinterpret_cast<const float4*>(src + 4);
-          }
-          const float4 b0 = *reinterpret_cast<const float4*>(misc + M_BETA + j0);
-          const float4 b1 = *reinterpret_cast<const float4*>(misc + M_BETA + j0 + 4);
-          const float v[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
-                              x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
-          st_row8_f16(sm + S_TP, t, j0, v);
-        }
+        if (tid < 128) build_tp(3, tid);  // T' block row 3
       }
       fence_proxy_async_smem();
       tc_fence_before();
