@@ -32,6 +32,11 @@ METRIC = "KDA prefill Mtokens/s (H=32,d=128) & decode state-update HBM GB/s vs p
 UNIT = "Mtokens/s"
 PREFILL_BYTES_PER_HEAD_TOKEN = 3 * 256 + 512 + 4 + 256  # q,k,v bf16 + z fp32 + beta + o bf16
 STATE_BYTES = 128 * 128 * 4
+# Algorithmic GEMM FLOPs per head-token of the chunked form at chunk C, d = dk = dv:
+# five C x C x d products (the two Gram matrices, T'K+, T'V, PU) and three C x d x d
+# (WS, Q+S, Khat^T U) per C tokens = 10 C d + 6 d^2.
+CHUNK = 64
+FLOPS_PER_HEAD_TOKEN = 10 * CHUNK * 128 + 6 * 128 * 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -100,16 +105,35 @@ def kernel_sources_sha256():
     return h.hexdigest()
 
 
+def read_record(path):
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#") and ":" in line:
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    return rec
+
+
+TENSOR_RECORD = os.path.join(ROOT, "profiles", "kda_chunk_tc_tensor_pipe_prefill.txt")
+
+
+def measured_tensor_pipe():
+    """ncu tensor-pipe utilisation of the prefill kernel (busy SM), or None if stale."""
+    try:
+        rec = read_record(TENSOR_RECORD)
+        if rec.get("sources_sha256") != kernel_sources_sha256():
+            return None
+        return float(rec["sm__pipe_tensor_cycles_active_pct"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_traffic(workload):
     """Bytes per launch from the record, or None if absent or stale."""
     try:
-        rec = {}
-        with open(TRAFFIC_RECORD) as f:
-            for line in f:
-                line = line.strip()
-                if line and not line.startswith("#") and ":" in line:
-                    k, v = line.split(":", 1)
-                    rec[k.strip()] = v.strip()
+        rec = read_record(TRAFFIC_RECORD)
         if rec.get("workload") != workload or rec.get("sources_sha256") != kernel_sources_sha256():
             return None
         return int(rec["dram__bytes_read.sum"]) + int(rec["dram__bytes_write.sum"])
@@ -455,7 +479,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu")
+    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long")
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
                     help="pass scratch so that few long sequences are split across SMs")
@@ -508,6 +532,14 @@ def main():
                 "traffic": None if args.split else measured_traffic(args.workload),
                 "kernel": "kda_chunk_fwd", "algorithmic_bytes_per_launch": alg_bytes,
                 "peak_source": f"{peak_src} hbm_gbs"}
+    flops = T * H * FLOPS_PER_HEAD_TOKEN
+    tflops = flops / (launch_ms * 1e-3) / 1e12
+    tc_burst, tc_sust = peaks.get("bf16_tflops"), peaks.get("bf16_tflops_sustained")
+    tensor = {"algorithmic_tflops": round(tflops, 2), "flops_per_head_token": FLOPS_PER_HEAD_TOKEN,
+              "chunk": CHUNK,
+              "frac_of_bf16_burst": round(tflops / tc_burst, 4) if tc_burst else None,
+              "frac_of_bf16_sustained": round(tflops / tc_sust, 4) if tc_sust else None,
+              "ncu_tensor_pipe_util_pct": measured_tensor_pipe()}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -518,9 +550,41 @@ def main():
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "split_long_sequences": bool(args.split)},
         "roofline": roofline,
+        "head_tokens_per_s_M": round(weak_scaling_value(T * H, world, total_ms / 1e3 / args.steps), 2),
+        "tensor": tensor,
+        "roofline_fraction_max": round(max(achieved / hbm_peak,
+                                           tflops / tc_burst if tc_burst else 0.0), 4),
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
     }
+
+    # ---- the long single-sequence workload, split across SMs ----
+    if "long" not in skip and args.workload != "long":
+        del p
+        torch.cuda.empty_cache()
+        pl = workloads.prefill_workload("long", device=device, seed=rank)
+        torch.cuda.synchronize()
+        lclk = clock_sampler(gpu_uuid)
+        l_ms, l_launch = bench_prefill(kda, pl, args.steps, args.warmup, dist, device, split=True,
+                                       clk=lclk)
+        l_ms = max_over_ranks(l_ms, dist, device)
+        Tl, Hl = pl.total_tokens, pl.meta["num_heads"]
+        l_bytes = Tl * Hl * PREFILL_BYTES_PER_HEAD_TOKEN + 4 * (pl.num_seqs + 1) + \
+            pl.num_seqs * Hl * STATE_BYTES
+        l_launch_ms = statistics.mean(l_launch)
+        l_gbs = l_bytes / (l_launch_ms * 1e-3) / 1e9
+        line["long"] = {
+            "value": round(weak_scaling_value(Tl, world, l_ms / 1e3 / args.steps), 3), "unit": UNIT,
+            "ms_per_step": round(l_ms / args.steps, 4), "workload": workloads.DESCRIPTIONS["long"],
+            "split_long_sequences": True,
+            "roofline": {"bound": "hbm", "achieved": round(l_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(l_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_launch": l_bytes},
+            "clocks": lclk.summary(),
+            "gpu_launches": 3 * args.steps}  # per step: segment pass, state scan, final pass
+        del pl
+        torch.cuda.empty_cache()
+        p = None
 
     # ---- decode ----
     if "decode" not in skip:
