@@ -93,6 +93,25 @@ typedef struct {
    * the split; results are the same either way. */
   void* workspace;
   size_t workspace_bytes;
+  /* Optional per-head log-scale A of the gate, DEVICE [H] fp32: the gate is
+   * g = -5 sigmoid(e^{A_h} z) (blog.higcp.com "猜想：K3 可能是最适合 TPU 的
+   * MoE 架构", section "下界衰减"; A is a learnable per-head log-scale).  NULL
+   * means A = 0, i.e. g = -5 sigmoid(z), with any scale already folded into z.
+   * Read by every call that takes z. */
+  const float* a_log;
+  /* Optional state checkpoints of the prefill calls (kda_chunk_fwd,
+   * kda_recurrent_fwd, kda_chunk_fwd_noalloc): with checkpoint_every = E > 0
+   * (a multiple of 64), checkpoint j of sequence n (j = 1 .. floor(len_n / E))
+   * is the state after its first j E tokens, written fp32 [dk][dv] per head to
+   * checkpoints[(checkpoint_offsets[n] + j - 1) * H + h].  checkpoint_offsets
+   * is a DEVICE [N + 1] int32 exclusive prefix sum of floor(len_n / E); both
+   * buffers are the caller's.  E = 0 writes none (the pointers are ignored).
+   * The pages place such states at fixed token offsets so that a prefix can
+   * be resumed (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构",
+   * "三条容易被忽略的代价" (2): states kept at hash-block ends). */
+  float* checkpoints;
+  const int32_t* checkpoint_offsets;
+  int32_t checkpoint_every;
 } kda_desc_t;
 
 /*

@@ -21,6 +21,7 @@ import torch
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
+           "checkpoint_offsets",
            "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
@@ -50,7 +51,9 @@ class KdaDesc(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("io_dtype", ctypes.c_int32), ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("a_log", ctypes.c_void_p), ("checkpoints", ctypes.c_void_p),
+                ("checkpoint_offsets", ctypes.c_void_p), ("checkpoint_every", ctypes.c_int32)]
 
 
 _lib = None
@@ -123,9 +126,10 @@ def _io_code(dtype):
 
 
 def make_desc(num_seqs, total_tokens, num_heads, dk, dv, io_dtype, cu_seqlens_host=None,
-              workspace=None):
+              workspace=None, a_log=None):
     """Build the C descriptor.  Returns (desc, keepalive) -- keep both alive
-    for the duration of the call."""
+    for the duration of the call.  a_log: optional device fp32 [H] tensor, the
+    per-head gate log-scale (g = -5 sigmoid(e^{A_h} z))."""
     d = KdaDesc()
     d.num_seqs, d.total_tokens, d.num_heads = int(num_seqs), int(total_tokens), int(num_heads)
     d.dk, d.dv, d.io_dtype = int(dk), int(dv), int(io_dtype)
@@ -136,11 +140,24 @@ def make_desc(num_seqs, total_tokens, num_heads, dk, dv, io_dtype, cu_seqlens_ho
     if workspace is not None:
         d.workspace = ctypes.c_void_p(workspace.data_ptr())
         d.workspace_bytes = workspace.numel() * workspace.element_size()
+    if a_log is not None:
+        d.a_log = ctypes.c_void_p(a_log.data_ptr())
     return d, keep
 
 
+def checkpoint_offsets(cu_seqlens_host, every):
+    """Exclusive prefix sums of floor(len_n / every) over the sequences: where
+    each sequence's state checkpoints start (and, last, how many there are)."""
+    cu = [int(x) for x in cu_seqlens_host]
+    offs = [0]
+    for n in range(len(cu) - 1):
+        offs.append(offs[-1] + (cu[n + 1] - cu[n]) // every)
+    return offs
+
+
 def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state,
-             output_final_state, cu_seqlens_host, workspace, stream):
+             output_final_state, cu_seqlens_host, workspace, stream, a_log=None,
+             checkpoint_every=0, checkpoints=None):
     lib = load()
     if q.dim() != 3:
         raise ValueError("q must be [T_tot, H, dk]")
@@ -156,6 +173,8 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
     _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
     if initial_state is not None:
         _check_tensor("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
     if out is None:
         out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
     _check_tensor("out", out, q.dtype, (T, H, dv), dev)
@@ -163,7 +182,20 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     if final_state is not None:
         _check_tensor("final_state", final_state, torch.float32, (N, H, dk, dv), dev)
-    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace)
+    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
+    offs_dev = None
+    if checkpoint_every:
+        if cu_seqlens_host is None:
+            raise ValueError("checkpoint_every needs cu_seqlens_host (to place the checkpoints)")
+        offs = checkpoint_offsets(cu_seqlens_host, checkpoint_every)
+        if checkpoints is None:
+            checkpoints = torch.empty((offs[-1], H, dk, dv), dtype=torch.float32, device=dev)
+        _check_tensor("checkpoints", checkpoints, torch.float32, (offs[-1], H, dk, dv), dev)
+        offs_dev = torch.tensor(offs, dtype=torch.int32, device=dev)
+        desc.checkpoint_every = int(checkpoint_every)
+        desc.checkpoints = ctypes.c_void_p(checkpoints.data_ptr()) if offs[-1] else \
+            ctypes.c_void_p(offs_dev.data_ptr())  # any valid pointer when there are none
+        desc.checkpoint_offsets = ctypes.c_void_p(offs_dev.data_ptr())
     with torch.cuda.device(dev):
         st = getattr(lib, name)(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
                                 _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
@@ -171,12 +203,20 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
     del keep
     if st != KDA_OK:
         raise KDAError(st, name)
+    if checkpoint_every:
+        return out, final_state, checkpoints
     return out, final_state
 
 
 def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, final_state=None,
-              output_final_state=True, cu_seqlens_host=None, workspace=None, stream=None):
-    """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state).
+              output_final_state=True, cu_seqlens_host=None, workspace=None, stream=None,
+              a_log=None, checkpoint_every=0, checkpoints=None):
+    """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state), or
+    (out, final_state, checkpoints) when ``checkpoint_every`` > 0.
+    ``a_log``: optional fp32 [H] per-head gate log-scale A (g = -5 sigmoid(e^A z)).
+    ``checkpoint_every``: a multiple of 64; the state after every that many
+    tokens of each sequence, [sum_n floor(len_n / E), H, dk, dv] fp32 in
+    sequence order (``checkpoint_offsets`` gives where each sequence starts).
 
     ``workspace``: a device tensor of scratch (at least
     ``chunk_fwd_workspace_size`` bytes, 256-byte aligned) that lets long
@@ -192,26 +232,31 @@ def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, fin
             if nbytes:
                 workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     return _prefill("kda_chunk_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
-                    final_state, output_final_state, cu_seqlens_host, workspace, stream)
+                    final_state, output_final_state, cu_seqlens_host, workspace, stream, a_log,
+                    checkpoint_every, checkpoints)
 
 
 def recurrent_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
-                  final_state=None, output_final_state=True, cu_seqlens_host=None, stream=None):
-    """Token-by-token KDA prefill (``kda_recurrent_fwd``).  Returns (out, final_state)."""
+                  final_state=None, output_final_state=True, cu_seqlens_host=None, stream=None,
+                  a_log=None, checkpoint_every=0, checkpoints=None):
+    """Token-by-token KDA prefill (``kda_recurrent_fwd``).  Returns (out, final_state)
+    (and the checkpoints, as ``chunk_fwd``)."""
     return _prefill("kda_recurrent_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
-                    final_state, output_final_state, cu_seqlens_host, None, stream)
+                    final_state, output_final_state, cu_seqlens_host, None, stream, a_log,
+                    checkpoint_every, checkpoints)
 
 
 def chunk_fwd_noalloc(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
                       final_state=None, output_final_state=True, cu_seqlens_host=None,
-                      stream=None):
+                      stream=None, a_log=None, checkpoint_every=0, checkpoints=None):
     """``kda_chunk_fwd_noalloc``: the chunked prefill for callers that cannot
     allocate device memory; its scratch for splitting long sequences is an
     array inside the library (NOALLOC_SCRATCH_BYTES).  Pass ``out`` and
     ``final_state`` to keep this wrapper from allocating them with torch.
     Returns (out, final_state)."""
     return _prefill("kda_chunk_fwd_noalloc", q, k, v, z, beta, cu_seqlens, initial_state, out,
-                    final_state, output_final_state, cu_seqlens_host, None, stream)
+                    final_state, output_final_state, cu_seqlens_host, None, stream, a_log,
+                    checkpoint_every, checkpoints)
 
 
 def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, cu_seqlens_host):
@@ -226,10 +271,11 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, c
     return int(n.value)
 
 
-def decode_step(q, k, v, z, beta, state, *, out=None, stream=None):
+def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
     """One decode step (``kda_decode_step``); ``state`` is updated in place.
     q, k: [N, H, dk]; v: [N, H, dv]; z: [N, H, dk] fp32; beta: [N, H] fp32;
-    state: [N, H, dk, dv] fp32.  Returns out [N, H, dv]."""
+    state: [N, H, dk, dv] fp32; a_log: optional [H] fp32 gate log-scale.
+    Returns out [N, H, dv]."""
     lib = load()
     N, H, dk = q.shape
     dv = v.shape[-1]
@@ -243,7 +289,9 @@ def decode_step(q, k, v, z, beta, state, *, out=None, stream=None):
     if out is None:
         out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
     _check_tensor("out", out, q.dtype, (N, H, dv), dev)
-    desc, _ = make_desc(N, N, H, dk, dv, _io_code(q.dtype))
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    desc, _ = make_desc(N, N, H, dk, dv, _io_code(q.dtype), a_log=a_log)
     with torch.cuda.device(dev):
         st = lib.kda_decode_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
                                  _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream))

@@ -85,6 +85,13 @@ kda_status_t prefill_common(const kda_desc_t* desc, const void* q, const void* k
   a.cu_seqlens = cu_seqlens;
   a.out = out;
   a.final_state = final_state;
+  a.a_log = desc->a_log;
+  if (desc->checkpoint_every < 0 || desc->checkpoint_every % 64 != 0) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->checkpoint_every > 0 && (!desc->checkpoints || !desc->checkpoint_offsets))
+    return KDA_ERR_INVALID_ARGUMENT;
+  a.ckpt_every = desc->checkpoint_every;
+  a.ckpt = desc->checkpoint_every > 0 ? desc->checkpoints : nullptr;
+  a.ckpt_off = desc->checkpoint_every > 0 ? desc->checkpoint_offsets : nullptr;
   a.err = device_error_word();
   if (!a.err) return KDA_ERR_CUDA;
   return KDA_OK;
@@ -153,7 +160,7 @@ kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* 
   if (out && (out == q || out == k || out == v || out == (const void*)state))
     return KDA_ERR_INVALID_ARGUMENT;
   const kda::Problem p = to_problem(desc);
-  cudaError_t e = kda::launch_decode(p, q, k, v, z, beta, state, out, nullptr,
+  cudaError_t e = kda::launch_decode(p, q, k, v, z, beta, desc->a_log, state, out, nullptr,
                                      (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -50,7 +50,9 @@ __global__ void __launch_bounds__(2 * DV)
 chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const float* __restrict__ z, const float* __restrict__ beta,
                   const float* initial_state, const int32_t* __restrict__ cu, T* __restrict__ out,
-                  float* final_state, int H, int total, int* err) {
+                  float* final_state, int H, int total, int* err,
+                  const float* __restrict__ a_log, float* ckpt,
+                  const int32_t* __restrict__ ckpt_off, int ckpt_every) {
   constexpr int NT = 2 * DV;
   constexpr int NW = NT / 32;
   constexpr int RH = DK / 2;  // rows per thread
@@ -60,6 +62,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
   const int n = blockIdx.x / H, h = blockIdx.x % H;
   int bos, eos;
   if (!seq_range(cu, n, total, err, bos, eos)) return;
+  const float zscale = gate_scale(a_log, h);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int col = tid >> 1, half = tid & 1, row0 = half * RH;
 
@@ -80,7 +83,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         const size_t o = ((size_t)(c0 + t) * H + h) * DK + c;
         a = IO<T>::ld(q + o);
         b = IO<T>::ld(k + o);
-        g = log_decay(__ldg(z + o));
+        g = log_decay(zscale * __ldg(z + o));
       }
       sm.qp[t][c] = a;
       sm.kp[t][c] = b;
@@ -176,6 +179,12 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
       for (int t = 0; t < kC; ++t) x += sm.kh[t][row0 + i] * u[t];
       s[i] = x;
     }
+    if (ckpt && (c0 + len - bos) % ckpt_every == 0) {  // state after a multiple of ckpt_every tokens
+      const size_t j = (size_t)__ldg(ckpt_off + n) + (c0 + len - bos) / ckpt_every - 1;
+      float* dst = ckpt + (j * H + h) * DK * DV;
+#pragma unroll
+      for (int i = 0; i < RH; ++i) dst[(size_t)(row0 + i) * DV + col] = s[i];
+    }
   }
   if (final_state) {
 #pragma unroll
@@ -192,7 +201,8 @@ cudaError_t dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   kern<<<blocks, 2 * DV, smem, st>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta,
                                      a.initial_state, a.cu_seqlens, (T*)a.out, a.final_state,
-                                     p.num_heads, p.total_tokens, a.err);
+                                     p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt,
+                                     a.ckpt_off, a.ckpt_every);
   return cudaGetLastError();
 }
 

@@ -134,6 +134,10 @@ constexpr int kFlagZeroV = 1;
 
 struct Params {
   const float* beta;
+  const float* a_log;   // per-head gate log-scale [H], may be null
+  float* ckpt;          // state checkpoints (null: none)
+  const int32_t* ckpt_off;
+  int ckpt_every;
   const float* initial_state;
   const int32_t* cu;
   __nv_bfloat16* out;   // may be null (no output written)
@@ -254,6 +258,20 @@ __device__ __forceinline__ void decay_state_cols(uint32_t my_lane, const float* 
   tmem_st_wait();
 }
 
+// S^T (fp32 in TMEM; lane n = value channel n) to dst[c][n], a [dk][dv]
+// fp32 state; warp part cq covers key channels 32 cq .. 32 cq + 31.
+__device__ __forceinline__ void write_state(float* dst, uint32_t my_lane, int row, int cq) {
+  dst += row;
+#pragma unroll
+  for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
+    float v[16];
+    tmem_ld16(my_lane + TS32 + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dst[(size_t)(c0 + i) * kD] = v[i];
+  }
+}
+
 // The end of a chunk, once its last products have landed in TMEM: O^T (lane
 // n = value channel, column t) to out[t0 + t][h][n] in bf16 for t < len, and
 // (conv_s) S^T fp32 -> fp16, the A operand of the next chunk's state products.
@@ -347,6 +365,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       seq = e[0]; bos = e[1]; eos = e[2]; in_slot = e[3]; out_slot = e[4]; flags = e[5];
     }
     const bool zero_v = (flags & kFlagZeroV) != 0;
+    const int sbeg = P.mode == 0 ? bos : __ldg(P.cu + seq);  // start of the sequence
+    const float zcoef = gate_coef(gate_scale(P.a_log, h));  // -e^{A_h} log2(e)
     if (bos < 0 || eos < bos || eos > P.total) {
       if (tid == 0) report_error(P.err, kErrDeviceCheck);
       continue;
@@ -403,6 +423,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     bool pend_l = false;  // the previous chunk still has to write O and convert S^T
     int l_t0 = 0, l_len = 0;
+    long long l_ck = -1;  // its state checkpoint slot, if it ends one
     for (int ci = 0; ci < nchunks; ++ci) {
       const int t0 = bos + ci * kC;
       const int len = min(kC, eos - t0);
@@ -458,6 +479,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           pend_mma = false;
           tc_fence_after();
           finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, true, absmax);
+          if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
         }
         pend_l = false;
       }
@@ -473,7 +495,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < 16; ++i) G[i] = Z[(16 * a + i) * kD + c];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) G[i] = (16 * a + i < len) ? log_decay(G[i]) : 0.f;
+        for (int i = 0; i < 16; ++i) G[i] = (16 * a + i < len) ? log_decay_c(G[i], zcoef) : 0.f;
 #pragma unroll
         for (int i = 1; i < 16; ++i) G[i] += G[i - 1];
         misc[M_TOT + a * kD + c] = G[15];
@@ -875,6 +897,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_l = true;
       l_t0 = t0;
       l_len = len;
+      l_ck = -1;
+      if (P.ckpt && (t0 + len - sbeg) % P.ckpt_every == 0)
+        l_ck = (long long)__ldg(P.ckpt_off + seq) + (t0 + len - sbeg) / P.ckpt_every - 1;
     }
     if (aborted) break;
     if (pend_l) {
@@ -885,6 +910,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         pend_mma = false;
         tc_fence_after();
         finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, false, absmax);
+        if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
       }
       pend_l = false;
       tc_fence_before();
@@ -895,20 +921,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ---- final state: lane n holds column n ----
     float* dst = nullptr;
     if (out_slot == kSlotUser) {
-      if (P.final_state) dst = P.final_state + ((size_t)seq * H + h) * kD * kD + row;
+      if (P.final_state) dst = P.final_state + ((size_t)seq * H + h) * kD * kD;
     } else if (out_slot >= 0) {
-      dst = P.ws + ((size_t)out_slot * H + h) * kD * kD + row;
+      dst = P.ws + ((size_t)out_slot * H + h) * kD * kD;
     }
-    if (dst) {
-#pragma unroll
-      for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
-        float v[16];
-        tmem_ld16(my_lane + TS32 + c0, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dst[(size_t)(c0 + i) * kD] = v[i];
-      }
-    }
+    if (dst) write_state(dst, my_lane, row, cq);
     sync_tc();
   }
 
@@ -1184,6 +1201,10 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
 
   static thread_local Params prm;  // large: keep off the stack
   prm.beta = a.beta;
+  prm.a_log = a.a_log;
+  prm.ckpt = a.ckpt;
+  prm.ckpt_off = a.ckpt_off;
+  prm.ckpt_every = a.ckpt_every;
   prm.initial_state = a.initial_state;
   prm.cu = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16*>(a.out);
@@ -1250,6 +1271,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     }
   }
   prm.out = nullptr;
+  prm.ckpt = nullptr;  // pass 1 runs segments from stand-in entry states
   if (ne > 0) {
     prm.num_units = ne * p.num_heads;
     chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
@@ -1286,6 +1308,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     put(sgi[1], tb, te, plan.base[sgi[1]] + sgi[2], sgi[2] + 1 == sgi[3] ? kSlotUser : kSlotNone, 0);
   }
   prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.ckpt = a.ckpt;
   prm.num_units = ne * p.num_heads;
   chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
   return cudaGetLastError();

@@ -43,6 +43,25 @@ __device__ __forceinline__ float log_decay(float z) {
   return __fdividef(kGateMin, 1.0f + __expf(-z));
 }
 
+// e^{A_h}, the scale applied to z before the gate (1 when no A is given).
+__device__ __forceinline__ float gate_scale(const float* a_log, int h) {
+  return a_log ? expf(__ldg(a_log + h)) : 1.f;
+}
+
+// 2^x by the hardware's approximate base-2 exponential (ex2.approx.ftz).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The gate with the head's scale folded into one coefficient (e^x = 2^{x log2 e}):
+// g = kGateMin sigmoid(s z) = kGateMin / (1 + 2^{c z}), c = -s log2(e).
+__device__ __forceinline__ float gate_coef(float zscale) { return -zscale * 1.4426950408889634f; }
+__device__ __forceinline__ float log_decay_c(float z, float c) {
+  return __fdividef(kGateMin, 1.0f + ex2_approx(c * z));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

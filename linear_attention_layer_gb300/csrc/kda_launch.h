@@ -27,6 +27,10 @@ struct Args {
   void* out;
   float* final_state;  // may be null
   int* err;            // device error word
+  const float* a_log;  // per-head gate log-scale [H], may be null (A = 0)
+  float* ckpt;               // state checkpoints (null: none)
+  const int32_t* ckpt_off;   // device [N + 1] prefix sums of checkpoints per sequence
+  int ckpt_every;            // tokens between checkpoints (0: none)
 };
 
 // One work item of a chunked launch: a (sequence, head) pair, processed
@@ -39,8 +43,8 @@ struct WorkItem {
 
 // Decode: one token per (request, head), state updated in place.
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, float* state, void* out,
-                          int* err, cudaStream_t stream);
+                          const float* z, const float* beta, const float* a_log, float* state,
+                          void* out, int* err, cudaStream_t stream);
 
 // Token-by-token prefill over a packed batch.
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);

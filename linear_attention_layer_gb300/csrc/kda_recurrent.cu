@@ -45,7 +45,7 @@ struct RecSmem {
 // partial sums |q|^2, |k|^2, q.k per warp.
 template <int DK, int DV, typename T>
 __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, const T* kp,
-                                            const T* vp, const float* zp) {
+                                            const T* vp, const float* zp, float zscale) {
   const int tid = threadIdx.x;
   float qq = 0.f, kk = 0.f, kq = 0.f;
   if (tid < DK) {
@@ -53,7 +53,7 @@ __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, co
     const float b = IO<T>::ld(kp + tid);
     sm.qs[tid] = a;
     sm.ks[tid] = b;
-    sm.as[tid] = __expf(log_decay(__ldg(zp + tid)));
+    sm.as[tid] = __expf(log_decay(zscale * __ldg(zp + tid)));
     qq = a * a;
     kk = b * b;
     kq = a * b;
@@ -124,7 +124,8 @@ template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kNT, 2)
 decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
               const float* __restrict__ z, const float* __restrict__ beta,
-              float* __restrict__ state, T* __restrict__ out) {
+              const float* __restrict__ a_log, int H, float* __restrict__ state,
+              T* __restrict__ out) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const size_t unit = blockIdx.x;  // n * H + h
@@ -133,7 +134,8 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   float4 s[SH::R];
 #pragma unroll
   for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
-  stage_token<DK, DV, T>(sm, q + unit * DK, k + unit * DK, v + unit * DV, z + unit * DK);
+  stage_token<DK, DV, T>(sm, q + unit * DK, k + unit * DK, v + unit * DV, z + unit * DK,
+                         gate_scale(a_log, (int)(unit % H)));
   __syncthreads();
   apply_token<DK, DV, T>(sm, s, __ldg(beta + unit), out + unit * DV);
 #pragma unroll
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(kNT, 2)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const float* __restrict__ z, const float* __restrict__ beta,
                  const float* initial_state, const int32_t* __restrict__ cu, T* __restrict__ out,
-                 float* final_state, int H, int total, int* err) {
+                 float* final_state, int H, int total, int* err, const float* __restrict__ a_log,
+                 float* ckpt, const int32_t* __restrict__ ckpt_off, int ckpt_every) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -161,12 +164,19 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                        (size_t)(rg + i * SH::RG) * SH::TPR + c4)
                : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  const float zscale = gate_scale(a_log, h);
   for (int t = bos; t < eos; ++t) {
     const size_t th = (size_t)t * H + h;
     __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK);
+    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK, zscale);
     __syncthreads();
     apply_token<DK, DV, T>(sm, s, __ldg(beta + th), out + th * DV);
+    if (ckpt && (t + 1 - bos) % ckpt_every == 0) {  // state after a multiple of ckpt_every tokens
+      const size_t j = (size_t)__ldg(ckpt_off + n) + (t + 1 - bos) / ckpt_every - 1;
+      float4* dst = reinterpret_cast<float4*>(ckpt + (j * H + h) * DK * DV);
+#pragma unroll
+      for (int i = 0; i < SH::R; ++i) dst[(size_t)(rg + i * SH::RG) * SH::TPR + c4] = s[i];
+    }
   }
   if (final_state) {
 #pragma unroll
@@ -177,11 +187,11 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
 template <int DK, int DV, typename T>
 cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, const void* v,
-                            const float* z, const float* beta, float* state, void* out,
-                            cudaStream_t st) {
+                            const float* z, const float* beta, const float* a_log, float* state,
+                            void* out, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   decode_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
-      (const T*)q, (const T*)k, (const T*)v, z, beta, state, (T*)out);
+      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, state, (T*)out);
   return cudaGetLastError();
 }
 
@@ -190,7 +200,8 @@ cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st)
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   recurrent_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
       (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
-      (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err);
+      (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt, a.ckpt_off,
+      a.ckpt_every);
   return cudaGetLastError();
 }
 
@@ -213,12 +224,13 @@ cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st)
 }  // namespace
 
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, float* state, void* out,
-                          int* /*err*/, cudaStream_t st) {
+                          const float* z, const float* beta, const float* a_log, float* state,
+                          void* out, int* /*err*/, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
-    return p.io_bf16 ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, state, out, st)
-                     : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, state, out, st);
+    return p.io_bf16
+               ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, a_log, state, out, st)
+               : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, state, out, st);
   });
 }
 

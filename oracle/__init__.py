@@ -60,7 +60,7 @@ def _load():
             lib.kda_oracle_recurrent.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.POINTER(ctypes.c_int64), dp, dp, dp, dp, dp, dp, dp, dp,
-                ctypes.c_int, ctypes.c_double, ctypes.c_int]
+                ctypes.c_int, ctypes.c_double, ctypes.c_int, dp]
             lib.kda_oracle_log_decay.restype = ctypes.c_double
             lib.kda_oracle_log_decay.argtypes = [ctypes.c_double]
             lib.kda_oracle_l2norm.restype = None
@@ -113,12 +113,13 @@ def l2norm(x, eps: float = DEFAULT_EPS) -> np.ndarray:
 
 def recurrent(q, k, v, z, beta, cu_seqlens, initial_state=None, *,
               raw_log_decay: bool = False, eps: float = DEFAULT_EPS,
-              threads: int = 0, with_final_state: bool = True):
+              threads: int = 0, with_final_state: bool = True, a_log=None):
     """Per-token KDA recurrence over a packed variable-length batch.
 
     q, k: [T_tot, H, dk]; v: [T_tot, H, dv]; z: [T_tot, H, dk] gate logits
     (or raw log-decay g when ``raw_log_decay``); beta: [T_tot, H];
-    cu_seqlens: [N + 1] int; initial_state: [N, H, dk, dv] or None (zeros).
+    cu_seqlens: [N + 1] int; initial_state: [N, H, dk, dv] or None (zeros);
+    a_log: [H] per-head gate log-scale A (g = -5 sigmoid(e^A z)) or None (A = 0).
 
     Returns ``(out [T_tot, H, dv], final_state [N, H, dk, dv] or None,
     threads_used)``, all float64.
@@ -137,19 +138,22 @@ def recurrent(q, k, v, z, beta, cu_seqlens, initial_state=None, *,
     assert cu[0] == 0 and cu[-1] == T
     if s0 is not None:
         assert s0.shape == (N, H, dk, dv)
+    al = _f64(a_log)
+    if al is not None:
+        assert al.shape == (H,)
     out = np.zeros((T, H, dv), dtype=np.float64)
     fin = np.zeros((N, H, dk, dv), dtype=np.float64) if with_final_state else None
     used = lib.kda_oracle_recurrent(
         N, H, dk, dv, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(s0),
-        _ptr(out), _ptr(fin), 1 if raw_log_decay else 0, float(eps), int(threads))
+        _ptr(out), _ptr(fin), 1 if raw_log_decay else 0, float(eps), int(threads), _ptr(al))
     if used < 0:
         raise ValueError("kda_oracle_recurrent rejected its arguments")
     return out, fin, used
 
 
 def decode_step(q, k, v, z, beta, state, *, eps: float = DEFAULT_EPS,
-                threads: int = 0, raw_log_decay: bool = False):
+                threads: int = 0, raw_log_decay: bool = False, a_log=None):
     """One recurrent step for a batch of live requests.
 
     q, k: [N, H, dk]; v: [N, H, dv]; z: [N, H, dk]; beta: [N, H];
@@ -160,5 +164,5 @@ def decode_step(q, k, v, z, beta, state, *, eps: float = DEFAULT_EPS,
     N = int(q.shape[0])
     cu = np.arange(N + 1, dtype=np.int64)
     out, fin, _ = recurrent(q, k, v, z, beta, cu, state, eps=eps,
-                            threads=threads, raw_log_decay=raw_log_decay)
+                            threads=threads, raw_log_decay=raw_log_decay, a_log=a_log)
     return out, fin

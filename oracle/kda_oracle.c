@@ -10,8 +10,9 @@
  *
  *   Gate  (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构",
  *          section "下界衰减：一个纯粹为硬件让步的算法改动"):
- *       g = gmin * sigmoid(z),  alpha = exp(g),  gmin = -5,
- *       with the per-head scale e^A already folded into z by the caller.
+ *       g = gmin * sigmoid(e^{A_h} z),  alpha = exp(g),  gmin = -5,
+ *       with A the per-head log-scale (optional argument; A = 0 when absent,
+ *       i.e. any scale already folded into z by the caller).
  *
  *   Q/K preprocessing (mhpq.cn/news/56770, the paragraph on Q/K
  *   preprocessing after "KDA 到底在算什么"): q and k are L2-normalised
@@ -68,6 +69,7 @@ typedef struct {
   const double *q, *k, *v, *z, *beta, *initial_state;
   double *out, *final_state;
   int z_is_raw_log_decay;
+  const double* a_log;
   double eps;
   /* work distribution */
   int64_t next_task;
@@ -82,6 +84,7 @@ static void run_pair(job_t* J, int n, int h) {
   double* a = (double*)malloc(sizeof(double) * dk);
   double* e = (double*)malloc(sizeof(double) * dv);
   const size_t sidx = ((size_t)n * H + h) * dk * dv;
+  const double zscale = J->a_log ? exp(J->a_log[h]) : 1.0; /* e^{A_h} */
   if (J->initial_state)
     memcpy(S, J->initial_state + sidx, sizeof(double) * (size_t)dk * dv);
   else
@@ -93,7 +96,7 @@ static void run_pair(job_t* J, int n, int h) {
     kda_oracle_l2norm(J->k + th * dk, kh, dk, J->eps);
     for (int c = 0; c < dk; ++c) {
       const double zc = J->z[th * dk + c];
-      const double g = J->z_is_raw_log_decay ? zc : kda_oracle_log_decay(zc);
+      const double g = J->z_is_raw_log_decay ? zc : kda_oracle_log_decay(zscale * zc);
       a[c] = exp(g);
     }
     const double b = J->beta[th];
@@ -152,13 +155,15 @@ int kda_oracle_available_cpus(void) {
  * used, or -1 on a bad argument.  initial_state may be NULL (zeros);
  * final_state may be NULL (not written).  z holds logits (gate applied
  * here) unless z_is_raw_log_decay != 0, in which case it holds g itself.
+ * a_log ([num_heads], may be NULL = zeros) is the gate's per-head log-scale.
  */
 int kda_oracle_recurrent(int num_seqs, int num_heads, int dk, int dv,
                          const int64_t* cu_seqlens, const double* q,
                          const double* k, const double* v, const double* z,
                          const double* beta, const double* initial_state,
                          double* out, double* final_state,
-                         int z_is_raw_log_decay, double eps, int num_threads) {
+                         int z_is_raw_log_decay, double eps, int num_threads,
+                         const double* a_log) {
   if (num_seqs < 0 || num_heads <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens)
     return -1;
   for (int n = 0; n < num_seqs; ++n)
@@ -168,6 +173,7 @@ int kda_oracle_recurrent(int num_seqs, int num_heads, int dk, int dv,
   J.cu_seqlens = cu_seqlens; J.q = q; J.k = k; J.v = v; J.z = z;
   J.beta = beta; J.initial_state = initial_state; J.out = out;
   J.final_state = final_state; J.z_is_raw_log_decay = z_is_raw_log_decay;
+  J.a_log = a_log;
   J.eps = eps; J.next_task = 0;
   pthread_mutex_init(&J.lock, NULL);
   int nt = num_threads > 0 ? num_threads : kda_oracle_available_cpus();

@@ -40,12 +40,26 @@ def test_status_strings(lib):
     assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
 
 
-def test_descriptor_layout_matches_header():
-    # 6 x int32, then three pointer-sized fields (LP64)
-    assert ctypes.sizeof(kda.KdaDesc) == 48
-    assert kda.KdaDesc.cu_seqlens_host.offset == 24
-    assert kda.KdaDesc.workspace.offset == 32
-    assert kda.KdaDesc.workspace_bytes.offset == 40
+def test_descriptor_layout_matches_header(tmp_path):
+    """The ctypes mirror of kda_desc_t against the C header itself: a small C
+    program compiled here prints sizeof and every field's offsetof."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fields = [f[0] for f in kda.KdaDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"kda.h\"\n"
+                   "int main(void) {\n  printf(\"%zu\\n\", sizeof(kda_desc_t));\n" +
+                   "".join(f'  printf("%zu\\n", offsetof(kda_desc_t, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(root, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(kda.KdaDesc)
+    assert got[1:] == [getattr(kda.KdaDesc, f).offset for f in fields]
 
 
 FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
@@ -80,6 +94,26 @@ def test_prefill_rejects_null_and_aliasing(lib):
     assert _call_chunk(lib, desc, out=FAKE) == 1         # out aliases q
     assert lib.kda_chunk_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None,
                              None) == 1
+
+
+@pytest.mark.parametrize("fn", ["kda_chunk_fwd", "kda_recurrent_fwd", "kda_chunk_fwd_noalloc"])
+@pytest.mark.parametrize("every,ckpt,offs", [
+    (32, FAKE, FAKE),          # not a multiple of 64
+    (-64, FAKE, FAKE),         # negative
+    (64, None, FAKE),          # no checkpoint buffer
+    (64, FAKE, None),          # no offsets
+])
+def test_prefill_rejects_bad_checkpoint_arguments(lib, fn, every, ckpt, offs):
+    desc, keep = kda.make_desc(2, 8, 2, 64, 64, kda.KDA_BF16, [0, 3, 8])
+    desc.checkpoint_every = every
+    desc.checkpoints = ckpt
+    desc.checkpoint_offsets = offs
+    assert _call_chunk(lib, desc, fn=fn) == 1  # KDA_ERR_INVALID_ARGUMENT
+
+
+def test_checkpoint_offsets_count_whole_intervals():
+    # lengths 63, 1, 0, 266, 1024
+    assert kda.checkpoint_offsets([0, 63, 64, 64, 330, 1354], 64) == [0, 0, 0, 0, 4, 20]
 
 
 def test_decode_rejects_bad_arguments(lib):

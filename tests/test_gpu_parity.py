@@ -179,6 +179,106 @@ def test_decode_chain_equals_prefill():
     assert_close(S, fin, torch.bfloat16, "decode chain vs chunk state")
 
 
+# ------------------------------------------------- gate log-scale A -------
+
+@pytest.mark.parametrize("entry,dtype,dk,dv", [
+    ("chunk_fwd", torch.bfloat16, 128, 128),   # tensor-core kernel
+    ("chunk_fwd", torch.float32, 64, 32),      # CUDA-core chunked kernel
+    ("recurrent_fwd", torch.bfloat16, 128, 64),
+    ("chunk_fwd_noalloc", torch.bfloat16, 128, 128),
+])
+def test_gate_log_scale(entry, dtype, dk, dv):
+    """g = -5 sigmoid(e^{A_h} z) with a different A per head, against the oracle
+    given the same A."""
+    p = workloads.random_problem(RAGGED, 3, dk, dv, dtype, z_std=1.5, init_std=0.1, seed=11,
+                                 device=DEV)
+    A = torch.tensor([0.6, -1.2, 1.7], dtype=torch.float32)
+    out, fin = getattr(kda, entry)(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                   cu_seqlens_host=p.cu_seqlens_host, a_log=A.to(DEV))
+    torch.cuda.synchronize()
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state,
+                                 a_log=A)
+    assert_close(out, ro, dtype, "out")
+    assert_close(fin, rf, dtype, "final_state")
+    # and A really acts: without it the result moves well outside the tolerance
+    ro0, _, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state)
+    assert rel_l2(out, ro0) > 10 * rel_l2(out, ro)
+    assert kda.get_device_error() == 0
+
+
+def test_decode_gate_log_scale():
+    d = workloads.decode_workload(4, 3, 128, 128, steps=3, io_dtype=torch.bfloat16, device=DEV,
+                                  seed=4)
+    A = torch.tensor([-0.8, 0.3, 2.0], dtype=torch.float32)
+    S = d.state.clone()
+    s_ref = d.state.cpu()
+    for t in range(3):
+        o = kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], S, a_log=A.to(DEV))
+        torch.cuda.synchronize()
+        ro, s_ref = oracle.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], s_ref, a_log=A)
+        assert_close(o, ro, torch.bfloat16, f"decode out step {t}")
+    assert_close(S, s_ref, torch.bfloat16, "decode state")
+
+
+# ------------------------------------------------------ state checkpoints ---
+
+def _oracle_checkpoints(p, every):
+    """State after every `every` tokens of each sequence: the oracle's final
+    state of that prefix (from the sequence's initial state)."""
+    cu = p.cu_seqlens_host
+    H = p.meta["num_heads"]
+    res = []
+    for n in range(len(cu) - 1):
+        for j in range(1, (cu[n + 1] - cu[n]) // every + 1):
+            a, b = cu[n], cu[n] + j * every
+            s0 = None if p.initial_state is None else p.initial_state[n:n + 1].cpu()
+            _, fin, _ = oracle.recurrent(p.q[a:b].cpu(), p.k[a:b].cpu(), p.v[a:b].cpu(),
+                                         p.z[a:b].cpu(), p.beta[a:b].cpu(), [0, b - a], s0)
+            res.append(fin[0])
+    return np.stack(res) if res else np.zeros((0, H, p.meta["dk"], p.meta["dv"]))
+
+
+@pytest.mark.parametrize("entry,dtype,dk,dv", [
+    ("chunk_fwd", torch.bfloat16, 128, 128),   # tensor-core kernel
+    ("chunk_fwd", torch.float32, 64, 32),      # CUDA-core chunked kernel
+    ("recurrent_fwd", torch.float32, 32, 64),
+    ("chunk_fwd_noalloc", torch.bfloat16, 128, 128),
+])
+def test_state_checkpoints(entry, dtype, dk, dv):
+    lens = [64, 200, 0, 130, 256, 63, 512]
+    p = workloads.random_problem(lens, 2, dk, dv, dtype, z_std=1.0, init_std=0.1, seed=13,
+                                 device=DEV)
+    out, fin, ck = getattr(kda, entry)(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                       cu_seqlens_host=p.cu_seqlens_host, checkpoint_every=64)
+    torch.cuda.synchronize()
+    assert ck.shape[0] == sum(n // 64 for n in lens) == 18
+    ref = _oracle_checkpoints(p, 64)
+    assert_close(ck, ref, dtype, "checkpoints")
+    # the checkpoint that ends a sequence equals its final state
+    offs = kda.checkpoint_offsets(p.cu_seqlens_host, 64)
+    assert torch.equal(ck[offs[1] - 1], fin[0])   # sequence 0 has length 64
+    assert torch.equal(ck[offs[5] - 1], fin[4])   # sequence 4 has length 256
+    assert kda.get_device_error() == 0
+
+
+def test_state_checkpoints_with_split_sequences():
+    """Long sequences split across SMs (workspace): checkpoints come from the
+    final pass, which runs every segment from its true entry state."""
+    p = workloads.random_problem([3000, 1100], 2, 128, 128, torch.bfloat16, z_mean=-1.0,
+                                 init_std=0.1, seed=14, device=DEV)
+    assert kda.chunk_fwd_workspace_size(2, 4100, 2, 128, 128, torch.bfloat16,
+                                        p.cu_seqlens_host) > 0  # the split is taken
+    out, fin, ck = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                 cu_seqlens_host=p.cu_seqlens_host, workspace="auto",
+                                 checkpoint_every=256)
+    torch.cuda.synchronize()
+    assert ck.shape[0] == 3000 // 256 + 1100 // 256
+    ref = _oracle_checkpoints(p, 256)
+    for i in range(ck.shape[0]):
+        assert_close(ck[i], ref[i], torch.bfloat16, f"checkpoint {i}")
+    assert kda.get_device_error() == 0
+
+
 # ------------------------------------------------- full-size workloads -----
 
 def _sampled_prefill(name, pairs_fn, **kw):

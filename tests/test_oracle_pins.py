@@ -158,6 +158,39 @@ def test_beta_zero_decays_rows_by_product_of_alpha():
     assert np.allclose(STz, math.exp(-2.5 * (T - 1)) * S1z, rtol=1e-13, atol=0)
 
 
+def test_gate_log_scale_per_head():
+    """The gate's per-head log-scale A (blog.higcp.com "下界衰减": g = g_min
+    sigmoid(e^A z)): two heads with different A against the independent dense
+    form with alpha built here from e^{A_h} z.  Catches A applied to g instead
+    of z, A used without the exponential, the wrong head's A, or A ignored."""
+    rng = np.random.default_rng(21)
+    T, dk, dv = 6, 5, 3
+    A = np.array([0.7, -1.3])
+    q = rng.standard_normal((T, 2, dk))
+    k = rng.standard_normal((T, 2, dk))
+    v = rng.standard_normal((T, 2, dv))
+    z = rng.normal(0, 1.5, size=(T, 2, dk))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, 2))))
+    S0 = rng.normal(0, 0.5, size=(1, 2, dk, dv))
+    eps = 1e-6
+    out, fin, _ = oracle.recurrent(q, k, v, z, beta, np.array([0, T]), S0, eps=eps, a_log=A)
+    for h in range(2):
+        alpha = np.exp(-5.0 / (1.0 + np.exp(-math.exp(A[h]) * z[:, h])))
+        outs, states = dense_states(q[:, h], k[:, h], v[:, h], alpha, beta[:, h], S0[0, h], eps)
+        assert np.max(np.abs(out[:, h] - outs)) < 1e-12
+        assert np.max(np.abs(fin[0, h] - states[-1])) < 1e-12
+    # beta = 0 after one write: rows decay by prod alpha with alpha = e^{-5 sigmoid(e^A z)}
+    b0 = np.zeros((T, 2))
+    b0[0] = 1.0
+    _, f1, _ = oracle.recurrent(q[:1], k[:1], v[:1], z[:1], b0[:1], np.array([0, 1]), None,
+                                eps=0.0, a_log=A)
+    _, fT, _ = oracle.recurrent(q, k, v, z, b0, np.array([0, T]), None, eps=0.0, a_log=A)
+    for h in range(2):
+        g = -5.0 / (1.0 + np.exp(-math.exp(A[h]) * z[1:, h]))
+        assert np.allclose(fT[0, h], np.exp(g.sum(axis=0))[:, None] * f1[0, h], rtol=1e-13,
+                           atol=0)
+
+
 @pytest.mark.parametrize("T", [1, 2, 5, 8])
 def test_dense_product_form(T):
     """North-star check (4): the explicit sum of dense matrix products agrees
