@@ -523,7 +523,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const uint32_t x = ((uint32_t)c & 63) >> 3;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float F = __expf(G[i]), E = __fdividef(1.0f, F);
+            const float F = ex2_approx(G[i] * 1.4426950408889634f), E = ex2_approx(G[i] * -1.4426950408889634f);
             const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
             const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qk + off)) *
                             misc[M_RQ + 16 * a + i];
