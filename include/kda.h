@@ -181,6 +181,46 @@ kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* 
                              float* state, void* out, kda_stream_t stream);
 
 /*
+ * Speculative decoding without per-position state snapshots.  The pages
+ * (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构", section "三条容易被
+ * 忽略的代价" (1)) note that the in-place state update cannot be rolled back
+ * when verification rejects drafted tokens, that a snapshot per draft
+ * position would multiply state traffic, and that K3 instead keeps the
+ * window's inputs and replays the accepted tokens to rebuild the state.
+ *
+ * kda_decode_window -- outputs of W draft tokens per request from the
+ * committed states, which are read and NOT changed: token i of request b
+ * sees the state after the committed tokens and drafts 0 .. i.
+ *
+ *   desc               num_seqs = B requests, total_tokens = B * W
+ *   window             W >= 1 draft tokens per request
+ *   q, k               device, [B * W, H, dk] io dtype (request-major: row
+ *                      b * W + i is draft i of request b)
+ *   v                  device, [B * W, H, dv] io dtype
+ *   z                  device, [B * W, H, dk] fp32
+ *   beta               device, [B * W, H] fp32
+ *   state              device, [B, H, dk, dv] fp32, read only
+ *   out                device, [B * W, H, dv] io dtype, written
+ *
+ * kda_decode_replay -- after verification: applies the first accept_len[b]
+ * drafts of request b (0 .. W; the same cached inputs as the window call) to
+ * its state, which is written once (state traffic: one read and one write
+ * per step instead of one snapshot per draft position).  accept_len is a
+ * DEVICE [B] int32; a value outside 0 .. W leaves that request's state
+ * unchanged and sets the device error word (KDA_ERR_DEVICE_CHECK).
+ *
+ * Both honour desc->a_log; cu_seqlens_host, workspace and the checkpoint
+ * fields are ignored.  Host-side argument errors return
+ * KDA_ERR_INVALID_ARGUMENT and enqueue nothing.
+ */
+kda_status_t kda_decode_window(const kda_desc_t* desc, int32_t window, const void* q,
+                               const void* k, const void* v, const float* z, const float* beta,
+                               const float* state, void* out, kda_stream_t stream);
+kda_status_t kda_decode_replay(const kda_desc_t* desc, int32_t window, const void* q,
+                               const void* k, const void* v, const float* z, const float* beta,
+                               const int32_t* accept_len, float* state, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
  * device memory.  The pages describe no counterpart of this entry point.
  *

@@ -21,7 +21,7 @@ import torch
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
-           "checkpoint_offsets",
+           "checkpoint_offsets", "decode_window", "decode_replay",
            "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
@@ -33,7 +33,7 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
 
 #: Every function include/kda.h declares.
 EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
-                    "kda_decode_step", "kda_status_string", "kda_get_device_error",
+                    "kda_decode_step", "kda_decode_window", "kda_decode_replay", "kda_status_string", "kda_get_device_error",
                     "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
@@ -298,6 +298,60 @@ def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_step")
     return out
+
+
+def _window_args(q, k, v, z, beta, state):
+    """Shapes of a speculative-decoding window: q, k [B, W, H, dk]; v [B, W, H, dv];
+    z [B, W, H, dk] fp32; beta [B, W, H] fp32; state [B, H, dk, dv] fp32."""
+    B, W, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (B, W, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (B, W, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (B, W, H, dv), dev)
+    _check_tensor("z", z, torch.float32, (B, W, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (B, W, H), dev)
+    _check_tensor("state", state, torch.float32, (B, H, dk, dv), dev)
+    return B, W, H, dk, dv, dev
+
+
+def decode_window(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
+    """``kda_decode_window``: outputs [B, W, H, dv] of W draft tokens per request
+    from the committed ``state`` (not changed); draft i sees drafts 0..i."""
+    lib = load()
+    B, W, H, dk, dv, dev = _window_args(q, k, v, z, beta, state)
+    if out is None:
+        out = torch.empty((B, W, H, dv), dtype=q.dtype, device=dev)
+    _check_tensor("out", out, q.dtype, (B, W, H, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_window(ctypes.byref(desc), ctypes.c_int32(W), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(z), _ptr(beta), _ptr(state), _ptr(out),
+                                   _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_window")
+    return out
+
+
+def decode_replay(q, k, v, z, beta, accept_len, state, *, stream=None, a_log=None):
+    """``kda_decode_replay``: apply the first accept_len[b] drafts of the cached
+    window to each request's ``state`` (in place).  accept_len: int32 [B] on
+    the device."""
+    lib = load()
+    B, W, H, dk, dv, dev = _window_args(q, k, v, z, beta, state)
+    _check_tensor("accept_len", accept_len, torch.int32, (B,), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_replay(ctypes.byref(desc), ctypes.c_int32(W), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(z), _ptr(beta), _ptr(accept_len), _ptr(state),
+                                   _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_replay")
+    return state
 
 
 def get_device_error(stream=None) -> int:

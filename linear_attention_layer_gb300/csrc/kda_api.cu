@@ -165,6 +165,52 @@ kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* 
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+namespace {
+kda_status_t check_window(const kda_desc_t* desc, int32_t window, const void* q, const void* k,
+                          const void* v, const float* z, const float* beta, const void* state) {
+  if (!desc) return KDA_ERR_INVALID_ARGUMENT;
+  kda_desc_t d = *desc;
+  d.cu_seqlens_host = nullptr;  // not used by the window calls
+  kda_status_t s = check_desc(&d, false);
+  if (s != KDA_OK) return s;
+  if (window < 1 || (int64_t)desc->num_seqs * window != desc->total_tokens)
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->num_seqs > 0 && (!q || !k || !v || !z || !beta || !state))
+    return KDA_ERR_INVALID_ARGUMENT;
+  return KDA_OK;
+}
+}  // namespace
+
+kda_status_t kda_decode_window(const kda_desc_t* desc, int32_t window, const void* q,
+                               const void* k, const void* v, const float* z, const float* beta,
+                               const float* state, void* out, kda_stream_t stream) {
+  kda_status_t s = check_window(desc, window, q, k, v, z, beta, state);
+  if (s != KDA_OK) return s;
+  if (desc->num_seqs > 0 && !out) return KDA_ERR_INVALID_ARGUMENT;
+  if (out && (out == q || out == k || out == v || out == (const void*)state ||
+              out == (const void*)z || out == (const void*)beta))
+    return KDA_ERR_INVALID_ARGUMENT;
+  int* err = device_error_word();
+  if (!err) return KDA_ERR_CUDA;
+  cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
+                                     const_cast<float*>(state), out, nullptr, err,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_replay(const kda_desc_t* desc, int32_t window, const void* q,
+                               const void* k, const void* v, const float* z, const float* beta,
+                               const int32_t* accept_len, float* state, kda_stream_t stream) {
+  kda_status_t s = check_window(desc, window, q, k, v, z, beta, state);
+  if (s != KDA_OK) return s;
+  if (desc->num_seqs > 0 && !accept_len) return KDA_ERR_INVALID_ARGUMENT;
+  int* err = device_error_word();
+  if (!err) return KDA_ERR_CUDA;
+  cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
+                                     state, nullptr, accept_len, err, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_status_string(kda_status_t status) {
   switch (status) {
     case KDA_OK: return "KDA_OK";

@@ -142,6 +142,50 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
 }
 
+// Speculative decoding.  One CTA per (request, head); the window's draft
+// tokens of request b are rows [b*W, b*W + W) of the [B*W, H, .] inputs.
+// window (replay == 0): outputs of all W tokens from the committed state,
+// which is read and left as it is.  replay (replay != 0): the first
+// accept[b] tokens (0 <= accept[b] <= W) are applied again and the state is
+// written once, without outputs.
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kNT, 2)
+window_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+              const float* __restrict__ z, const float* __restrict__ beta,
+              const float* __restrict__ a_log, int H, int W, float* __restrict__ state,
+              T* __restrict__ out, const int32_t* __restrict__ accept, int replay, int* err) {
+  using SH = RecShape<DK, DV>;
+  __shared__ __align__(16) RecSmem<DK, DV> sm;
+  const size_t unit = blockIdx.x;  // b * H + h
+  const int b = (int)(unit / H), h = (int)(unit % H);
+  int ntok = W;
+  if (replay) {
+    ntok = __ldg(accept + b);
+    if (ntok < 0 || ntok > W) {  // bad acceptance length: leave this state alone
+      if (threadIdx.x == 0) report_error(err, kErrDeviceCheck);
+      return;
+    }
+    if (ntok == 0) return;
+  }
+  const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
+  float4* S = reinterpret_cast<float4*>(state + unit * DK * DV);
+  float4 s[SH::R];
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
+  const float zscale = gate_scale(a_log, h);
+  for (int t = 0; t < ntok; ++t) {
+    const size_t th = ((size_t)b * W + t) * H + h;
+    __syncthreads();  // previous token finished reading shared memory
+    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK, zscale);
+    __syncthreads();
+    apply_token<DK, DV, T>(sm, s, __ldg(beta + th), replay ? nullptr : out + th * DV);
+  }
+  if (replay) {
+#pragma unroll
+    for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
+  }
+}
+
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kNT, 2)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
@@ -196,6 +240,17 @@ cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, cons
 }
 
 template <int DK, int DV, typename T>
+cudaError_t window_dispatch(const Problem& p, int W, const void* q, const void* k, const void* v,
+                            const float* z, const float* beta, const float* a_log, float* state,
+                            void* out, const int32_t* accept, int* err, cudaStream_t st) {
+  const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
+      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, W, state, (T*)out,
+      accept, accept ? 1 : 0, err);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename T>
 cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   recurrent_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
@@ -231,6 +286,18 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
     return p.io_bf16
                ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, a_log, state, out, st)
                : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, state, out, st);
+  });
+}
+
+cudaError_t launch_window(const Problem& p, int W, const void* q, const void* k, const void* v,
+                          const float* z, const float* beta, const float* a_log, float* state,
+                          void* out, const int32_t* accept, int* err, cudaStream_t st) {
+  if (p.num_seqs == 0 || W == 0) return cudaSuccess;
+  return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
+    return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, W, q, k, v, z, beta, a_log, state,
+                                                              out, accept, err, st)
+                     : window_dispatch<DK, DV, float>(p, W, q, k, v, z, beta, a_log, state, out,
+                                                      accept, err, st);
   });
 }
 

@@ -129,6 +129,26 @@ def test_decode_rejects_bad_arguments(lib):
     assert f(ctypes.byref(d3), FAKE, FAKE, FAKE, FAKE, FAKE, st, out, None) == 1
 
 
+@pytest.mark.parametrize("window,total,null_q", [(0, 0, False), (2, 7, False), (2, 8, True)])
+def test_window_calls_reject_bad_arguments(lib, window, total, null_q):
+    d, _ = kda.make_desc(4, total, 2, 128, 128, kda.KDA_BF16)
+    q = None if null_q else FAKE
+    assert lib.kda_decode_window(ctypes.byref(d), window, q, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 ctypes.c_void_p(0x2000), None) == 1
+    assert lib.kda_decode_replay(ctypes.byref(d), window, q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 None) == 1
+
+
+def test_window_rejects_missing_out_and_replay_missing_accept(lib):
+    d, _ = kda.make_desc(4, 8, 2, 128, 128, kda.KDA_BF16)
+    assert lib.kda_decode_window(ctypes.byref(d), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                 None) == 1
+    assert lib.kda_decode_window(ctypes.byref(d), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 None) == 1  # out aliases q
+    assert lib.kda_decode_replay(ctypes.byref(d), 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                 None) == 1
+
+
 def test_workspace_size_query(lib):
     d, keep = kda.make_desc(1, 65536, 32, 128, 128, kda.KDA_BF16, [0, 65536])
     n = ctypes.c_size_t(123)

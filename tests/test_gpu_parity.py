@@ -220,6 +220,106 @@ def test_decode_gate_log_scale():
     assert_close(S, s_ref, torch.bfloat16, "decode state")
 
 
+# ------------------------------------------------ speculative decoding -----
+
+def _window_inputs(B, W, H, dk, dv, dtype, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    f32 = dict(dtype=torch.float32, device=DEV, generator=g)
+    unit = lambda x: x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+    q = unit(torch.randn((B, W, H, dk), **f32)).to(dtype)
+    k = unit(torch.randn((B, W, H, dk), **f32)).to(dtype)
+    v = torch.randn((B, W, H, dv), **f32).to(dtype)
+    z = torch.randn((B, W, H, dk), **f32)
+    beta = torch.sigmoid(torch.randn((B, W, H), **f32))
+    state = torch.randn((B, H, dk, dv), **f32) * 0.1
+    return q, k, v, z, beta, state
+
+
+def _oracle_window(q, k, v, z, beta, state, ntok, a_log=None):
+    """Per request b: its first ntok[b] drafts as a sequence from state[b]."""
+    B, W = q.shape[:2]
+    outs, fins = [], []
+    for b in range(B):
+        n = int(ntok[b])
+        o, f, _ = oracle.recurrent(q[b, :n].cpu(), k[b, :n].cpu(), v[b, :n].cpu(),
+                                   z[b, :n].cpu(), beta[b, :n].cpu(), [0, n],
+                                   state[b:b + 1].cpu(), a_log=a_log)
+        outs.append(o)
+        fins.append(f[0])
+    return outs, np.stack(fins)
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 32)])
+def test_decode_window_outputs_and_state_untouched(dtype, dk, dv):
+    B, W, H = 5, 4, 3
+    q, k, v, z, beta, state = _window_inputs(B, W, H, dk, dv, dtype, 21)
+    A = torch.tensor([0.3, -0.5, 1.0])
+    before = state.clone()
+    out = kda.decode_window(q, k, v, z, beta, state, a_log=A.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(state, before)
+    ref, _ = _oracle_window(q, k, v, z, beta, before, [W] * B, a_log=A)
+    assert_close(out, np.stack(ref), dtype, "window outputs")
+    assert kda.get_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_replay_applies_accepted_prefix(dtype):
+    B, W, H, dk, dv = 6, 5, 2, 128, 64
+    q, k, v, z, beta, state = _window_inputs(B, W, H, dk, dv, dtype, 22)
+    acc = [0, 5, 1, 3, 2, 4]
+    before = state.clone()
+    kda.decode_replay(q, k, v, z, beta, torch.tensor(acc, dtype=torch.int32, device=DEV), state)
+    torch.cuda.synchronize()
+    _, ref = _oracle_window(q, k, v, z, beta, before, acc)
+    assert torch.equal(state[0], before[0])   # nothing accepted: state untouched
+    assert_close(state, ref, dtype, "replayed states")
+    assert kda.get_device_error() == 0
+
+
+def test_draft_verify_replay_loop_equals_prefill_of_accepted_tokens():
+    """Three rounds of window + replay; the final states equal a prefill over
+    the accepted tokens only, and every window output the oracle's."""
+    B, W, H, dk, dv = 4, 4, 2, 128, 128
+    torch.manual_seed(0)
+    state = torch.randn((B, H, dk, dv), device=DEV) * 0.1
+    s0 = state.clone()
+    accepted = [[] for _ in range(B)]
+    rng = np.random.default_rng(5)
+    for r in range(3):
+        q, k, v, z, beta, _ = _window_inputs(B, W, H, dk, dv, torch.bfloat16, 30 + r)
+        out = kda.decode_window(q, k, v, z, beta, state)
+        ref, _ = _oracle_window(q, k, v, z, beta, state, [W] * B)
+        assert_close(out, np.stack(ref), torch.bfloat16, f"round {r} outputs")
+        acc = rng.integers(0, W + 1, size=B)
+        kda.decode_replay(q, k, v, z, beta, torch.tensor(acc, dtype=torch.int32, device=DEV),
+                          state)
+        for b in range(B):
+            accepted[b] += [(q[b, i], k[b, i], v[b, i], z[b, i], beta[b, i]) for i in range(acc[b])]
+    torch.cuda.synchronize()
+    for b in range(B):
+        n = len(accepted[b])
+        if n == 0:
+            assert torch.equal(state[b], s0[b])
+            continue
+        cols = [torch.stack([t[j] for t in accepted[b]]).cpu() for j in range(5)]
+        _, fin, _ = oracle.recurrent(*cols, [0, n], s0[b:b + 1].cpu())
+        assert_close(state[b], fin[0], torch.bfloat16, f"request {b} after {n} accepted")
+
+
+def test_decode_replay_bad_accept_length_sets_error_and_keeps_state():
+    B, W, H = 3, 2, 2
+    q, k, v, z, beta, state = _window_inputs(B, W, H, 64, 64, torch.float32, 23)
+    before = state.clone()
+    kda.decode_replay(q, k, v, z, beta, torch.tensor([1, 3, -1], dtype=torch.int32, device=DEV),
+                      state)
+    assert kda.get_device_error() == 5  # KDA_ERR_DEVICE_CHECK
+    assert torch.equal(state[1], before[1]) and torch.equal(state[2], before[2])
+    assert not torch.equal(state[0], before[0])
+    assert kda.get_device_error() == 0
+
+
 # ------------------------------------------------------ state checkpoints ---
 
 def _oracle_checkpoints(p, every):
