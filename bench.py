@@ -407,6 +407,49 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False, clk=None):
     return total_ms, per_launch
 
 
+def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
+    """Speculative decoding: per step a window of W drafts per request
+    (kda_decode_window) and the replay of its accepted prefix
+    (kda_decode_replay).  Acceptance lengths are drawn U{0..W} (seeded).
+    Returns (ms per step, accepted tokens per step)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    f32 = dict(dtype=torch.float32, device=device, generator=g)
+    unit = lambda x: x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+    q = unit(torch.randn((B, W, H, 128), **f32)).to(torch.bfloat16)
+    k = unit(torch.randn((B, W, H, 128), **f32)).to(torch.bfloat16)
+    v = torch.randn((B, W, H, 128), **f32).to(torch.bfloat16)
+    z = torch.randn((B, W, H, 128), **f32)
+    beta = torch.sigmoid(torch.randn((B, W, H), **f32))
+    state = torch.randn((B, H, 128, 128), **f32) * 0.1
+    out = torch.empty((B, W, H, 128), dtype=torch.bfloat16, device=device)
+    acc = torch.randint(0, W + 1, (steps + 3, B), generator=g, device=device, dtype=torch.int32)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kda.decode_window(q, k, v, z, beta, state, out=out)
+        kda.decode_replay(q, k, v, z, beta, acc[i], state)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
+    a.record(stream)
+    for i in range(steps):
+        step(3 + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
+    if kda.get_device_error() != 0:
+        raise RuntimeError("device error word set after the speculative-decoding steps")
+    return a.elapsed_time(b) / steps, float(acc[3:].sum().item()) / steps
+
+
 def bench_decode(kda, d, steps, device, clk=None):
     import torch
     stream = torch.cuda.current_stream()
@@ -479,7 +522,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long")
+    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long,spec")
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
                     help="pass scratch so that few long sequences are split across SMs")
@@ -609,6 +652,26 @@ def main():
             "clocks": dclk.summary(), "gpu_launches": args.decode_steps}
         del d
         torch.cuda.empty_cache()
+
+    # ---- speculative decoding: window of drafts + replay of the accepted prefix ----
+    if "spec" not in skip:
+        Bs, Hs, Ws, ns = 256, 32, 4, 200
+        sclk = clock_sampler(gpu_uuid)
+        s_ms, s_acc = bench_spec_decode(kda, Bs, Hs, Ws, ns, device, seed=rank, clk=sclk)
+        # per (request, head): the state read by the window and read + written by
+        # the replay; the W drafts' inputs (q, k, v bf16, z fp32, beta) and outputs;
+        # the accepted drafts' inputs again in the replay
+        tok_in = 3 * 256 + 512 + 4
+        s_bytes = int(Bs * Hs * (3 * STATE_BYTES + Ws * (tok_in + 256)) + s_acc * Hs * tok_in)
+        s_gbs = s_bytes / (s_ms * 1e-3) / 1e9
+        line["spec_decode"] = {
+            "value": round(s_acc * Hs / (s_ms * 1e-3) / 1e6, 3), "unit": "M accepted head-tokens/s",
+            "ms_per_step": round(s_ms, 5), "window": Ws, "accepted_tokens_per_step": s_acc,
+            "workload": f"{Bs} requests x H={Hs}, dk=dv=128, window {Ws}, acceptance U{{0..{Ws}}}",
+            "roofline": {"bound": "hbm", "achieved": round(s_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(s_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_step": s_bytes},
+            "clocks": sclk.summary(), "gpu_launches": 2 * ns}
 
     # ---- end to end through host buffers ----
     if "e2e" not in skip:
