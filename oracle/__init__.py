@@ -61,6 +61,10 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.POINTER(ctypes.c_int64), dp, dp, dp, dp, dp, dp, dp, dp,
                 ctypes.c_int, ctypes.c_double, ctypes.c_int, dp]
+            lib.kda_oracle_backward.restype = ctypes.c_int
+            lib.kda_oracle_backward.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(ctypes.c_int64)] + [dp] * 15 + [ctypes.c_double, ctypes.c_int]
             lib.kda_oracle_log_decay.restype = ctypes.c_double
             lib.kda_oracle_log_decay.argtypes = [ctypes.c_double]
             lib.kda_oracle_l2norm.restype = None
@@ -150,6 +154,34 @@ def recurrent(q, k, v, z, beta, cu_seqlens, initial_state=None, *,
     if used < 0:
         raise ValueError("kda_oracle_recurrent rejected its arguments")
     return out, fin, used
+
+
+def backward(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=None, *,
+             a_log=None, eps: float = DEFAULT_EPS, threads: int = 0):
+    """Reverse mode of ``recurrent``: given dL/d out [T_tot, H, dv] and dL/d
+    final_state [N, H, dk, dv] (or None = 0), the gradients
+    ``(dq, dk, dv, dz, dbeta, d_initial_state)`` in float64 (dz with respect
+    to the gate logits z; d_initial_state also when no initial state was given).
+    """
+    lib = _load()
+    q, k, v, z, beta, do = (_f64(a) for a in (q, k, v, z, beta, d_out))
+    s0, dfin, al = _f64(initial_state), _f64(d_final), _f64(a_log)
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+        dtype=np.int64))
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu.shape[0] - 1
+    assert do.shape == (T, H, dv)
+    outs = [np.zeros((T, H, dk)), np.zeros((T, H, dk)), np.zeros((T, H, dv)),
+            np.zeros((T, H, dk)), np.zeros((T, H)), np.zeros((N, H, dk, dv))]
+    used = lib.kda_oracle_backward(
+        N, H, dk, dv, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(s0), _ptr(al), _ptr(do),
+        _ptr(dfin), *[_ptr(o) for o in outs], float(eps), int(threads))
+    if used < 0:
+        raise ValueError("kda_oracle_backward rejected its arguments")
+    return tuple(outs)
 
 
 def decode_step(q, k, v, z, beta, state, *, eps: float = DEFAULT_EPS,
