@@ -112,6 +112,13 @@ typedef struct {
   float* checkpoints;
   const int32_t* checkpoint_offsets;
   int32_t checkpoint_every;
+  /* 0: one gate logit per key channel, z [T_tot, H, dk] (KDA).  1: one per
+   * head, z [T_tot, H] (decode: [N, H]), the same retention for every row of
+   * S -- the scalar-alpha case, which the pages identify with Gated DeltaNet
+   * (mhpq.cn/news/56770, section "KDA 到底在算什么": Gated DeltaNet has one
+   * scalar alpha_t per token where KDA has one per key channel).  Every call
+   * that takes z honours it. */
+  int32_t gate_per_head;
 } kda_desc_t;
 
 /*

@@ -53,7 +53,8 @@ class KdaDesc(ctypes.Structure):
                 ("io_dtype", ctypes.c_int32), ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("a_log", ctypes.c_void_p), ("checkpoints", ctypes.c_void_p),
-                ("checkpoint_offsets", ctypes.c_void_p), ("checkpoint_every", ctypes.c_int32)]
+                ("checkpoint_offsets", ctypes.c_void_p), ("checkpoint_every", ctypes.c_int32),
+                ("gate_per_head", ctypes.c_int32)]
 
 
 _lib = None
@@ -168,7 +169,8 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
     _check_tensor("q", q, q.dtype, (T, H, dk), dev)
     _check_tensor("k", k, q.dtype, (T, H, dk), dev)
     _check_tensor("v", v, q.dtype, (T, H, dv), dev)
-    _check_tensor("z", z, torch.float32, (T, H, dk), dev)
+    per_head = z.dim() == 2  # [T, H]: one gate per head (scalar alpha)
+    _check_tensor("z", z, torch.float32, (T, H) if per_head else (T, H, dk), dev)
     _check_tensor("beta", beta, torch.float32, (T, H), dev)
     _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
     if initial_state is not None:
@@ -183,6 +185,7 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
     if final_state is not None:
         _check_tensor("final_state", final_state, torch.float32, (N, H, dk, dv), dev)
     desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
+    desc.gate_per_head = 1 if per_head else 0
     offs_dev = None
     if checkpoint_every:
         if cu_seqlens_host is None:
@@ -213,6 +216,8 @@ def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, fin
               a_log=None, checkpoint_every=0, checkpoints=None):
     """Chunked KDA prefill (``kda_chunk_fwd``).  Returns (out, final_state), or
     (out, final_state, checkpoints) when ``checkpoint_every`` > 0.
+    ``z``: [T, H, dk] gate logits (one per key channel), or [T, H] for one gate
+    per head (the scalar-alpha, Gated DeltaNet case).
     ``a_log``: optional fp32 [H] per-head gate log-scale A (g = -5 sigmoid(e^A z)).
     ``checkpoint_every``: a multiple of 64; the state after every that many
     tokens of each sequence, [sum_n floor(len_n / E), H, dk, dv] fp32 in
@@ -283,7 +288,8 @@ def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
     _check_tensor("q", q, q.dtype, (N, H, dk), dev)
     _check_tensor("k", k, q.dtype, (N, H, dk), dev)
     _check_tensor("v", v, q.dtype, (N, H, dv), dev)
-    _check_tensor("z", z, torch.float32, (N, H, dk), dev)
+    per_head = z.dim() == 2  # [N, H]: one gate per head
+    _check_tensor("z", z, torch.float32, (N, H) if per_head else (N, H, dk), dev)
     _check_tensor("beta", beta, torch.float32, (N, H), dev)
     _check_tensor("state", state, torch.float32, (N, H, dk, dv), dev)
     if out is None:
@@ -292,6 +298,7 @@ def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
     if a_log is not None:
         _check_tensor("a_log", a_log, torch.float32, (H,), dev)
     desc, _ = make_desc(N, N, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
     with torch.cuda.device(dev):
         st = lib.kda_decode_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
                                  _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream))
@@ -309,23 +316,25 @@ def _window_args(q, k, v, z, beta, state):
     _check_tensor("q", q, q.dtype, (B, W, H, dk), dev)
     _check_tensor("k", k, q.dtype, (B, W, H, dk), dev)
     _check_tensor("v", v, q.dtype, (B, W, H, dv), dev)
-    _check_tensor("z", z, torch.float32, (B, W, H, dk), dev)
+    per_head = z.dim() == 3  # [B, W, H]: one gate per head
+    _check_tensor("z", z, torch.float32, (B, W, H) if per_head else (B, W, H, dk), dev)
     _check_tensor("beta", beta, torch.float32, (B, W, H), dev)
     _check_tensor("state", state, torch.float32, (B, H, dk, dv), dev)
-    return B, W, H, dk, dv, dev
+    return B, W, H, dk, dv, dev, per_head
 
 
 def decode_window(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):
     """``kda_decode_window``: outputs [B, W, H, dv] of W draft tokens per request
     from the committed ``state`` (not changed); draft i sees drafts 0..i."""
     lib = load()
-    B, W, H, dk, dv, dev = _window_args(q, k, v, z, beta, state)
+    B, W, H, dk, dv, dev, per_head = _window_args(q, k, v, z, beta, state)
     if out is None:
         out = torch.empty((B, W, H, dv), dtype=q.dtype, device=dev)
     _check_tensor("out", out, q.dtype, (B, W, H, dv), dev)
     if a_log is not None:
         _check_tensor("a_log", a_log, torch.float32, (H,), dev)
     desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
     with torch.cuda.device(dev):
         st = lib.kda_decode_window(ctypes.byref(desc), ctypes.c_int32(W), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(z), _ptr(beta), _ptr(state), _ptr(out),
@@ -340,11 +349,12 @@ def decode_replay(q, k, v, z, beta, accept_len, state, *, stream=None, a_log=Non
     window to each request's ``state`` (in place).  accept_len: int32 [B] on
     the device."""
     lib = load()
-    B, W, H, dk, dv, dev = _window_args(q, k, v, z, beta, state)
+    B, W, H, dk, dv, dev, per_head = _window_args(q, k, v, z, beta, state)
     _check_tensor("accept_len", accept_len, torch.int32, (B,), dev)
     if a_log is not None:
         _check_tensor("a_log", a_log, torch.float32, (H,), dev)
     desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
     with torch.cuda.device(dev):
         st = lib.kda_decode_replay(ctypes.byref(desc), ctypes.c_int32(W), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(z), _ptr(beta), _ptr(accept_len), _ptr(state),

@@ -92,6 +92,8 @@ kda_status_t prefill_common(const kda_desc_t* desc, const void* q, const void* k
   a.ckpt_every = desc->checkpoint_every;
   a.ckpt = desc->checkpoint_every > 0 ? desc->checkpoints : nullptr;
   a.ckpt_off = desc->checkpoint_every > 0 ? desc->checkpoint_offsets : nullptr;
+  if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  a.gate_per_head = desc->gate_per_head;
   a.err = device_error_word();
   if (!a.err) return KDA_ERR_CUDA;
   return KDA_OK;
@@ -160,8 +162,9 @@ kda_status_t kda_decode_step(const kda_desc_t* desc, const void* q, const void* 
   if (out && (out == q || out == k || out == v || out == (const void*)state))
     return KDA_ERR_INVALID_ARGUMENT;
   const kda::Problem p = to_problem(desc);
-  cudaError_t e = kda::launch_decode(p, q, k, v, z, beta, desc->a_log, state, out, nullptr,
-                                     (cudaStream_t)stream);
+  if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  cudaError_t e = kda::launch_decode(p, q, k, v, z, beta, desc->a_log, desc->gate_per_head, state,
+                                     out, nullptr, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -171,6 +174,7 @@ kda_status_t check_window(const kda_desc_t* desc, int32_t window, const void* q,
   if (!desc) return KDA_ERR_INVALID_ARGUMENT;
   kda_desc_t d = *desc;
   d.cu_seqlens_host = nullptr;  // not used by the window calls
+  if (d.gate_per_head != 0 && d.gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
   kda_status_t s = check_desc(&d, false);
   if (s != KDA_OK) return s;
   if (window < 1 || (int64_t)desc->num_seqs * window != desc->total_tokens)
@@ -193,8 +197,8 @@ kda_status_t kda_decode_window(const kda_desc_t* desc, int32_t window, const voi
   int* err = device_error_word();
   if (!err) return KDA_ERR_CUDA;
   cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
-                                     const_cast<float*>(state), out, nullptr, err,
-                                     (cudaStream_t)stream);
+                                     desc->gate_per_head, const_cast<float*>(state), out, nullptr,
+                                     err, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -207,7 +211,8 @@ kda_status_t kda_decode_replay(const kda_desc_t* desc, int32_t window, const voi
   int* err = device_error_word();
   if (!err) return KDA_ERR_CUDA;
   cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
-                                     state, nullptr, accept_len, err, (cudaStream_t)stream);
+                                     desc->gate_per_head, state, nullptr, accept_len, err,
+                                     (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -52,7 +52,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                   const float* initial_state, const int32_t* __restrict__ cu, T* __restrict__ out,
                   float* final_state, int H, int total, int* err,
                   const float* __restrict__ a_log, float* ckpt,
-                  const int32_t* __restrict__ ckpt_off, int ckpt_every) {
+                  const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
   constexpr int NT = 2 * DV;
   constexpr int NW = NT / 32;
   constexpr int RH = DK / 2;  // rows per thread
@@ -83,7 +83,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         const size_t o = ((size_t)(c0 + t) * H + h) * DK + c;
         a = IO<T>::ld(q + o);
         b = IO<T>::ld(k + o);
-        g = log_decay(zscale * __ldg(z + o));
+        g = log_decay(zscale * __ldg(zhead ? z + (size_t)(c0 + t) * H + h : z + o));
       }
       sm.qp[t][c] = a;
       sm.kp[t][c] = b;
@@ -202,7 +202,7 @@ cudaError_t dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   kern<<<blocks, 2 * DV, smem, st>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta,
                                      a.initial_state, a.cu_seqlens, (T*)a.out, a.final_state,
                                      p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt,
-                                     a.ckpt_off, a.ckpt_every);
+                                     a.ckpt_off, a.ckpt_every, a.gate_per_head);
   return cudaGetLastError();
 }
 

@@ -138,6 +138,7 @@ struct Params {
   float* ckpt;          // state checkpoints (null: none)
   const int32_t* ckpt_off;
   int ckpt_every;
+  const float* zh;      // one gate logit per (token, head), [T, H] (null: z tiles per channel)
   const float* initial_state;
   const int32_t* cu;
   __nv_bfloat16* out;   // may be null (no output written)
@@ -307,6 +308,8 @@ __device__ __forceinline__ void finish_chunk(__nv_bfloat16* out, int H, int h, i
   }
 }
 
+// kZHead: one gate logit per (token, head) (P.zh) instead of z tiles per channel.
+template <bool kZHead>
 __global__ void __launch_bounds__(kNT, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -374,12 +377,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int nchunks = (eos - bos + kC - 1) / kC;
     if (tid == 0 && nchunks > 0) {
       // (testing) 16 expected bytes that no copy delivers: the wait below expires
-      mbar_arrive_expect_tx(bar_qkz, 65536u + (P.inject_timeout ? 16u : 0u));
+      mbar_arrive_expect_tx(bar_qkz, (kZHead ? 32768u : 65536u) + (P.inject_timeout ? 16u : 0u));
       tma_load_3d(sm + OFF_Q, &tm_q, 0, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_K, &tm_k, 0, h, bos, bar_qkz);
       tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, bos, bar_qkz);
-      tma_load_3d(sm + OFF_Z, &tm_z, 0, h, bos, bar_qkz);
+      if (!kZHead) tma_load_3d(sm + OFF_Z, &tm_z, 0, h, bos, bar_qkz);
       if (!zero_v) {
         mbar_arrive_expect_tx(bar_v, 16384u);
         tma_load_3d(sm + OFF_V, &tm_v, 0, h, bos, bar_v);
@@ -492,8 +495,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float G[16];
       {
         const float* Z = reinterpret_cast<const float*>(sm + OFF_Z);
+        if (kZHead) {  // one logit per (token, head): every channel gets the same gate
 #pragma unroll
-        for (int i = 0; i < 16; ++i) G[i] = Z[(16 * a + i) * kD + c];
+          for (int i = 0; i < 16; ++i)
+            G[i] = 16 * a + i < len ? __ldg(P.zh + (size_t)(t0 + 16 * a + i) * H + h) : 0.f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) G[i] = Z[(16 * a + i) * kD + c];
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) G[i] = (16 * a + i < len) ? log_decay_c(G[i], zcoef) : 0.f;
 #pragma unroll
@@ -636,12 +645,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_after();
       if (tid == 0 && ci + 1 < nchunks) {  // q / k / z stages are free: prefetch the next chunk
         const int tn = t0 + kC;
-        mbar_arrive_expect_tx(bar_qkz, 65536u);
+        mbar_arrive_expect_tx(bar_qkz, kZHead ? 32768u : 65536u);
         tma_load_3d(sm + OFF_Q, &tm_q, 0, h, tn, bar_qkz);
         tma_load_3d(sm + OFF_Q + 8192, &tm_q, 64, h, tn, bar_qkz);
         tma_load_3d(sm + OFF_K, &tm_k, 0, h, tn, bar_qkz);
         tma_load_3d(sm + OFF_K + 8192, &tm_k, 64, h, tn, bar_qkz);
-        tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
+        if (!kZHead) tma_load_3d(sm + OFF_Z, &tm_z, 0, h, tn, bar_qkz);
       }
       pend_qkz = ci + 1 < nchunks;
       {
@@ -1178,8 +1187,12 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(chunk_tc_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(chunk_tc_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)SMEM_BYTES);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(state_scan_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1194,17 +1207,28 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mz, a.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.num_heads, T, 128,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+                CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (a.gate_per_head) {
+    mz = mq;  // z is [T, H] and read directly; the z tile map is never used
+  } else if (!make_map(&mz, a.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.num_heads, T, 128,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    return cudaErrorInvalidValue;
+  }
 
   static thread_local Params prm;  // large: keep off the stack
+  auto launch_tc = [&](int grid) {
+    if (a.gate_per_head)
+      chunk_tc_kernel<true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    else
+      chunk_tc_kernel<false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+  };
   prm.beta = a.beta;
   prm.a_log = a.a_log;
   prm.ckpt = a.ckpt;
   prm.ckpt_off = a.ckpt_off;
   prm.ckpt_every = a.ckpt_every;
+  prm.zh = a.gate_per_head ? a.z : nullptr;
   prm.initial_state = a.initial_state;
   prm.cu = a.cu_seqlens;
   prm.out = static_cast<__nv_bfloat16*>(a.out);
@@ -1240,7 +1264,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
       for (int i = 0; i < p.num_seqs; ++i) prm.list[i] = idx[i];
       prm.use_order = 1;
     }
-    chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    launch_tc(std::min(prm.num_units, sms));
     return cudaGetLastError();
   }
 
@@ -1274,7 +1298,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.ckpt = nullptr;  // pass 1 runs segments from stand-in entry states
   if (ne > 0) {
     prm.num_units = ne * p.num_heads;
-    chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    launch_tc(std::min(prm.num_units, sms));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1310,7 +1334,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.ckpt = a.ckpt;
   prm.num_units = ne * p.num_heads;
-  chunk_tc_kernel<<<std::min(prm.num_units, sms), kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+  launch_tc(std::min(prm.num_units, sms));
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ struct Args {
   float* ckpt;               // state checkpoints (null: none)
   const int32_t* ckpt_off;   // device [N + 1] prefix sums of checkpoints per sequence
   int ckpt_every;            // tokens between checkpoints (0: none)
+  int gate_per_head;         // 1: z is [T, H], one gate per head (scalar alpha)
 };
 
 // One work item of a chunked launch: a (sequence, head) pair, processed
@@ -43,16 +44,17 @@ struct WorkItem {
 
 // Decode: one token per (request, head), state updated in place.
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, float* state,
-                          void* out, int* err, cudaStream_t stream);
+                          const float* z, const float* beta, const float* a_log, int gate_per_head,
+                          float* state, void* out, int* err, cudaStream_t stream);
 
 // Speculative decoding over a window of W draft tokens per request
 // (inputs [B*W, H, .]): accept == nullptr computes the W outputs from the
 // state without changing it; otherwise the first accept[b] tokens are
 // applied again and the state is written.
 cudaError_t launch_window(const Problem& p, int W, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, float* state,
-                          void* out, const int32_t* accept, int* err, cudaStream_t stream);
+                          const float* z, const float* beta, const float* a_log, int gate_per_head,
+                          float* state, void* out, const int32_t* accept, int* err,
+                          cudaStream_t stream);
 
 // Token-by-token prefill over a packed batch.
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);

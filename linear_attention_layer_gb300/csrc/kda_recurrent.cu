@@ -45,7 +45,8 @@ struct RecSmem {
 // partial sums |q|^2, |k|^2, q.k per warp.
 template <int DK, int DV, typename T>
 __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, const T* kp,
-                                            const T* vp, const float* zp, float zscale) {
+                                            const T* vp, const float* zp, float zscale,
+                                            bool zhead) {
   const int tid = threadIdx.x;
   float qq = 0.f, kk = 0.f, kq = 0.f;
   if (tid < DK) {
@@ -53,7 +54,7 @@ __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, co
     const float b = IO<T>::ld(kp + tid);
     sm.qs[tid] = a;
     sm.ks[tid] = b;
-    sm.as[tid] = __expf(log_decay(zscale * __ldg(zp + tid)));
+    sm.as[tid] = __expf(log_decay(zscale * __ldg(zp + (zhead ? 0 : tid))));
     qq = a * a;
     kk = b * b;
     kq = a * b;
@@ -124,7 +125,7 @@ template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kNT, 2)
 decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
               const float* __restrict__ z, const float* __restrict__ beta,
-              const float* __restrict__ a_log, int H, float* __restrict__ state,
+              const float* __restrict__ a_log, int H, int zhead, float* __restrict__ state,
               T* __restrict__ out) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
@@ -134,8 +135,8 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   float4 s[SH::R];
 #pragma unroll
   for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
-  stage_token<DK, DV, T>(sm, q + unit * DK, k + unit * DK, v + unit * DV, z + unit * DK,
-                         gate_scale(a_log, (int)(unit % H)));
+  stage_token<DK, DV, T>(sm, q + unit * DK, k + unit * DK, v + unit * DV,
+                         z + unit * (zhead ? 1 : DK), gate_scale(a_log, (int)(unit % H)), zhead);
   __syncthreads();
   apply_token<DK, DV, T>(sm, s, __ldg(beta + unit), out + unit * DV);
 #pragma unroll
@@ -152,8 +153,9 @@ template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kNT, 2)
 window_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
               const float* __restrict__ z, const float* __restrict__ beta,
-              const float* __restrict__ a_log, int H, int W, float* __restrict__ state,
-              T* __restrict__ out, const int32_t* __restrict__ accept, int replay, int* err) {
+              const float* __restrict__ a_log, int H, int W, int zhead,
+              float* __restrict__ state, T* __restrict__ out,
+              const int32_t* __restrict__ accept, int replay, int* err) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const size_t unit = blockIdx.x;  // b * H + h
@@ -176,7 +178,8 @@ window_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   for (int t = 0; t < ntok; ++t) {
     const size_t th = ((size_t)b * W + t) * H + h;
     __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK, zscale);
+    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * (zhead ? 1 : DK),
+                           zscale, zhead);
     __syncthreads();
     apply_token<DK, DV, T>(sm, s, __ldg(beta + th), replay ? nullptr : out + th * DV);
   }
@@ -192,7 +195,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  const float* __restrict__ z, const float* __restrict__ beta,
                  const float* initial_state, const int32_t* __restrict__ cu, T* __restrict__ out,
                  float* final_state, int H, int total, int* err, const float* __restrict__ a_log,
-                 float* ckpt, const int32_t* __restrict__ ckpt_off, int ckpt_every) {
+                 float* ckpt, const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const int n = blockIdx.x / H, h = blockIdx.x % H;
@@ -212,7 +215,8 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
   for (int t = bos; t < eos; ++t) {
     const size_t th = (size_t)t * H + h;
     __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * DK, zscale);
+    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * (zhead ? 1 : DK),
+                           zscale, zhead);
     __syncthreads();
     apply_token<DK, DV, T>(sm, s, __ldg(beta + th), out + th * DV);
     if (ckpt && (t + 1 - bos) % ckpt_every == 0) {  // state after a multiple of ckpt_every tokens
@@ -231,22 +235,23 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
 template <int DK, int DV, typename T>
 cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, const void* v,
-                            const float* z, const float* beta, const float* a_log, float* state,
-                            void* out, cudaStream_t st) {
+                            const float* z, const float* beta, const float* a_log, int zhead,
+                            float* state, void* out, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   decode_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
-      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, state, (T*)out);
+      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, zhead, state, (T*)out);
   return cudaGetLastError();
 }
 
 template <int DK, int DV, typename T>
 cudaError_t window_dispatch(const Problem& p, int W, const void* q, const void* k, const void* v,
-                            const float* z, const float* beta, const float* a_log, float* state,
-                            void* out, const int32_t* accept, int* err, cudaStream_t st) {
+                            const float* z, const float* beta, const float* a_log, int zhead,
+                            float* state, void* out, const int32_t* accept, int* err,
+                            cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
-      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, W, state, (T*)out,
-      accept, accept ? 1 : 0, err);
+      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, W, zhead, state,
+      (T*)out, accept, accept ? 1 : 0, err);
   return cudaGetLastError();
 }
 
@@ -256,7 +261,7 @@ cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st)
   recurrent_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
       (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
       (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt, a.ckpt_off,
-      a.ckpt_every);
+      a.ckpt_every, a.gate_per_head);
   return cudaGetLastError();
 }
 
@@ -279,25 +284,27 @@ cudaError_t recurrent_dispatch(const Problem& p, const Args& a, cudaStream_t st)
 }  // namespace
 
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, float* state,
-                          void* out, int* /*err*/, cudaStream_t st) {
+                          const float* z, const float* beta, const float* a_log, int zhead,
+                          float* state, void* out, int* /*err*/, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
-    return p.io_bf16
-               ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, a_log, state, out, st)
-               : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, state, out, st);
+    return p.io_bf16 ? decode_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, a_log, zhead,
+                                                              state, out, st)
+                     : decode_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, zhead, state,
+                                                      out, st);
   });
 }
 
 cudaError_t launch_window(const Problem& p, int W, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, float* state,
-                          void* out, const int32_t* accept, int* err, cudaStream_t st) {
+                          const float* z, const float* beta, const float* a_log, int zhead,
+                          float* state, void* out, const int32_t* accept, int* err,
+                          cudaStream_t st) {
   if (p.num_seqs == 0 || W == 0) return cudaSuccess;
   return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
-    return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, W, q, k, v, z, beta, a_log, state,
-                                                              out, accept, err, st)
-                     : window_dispatch<DK, DV, float>(p, W, q, k, v, z, beta, a_log, state, out,
-                                                      accept, err, st);
+    return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, W, q, k, v, z, beta, a_log, zhead,
+                                                              state, out, accept, err, st)
+                     : window_dispatch<DK, DV, float>(p, W, q, k, v, z, beta, a_log, zhead,
+                                                      state, out, accept, err, st);
   });
 }
 

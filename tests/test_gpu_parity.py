@@ -220,6 +220,53 @@ def test_decode_gate_log_scale():
     assert_close(S, s_ref, torch.bfloat16, "decode state")
 
 
+# ------------------------------------------- one gate per head (scalar alpha) --
+
+@pytest.mark.parametrize("entry,dtype,dk,dv", [
+    ("chunk_fwd", torch.bfloat16, 128, 128),   # tensor-core kernel
+    ("chunk_fwd", torch.float32, 32, 64),      # CUDA-core chunked kernel
+    ("recurrent_fwd", torch.bfloat16, 64, 128),
+])
+def test_gate_per_head(entry, dtype, dk, dv):
+    """z [T, H]: every key channel of a head gets the same retention.  The
+    oracle runs the per-channel gate with that logit broadcast over dk."""
+    p = workloads.random_problem(RAGGED, 3, dk, dv, dtype, z_std=1.5, init_std=0.1, seed=17,
+                                 device=DEV)
+    zh = p.z[:, :, 0].contiguous()  # [T, H]
+    A = torch.tensor([0.2, -0.9, 1.1])
+    out, fin = getattr(kda, entry)(p.q, p.k, p.v, zh, p.beta, p.cu_seqlens, p.initial_state,
+                                   cu_seqlens_host=p.cu_seqlens_host, a_log=A.to(DEV))
+    torch.cuda.synchronize()
+    zb = zh.cpu()[:, :, None].expand(-1, -1, dk).contiguous()
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, p.initial_state,
+                                 a_log=A)
+    assert_close(out, ro, dtype, "out")
+    assert_close(fin, rf, dtype, "final_state")
+    assert kda.get_device_error() == 0
+
+
+def test_gate_per_head_decode_and_window():
+    d = workloads.decode_workload(4, 2, 128, 128, steps=2, io_dtype=torch.bfloat16, device=DEV,
+                                  seed=8)
+    S = d.state.clone()
+    s_ref = d.state.cpu()
+    for t in range(2):
+        zh = d.z[t][:, :, 0].contiguous()
+        o = kda.decode_step(d.q[t], d.k[t], d.v[t], zh, d.beta[t], S)
+        torch.cuda.synchronize()
+        ro, s_ref = oracle.decode_step(d.q[t], d.k[t], d.v[t],
+                                       zh.cpu()[:, :, None].expand(-1, -1, 128), d.beta[t],
+                                       s_ref)
+        assert_close(o, ro, torch.bfloat16, f"decode out step {t}")
+    assert_close(S, s_ref, torch.bfloat16, "decode state")
+    q, k, v, z, beta, state = _window_inputs(3, 4, 2, 128, 128, torch.bfloat16, 24)
+    zh = z[..., 0].contiguous()  # [B, W, H]
+    out = kda.decode_window(q, k, v, zh, beta, state)
+    ref, _ = _oracle_window(q, k, v, zh[..., None].expand(-1, -1, -1, 128).contiguous(), beta,
+                            state, [4] * 3)
+    assert_close(out, np.stack(ref), torch.bfloat16, "window outputs")
+
+
 # ------------------------------------------------ speculative decoding -----
 
 def _window_inputs(B, W, H, dk, dv, dtype, seed):
