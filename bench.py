@@ -408,9 +408,10 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False, clk=None):
 
 
 def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
-    """Speculative decoding: per step a window of W drafts per request
-    (kda_decode_window) and the replay of its accepted prefix
-    (kda_decode_replay).  Acceptance lengths are drawn U{0..W} (seeded).
+    """Speculative decoding: per step one kda_decode_replay_window call -- the
+    replay of the previous window's accepted prefix and the outputs of the
+    next window of W drafts, one state read and one write.  Acceptance
+    lengths are drawn U{0..W} (seeded).
     Returns (ms per step, accepted tokens per step)."""
     import torch
     g = torch.Generator(device=device)
@@ -427,9 +428,10 @@ def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
     acc = torch.randint(0, W + 1, (steps + 3, B), generator=g, device=device, dtype=torch.int32)
     stream = torch.cuda.current_stream()
 
-    def step(i):
-        kda.decode_window(q, k, v, z, beta, state, out=out)
-        kda.decode_replay(q, k, v, z, beta, acc[i], state)
+    prev = (q, k, v, z, beta)
+
+    def step(i):  # replay the last window's accepted prefix, then the next window's outputs
+        kda.decode_replay_window(prev, acc[i], q, k, v, z, beta, state, out=out)
 
     for i in range(3):
         step(i)
@@ -658,11 +660,10 @@ def main():
         Bs, Hs, Ws, ns = 256, 32, 4, 200
         sclk = clock_sampler(gpu_uuid)
         s_ms, s_acc = bench_spec_decode(kda, Bs, Hs, Ws, ns, device, seed=rank, clk=sclk)
-        # per (request, head): the state read by the window and read + written by
-        # the replay; the W drafts' inputs (q, k, v bf16, z fp32, beta) and outputs;
-        # the accepted drafts' inputs again in the replay
+        # per (request, head): the state read and written once; the W new drafts'
+        # inputs (q, k, v bf16, z fp32, beta) and outputs; the accepted drafts' inputs
         tok_in = 3 * 256 + 512 + 4
-        s_bytes = int(Bs * Hs * (3 * STATE_BYTES + Ws * (tok_in + 256)) + s_acc * Hs * tok_in)
+        s_bytes = int(Bs * Hs * (2 * STATE_BYTES + Ws * (tok_in + 256)) + s_acc * Hs * tok_in)
         s_gbs = s_bytes / (s_ms * 1e-3) / 1e9
         line["spec_decode"] = {
             "value": round(s_acc * Hs / (s_ms * 1e-3) / 1e6, 3), "unit": "M accepted head-tokens/s",
@@ -671,7 +672,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(s_gbs, 1), "peak": hbm_peak,
                          "unit": "GB/s", "frac": round(s_gbs / hbm_peak, 4),
                          "algorithmic_bytes_per_step": s_bytes},
-            "clocks": sclk.summary(), "gpu_launches": 2 * ns}
+            "clocks": sclk.summary(), "gpu_launches": ns}
 
     # ---- end to end through host buffers ----
     if "e2e" not in skip:

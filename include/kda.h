@@ -228,6 +228,25 @@ kda_status_t kda_decode_replay(const kda_desc_t* desc, int32_t window, const voi
                                const int32_t* accept_len, float* state, kda_stream_t stream);
 
 /*
+ * kda_decode_replay_window -- the two calls above fused into one pass over
+ * each request's state, as the pages describe the replay (one recurrent
+ * loop): the first accept_len[b] drafts of the previous window (inputs
+ * prev_*, [B * prev_window, H, .]) are applied and the state is written,
+ * then the outputs of the new window (q .. beta, [B * window, H, .]) are
+ * computed from it (the new drafts do not change the stored state).  The
+ * state is read once and written once per call.  desc->total_tokens =
+ * B * window.  A request whose accept_len is outside 0 .. prev_window keeps
+ * its state, gets no outputs and sets the device error word.
+ */
+kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_window,
+                                      const void* prev_q, const void* prev_k, const void* prev_v,
+                                      const float* prev_z, const float* prev_beta,
+                                      const int32_t* accept_len, int32_t window, const void* q,
+                                      const void* k, const void* v, const float* z,
+                                      const float* beta, float* state, void* out,
+                                      kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
  * device memory.  The pages describe no counterpart of this entry point.
  *

@@ -21,7 +21,7 @@ import torch
 __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
-           "checkpoint_offsets", "decode_window", "decode_replay",
+           "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
            "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
@@ -33,7 +33,8 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
 
 #: Every function include/kda.h declares.
 EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
-                    "kda_decode_step", "kda_decode_window", "kda_decode_replay", "kda_status_string", "kda_get_device_error",
+                    "kda_decode_step", "kda_decode_window", "kda_decode_replay",
+                    "kda_decode_replay_window", "kda_status_string", "kda_get_device_error",
                     "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
@@ -362,6 +363,35 @@ def decode_replay(q, k, v, z, beta, accept_len, state, *, stream=None, a_log=Non
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_replay")
     return state
+
+
+def decode_replay_window(prev, accept_len, q, k, v, z, beta, state, *, out=None, stream=None,
+                         a_log=None):
+    """``kda_decode_replay_window``: replay the first accept_len[b] drafts of the
+    previous window ``prev`` = (q, k, v, z, beta) into ``state`` (in place),
+    then return the outputs [B, W, H, dv] of the new window from it."""
+    lib = load()
+    B, W, H, dk, dv, dev, per_head = _window_args(q, k, v, z, beta, state)
+    pq, pk, pv, pz, pb = prev
+    Bp, Wp, Hp, dkp, dvp, _, per_head_p = _window_args(pq, pk, pv, pz, pb, state)
+    if (Bp, Hp, dkp, dvp, per_head_p) != (B, H, dk, dv, per_head) or pq.dtype != q.dtype:
+        raise ValueError("the previous window must match the new one but for its length")
+    _check_tensor("accept_len", accept_len, torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, W, H, dv), dtype=q.dtype, device=dev)
+    _check_tensor("out", out, q.dtype, (B, W, H, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_replay_window(
+            ctypes.byref(desc), ctypes.c_int32(Wp), _ptr(pq), _ptr(pk), _ptr(pv), _ptr(pz),
+            _ptr(pb), _ptr(accept_len), ctypes.c_int32(W), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+            _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_replay_window")
+    return out
 
 
 def get_device_error(stream=None) -> int:

@@ -196,9 +196,10 @@ kda_status_t kda_decode_window(const kda_desc_t* desc, int32_t window, const voi
     return KDA_ERR_INVALID_ARGUMENT;
   int* err = device_error_word();
   if (!err) return KDA_ERR_CUDA;
-  cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
-                                     desc->gate_per_head, const_cast<float*>(state), out, nullptr,
-                                     err, (cudaStream_t)stream);
+  kda::WinInputs rp, wn;
+  wn.q = q; wn.k = k; wn.v = v; wn.z = z; wn.beta = beta; wn.W = window;
+  cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
+                                     const_cast<float*>(state), out, err, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -210,9 +211,37 @@ kda_status_t kda_decode_replay(const kda_desc_t* desc, int32_t window, const voi
   if (desc->num_seqs > 0 && !accept_len) return KDA_ERR_INVALID_ARGUMENT;
   int* err = device_error_word();
   if (!err) return KDA_ERR_CUDA;
-  cudaError_t e = kda::launch_window(to_problem(desc), window, q, k, v, z, beta, desc->a_log,
-                                     desc->gate_per_head, state, nullptr, accept_len, err,
-                                     (cudaStream_t)stream);
+  kda::WinInputs rp, wn;
+  rp.q = q; rp.k = k; rp.v = v; rp.z = z; rp.beta = beta; rp.W = window; rp.accept = accept_len;
+  cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
+                                     state, nullptr, err, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_window,
+                                      const void* prev_q, const void* prev_k, const void* prev_v,
+                                      const float* prev_z, const float* prev_beta,
+                                      const int32_t* accept_len, int32_t window, const void* q,
+                                      const void* k, const void* v, const float* z,
+                                      const float* beta, float* state, void* out,
+                                      kda_stream_t stream) {
+  kda_status_t s = check_window(desc, window, q, k, v, z, beta, state);
+  if (s != KDA_OK) return s;
+  if (prev_window < 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->num_seqs > 0 &&
+      (!prev_q || !prev_k || !prev_v || !prev_z || !prev_beta || !accept_len || !out))
+    return KDA_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {q, k, v, z, beta, prev_q, prev_k, prev_v, prev_z, prev_beta, state};
+  for (const void* x : ins)
+    if (out && out == x) return KDA_ERR_INVALID_ARGUMENT;
+  int* err = device_error_word();
+  if (!err) return KDA_ERR_CUDA;
+  kda::WinInputs rp, wn;
+  rp.q = prev_q; rp.k = prev_k; rp.v = prev_v; rp.z = prev_z; rp.beta = prev_beta;
+  rp.W = prev_window; rp.accept = accept_len;
+  wn.q = q; wn.k = k; wn.v = v; wn.z = z; wn.beta = beta; wn.W = window;
+  cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
+                                     state, out, err, (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

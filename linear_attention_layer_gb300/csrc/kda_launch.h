@@ -47,14 +47,22 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
                           const float* z, const float* beta, const float* a_log, int gate_per_head,
                           float* state, void* out, int* err, cudaStream_t stream);
 
-// Speculative decoding over a window of W draft tokens per request
-// (inputs [B*W, H, .]): accept == nullptr computes the W outputs from the
-// state without changing it; otherwise the first accept[b] tokens are
-// applied again and the state is written.
-cudaError_t launch_window(const Problem& p, int W, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, int gate_per_head,
-                          float* state, void* out, const int32_t* accept, int* err,
-                          cudaStream_t stream);
+// Speculative decoding (inputs of a window: [B*W, H, .]).  rp: a window
+// whose first accept[b] tokens are applied again and the state written
+// (rp.accept == nullptr: none); wn: a window whose W outputs are computed
+// from the (replayed) state, which it does not write (W == 0: none).
+struct WinInputs {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  const float* z = nullptr;
+  const float* beta = nullptr;
+  int W = 0;
+  const int32_t* accept = nullptr;
+};
+cudaError_t launch_window(const Problem& p, const WinInputs& rp, const WinInputs& wn,
+                          const float* a_log, int gate_per_head, float* state, void* out,
+                          int* err, cudaStream_t stream);
 
 // Token-by-token prefill over a packed batch.
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);

@@ -143,49 +143,68 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
 }
 
-// Speculative decoding.  One CTA per (request, head); the window's draft
-// tokens of request b are rows [b*W, b*W + W) of the [B*W, H, .] inputs.
-// window (replay == 0): outputs of all W tokens from the committed state,
-// which is read and left as it is.  replay (replay != 0): the first
-// accept[b] tokens (0 <= accept[b] <= W) are applied again and the state is
-// written once, without outputs.
+// Speculative decoding.  One CTA per (request, head).  A window's draft
+// tokens of request b are rows [b*W, b*W + W) of its [B*W, H, .] inputs.
+// With a replay part (rp.accept != null): the first accept[b] tokens of the
+// previous window rp (0 <= accept[b] <= rp.W) are applied again and the
+// state is written once, without outputs.  With a window part (wn.W > 0):
+// the outputs of its W tokens, from the (replayed) state, which the window
+// part does not write back.  Both parts in one launch read the state from
+// HBM once and write it once.
+template <typename T>
+struct WinPart {
+  const T* q;
+  const T* k;
+  const T* v;
+  const float* z;
+  const float* beta;
+  int W;
+  const int32_t* accept;  // replay part only
+};
+
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kNT, 2)
-window_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-              const float* __restrict__ z, const float* __restrict__ beta,
-              const float* __restrict__ a_log, int H, int W, int zhead,
-              float* __restrict__ state, T* __restrict__ out,
-              const int32_t* __restrict__ accept, int replay, int* err) {
+window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int H, int zhead,
+              float* __restrict__ state, T* __restrict__ out, int* err) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const size_t unit = blockIdx.x;  // b * H + h
   const int b = (int)(unit / H), h = (int)(unit % H);
-  int ntok = W;
-  if (replay) {
-    ntok = __ldg(accept + b);
-    if (ntok < 0 || ntok > W) {  // bad acceptance length: leave this state alone
+  int nrep = 0;
+  if (rp.accept) {
+    nrep = __ldg(rp.accept + b);
+    if (nrep < 0 || nrep > rp.W) {  // bad acceptance length: leave this request alone
       if (threadIdx.x == 0) report_error(err, kErrDeviceCheck);
       return;
     }
-    if (ntok == 0) return;
   }
+  if (nrep == 0 && wn.W == 0) return;
   const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
   float4* S = reinterpret_cast<float4*>(state + unit * DK * DV);
   float4 s[SH::R];
 #pragma unroll
   for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
   const float zscale = gate_scale(a_log, h);
-  for (int t = 0; t < ntok; ++t) {
-    const size_t th = ((size_t)b * W + t) * H + h;
+  const int zs = zhead ? 1 : DK;
+  for (int t = 0; t < nrep; ++t) {
+    const size_t th = ((size_t)b * rp.W + t) * H + h;
     __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T>(sm, q + th * DK, k + th * DK, v + th * DV, z + th * (zhead ? 1 : DK),
+    stage_token<DK, DV, T>(sm, rp.q + th * DK, rp.k + th * DK, rp.v + th * DV, rp.z + th * zs,
                            zscale, zhead);
     __syncthreads();
-    apply_token<DK, DV, T>(sm, s, __ldg(beta + th), replay ? nullptr : out + th * DV);
+    apply_token<DK, DV, T>(sm, s, __ldg(rp.beta + th), nullptr);
   }
-  if (replay) {
+  if (nrep > 0) {
 #pragma unroll
     for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
+  }
+  for (int t = 0; t < wn.W; ++t) {
+    const size_t th = ((size_t)b * wn.W + t) * H + h;
+    __syncthreads();
+    stage_token<DK, DV, T>(sm, wn.q + th * DK, wn.k + th * DK, wn.v + th * DV, wn.z + th * zs,
+                           zscale, zhead);
+    __syncthreads();
+    apply_token<DK, DV, T>(sm, s, __ldg(wn.beta + th), out + th * DV);
   }
 }
 
@@ -244,14 +263,15 @@ cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, cons
 }
 
 template <int DK, int DV, typename T>
-cudaError_t window_dispatch(const Problem& p, int W, const void* q, const void* k, const void* v,
-                            const float* z, const float* beta, const float* a_log, int zhead,
-                            float* state, void* out, const int32_t* accept, int* err,
+cudaError_t window_dispatch(const Problem& p, const WinInputs& rp, const WinInputs& wn,
+                            const float* a_log, int zhead, float* state, void* out, int* err,
                             cudaStream_t st) {
+  auto part = [](const WinInputs& x) {
+    return WinPart<T>{(const T*)x.q, (const T*)x.k, (const T*)x.v, x.z, x.beta, x.W, x.accept};
+  };
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
-  window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
-      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, W, zhead, state,
-      (T*)out, accept, accept ? 1 : 0, err);
+  window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(part(rp), part(wn), a_log, p.num_heads, zhead,
+                                                   state, (T*)out, err);
   return cudaGetLastError();
 }
 
@@ -295,16 +315,15 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
   });
 }
 
-cudaError_t launch_window(const Problem& p, int W, const void* q, const void* k, const void* v,
-                          const float* z, const float* beta, const float* a_log, int zhead,
-                          float* state, void* out, const int32_t* accept, int* err,
+cudaError_t launch_window(const Problem& p, const WinInputs& rp, const WinInputs& wn,
+                          const float* a_log, int zhead, float* state, void* out, int* err,
                           cudaStream_t st) {
-  if (p.num_seqs == 0 || W == 0) return cudaSuccess;
+  if (p.num_seqs == 0 || (!rp.accept && wn.W == 0)) return cudaSuccess;
   return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
-    return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, W, q, k, v, z, beta, a_log, zhead,
-                                                              state, out, accept, err, st)
-                     : window_dispatch<DK, DV, float>(p, W, q, k, v, z, beta, a_log, zhead,
-                                                      state, out, accept, err, st);
+    return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, rp, wn, a_log, zhead, state, out,
+                                                              err, st)
+                     : window_dispatch<DK, DV, float>(p, rp, wn, a_log, zhead, state, out, err,
+                                                      st);
   });
 }
 

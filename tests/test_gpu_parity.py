@@ -355,6 +355,30 @@ def test_draft_verify_replay_loop_equals_prefill_of_accepted_tokens():
         assert_close(state[b], fin[0], torch.bfloat16, f"request {b} after {n} accepted")
 
 
+def test_fused_replay_window_equals_replay_then_window():
+    """One launch per step (replay of the previous window's accepted prefix,
+    then the new window's outputs) against the two separate calls."""
+    B, W, H, dk, dv = 5, 3, 2, 128, 128
+    torch.manual_seed(1)
+    s_sep = torch.randn((B, H, dk, dv), device=DEV) * 0.1
+    s_fused = s_sep.clone()
+    prev = _window_inputs(B, W, H, dk, dv, torch.bfloat16, 40)[:5]
+    kda.decode_window(*prev, s_sep)
+    rng = np.random.default_rng(9)
+    for r in range(3):
+        nxt = _window_inputs(B, W + r, H, dk, dv, torch.bfloat16, 41 + r)[:5]
+        acc = torch.tensor(rng.integers(0, W + 1, size=B), dtype=torch.int32, device=DEV)
+        kda.decode_replay(*prev, acc, s_sep)
+        o_sep = kda.decode_window(*nxt, s_sep)
+        o_fused = kda.decode_replay_window(prev, acc, *nxt, s_fused)
+        torch.cuda.synchronize()
+        assert torch.equal(o_fused, o_sep)
+        assert torch.equal(s_fused, s_sep)
+        prev = nxt
+        W = W + r
+    assert kda.get_device_error() == 0
+
+
 def test_decode_replay_bad_accept_length_sets_error_and_keeps_state():
     B, W, H = 3, 2, 2
     q, k, v, z, beta, state = _window_inputs(B, W, H, 64, 64, torch.float32, 23)
