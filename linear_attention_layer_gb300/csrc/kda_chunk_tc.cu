@@ -239,26 +239,6 @@ __device__ __forceinline__ void sync_tc() {
 
 __device__ __forceinline__ bool f16_ok(float x) { return fabsf(x) < kF16Max; }
 
-// S^T (fp32 in TMEM, this warp's lane quadrant) <- S^T Diag(e^{G_C}) for
-// columns [c0, c0 + 16 * n16).
-__device__ __forceinline__ void decay_state_cols(uint32_t my_lane, const float* dec, int c0,
-                                                 int n16) {
-#pragma unroll 2
-  for (int k = 0; k < n16; ++k) {
-    const int col = c0 + 16 * k;
-    float v[16];
-    tmem_ld16(my_lane + TS32 + col, v);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const float4 d4 = *reinterpret_cast<const float4*>(dec + col + i);
-      v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
-    }
-    tmem_st16(my_lane + TS32 + col, v);
-  }
-  tmem_st_wait();
-}
-
 // S^T (fp32 in TMEM; lane n = value channel n) to dst[c][n], a [dk][dv]
 // fp32 state; warp part cq covers key channels 32 cq .. 32 cq + 31.
 __device__ __forceinline__ void write_state(float* dst, uint32_t my_lane, int row, int cq) {
@@ -274,38 +254,46 @@ __device__ __forceinline__ void write_state(float* dst, uint32_t my_lane, int ro
 }
 
 // The end of a chunk, once its last products have landed in TMEM: O^T (lane
-// n = value channel, column t) to out[t0 + t][h][n] in bf16 for t < len, and
-// (conv_s) S^T fp32 -> fp16, the A operand of the next chunk's state products.
-// Warp part cq covers 16 columns of O^T and 32 of S^T.
-__device__ __forceinline__ void finish_chunk(__nv_bfloat16* out, int H, int h, int t0, int len,
-                                             uint32_t my_lane, uint32_t tmem, int row, int cq,
-                                             bool conv_s, float& absmax) {
-  if (out) {
-    __nv_bfloat16* ocol = out + ((size_t)t0 * H + h) * kD + row;
-    const int col = 16 * cq;
+// n = value channel, column t) to out[t0 + t][h][n] in bf16 for t < len.
+// Warp part cq covers 16 columns.
+__device__ __forceinline__ void write_o(__nv_bfloat16* out, int H, int h, int t0, int len,
+                                        uint32_t my_lane, int row, int cq) {
+  __nv_bfloat16* ocol = out + ((size_t)t0 * H + h) * kD + row;
+  const int col = 16 * cq;
+  float v[16];
+  tmem_ld16(my_lane + TO + col, v);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
+}
+
+// The state entering a chunk, in one TMEM read of S^T (fp32; this warp's lane
+// quadrant, key channels 32 cq .. 32 cq + 31): its fp16 copy (the A operand
+// of the chunk's state products) and S^T <- S^T Diag(e^{G_C}) (dec = e^{G_C}
+// per key channel) ahead of the chunk's update.
+__device__ __forceinline__ void prep_state(uint32_t my_lane, const float* dec, int cq,
+                                           float& absmax) {
+#pragma unroll
+  for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
     float v[16];
-    tmem_ld16(my_lane + TO + col, v);
+    tmem_ld16(my_lane + TS32 + c0, v);
     tmem_ld_wait();
+    uint32_t hp[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (col + i < len) ocol[(size_t)(col + i) * H * kD] = __float2bfloat16_rn(v[i]);
-  }
-  if (conv_s) {
-#pragma unroll
-    for (int c0 = 32 * cq; c0 < 32 * cq + 32; c0 += 16) {
-      float v[16];
-      tmem_ld16(my_lane + TS32 + c0, v);
-      tmem_ld_wait();
-      uint32_t hp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
-        absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-      }
-      tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
+    for (int i = 0; i < 8; ++i) {
+      hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
+      absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
     }
-    tmem_st_wait();
+    tmem_st8(my_lane + TS16 + (c0 >> 1), hp);
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 d4 = *reinterpret_cast<const float4*>(dec + c0 + i);
+      v[i] *= d4.x; v[i + 1] *= d4.y; v[i + 2] *= d4.z; v[i + 3] *= d4.w;
+    }
+    tmem_st16(my_lane + TS32 + c0, v);
   }
+  tmem_st_wait();
 }
 
 // kZHead: one gate logit per (token, head) (P.zh) instead of z tiles per channel.
@@ -474,19 +462,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
 
-      if (pend_l) {
-        // ---------------- L (previous chunk): write O; S^T -> fp16 ----------------
-        ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
-        if (ok) {
-          ph_mma ^= 1;
-          pend_mma = false;
-          tc_fence_after();
-          finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, true, absmax);
-          if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
-        }
-        pend_l = false;
-      }
-
       // ---------------- C: gate and cumulative decay ----------------
       // thread = (subtile a, key channel c) with its 16 tokens t = 16a + i; a
       // warp covers 32 channels of one subtile.  G[i] is the cumulative
@@ -544,6 +519,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             kt[i] = k * E;
           }
         }
+        // The previous chunk's last products read Khat, overwritten below: wait for them.
+        bool okl = true;
+        if (pend_l) {
+          okl = wait_bar(bar_mma, ph_mma, P.spin_cycles);
+          if (okl) {
+            ph_mma ^= 1;
+            pend_mma = false;
+          }
+          ok = ok && okl;
+        }
         // adjacent-subtile factors e^{r_{b+1} - r_b} = e^{tot_b} (r_4 = G_C), each >= e^-80
         float ed[4];
 #pragma unroll
@@ -598,6 +583,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
+      // ---------------- L: the previous chunk's O; this chunk's entering state ----------------
+      // The previous chunk's O to HBM (and its checkpoint), then in one TMEM read of S^T
+      // (fp32) its fp16 copy (the A operand of this chunk's state products) and
+      // S^T <- S^T Diag(e^{G_C}) ahead of this chunk's update.
+      if (ok) {
+        tc_fence_after();
+        if (pend_l) {
+          if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
+          if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
+        }
+        prep_state(my_lane, misc + M_DECAY, cq, absmax);
+      }
+      pend_l = false;
       fence_proxy_async_smem();
       sync_tc();
       if (tid == 0) {
@@ -616,11 +614,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // ---------------- E: v -> fp16 while the Gram runs; read back P and A ----------------
       {
         if (!zero_v) {
-          ok = wait_bar(bar_v, ph_v, P.spin_cycles);
-          if (ok) {
+          const bool okv = wait_bar(bar_v, ph_v, P.spin_cycles);
+          if (okv) {
             ph_v ^= 1;
             pend_v = false;
           }
+          ok = ok && okv;
         }
         // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
         uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
@@ -734,9 +733,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i) T[(base + i) * kLS + base + cc] = x[i];
           }
-        } else if (warp < 12) {
-          decay_state_cols(my_lane, misc + M_DECAY, 64 * ((warp - 4) >> 2), 4);
-        } else {
+        } else if (warp >= 12) {
           if (warp == 12 && lane == 0) {
             const uint32_t id_o = make_idesc_f16(128, kC, false, true);
 #pragma unroll
@@ -918,7 +915,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ph_mma ^= 1;
         pend_mma = false;
         tc_fence_after();
-        finish_chunk(P.out, H, h, l_t0, l_len, my_lane, tmem, row, cq, false, absmax);
+        if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
         if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
       }
       pend_l = false;
