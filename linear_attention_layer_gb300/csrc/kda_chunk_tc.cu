@@ -562,23 +562,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncthreads();  // every thread is done with the q / k / z stages
         {
-          const uint32_t x = ((uint32_t)c & 31) >> 2;
-          unsigned char* gm = sm + G_M + (c >> 5) * kGMAtom + 2048 * a + (c & 3) * 4;
-          unsigned char* gn = sm + G_N + (c >> 5) * kGNAtom + 2048 * a + (c & 3) * 4;
+          // A warp holds 32 consecutive channels (lane = c % 32) of 16 tokens; four
+          // tokens go out per stmatrix: matrix j = token i0 + j, its row r = channels
+          // 4r .. 4r+3, one 16-byte chunk of that token's 128-byte swizzled row.
+          const uint32_t lj = (uint32_t)lane >> 3, lr = (uint32_t)lane & 7;
+          const uint32_t so0 = 128u * lj + ((lr ^ lj) << 4);
+          const uint32_t so4 = 128u * lj + ((lr ^ (4u | lj)) << 4);
+          const uint32_t gm = smem_u32(sm) + G_M + (c >> 5) * kGMAtom + 2048 * a;
+          const uint32_t gn = smem_u32(sm) + G_N + (c >> 5) * kGNAtom + 2048 * a;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
+          for (int i0 = 0; i0 < 16; i0 += 4) {
+            const uint32_t so = 128u * i0 + ((i0 & 4) ? so4 : so0);
             // M-side rows: Q~ at t, K~q at 64 + t
-            *reinterpret_cast<float*>(gm + off) = tf32f(qt[i]);
-            *reinterpret_cast<float*>(gm + 64 * 128 + off) = tf32f(kq[i]);
+            stmatrix_x4(gm + so, to_tf32(qt[i0]), to_tf32(qt[i0 + 1]), to_tf32(qt[i0 + 2]),
+                        to_tf32(qt[i0 + 3]));
+            stmatrix_x4(gm + 64 * 128 + so, to_tf32(kq[i0]), to_tf32(kq[i0 + 1]),
+                        to_tf32(kq[i0 + 2]), to_tf32(kq[i0 + 3]));
             // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, rows ka_row(a') + t, by
             // the chain K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80)
-            float v = kt[i];
+            float v0 = kt[i0], v1 = kt[i0 + 1], v2 = kt[i0 + 2], v3 = kt[i0 + 3];
 #pragma unroll
             for (int ap = 0; ap < 4; ++ap) {
               if (ap < a) continue;
-              if (ap > a) v *= ed[ap - 1];
-              *reinterpret_cast<float*>(gn + ka_row(ap) * 128 + off) = tf32f(v);
+              if (ap > a) {
+                const float e = ed[ap - 1];
+                v0 *= e; v1 *= e; v2 *= e; v3 *= e;
+              }
+              stmatrix_x4(gn + ka_row(ap) * 128 + so, to_tf32(v0), to_tf32(v1), to_tf32(v2),
+                          to_tf32(v3));
             }
           }
         }

@@ -272,6 +272,16 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32
                : "r"(saddr));
 }
 
+// Four 8x8 matrices of 16-bit pairs to shared memory: lane l's register j is
+// word l % 4 of row l / 4 of matrix j; lane 8 j + r gives the address of row r
+// of matrix j (16 bytes).  Used for 32-bit data as well: it only moves bits.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1) {
