@@ -594,24 +594,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
-      // ---------------- L: the previous chunk's O; this chunk's entering state ----------------
-      // The previous chunk's O to HBM (and its checkpoint), then in one TMEM read of S^T
-      // (fp32) its fp16 copy (the A operand of this chunk's state products) and
-      // S^T <- S^T Diag(e^{G_C}) ahead of this chunk's update.
-      if (ok) {
-        tc_fence_after();
-        if (pend_l) {
-          if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
-          if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
-        }
-        prep_state(my_lane, misc + M_DECAY, cq, absmax);
-      }
-      pend_l = false;
       fence_proxy_async_smem();
       sync_tc();
-      if (tid == 0) {
+      if (tid == kNT - 32) {
         // Gram, tf32: D[r][p] = M_r . N_p over the 128 channels, M = [Q~; K~q]
-        // (128 rows), N = the packed K^(a) (160 rows)
+        // (128 rows), N = the packed K^(a) (160 rows).  Issued from the last warp,
+        // the one with the least work until the Gram has landed.
         const uint32_t id_g = make_idesc_tf32(128, kGN);
 #pragma unroll
         for (int kb = 0; kb < kD / 32; ++kb)
@@ -621,6 +609,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         desc_k(dbase, G_N + kb * kGNAtom + k8 * 32), id_g, (kb | k8) != 0);
         mma_commit(bar_mma);
       }
+
+      // ---------------- L: the previous chunk's O; this chunk's entering state ----------------
+      // While the Gram runs: the previous chunk's O to HBM (and its checkpoint), then in
+      // one TMEM read of S^T (fp32) its fp16 copy (the A operand of this chunk's state
+      // products) and S^T <- S^T Diag(e^{G_C}) ahead of this chunk's update.
+      if (ok) {
+        if (pend_l) {
+          if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
+          if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
+        }
+        prep_state(my_lane, misc + M_DECAY, cq, absmax);
+      }
+      pend_l = false;
 
       // ---------------- E: v -> fp16 while the Gram runs; read back P and A ----------------
       {
