@@ -292,6 +292,49 @@ kda_status_t kda_chunk_fwd_noalloc(const kda_desc_t* desc, const void* q, const 
 void kda_testing_inject_wait_timeout(int launches);
 
 /* Static, human-readable name of a status. */
+/*
+ * kda_recurrent_bwd -- reverse mode of kda_chunk_fwd / kda_recurrent_fwd:
+ * the gradients of a loss L with respect to every input, given dL/d out and
+ * dL/d final_state.  The pages give the forward only (mhpq.cn/news/56770,
+ * section "KDA 到底在算什么"; the gate of blog.higcp.com "猜想：K3 可能是最
+ * 适合 TPU 的 MoE 架构", section "下界衰减"); the gradients are the chain rule
+ * through those definitions, L2-normalisation and gate included, evaluated
+ * token by token in fp32 in reverse order.  The states S_{t-1} it needs are
+ * rebuilt forward from states the call itself keeps every 8 tokens in the
+ * workspace.
+ *
+ *   desc               as for kda_chunk_fwd; dk = dv = 128 and
+ *                      gate_per_head = 0 (else KDA_ERR_UNSUPPORTED);
+ *                      cu_seqlens_host is REQUIRED; workspace /
+ *                      workspace_bytes must hold
+ *                      kda_recurrent_bwd_workspace_size() bytes (16-byte
+ *                      aligned); a_log is honoured; checkpoint fields are
+ *                      ignored.
+ *   q, k, v, z, beta, initial_state, cu_seqlens
+ *                      the forward call's inputs (initial_state may be NULL)
+ *   d_out              device, [T_tot, H, dv] io dtype: dL/d out
+ *   d_final_state      device, [N, H, dk, dv] fp32, or NULL for zeros
+ *   dq, dk, dv, dz     device, [T_tot, H, 128] fp32, written (dz is the
+ *                      gradient w.r.t. the gate logits z as passed)
+ *   dbeta              device, [T_tot, H] fp32, written
+ *   d_initial_state    device, [N, H, dk, dv] fp32, written, or NULL
+ * Every pointer to per-token or state data must be 16-byte aligned, and no
+ * output may alias an input.  Errors as for kda_chunk_fwd; a device copy of
+ * cu_seqlens whose lengths exceed those of the host copy skips the
+ * offending sequences and sets the device error word.
+ */
+kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void* k,
+                               const void* v, const float* z, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens,
+                               const void* d_out, const float* d_final_state, float* dq,
+                               float* dk, float* dv, float* dz, float* dbeta,
+                               float* d_initial_state, kda_stream_t stream);
+
+/* Bytes of device workspace kda_recurrent_bwd needs for this descriptor
+ * (needs desc->cu_seqlens_host): for every resident CTA (at most one per
+ * SM) 64 KiB per 8 tokens of the longest sequence, plus 512 KiB. */
+kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
+
 const char* kda_status_string(kda_status_t status);
 
 /* Synchronise `stream`, then read and clear the device error word of the

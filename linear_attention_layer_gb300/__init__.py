@@ -22,7 +22,7 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
            "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
-           "EXPORTED_SYMBOLS"]
+           "recurrent_bwd", "recurrent_bwd_workspace_size", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -35,7 +35,8 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
 EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_fwd",
                     "kda_decode_step", "kda_decode_window", "kda_decode_replay",
                     "kda_decode_replay_window", "kda_status_string", "kda_get_device_error",
-                    "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout")
+                    "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout",
+                    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -82,6 +83,10 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_recurrent_bwd.restype = ctypes.c_int
+        lib.kda_recurrent_bwd.argtypes = [dp] + [vp] * 16
+        lib.kda_recurrent_bwd_workspace_size.restype = ctypes.c_int
+        lib.kda_recurrent_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_testing_inject_wait_timeout.restype = None
@@ -275,6 +280,69 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, c
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_workspace_size")
     return int(n.value)
+
+
+def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host):
+    """Bytes of device workspace ``recurrent_bwd`` needs (dk = dv = 128)."""
+    N = len(cu_seqlens_host) - 1
+    desc, keep = make_desc(N, int(cu_seqlens_host[-1]), num_heads, 128, 128, _io_code(dtype),
+                           cu_seqlens_host)
+    n = ctypes.c_size_t(0)
+    st = load().kda_recurrent_bwd_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_recurrent_bwd_workspace_size")
+    return int(n.value)
+
+
+def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=None, *,
+                  cu_seqlens_host, a_log=None, workspace=None, grads=None, stream=None):
+    """Reverse mode of the prefill (``kda_recurrent_bwd``): given dL/d out and
+    dL/d final_state (None: zeros), returns (dq, dk, dv, dz, dbeta,
+    d_initial_state), fp32, for the inputs of the forward call (same q, k, v,
+    z, beta, cu_seqlens, initial_state and a_log; dk = dv = 128, one gate per
+    key channel).  ``cu_seqlens_host`` is required; ``workspace`` (a device
+    tensor of ``recurrent_bwd_workspace_size`` bytes) is allocated here when
+    None; ``grads`` may give the six output tensors to fill."""
+    lib = load()
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (T, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (T, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (T, H, dv), dev)
+    _check_tensor("z", z, torch.float32, (T, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (T, H), dev)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    _check_tensor("d_out", d_out, q.dtype, (T, H, dv), dev)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+    if d_final is not None:
+        _check_tensor("d_final", d_final, torch.float32, (N, H, dk, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    if grads is None:
+        f32 = dict(dtype=torch.float32, device=dev)
+        grads = (torch.empty((T, H, dk), **f32), torch.empty((T, H, dk), **f32),
+                 torch.empty((T, H, dv), **f32), torch.empty((T, H, dk), **f32),
+                 torch.empty((T, H), **f32), torch.empty((N, H, dk, dv), **f32))
+    shapes = ((T, H, dk), (T, H, dk), (T, H, dv), (T, H, dk), (T, H), (N, H, dk, dv))
+    for name, g, shp in zip(("dq", "dk", "dv", "dz", "dbeta", "d_initial"), grads, shapes):
+        _check_tensor(name, g, torch.float32, shp, dev)
+    if workspace is None:
+        nbytes = recurrent_bwd_workspace_size(H, q.dtype, cu_seqlens_host)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
+    with torch.cuda.device(dev):
+        st = lib.kda_recurrent_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                   _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                                   _ptr(d_out), _ptr(d_final), *[_ptr(g) for g in grads],
+                                   _stream_handle(stream))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_recurrent_bwd")
+    return grads
 
 
 def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):

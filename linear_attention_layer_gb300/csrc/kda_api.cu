@@ -99,6 +99,33 @@ kda_status_t prefill_common(const kda_desc_t* desc, const void* q, const void* k
   return KDA_OK;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+kda_status_t check_bwd(const kda_desc_t* desc, const void* q, const void* k, const void* v,
+                       const float* z, const float* beta, const float* initial_state,
+                       const int32_t* cu_seqlens, const void* d_out, const float* d_final,
+                       const float* dq, const float* dk, const float* dv, const float* dz,
+                       const float* dbeta, const float* d_initial) {
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (!desc->cu_seqlens_host || !cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->dk != 128 || desc->dv != 128 || desc->gate_per_head != 0) return KDA_ERR_UNSUPPORTED;
+  if (desc->total_tokens > 0) {
+    const void* need[] = {q, k, v, z, beta, d_out, dq, dk, dv, dz, dbeta};
+    for (const void* x : need)
+      if (!x) return KDA_ERR_INVALID_ARGUMENT;
+    const void* outs[] = {dq, dk, dv, dz, dbeta};
+    const void* ins[] = {q, k, v, z, beta, d_out};
+    for (const void* o : outs)
+      for (const void* i : ins)
+        if (o == i) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  const void* al[] = {q, k, v, z, d_out, dq, dk, dv, dz, initial_state, d_final, d_initial};
+  for (const void* x : al)
+    if (x && !aligned16(x)) return KDA_ERR_INVALID_ARGUMENT;
+  return KDA_OK;
+}
 }  // namespace
 
 namespace kda {
@@ -242,6 +269,44 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
   wn.q = q; wn.k = k; wn.v = v; wn.z = z; wn.beta = beta; wn.W = window;
   cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
                                      state, out, err, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes) {
+  if (!bytes || !desc) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (!desc->cu_seqlens_host) return KDA_ERR_INVALID_ARGUMENT;
+  *bytes = kda::recurrent_bwd_workspace_bytes(to_problem(desc), desc->cu_seqlens_host);
+  return KDA_OK;
+}
+
+kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void* k,
+                               const void* v, const float* z, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens,
+                               const void* d_out, const float* d_final_state, float* dq,
+                               float* dk, float* dv, float* dz, float* dbeta,
+                               float* d_initial_state, kda_stream_t stream) {
+  kda_status_t s = check_bwd(desc, q, k, v, z, beta, initial_state, cu_seqlens, d_out,
+                             d_final_state, dq, dk, dv, dz, dbeta, d_initial_state);
+  if (s != KDA_OK) return s;
+  const kda::Problem p = to_problem(desc);
+  const size_t need = kda::recurrent_bwd_workspace_bytes(p, desc->cu_seqlens_host);
+  if (need > 0 && (!desc->workspace || desc->workspace_bytes < need || !aligned16(desc->workspace)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  kda::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.z = z; a.beta = beta;
+  a.initial_state = initial_state;
+  a.cu_seqlens = cu_seqlens;
+  a.d_out = d_out;
+  a.d_final = d_final_state;
+  a.a_log = desc->a_log;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dz = dz; a.dbeta = dbeta;
+  a.d_initial = d_initial_state;
+  a.err = device_error_word();
+  if (!a.err) return KDA_ERR_CUDA;
+  cudaError_t e = kda::launch_recurrent_bwd(p, a, desc->cu_seqlens_host, desc->workspace,
+                                            (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

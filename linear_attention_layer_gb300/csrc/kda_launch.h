@@ -79,6 +79,30 @@ size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,
                             size_t ws_bytes, cudaStream_t stream);
 
+// Reverse mode of the recurrence, token by token (fp32; dk = dv = 128).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* z;
+  const float* beta;
+  const float* initial_state;  // may be null (zeros)
+  const int32_t* cu_seqlens;   // device
+  const void* d_out;           // io dtype, like out
+  const float* d_final;        // may be null (zeros)
+  const float* a_log;          // may be null (A = 0)
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dz;
+  float* dbeta;
+  float* d_initial;  // may be null
+  int* err;
+};
+size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host);
+cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                 void* ws, cudaStream_t stream);
+
 }  // namespace kda
 
 #include "../../include/kda.h"
