@@ -37,6 +37,16 @@ STATE_BYTES = 128 * 128 * 4
 # (WS, Q+S, Khat^T U) per C tokens = 10 C d + 6 d^2.
 CHUNK = 64
 FLOPS_PER_HEAD_TOKEN = 10 * CHUNK * 128 + 6 * 128 * 128
+# Reverse mode (kda_recurrent_bwd), fp32 CUDA cores, per head-token: two
+# forward passes over the state (the stored states, then the rebuild) at 5
+# flops per state element (decay, the e reduction, the rank-1 write) and the
+# reverse step at 16 (read-out, y, dq^, dk^, dalpha and the decayed dS).
+BWD_FLOPS_PER_HEAD_TOKEN = (2 * 5 + 16) * 128 * 128
+# Bytes a reverse pass cannot avoid per head-token: q, k, v, d out (bf16),
+# z (fp32) and beta read; dq, dk, dv, dz (fp32) and dbeta written.
+BWD_BYTES_PER_HEAD_TOKEN = 4 * 256 + 512 + 4 + 4 * 512 + 4
+# fp32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 flops per FMA x 2.07 GHz.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -407,6 +417,50 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False, clk=None):
     return total_ms, per_launch
 
 
+def bench_backward(kda, p, steps, warmup, device, clk=None):
+    """kda_recurrent_bwd over the prefill workload with random cotangents
+    (d out bf16, d final state fp32).  Returns (total ms, per-launch ms)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(99)
+    H = p.meta["num_heads"]
+    d_out = torch.randn(p.v.shape, device=device, generator=g).to(p.q.dtype)
+    d_fin = torch.randn((p.num_seqs, H, 128, 128), device=device, generator=g)
+    nbytes = kda.recurrent_bwd_workspace_size(H, p.q.dtype, p.cu_seqlens_host)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    T = p.total_tokens
+    f32 = dict(dtype=torch.float32, device=device)
+    grads = (torch.empty((T, H, 128), **f32), torch.empty((T, H, 128), **f32),
+             torch.empty((T, H, 128), **f32), torch.empty((T, H, 128), **f32),
+             torch.empty((T, H), **f32), torch.empty((p.num_seqs, H, 128, 128), **f32))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.recurrent_bwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out,
+                          d_fin, cu_seqlens_host=p.cu_seqlens_host, workspace=ws, grads=grads)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = []
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
+    t0.record(stream)
+    for _ in range(steps):
+        evs.append(event_time_ms(step, stream))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
+    err = kda.get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err} after the timed backward")
+    del grads, ws, d_out, d_fin
+    torch.cuda.empty_cache()
+    return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs]
+
+
 def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
     """Speculative decoding: per step one kda_decode_replay_window call -- the
     replay of the previous window's accepted prefix and the outputs of the
@@ -524,7 +578,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long,spec")
+    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long,spec,bwd")
+    ap.add_argument("--bwd-steps", type=int, default=3)
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
                     help="pass scratch so that few long sequences are split across SMs")
@@ -602,6 +657,30 @@ def main():
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
     }
+
+    # ---- reverse mode over the same workload ----
+    if "bwd" not in skip:
+        bclk = clock_sampler(gpu_uuid)
+        b_ms, b_launch = bench_backward(kda, p, args.bwd_steps, args.warmup, device, clk=bclk)
+        b_launch_ms = statistics.mean(b_launch)
+        b_flops = T * H * BWD_FLOPS_PER_HEAD_TOKEN
+        b_tf = b_flops / (b_launch_ms * 1e-3) / 1e12
+        b_bytes = T * H * BWD_BYTES_PER_HEAD_TOKEN + 3 * N * H * STATE_BYTES
+        b_gbs = b_bytes / (b_launch_ms * 1e-3) / 1e9
+        line["backward"] = {
+            "value": round(weak_scaling_value(T, world, b_ms / 1e3 / args.bwd_steps), 3),
+            "unit": UNIT, "ms_per_step": round(b_ms / args.bwd_steps, 3),
+            "steps": args.bwd_steps, "kernel": "kda_recurrent_bwd",
+            "workload": workloads.DESCRIPTIONS[args.workload] + "; random d out and d final state",
+            "roofline": {"bound": "alu", "achieved": round(b_tf, 2),
+                         "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+                         "frac": round(b_tf / FP32_ALU_TFLOPS, 4), "traffic": None,
+                         "flops_per_head_token": BWD_FLOPS_PER_HEAD_TOKEN,
+                         "peak_source": "fp32 CUDA-core peak from unit counts and the 2.07 GHz "
+                                        "maximum SM clock"},
+            "hbm": {"achieved": round(b_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(b_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": b_bytes},
+            "clocks": bclk.summary(), "gpu_launches": args.bwd_steps}
 
     # ---- the long single-sequence workload, split across SMs ----
     if "long" not in skip and args.workload != "long":
