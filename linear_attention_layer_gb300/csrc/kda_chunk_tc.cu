@@ -464,25 +464,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
       // ---------------- C: gate and cumulative decay ----------------
       // thread = (subtile a, key channel c) with its 16 tokens t = 16a + i; a
-      // warp covers 32 channels of one subtile.  G[i] is the cumulative
-      // log-decay from the start of the subtile through token t, i.e. G_t - r_a.
+      // warp covers 32 channels of one subtile.  With G[i] the cumulative
+      // log-decay from the start of the subtile through token t (G_t - r_a),
+      // F[i] = e^{G[i]} is the running product of the per-token retentions
+      // alpha = e^g and E[i] = e^{-G[i]} = (1 / F[15]) prod_{j > i} alpha_j, so
+      // one exponential per token gives both (no factor leaves [e^-80, e^80]).
       const int c = tid & 127, a = tid >> 7;
-      float G[16];
+      float F[16], E[16];
       {
         const float* Z = reinterpret_cast<const float*>(sm + OFF_Z);
         if (kZHead) {  // one logit per (token, head): every channel gets the same gate
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            G[i] = 16 * a + i < len ? __ldg(P.zh + (size_t)(t0 + 16 * a + i) * H + h) : 0.f;
+            F[i] = 16 * a + i < len ? __ldg(P.zh + (size_t)(t0 + 16 * a + i) * H + h) : 0.f;
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) G[i] = Z[(16 * a + i) * kD + c];
+          for (int i = 0; i < 16; ++i) F[i] = Z[(16 * a + i) * kD + c];
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) G[i] = (16 * a + i < len) ? log_decay_c(G[i], zcoef) : 0.f;
+        for (int i = 0; i < 16; ++i)  // alpha = e^g = 2^{g log2 e}; 1 past the sequence end
+          F[i] = (16 * a + i < len) ? ex2_approx(log_decay_c(F[i], zcoef) * 1.4426950408889634f)
+                                    : 1.f;
+        E[15] = 1.f;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) G[i] += G[i - 1];
-        misc[M_TOT + a * kD + c] = G[15];
+        for (int i = 14; i >= 0; --i) E[i] = E[i + 1] * F[i + 1];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) F[i] *= F[i - 1];
+        const float inv = __frcp_rn(F[15]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) E[i] *= inv;
+        misc[M_TOT + a * kD + c] = F[15];  // e^{tot_a}, the subtile's whole decay
       }
       tc_fence_before();
       if (__syncthreads_or(!ok)) { aborted = true; break; }  // subtile totals, token norms
@@ -493,11 +504,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // barrier, writes the Gram operands over the stages and the fp16
       // operands of the dense products.
       {
-        float tot[4];
+        float et[4];  // e^{tot_b}: each subtile's decay
 #pragma unroll
-        for (int b = 0; b < 4; ++b) tot[b] = misc[M_TOT + b * kD + c];
-        const float r = (a > 0 ? tot[0] : 0.f) + (a > 1 ? tot[1] : 0.f) + (a > 2 ? tot[2] : 0.f);
-        if (a == 0) misc[M_DECAY + c] = __expf(tot[0] + tot[1] + tot[2] + tot[3]);
+        for (int b = 0; b < 4; ++b) et[b] = misc[M_TOT + b * kD + c];
+        if (a == 0) misc[M_DECAY + c] = et[0] * et[1] * et[2] * et[3];
         float qt[16], kq[16], kt[16];  // Q~, K~q (<= 1) and K~ = K^(a) (<= e^80)
         // Row t = 16a + i of a 128-byte-swizzled tile holds this thread's element in
         // 16-byte chunk (x ^ (i % 8)) with x its unswizzled chunk, so the address is
@@ -507,16 +517,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const uint32_t x = ((uint32_t)c & 63) >> 3;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float F = ex2_approx(G[i] * 1.4426950408889634f), E = ex2_approx(G[i] * -1.4426950408889634f);
             const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
             const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qk + off)) *
                             misc[M_RQ + 16 * a + i];
             const float k = __bfloat162float(
                                 *reinterpret_cast<const __nv_bfloat16*>(qk + OFF_K - OFF_Q + off)) *
                             misc[M_RK + 16 * a + i];
-            qt[i] = q * F;
-            kq[i] = k * F;
-            kt[i] = k * E;
+            qt[i] = q * F[i];
+            kq[i] = k * F[i];
+            kt[i] = k * E[i];
           }
         }
         // The previous chunk's last products read Khat, overwritten below: wait for them.
@@ -532,10 +541,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // adjacent-subtile factors e^{r_{b+1} - r_b} = e^{tot_b} (r_4 = G_C), each >= e^-80
         float ed[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) ed[b] = b >= a ? __expf(tot[b]) : 1.f;
+        for (int b = 0; b < 4; ++b) ed[b] = b >= a ? et[b] : 1.f;
         // fp16 dense operands (outside the input stages, so before the barrier), row c
         // of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a}, K+ = K~q e^{r_a}, Khat
-        const float er = __expf(r);
+        const float er = (a > 0 ? et[0] : 1.f) * (a > 1 ? et[1] : 1.f) * (a > 2 ? et[2] : 1.f);
         const uint32_t rowoff = (uint32_t)c * 128u;
 #pragma unroll
         for (int h8 = 0; h8 < 2; ++h8) {
