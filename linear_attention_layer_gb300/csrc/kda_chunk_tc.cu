@@ -103,7 +103,7 @@ constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major
 constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-major B
 constexpr uint32_t OFF_MISC = 212992;
 // misc floats
-constexpr int M_BETA = 0, M_RQ = 64, M_RK = 128, M_DECAY = 192, M_TOT = 320,
+constexpr int M_BETA = 0, M_RQK = 64, M_DECAY = 192, M_TOT = 320,
               M_END = 320 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
@@ -226,7 +226,15 @@ __device__ __forceinline__ uint64_t desc_mn(uint64_t base, uint32_t off) {
 }
 
 // x rounded to tf32 (nearest, ties away), kept as an fp32 bit pattern
-__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
+// The Gram's fp32 operands go to the tensor core as they are; it reads them as
+// tf32, keeping the top 10 fraction bits (truncation toward zero, a mean error
+// of -1/2 tf32 ulp).  Scaling them by 1 + ln(2)/2048 beforehand lifts a value
+// of significand m by m ln(2)/2 ulp, which centres that error for significands
+// spread log-uniformly over [1, 2) (their mean is 1/ln 2); the error stays
+// within one ulp.  The lift rides on the token norms; the fp16 operands made
+// from the same values take it back out.
+constexpr float kTf32Lift = 1.0003384f;
+constexpr float kTf32Unlift = 0.9996617f;
 
 // Barrier of warps 0-11 (the ones inverting I + A), id 1.
 __device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 384;" ::: "memory"); }
@@ -452,8 +460,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           sk += __shfl_xor_sync(0xffffffffu, sk, o);
         }
         if (e == 0) {
-          misc[M_RQ + t] = t < len ? rsqrtf(sq + kNormEps) : 0.f;
-          misc[M_RK + t] = t < len ? rsqrtf(sk + kNormEps) : 0.f;
+          // (rq, rk) per token, both times kTf32Lift (see the Gram operands)
+          *reinterpret_cast<float2*>(misc + M_RQK + 2 * t) =
+              t < len ? make_float2(rsqrtf(sq + kNormEps) * kTf32Lift,
+                                    rsqrtf(sk + kNormEps) * kTf32Lift)
+                      : make_float2(0.f, 0.f);
         }
         if (tid < kC) {
           misc[M_BETA + tid] = beta_pf;
@@ -518,11 +529,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
+            const float2 rqk = *reinterpret_cast<const float2*>(misc + M_RQK + 2 * (16 * a + i));
             const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qk + off)) *
-                            misc[M_RQ + 16 * a + i];
+                            rqk.x;
             const float k = __bfloat162float(
                                 *reinterpret_cast<const __nv_bfloat16*>(qk + OFF_K - OFF_Q + off)) *
-                            misc[M_RK + 16 * a + i];
+                            rqk.y;
             qt[i] = q * F[i];
             kq[i] = k * F[i];
             kt[i] = k * E[i];
@@ -544,7 +556,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int b = 0; b < 4; ++b) ed[b] = b >= a ? et[b] : 1.f;
         // fp16 dense operands (outside the input stages, so before the barrier), row c
         // of [c][t] (tokens 16a .. 16a+15): Q+ = Q~ e^{r_a}, K+ = K~q e^{r_a}, Khat
-        const float er = (a > 0 ? et[0] : 1.f) * (a > 1 ? et[1] : 1.f) * (a > 2 ? et[2] : 1.f);
+        // (the fp16 operands drop the tf32 lift carried by qt, kq and kt)
+        const float er = (a > 0 ? et[0] : 1.f) * (a > 1 ? et[1] : 1.f) * (a > 2 ? et[2] : 1.f) *
+                         kTf32Unlift;
+        const float ed3 = ed[3] * kTf32Unlift;
         const uint32_t rowoff = (uint32_t)c * 128u;
 #pragma unroll
         for (int h8 = 0; h8 < 2; ++h8) {
@@ -555,9 +570,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i = 0; i < 8; ++i) {
             float x = kt[i0 + i];
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int b = 0; b < 3; ++b)
               if (b >= a) x *= ed[b];
-            kh[i] = x;
+            kh[i] = x * ed3;
           }
           *reinterpret_cast<uint4*>(sm + OFF_QPT + off) = make_uint4(
               pack_f16(qt[i0] * er, qt[i0 + 1] * er), pack_f16(qt[i0 + 2] * er, qt[i0 + 3] * er),
@@ -583,10 +598,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i0 = 0; i0 < 16; i0 += 4) {
             const uint32_t so = 128u * i0 + ((i0 & 4) ? so4 : so0);
             // M-side rows: Q~ at t, K~q at 64 + t
-            stmatrix_x4(gm + so, to_tf32(qt[i0]), to_tf32(qt[i0 + 1]), to_tf32(qt[i0 + 2]),
-                        to_tf32(qt[i0 + 3]));
-            stmatrix_x4(gm + 64 * 128 + so, to_tf32(kq[i0]), to_tf32(kq[i0 + 1]),
-                        to_tf32(kq[i0 + 2]), to_tf32(kq[i0 + 3]));
+            stmatrix_x4(gm + so, __float_as_uint(qt[i0]), __float_as_uint(qt[i0 + 1]),
+                        __float_as_uint(qt[i0 + 2]), __float_as_uint(qt[i0 + 3]));
+            stmatrix_x4(gm + 64 * 128 + so, __float_as_uint(kq[i0]), __float_as_uint(kq[i0 + 1]),
+                        __float_as_uint(kq[i0 + 2]), __float_as_uint(kq[i0 + 3]));
             // N side: K^(a') = k^ e^{r_a' - G} for a' = a .. 3, rows ka_row(a') + t, by
             // the chain K^(a'+1) = K^(a') e^{r_a'+1 - r_a'} (no factor below e^-80)
             float v0 = kt[i0], v1 = kt[i0 + 1], v2 = kt[i0 + 2], v3 = kt[i0 + 3];
@@ -597,8 +612,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float e = ed[ap - 1];
                 v0 *= e; v1 *= e; v2 *= e; v3 *= e;
               }
-              stmatrix_x4(gn + ka_row(ap) * 128 + so, to_tf32(v0), to_tf32(v1), to_tf32(v2),
-                          to_tf32(v3));
+              stmatrix_x4(gn + ka_row(ap) * 128 + so, __float_as_uint(v0), __float_as_uint(v1),
+                          __float_as_uint(v2), __float_as_uint(v3));
             }
           }
         }
