@@ -198,3 +198,7 @@ def decode_step(q, k, v, z, beta, state, *, eps: float = DEFAULT_EPS,
     out, fin, _ = recurrent(q, k, v, z, beta, cu, state, eps=eps,
                             threads=threads, raw_log_decay=raw_log_decay, a_log=a_log)
     return out, fin
+
+
+# The Q/K preprocessing convolution + Swish (pure numpy, fp64).
+from .short_conv import short_conv, swish  # noqa: E402,F401
