@@ -461,6 +461,45 @@ def bench_backward(kda, p, steps, warmup, device, clk=None):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs]
 
 
+def bench_short_conv(kda, p, steps, warmup, device, width=4, clk=None):
+    """kda_short_conv on q and on k of the prefill workload (width 4, with an
+    incoming and an outgoing convolution state).  Returns (total ms, per-step ms)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    H, D, N = p.meta["num_heads"], p.meta["dk"], p.num_seqs
+    wq = torch.randn((H, D, width), device=device, generator=g) * 0.5
+    wk = torch.randn((H, D, width), device=device, generator=g) * 0.5
+    sq = torch.randn((N, H, D, width - 1), device=device, generator=g)
+    sk = torch.randn((N, H, D, width - 1), device=device, generator=g)
+    yq, yk = torch.empty_like(p.q), torch.empty_like(p.k)
+    fq, fk = torch.empty_like(sq), torch.empty_like(sk)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.short_conv(p.q, wq, p.cu_seqlens, sq, out=yq, final_state=fq)
+        kda.short_conv(p.k, wk, p.cu_seqlens, sk, out=yk, final_state=fk)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = []
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
+    t0.record(stream)
+    for _ in range(steps):
+        evs.append(event_time_ms(step, stream))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
+    err = kda.get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err} after the timed convolution")
+    return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs]
+
+
 def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
     """Speculative decoding: per step one kda_decode_replay_window call -- the
     replay of the previous window's accepted prefix and the outputs of the
@@ -578,7 +617,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--skip", default="", help="comma list of: decode,e2e,cpu,long,spec,bwd")
+    ap.add_argument("--skip", default="",
+                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv")
     ap.add_argument("--bwd-steps", type=int, default=3)
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
@@ -681,6 +721,24 @@ def main():
             "hbm": {"achieved": round(b_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(b_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": b_bytes},
             "clocks": bclk.summary(), "gpu_launches": args.bwd_steps}
+
+    # ---- the Q/K short convolution + Swish over the same workload ----
+    if "conv" not in skip:
+        cclk = clock_sampler(gpu_uuid)
+        c_ms, c_steps = bench_short_conv(kda, p, args.steps, args.warmup, device, clk=cclk)
+        c_step_ms = statistics.mean(c_steps)
+        # per head-token: q and k read and their outputs written (bf16); per
+        # (sequence, head): both states read and written, 3 x 128 fp32 each
+        c_bytes = T * H * 4 * 256 + 4 * N * H * 128 * 3 * 4 + 2 * H * 128 * 4 * 4
+        c_gbs = c_bytes / (c_step_ms * 1e-3) / 1e9
+        line["short_conv"] = {
+            "value": round(c_gbs, 1), "unit": "GB/s", "ms_per_step": round(c_ms / args.steps, 4),
+            "steps": args.steps, "kernel": "kda_short_conv", "width": 4,
+            "workload": workloads.DESCRIPTIONS[args.workload] + "; q and k, width 4, with states",
+            "roofline": {"bound": "hbm", "achieved": round(c_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(c_gbs / hbm_peak, 4), "traffic": None,
+                         "algorithmic_bytes_per_step": c_bytes},
+            "clocks": cclk.summary(), "gpu_launches": 4 * args.steps}
 
     # ---- the long single-sequence workload, split across SMs ----
     if "long" not in skip and args.workload != "long":

@@ -335,6 +335,44 @@ kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void
  * SM) 64 KiB per 8 tokens of the longest sequence, plus 512 KiB. */
 kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
 
+/*
+ * kda_short_conv -- the Q/K preprocessing before the recurrence
+ * (mhpq.cn/news/56770, section "KDA 到底在算什么", the Q/K preprocessing
+ * paragraph: a short causal convolution over the most recent few positions,
+ * then a Swish activation, then the L2 normalisation that kda_chunk_fwd and
+ * kda_decode_step apply themselves).  The page gives neither width nor form;
+ * this call is a depthwise causal convolution of width W (1..4) without bias:
+ *
+ *     y[t, h, d] = swish( sum_{j<W} weight[h, d, j] x[t - (W-1) + j, h, d] ),
+ *     swish(u) = u / (1 + e^{-u}),
+ *
+ * where the positions before a sequence's first token read its convolution
+ * state.  Apply it to q and to k (one call each, with their own weights).
+ *
+ *   desc             num_seqs, total_tokens, num_heads, io_dtype as for
+ *                    kda_chunk_fwd; the channel count is desc->dk (32, 64
+ *                    or 128); other fields are ignored.  For a decode step
+ *                    pass cu_seqlens = 0, 1, .., N.
+ *   width            W, 1..4 (KDA_ERR_UNSUPPORTED above 4)
+ *   x                device, [T_tot, H, dk] io dtype, read
+ *   weight           device, [H, dk, W] fp32 (tap j multiplies x[t-(W-1)+j])
+ *   conv_state_in    device, [N, H, dk, W-1] fp32: each sequence's W-1 inputs
+ *                    before its first token, oldest first; NULL for zeros
+ *   cu_seqlens       device, [N + 1] int32
+ *   y                device, [T_tot, H, dk] io dtype, written; must not
+ *                    alias x, weight or conv_state_in
+ *   conv_state_out   device, [N, H, dk, W-1] fp32, written with each
+ *                    sequence's last W-1 inputs (continued from
+ *                    conv_state_in when shorter), or NULL; may alias
+ *                    conv_state_in exactly (it is written after every read)
+ * x and y must be 16-byte aligned.  A device cu_seqlens that does not start
+ * at 0, end at T_tot and rise monotonically sets the device error word.
+ */
+kda_status_t kda_short_conv(const kda_desc_t* desc, int32_t width, const void* x,
+                            const float* weight, const float* conv_state_in,
+                            const int32_t* cu_seqlens, void* y, float* conv_state_out,
+                            kda_stream_t stream);
+
 const char* kda_status_string(kda_status_t status);
 
 /* Synchronise `stream`, then read and clear the device error word of the

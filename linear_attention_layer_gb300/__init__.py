@@ -22,7 +22,7 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
            "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
-           "recurrent_bwd", "recurrent_bwd_workspace_size", "EXPORTED_SYMBOLS"]
+           "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_decode_step", "kda_decode_window", "kda_decode_replay",
                     "kda_decode_replay_window", "kda_status_string", "kda_get_device_error",
                     "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout",
-                    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size")
+                    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "kda_short_conv")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -85,6 +85,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_recurrent_bwd.restype = ctypes.c_int
         lib.kda_recurrent_bwd.argtypes = [dp] + [vp] * 16
+        lib.kda_short_conv.restype = ctypes.c_int
+        lib.kda_short_conv.argtypes = [dp, ctypes.c_int32] + [vp] * 7
         lib.kda_recurrent_bwd_workspace_size.restype = ctypes.c_int
         lib.kda_recurrent_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_status_string.restype = ctypes.c_char_p
@@ -280,6 +282,41 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, c
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_workspace_size")
     return int(n.value)
+
+
+def short_conv(x, weight, cu_seqlens, conv_state=None, *, out=None, final_state=None,
+               output_final_state=True, stream=None):
+    """The Q/K preprocessing (``kda_short_conv``): depthwise causal convolution
+    of width W = weight.shape[-1] (1..4) over each sequence, then Swish.
+    x [T, H, D] (bf16 or fp32), weight [H, D, W] fp32, conv_state [N, H, D,
+    W - 1] fp32 or None (zeros).  Returns (y, final conv state or None);
+    ``final_state`` may be ``conv_state`` itself (updated in place)."""
+    lib = load()
+    T, H, D = x.shape
+    W = weight.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = x.device
+    _check_tensor("x", x, x.dtype, (T, H, D), dev)
+    _check_tensor("weight", weight, torch.float32, (H, D, W), dev)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if conv_state is not None:
+        _check_tensor("conv_state", conv_state, torch.float32, (N, H, D, W - 1), dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _check_tensor("out", out, x.dtype, (T, H, D), dev)
+    if final_state is None and output_final_state and W > 1:
+        final_state = torch.empty((N, H, D, W - 1), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check_tensor("final_state", final_state, torch.float32, (N, H, D, W - 1), dev)
+    desc, keep = make_desc(N, T, H, D, D, _io_code(x.dtype))
+    with torch.cuda.device(dev):
+        st = lib.kda_short_conv(ctypes.byref(desc), int(W), _ptr(x), _ptr(weight),
+                                _ptr(conv_state), _ptr(cu_seqlens), _ptr(out),
+                                _ptr(final_state), _stream_handle(stream))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_short_conv")
+    return out, final_state
 
 
 def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host):

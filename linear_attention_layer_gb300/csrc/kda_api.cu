@@ -272,6 +272,38 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_short_conv(const kda_desc_t* desc, int32_t width, const void* x,
+                            const float* weight, const float* conv_state_in,
+                            const int32_t* cu_seqlens, void* y, float* conv_state_out,
+                            kda_stream_t stream) {
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (width < 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (width > 4) return KDA_ERR_UNSUPPORTED;
+  if (!cu_seqlens || !weight) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->total_tokens > 0 && (!x || !y)) return KDA_ERR_INVALID_ARGUMENT;
+  if (y && (y == x || y == (const void*)weight || y == (const void*)conv_state_in))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (conv_state_out && conv_state_out != conv_state_in &&
+      ((const void*)conv_state_out == x || (const void*)conv_state_out == y))
+    return KDA_ERR_INVALID_ARGUMENT;
+  const void* al[] = {x, y};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARGUMENT;
+  kda::ConvArgs a;
+  a.x = x;
+  a.weight = weight;
+  a.state_in = conv_state_in;
+  a.cu_seqlens = cu_seqlens;
+  a.y = y;
+  a.state_out = conv_state_out;
+  a.width = width;
+  a.err = device_error_word();
+  if (!a.err) return KDA_ERR_CUDA;
+  cudaError_t e = kda::launch_short_conv(to_problem(desc), a, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes) {
   if (!bytes || !desc) return KDA_ERR_INVALID_ARGUMENT;
   kda_status_t s = check_desc(desc, false);

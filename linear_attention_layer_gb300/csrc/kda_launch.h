@@ -103,6 +103,19 @@ size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
                                  void* ws, cudaStream_t stream);
 
+// The Q/K preprocessing convolution (depthwise, causal, width 1..4) + Swish.
+struct ConvArgs {
+  const void* x;           // [T, H, D] io dtype
+  const float* weight;     // [H, D, W]
+  const float* state_in;   // [N, H, D, W - 1] or null (zeros)
+  const int32_t* cu_seqlens;
+  void* y;                 // [T, H, D] io dtype
+  float* state_out;        // [N, H, D, W - 1] or null; may equal state_in
+  int width;
+  int* err;
+};
+cudaError_t launch_short_conv(const Problem& p, const ConvArgs& a, cudaStream_t stream);
+
 }  // namespace kda
 
 #include "../../include/kda.h"

@@ -194,3 +194,20 @@ def test_backward_workspace_size_query(lib):
     assert n.value > 0 and n.value % (16 * 64 * 1024) == 0
     nohost, keep2 = kda.make_desc(2, 100, 4, 128, 128, kda.KDA_BF16)
     assert lib.kda_recurrent_bwd_workspace_size(ctypes.byref(nohost), ctypes.byref(n)) == 1
+
+
+def test_short_conv_rejects_bad_arguments(lib):
+    d, keep = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16)
+    y = ctypes.c_void_p(0x2000)
+    f = lib.kda_short_conv
+    assert f(ctypes.byref(d), 0, FAKE, FAKE, None, FAKE, y, None, None) == 1       # width 0
+    assert f(ctypes.byref(d), 5, FAKE, FAKE, None, FAKE, y, None, None) == 2       # width 5
+    assert f(ctypes.byref(d), 4, FAKE, None, None, FAKE, y, None, None) == 1       # no weight
+    assert f(ctypes.byref(d), 4, FAKE, FAKE, None, None, y, None, None) == 1       # no cu_seqlens
+    assert f(ctypes.byref(d), 4, None, FAKE, None, FAKE, y, None, None) == 1       # no x
+    assert f(ctypes.byref(d), 4, FAKE, ctypes.c_void_p(0x3000), None, FAKE, FAKE, None,
+             None) == 1                                                           # y aliases x
+    assert f(ctypes.byref(d), 4, ctypes.c_void_p(0x1008), ctypes.c_void_p(0x3000), None, FAKE,
+             y, None, None) == 1                                                  # x misaligned
+    bad, keep2 = kda.make_desc(2, 8, 2, 48, 48, kda.KDA_BF16)
+    assert f(ctypes.byref(bad), 4, FAKE, FAKE, None, FAKE, y, None, None) == 1    # dk = 48

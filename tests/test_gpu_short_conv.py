@@ -1,0 +1,121 @@
+"""GPU parity of the Q/K preprocessing convolution (``kda_short_conv``)
+against the fp64 oracle (oracle/short_conv.py), element by element.
+
+Tolerances: fp32 io, relative L2 <= 1e-5 and max |err| <= 1e-5 (a width-4
+fp32 dot product, one exponential and one division); bf16 io, every output
+within half a bf16 ulp of the oracle's value plus 1e-5 (the single rounding of
+the store).  The outgoing convolution state is a copy of inputs and must match
+exactly."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_layer_gb300 as kda
+import oracle
+from tests.parity import as64, half_ulp, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.load()
+    torch.cuda.set_device(0)
+
+
+def _inputs(lengths, H, D, W, dtype, seed, with_state=True):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    T, N = int(cu[-1]), len(lengths)
+    x = (torch.randn((T, H, D), device=DEV, generator=g) * 1.5).to(dtype)
+    w = torch.randn((H, D, W), device=DEV, generator=g) * 0.6
+    st = torch.randn((N, H, D, W - 1), device=DEV, generator=g) if with_state and W > 1 else None
+    return x, w, st, torch.tensor(cu, dtype=torch.int32, device=DEV), [int(c) for c in cu]
+
+
+def _check(y, ref, dtype):
+    y64, r = as64(y), as64(ref)
+    if dtype == torch.float32:
+        assert rel_l2(y64, r) <= 1e-5
+        assert np.max(np.abs(y64 - r), initial=0.0) <= 1e-5
+    else:
+        bound = half_ulp(r, torch.bfloat16) + 1e-5 + 1e-5 * np.abs(r)
+        assert np.all(np.abs(y64 - r) <= bound), np.max(np.abs(y64 - r) - bound)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_short_conv_ragged(dtype, W):
+    # segment boundaries every 64 tokens fall inside, at the start of and
+    # between sequences; one empty sequence and several shorter than W - 1
+    lengths = [1, 2, 0, 63, 64, 65, 3, 130, 1]
+    x, w, st, cu, cu_h = _inputs(lengths, 3, 128, W, dtype, seed=10 + W)
+    y, fin = kda.short_conv(x, w, cu, st)
+    torch.cuda.synchronize()
+    ry, rfin = oracle.short_conv(x, w, cu_h, st)
+    _check(y, ry, dtype)
+    if W > 1:
+        assert np.array_equal(as64(fin), rfin)
+    assert kda.get_device_error() == 0
+
+
+@pytest.mark.parametrize("D", [32, 64])
+def test_short_conv_small_channels_no_state(D):
+    x, w, _, cu, cu_h = _inputs([5, 70], 2, D, 4, torch.bfloat16, seed=3, with_state=False)
+    y, fin = kda.short_conv(x, w, cu, None)
+    torch.cuda.synchronize()
+    ry, rfin = oracle.short_conv(x, w, cu_h, None)
+    _check(y, ry, torch.bfloat16)
+    assert np.array_equal(as64(fin), rfin)
+
+
+def test_short_conv_decode_steps_in_place():
+    """Decode: one token per request, the state updated in place, three steps
+    equal to one pass over the three tokens."""
+    N, H, D, W = 37, 4, 128, 4
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    xs = (torch.randn((3, N, H, D), device=DEV, generator=g)).to(torch.bfloat16)
+    w = torch.randn((H, D, W), device=DEV, generator=g) * 0.6
+    st = torch.randn((N, H, D, W - 1), device=DEV, generator=g)
+    st0 = st.clone()
+    cu = torch.arange(N + 1, dtype=torch.int32, device=DEV)
+    ys = []
+    for s in range(3):
+        y, _ = kda.short_conv(xs[s], w, cu, st, final_state=st)
+        ys.append(y)
+    torch.cuda.synchronize()
+    # the same three tokens as one sequence per request
+    packed = xs.permute(1, 0, 2, 3).reshape(N * 3, H, D)
+    ry, rfin = oracle.short_conv(packed, w, list(range(0, 3 * N + 1, 3)), st0)
+    got = torch.stack(ys, 1).reshape(N * 3, H, D)
+    _check(got, ry, torch.bfloat16)
+    assert np.array_equal(as64(st), rfin)
+
+
+def test_short_conv_feeds_the_prefill():
+    """q and k through the convolution, then the chunked prefill, against the
+    oracle applied step by step (conv + Swish, then the recurrence)."""
+    import workloads
+    p = workloads.random_problem([100, 37], 2, 128, 128, torch.bfloat16, init_std=0.1, seed=6,
+                                 device=DEV, normalize_qk=False)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(7)
+    wq = torch.randn((2, 128, 4), device=DEV, generator=g) * 0.6
+    wk = torch.randn((2, 128, 4), device=DEV, generator=g) * 0.6
+    qc, _ = kda.short_conv(p.q, wq, p.cu_seqlens, None, output_final_state=False)
+    kc, _ = kda.short_conv(p.k, wk, p.cu_seqlens, None, output_final_state=False)
+    out, fin = kda.chunk_fwd(qc, kc, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    # the oracle's recurrence on the library's own bf16 conv outputs (their
+    # parity is checked above), so this checks the composition
+    ro, rf, _ = oracle.recurrent(qc, kc, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state)
+    from tests.parity import assert_close
+    assert_close(out, ro, torch.bfloat16, "out")
+    assert_close(fin, rf, torch.bfloat16, "final_state")
