@@ -420,6 +420,52 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     sync_tc();
 
+    // ---------------- B: token norms and beta of the chunk at tc0 (lenc tokens) ----------------
+    // (from the q / k stages, once they hold that chunk).  Warps 0-7 only, so
+    // that warp 8 can issue the U products meanwhile.
+    auto norms_and_beta = [&](int tc0, int lenc) {
+      if (tid >= 256) return;
+      // four threads per token, one half row (32 channels, four 16-byte chunks)
+      // of one 64-channel block each; the sum over a row does not depend on
+      // which chunk holds which channels.  Chunk x of row t is read at
+      // x ^ (t % 8), and the second block walks its chunks in the order j ^ 2,
+      // so the eight lanes of a quarter warp hit eight different bank groups.
+      const int t = tid >> 2, e = tid & 3;
+      const int boff = (e >> 1) * 8192 + t * 128;
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int x = (((e & 1) * 4 + (j ^ ((e >> 1) << 1))) ^ (t & 7)) << 4;
+        const uint4 a = *reinterpret_cast<const uint4*>(sm + OFF_Q + boff + x);
+        const uint4 b = *reinterpret_cast<const uint4*>(sm + OFF_K + boff + x);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float u = bf16_lo(aw[i]), w = bf16_hi(aw[i]);
+          sq += u * u + w * w;
+          u = bf16_lo(bw[i]); w = bf16_hi(bw[i]);
+          sk += u * u + w * w;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      if (e == 0) {
+        // (rq, rk) per token, both times kTf32Lift (see the Gram operands)
+        *reinterpret_cast<float2*>(misc + M_RQK + 2 * t) =
+            t < lenc ? make_float2(rsqrtf(sq + kNormEps) * kTf32Lift,
+                                  rsqrtf(sk + kNormEps) * kTf32Lift)
+                    : make_float2(0.f, 0.f);
+      }
+      if (tid < kC) {
+        misc[M_BETA + tid] = beta_pf;
+        beta_pf = 0.f;
+        if (tid < min(kC, eos - tc0 - kC)) beta_pf = __ldg(P.beta + (size_t)(tc0 + kC + tid) * H + h);
+      }
+    };
+
     bool pend_l = false;  // the previous chunk still has to write O and convert S^T
     int l_t0 = 0, l_len = 0;
     long long l_ck = -1;  // its state checkpoint slot, if it ends one
@@ -427,50 +473,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int t0 = bos + ci * kC;
       const int len = min(kC, eos - t0);
       // ---------------- A: inputs ----------------
-      bool ok = wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
-      if (ok) {
-        ph_qkz ^= 1;
-        pend_qkz = false;
-      }
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-
-      // ---------------- B: token norms and beta ----------------
-      {
-        // eight threads per token, 16 channels each (two 16-byte chunks)
-        const int t = tid >> 3, e = tid & 7;
-        const int boff = (e >> 2) * 8192 + t * 128 + (e & 3) * 32;
-        float sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int jj = j ^ (e >> 2);  // either order covers both chunks; this one is conflict-free
-          const uint4 a = *reinterpret_cast<const uint4*>(sm + OFF_Q + boff + (jj << 4));
-          const uint4 b = *reinterpret_cast<const uint4*>(sm + OFF_K + boff + (jj << 4));
-          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float x = bf16_lo(aw[i]), y = bf16_hi(aw[i]);
-            sq += x * x + y * y;
-            x = bf16_lo(bw[i]); y = bf16_hi(bw[i]);
-            sk += x * x + y * y;
-          }
+      // (from the second chunk on, A and B ran during the previous chunk's U products)
+      bool ok = true;
+      if (ci == 0) {
+        ok = wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
+        if (ok) {
+          ph_qkz ^= 1;
+          pend_qkz = false;
         }
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          sq += __shfl_xor_sync(0xffffffffu, sq, o);
-          sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        if (e == 0) {
-          // (rq, rk) per token, both times kTf32Lift (see the Gram operands)
-          *reinterpret_cast<float2*>(misc + M_RQK + 2 * t) =
-              t < len ? make_float2(rsqrtf(sq + kNormEps) * kTf32Lift,
-                                    rsqrtf(sk + kNormEps) * kTf32Lift)
-                      : make_float2(0.f, 0.f);
-        }
-        if (tid < kC) {
-          misc[M_BETA + tid] = beta_pf;
-          beta_pf = 0.f;
-          if (tid < min(kC, eos - t0 - kC)) beta_pf = __ldg(P.beta + (size_t)(t0 + kC + tid) * H + h);
-        }
+        if (__syncthreads_or(!ok)) { aborted = true; break; }
+        norms_and_beta(t0, len);
       }
 
       // ---------------- C: gate and cumulative decay ----------------
@@ -878,7 +890,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pend_mma2 = false;
 
       // ---------------- G: U^T = V^T T'^T - Y^T T'^T ----------------
-      if (tid == 0) {
+      if (tid == 256) {  // warp 8: no norm work below
         const uint32_t id_u = make_idesc_f16(128, kC, true, false);
         const uint32_t id_n = make_idesc_f16(128, kC, false, false, true);
 #pragma unroll
@@ -891,12 +903,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mma_commit(bar_mma);
       }
       pend_mma = true;
+      // A and B of the next chunk (its q / k / z landed during this one) while
+      // the U products run
+      bool okq = true;
+      if (ci + 1 < nchunks) {
+        okq = wait_bar(bar_qkz, ph_qkz, P.spin_cycles);
+        if (okq) {
+          ph_qkz ^= 1;
+          pend_qkz = false;
+        }
+        // every lane runs it (its shuffles need the whole warp); after a timeout
+        // the values are not used
+        norms_and_beta(t0 + kC, min(kC, eos - t0 - kC));
+      }
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
       if (ok) {
         ph_mma ^= 1;
         pend_mma = false;
       }
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
+      if (__syncthreads_or(!ok || !okq)) { aborted = true; break; }
       tc_fence_after();
       if (tid == 0 && ci + 1 < nchunks && !zero_v) {  // v stage consumed: prefetch
         const int tn = t0 + kC;
