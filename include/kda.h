@@ -293,6 +293,40 @@ void kda_testing_inject_wait_timeout(int launches);
 
 /* Static, human-readable name of a status. */
 /*
+ * kda_chunk_fwd_host -- kda_chunk_fwd over inputs and outputs in HOST memory
+ * (page-locked for the copies to overlap), for callers whose batch is not yet
+ * on the device.  The batch is cut into `groups` groups of whole sequences of
+ * about equal token count; the copies of one group into the device overlap
+ * the kernel of the previous one and the copies of the one before back out.
+ * Results equal those of kda_chunk_fwd on the same data except that the long-
+ * sequence split across SMs is not used.
+ *
+ *   desc               as for kda_chunk_fwd; workspace / workspace_bytes:
+ *                      DEVICE staging area of at least
+ *                      kda_chunk_fwd_host_workspace_size() bytes, 256-byte
+ *                      aligned, owned by the caller (one call at a time per
+ *                      area); checkpoint_every must be 0 (else
+ *                      KDA_ERR_UNSUPPORTED); a_log stays a DEVICE pointer
+ *   groups             >= 1 (8 is a good default)
+ *   q, k, v, z, beta, initial_state (or NULL), out, final_state (or NULL)
+ *                      HOST, layouts as for kda_chunk_fwd
+ *   cu_seqlens         HOST [N + 1] int32 (desc->cu_seqlens_host may be NULL
+ *                      or this same pointer)
+ * The call returns once the work is enqueued; work later enqueued on
+ * `stream` runs after out and final_state are written to host memory, so a
+ * cudaStreamSynchronize(stream) makes them readable.  The host buffers must
+ * stay valid (and the inputs unchanged) until then.
+ */
+kda_status_t kda_chunk_fwd_host(const kda_desc_t* desc, int32_t groups, const void* q,
+                                const void* k, const void* v, const float* z, const float* beta,
+                                const float* initial_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, kda_stream_t stream);
+
+/* Bytes of device staging area kda_chunk_fwd_host needs for this descriptor
+ * (all inputs and outputs of the batch, both state arrays reserved). */
+kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* bytes);
+
+/*
  * kda_recurrent_bwd -- reverse mode of kda_chunk_fwd / kda_recurrent_fwd:
  * the gradients of a loss L with respect to every input, given dL/d out and
  * dL/d final_state.  The pages give the forward only (mhpq.cn/news/56770,

@@ -22,7 +22,8 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "chunk_fwd_workspace_size", "NOALLOC_SCRATCH_BYTES",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
            "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
-           "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "EXPORTED_SYMBOLS"]
+           "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "chunk_fwd_host",
+           "chunk_fwd_host_workspace_size", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_decode_step", "kda_decode_window", "kda_decode_replay",
                     "kda_decode_replay_window", "kda_status_string", "kda_get_device_error",
                     "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout",
-                    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "kda_short_conv")
+                    "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "kda_short_conv",
+                    "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -85,6 +87,10 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_recurrent_bwd.restype = ctypes.c_int
         lib.kda_recurrent_bwd.argtypes = [dp] + [vp] * 16
+        lib.kda_chunk_fwd_host.restype = ctypes.c_int
+        lib.kda_chunk_fwd_host.argtypes = [dp, ctypes.c_int32] + [vp] * 10
+        lib.kda_chunk_fwd_host_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_fwd_host_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_short_conv.restype = ctypes.c_int
         lib.kda_short_conv.argtypes = [dp, ctypes.c_int32] + [vp] * 7
         lib.kda_recurrent_bwd_workspace_size.restype = ctypes.c_int
@@ -118,6 +124,19 @@ def _check_tensor(name, t, dtype, shape, device):
         raise ValueError(f"{name} is required")
     if t.device != device or not t.is_cuda:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_host(name, t, dtype, shape):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor, got {t.device}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
@@ -282,6 +301,68 @@ def chunk_fwd_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype, c
     if st != KDA_OK:
         raise KDAError(st, "kda_chunk_fwd_workspace_size")
     return int(n.value)
+
+
+def chunk_fwd_host_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype,
+                                  gate_per_head=False):
+    """Bytes of device staging area ``chunk_fwd_host`` needs."""
+    desc, keep = make_desc(num_seqs, total_tokens, num_heads, dk, dv, _io_code(dtype))
+    desc.gate_per_head = 1 if gate_per_head else 0
+    n = ctypes.c_size_t(0)
+    st = load().kda_chunk_fwd_host_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_host_workspace_size")
+    return int(n.value)
+
+
+def chunk_fwd_host(q, k, v, z, beta, cu_seqlens_host, initial_state=None, *, out=None,
+                   final_state=None, output_final_state=True, workspace=None, groups=8,
+                   device=None, stream=None, a_log=None):
+    """``kda_chunk_fwd_host``: the chunked prefill over HOST tensors (pinned for
+    the copies to overlap the kernels).  q, k, v, z, beta, initial_state and the
+    returned out / final_state live in host memory; ``workspace`` is a device
+    uint8 tensor of ``chunk_fwd_host_workspace_size`` bytes (allocated here when
+    None).  Returns (out, final_state) once they are written (the call
+    synchronises the stream)."""
+    lib = load()
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    cu = [int(c) for c in cu_seqlens_host]
+    N = len(cu) - 1
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    per_head = z.dim() == 2
+    _check_host("q", q, q.dtype, (T, H, dk))
+    _check_host("k", k, q.dtype, (T, H, dk))
+    _check_host("v", v, q.dtype, (T, H, dv))
+    _check_host("z", z, torch.float32, (T, H) if per_head else (T, H, dk))
+    _check_host("beta", beta, torch.float32, (T, H))
+    if initial_state is not None:
+        _check_host("initial_state", initial_state, torch.float32, (N, H, dk, dv))
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
+    _check_host("out", out, q.dtype, (T, H, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+    if final_state is not None:
+        _check_host("final_state", final_state, torch.float32, (N, H, dk, dv))
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    if workspace is None:
+        nbytes = chunk_fwd_host_workspace_size(N, T, H, dk, dv, q.dtype, per_head)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), None, workspace, a_log)
+    desc.gate_per_head = 1 if per_head else 0
+    cu_arr = (ctypes.c_int32 * len(cu))(*cu)
+    with torch.cuda.device(dev):
+        st = lib.kda_chunk_fwd_host(ctypes.byref(desc), int(groups), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(z), _ptr(beta), _ptr(initial_state), cu_arr, _ptr(out),
+                                    _ptr(final_state), _stream_handle(stream))
+        if st == KDA_OK:
+            (stream or torch.cuda.current_stream()).synchronize()
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_host")
+    return out, final_state
 
 
 def short_conv(x, weight, cu_seqlens, conv_state=None, *, out=None, final_state=None,

@@ -272,6 +272,49 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* bytes) {
+  if (!bytes || !desc) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  *bytes = kda::chunk_fwd_host_workspace_bytes(to_problem(desc), desc->gate_per_head == 1);
+  return KDA_OK;
+}
+
+kda_status_t kda_chunk_fwd_host(const kda_desc_t* desc, int32_t groups, const void* q,
+                                const void* k, const void* v, const float* z, const float* beta,
+                                const float* initial_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, kda_stream_t stream) {
+  if (!desc || !cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
+  if (desc->cu_seqlens_host && desc->cu_seqlens_host != cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
+  kda_desc_t d = *desc;
+  d.cu_seqlens_host = cu_seqlens;  // validated as the host copy
+  kda_status_t s = check_desc(&d, false);
+  if (s != KDA_OK) return s;
+  if (groups < 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (d.gate_per_head != 0 && d.gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (d.checkpoint_every != 0) return KDA_ERR_UNSUPPORTED;
+  if (d.total_tokens > 0 && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+  const kda::Problem p = to_problem(&d);
+  const size_t need = kda::chunk_fwd_host_workspace_bytes(p, d.gate_per_head == 1);
+  if (!d.workspace || d.workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(d.workspace) & 255) != 0)
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (d.num_seqs == 0) return KDA_OK;
+  kda::HostArgs h;
+  h.q = q; h.k = k; h.v = v; h.z = z; h.beta = beta;
+  h.initial_state = initial_state;
+  h.cu_seqlens = cu_seqlens;
+  h.out = out;
+  h.final_state = final_state;
+  h.a_log = d.a_log;
+  h.gate_per_head = d.gate_per_head;
+  h.err = device_error_word();
+  if (!h.err) return KDA_ERR_CUDA;
+  cudaError_t e = kda::launch_chunk_fwd_host(p, h, groups, d.workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_short_conv(const kda_desc_t* desc, int32_t width, const void* x,
                             const float* weight, const float* conv_state_in,
                             const int32_t* cu_seqlens, void* y, float* conv_state_out,

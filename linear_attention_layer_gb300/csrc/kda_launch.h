@@ -116,6 +116,25 @@ struct ConvArgs {
 };
 cudaError_t launch_short_conv(const Problem& p, const ConvArgs& a, cudaStream_t stream);
 
+// The prefill over host buffers with copies overlapped (kda_host.cu).
+struct HostArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* z;
+  const float* beta;
+  const float* initial_state;  // host, may be null
+  const int32_t* cu_seqlens;   // host
+  void* out;
+  float* final_state;  // host, may be null
+  const float* a_log;  // device, may be null
+  int gate_per_head;
+  int* err;
+};
+size_t chunk_fwd_host_workspace_bytes(const Problem& p, bool gate_per_head);
+cudaError_t launch_chunk_fwd_host(const Problem& p, const HostArgs& h, int groups, void* ws,
+                                  cudaStream_t stream);
+
 }  // namespace kda
 
 #include "../../include/kda.h"

@@ -211,3 +211,24 @@ def test_short_conv_rejects_bad_arguments(lib):
              y, None, None) == 1                                                  # x misaligned
     bad, keep2 = kda.make_desc(2, 8, 2, 48, 48, kda.KDA_BF16)
     assert f(ctypes.byref(bad), 4, FAKE, FAKE, None, FAKE, y, None, None) == 1    # dk = 48
+
+
+def test_host_prefill_rejects_bad_arguments(lib):
+    cu = (ctypes.c_int32 * 3)(0, 3, 8)
+    d, keep = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16)
+    f = lib.kda_chunk_fwd_host
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, None, cu, ctypes.c_void_p(0x2000), None, None]
+    assert f(ctypes.byref(d), 4, *args) == 1                        # no staging area
+    d.workspace, d.workspace_bytes = ctypes.c_void_p(0x10000), 1 << 40
+    assert f(ctypes.byref(d), 0, *args) == 1                        # groups < 1
+    d.checkpoint_every = 64
+    assert f(ctypes.byref(d), 4, *args) == 2                        # no checkpoints here
+    d.checkpoint_every = 0
+    bad = (ctypes.c_int32 * 3)(0, 5, 3)
+    assert f(ctypes.byref(d), 4, *args[:6], bad, *args[7:]) == 1    # host cu not monotone
+    d.workspace = ctypes.c_void_p(0x10010)                          # not 256-byte aligned
+    assert f(ctypes.byref(d), 4, *args) == 1
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    # q, k, v, out bf16 + z fp32 + beta, 8 tokens x 2 heads x 128, two states each way, cu
+    assert n.value >= 8 * 2 * 128 * (2 * 4 + 4) + 8 * 2 * 4 + 2 * 2 * 2 * 128 * 128 * 4
