@@ -75,14 +75,16 @@ struct Params {
 };
 
 struct Smem {
-  float qh[kBlk][kD];   // q^ ; after token t is done: dq^
+  float qh[kBlk][kD];   // q^
   float kh[kBlk][kD];   // k^
   float al[kBlk][kD];   // alpha
   float v[kBlk][kD];    // v ; after token t is done: dk^
   float dO[kBlk][kD];   // d out
+  float dqh[kBlk][kD];  // dq^
   float e[kSub][kD];    // e of the sub-block being reversed
   float redy[2][4][kD];       // sums over c, per warp row (w >> 2)
-  float red3[2][3][4][kD];    // sums over n (dq^, dk^, dalpha), per warp column (w & 3)
+  float red3[2][3][4][kD];    // sums over n (dq^ of the token before, dk^, dalpha), per warp column (w & 3)
+  float redq[4][kD];          // sums over n: dq^ of a sub-block's last token
   float beta[kBlk], rq[kBlk], rk[kBlk], db[kBlk];
 };
 
@@ -309,30 +311,43 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
       for (int j0 = ((bl - 1) / kSub) * kSub; j0 >= 0; j0 -= kSub) {
         const int sl = min(kSub, bl - j0);
         const float* const sub_in = subck + (size_t)((b0 + j0) / kSub) * kState;
-        // rebuild S_t for the sub-block's tokens, and their e
+        // rebuild S_t for the sub-block's tokens, and their e.  The ring keeps
+        // S_t for all but the last token: the reverse step of token t reads only
+        // S_{t-1}, and takes dq^ of token t - 1 (= S_{t-1} do_{t-1}) from it too.
         ld_state(sub_in, s, cgp, ng);
         for (int i = 0; i < sl; ++i) {
           const float4 e = fwd_token(sm, s, j0 + i, par, w, l, cgp, ng);
           par ^= 1;
           if (w < 4 && l < 8) st4(sm.e[i] + 4 * ng, e);  // cgp == 0: one writer per n
-          st_state(ring + (size_t)i * kState, s, cgp, ng);
+          if (i + 1 < sl) st_state(ring + (size_t)i * kState, s, cgp, ng);
         }
-        __syncthreads();  // e rows visible
+        {  // dq^ of the sub-block's last token from the state after it, still in s
+          const float4 d4 = ld4(sm.dO[j0 + sl - 1] + 4 * ng);
+          float p1[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            p1[r] = s[r][0] * d4.x + s[r][1] * d4.y + s[r][2] * d4.z + s[r][3] * d4.w;
+          fold<8>(p1, l & 4, 4);
+          fold<4>(p1, l & 2, 2);
+          fold<2>(p1, l & 1, 1);
+          sm.redq[w & 3][8 * cgp + (l & 7)] = p1[0];
+        }
+        __syncthreads();  // e rows and the last token's dq^ parts visible
+        if (tid < kD)
+          sm.dqh[j0 + sl - 1][tid] =
+              sm.redq[0][tid] + sm.redq[1][tid] + sm.redq[2][tid] + sm.redq[3][tid];
         for (int i = sl - 1; i >= 0; --i) {
           const int t = j0 + i;
-          const float* const st_t = ring + (size_t)i * kState;
           const float* const st_p = i > 0 ? ring + (size_t)(i - 1) * kState : sub_in;
-          // (a) dS += q^ do^T; dq^ = S_t do; y = dS^T k^
+          // (a) dS += q^ do^T; y = dS^T k^
           const float4 d4 = ld4(sm.dO[t] + 4 * ng);
           const float dov[4] = {d4.x, d4.y, d4.z, d4.w};
           const float* const qrow = sm.qh[t] + 8 * cgp;
           const float* const krow = sm.kh[t] + 8 * cgp;
           const float* const arow = sm.al[t] + 8 * cgp;
-          float p1[8], y[4] = {0.f, 0.f, 0.f, 0.f};
+          float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            const float4 a = ld4(st_t + (size_t)(8 * cgp + r) * kD + 4 * ng);
-            p1[r] = a.x * dov[0] + a.y * dov[1] + a.z * dov[2] + a.w * dov[3];
             const float qc = qrow[r], kc = krow[r];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -343,12 +358,9 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
           fold<4>(y, l & 16, 16);
           fold<2>(y, l & 8, 8);
           sm.redy[par][w >> 2][4 * ng + ((l >> 3) & 3)] = y[0];
-          fold<8>(p1, l & 4, 4);
-          fold<4>(p1, l & 2, 2);
-          fold<2>(p1, l & 1, 1);
-          sm.red3[par][0][w & 3][8 * cgp + (l & 7)] = p1[0];
           __syncthreads();
-          // (b) de = beta y; dv; dbeta; dk^ = beta dS e - Sbar de; dSbar; dalpha; dS <- Diag(alpha) dSbar
+          // (b) de = beta y; dv; dbeta; dk^ = beta dS e - Sbar de; dSbar; dalpha;
+          //     dS <- Diag(alpha) dSbar; dq^ of token t - 1 = S_{t-1} do_{t-1}
           float4 yy = ld4(sm.redy[par][0] + 4 * ng);
 #pragma unroll
           for (int r = 1; r < 4; ++r) {
@@ -368,7 +380,9 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
             yb += __shfl_xor_sync(0x000000ffu, yb, 4);
             if (l == 0) atomicAdd(&sm.db[t], yb);
           }
-          float p2[8], p3[8];
+          const float4 dp4 = ld4(sm.dO[t > 0 ? t - 1 : 0] + 4 * ng);
+          const float dop[4] = {dp4.x, dp4.y, dp4.z, dp4.w};
+          float p1[8], p2[8], p3[8];
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
             const float4 a = ld4(st_p + (size_t)(8 * cgp + r) * kD + 4 * ng);
@@ -384,19 +398,26 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
               x3 = fmaf(dsb, sp[j], x3);
               ds[r][j] = ac * dsb;
             }
+            p1[r] = sp[0] * dop[0] + sp[1] * dop[1] + sp[2] * dop[2] + sp[3] * dop[3];
             p2[r] = x2;
             p3[r] = x3;
           }
+          fold<8>(p1, l & 4, 4);
+          fold<4>(p1, l & 2, 2);
+          fold<2>(p1, l & 1, 1);
           fold<8>(p2, l & 4, 4);
           fold<4>(p2, l & 2, 2);
           fold<2>(p2, l & 1, 1);
           fold<8>(p3, l & 4, 4);
           fold<4>(p3, l & 2, 2);
           fold<2>(p3, l & 1, 1);
+          sm.red3[par][0][w & 3][8 * cgp + (l & 7)] = p1[0];
           sm.red3[par][1][w & 3][8 * cgp + (l & 7)] = p2[0];
           sm.red3[par][2][w & 3][8 * cgp + (l & 7)] = p3[0];
           __syncthreads();
-          // (c) per key channel: dq^, dk^ kept for the block's norm pass; dz out
+          // (c) per key channel: dq^ of token t - 1 and dk^ kept for the block's norm
+          //     pass (a sub-block's first token gets its dq^ from the sub-block before
+          //     it, whose last token it is); dz out
           if (tid < kD) {
             const int c = tid;
             float dqh = 0.f, dkh = 0.f, dal = 0.f;
@@ -406,8 +427,8 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
               dkh += sm.red3[par][1][r][c];
               dal += sm.red3[par][2][r][c];
             }
-            sm.dO[t][c] = dqh;  // this token's d out is no longer read
-            sm.v[t][c] = dkh;   // nor its v
+            if (i > 0) sm.dqh[t - 1][c] = dqh;
+            sm.v[t][c] = dkh;  // this token's v is no longer read
             const float a = sm.al[t][c], g = __logf(a);
             P.dz[((size_t)(bos + b0 + t) * P.H + h) * kD + c] = dal * a * g * (1.f + g / 5.f) * zs;
           }
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
 #pragma unroll
           for (int pass = 0; pass < 2; ++pass) {
             const float* xh = pass == 0 ? sm.qh[t] : sm.kh[t];
-            const float* dxh = pass == 0 ? sm.dO[t] : sm.v[t];
+            const float* dxh = pass == 0 ? sm.dqh[t] : sm.v[t];
             float dot = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) dot = fmaf(xh[c0 + i], dxh[c0 + i], dot);
