@@ -139,3 +139,15 @@ def test_backward_prefill_workload_sampled():
                               sl(d_out), d_fin[n:n + 1, h:h + 1].cpu())
         mine = [g[a:b, h:h + 1] for g in got[:5]] + [got[5][n:n + 1, h:h + 1]]
         _compare(mine, ref)
+
+
+def test_backward_all_sequences_empty():
+    """No tokens at all: the only gradient is the final state's, handed to the
+    initial state unchanged."""
+    p = workloads.random_problem([0, 0], 2, 128, 128, torch.bfloat16, init_std=0.3, seed=26,
+                                 device=DEV)
+    d_out = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    d_fin = torch.randn((2, 2, 128, 128), device=DEV)
+    got = _run(p, d_out, d_fin)
+    assert torch.equal(got[5], d_fin)
+    assert all(g.numel() == 0 for g in got[:5])

@@ -63,3 +63,15 @@ def test_host_prefill_no_state_gate_scale_per_head_gate_and_oracle():
     out, _ = kda.chunk_fwd_host(_host(p.q), _host(p.k), _host(p.v), _host(p.z), _host(p.beta),
                                 p.cu_seqlens_host, None, groups=3, a_log=a_log)
     assert_close(out, ro, torch.bfloat16, "out")
+
+
+def test_host_prefill_empty_sequences_keep_their_state():
+    p = workloads.random_problem([0, 5, 0], 2, 128, 128, torch.bfloat16, init_std=0.2, seed=33,
+                                 device=DEV)
+    out, fin = kda.chunk_fwd_host(_host(p.q), _host(p.k), _host(p.v), _host(p.z), _host(p.beta),
+                                  p.cu_seqlens_host, _host(p.initial_state), groups=3)
+    ref_out, ref_fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                     cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out.cpu()) and torch.equal(fin, ref_fin.cpu())
+    assert torch.equal(fin[0], p.initial_state[0].cpu()) and torch.equal(fin[2], p.initial_state[2].cpu())

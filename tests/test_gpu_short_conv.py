@@ -119,3 +119,12 @@ def test_short_conv_feeds_the_prefill():
     from tests.parity import assert_close
     assert_close(out, ro, torch.bfloat16, "out")
     assert_close(fin, rf, torch.bfloat16, "final_state")
+
+
+def test_short_conv_no_tokens_keeps_states():
+    x, w, st, cu, cu_h = _inputs([0, 0, 0], 2, 64, 4, torch.bfloat16, seed=9)
+    y, fin = kda.short_conv(x, w, cu, st)
+    torch.cuda.synchronize()
+    assert y.numel() == 0
+    assert torch.equal(fin, st)
+    assert kda.get_device_error() == 0
