@@ -208,6 +208,7 @@ kda_status_t check_window(const kda_desc_t* desc, int32_t window, const void* q,
     return KDA_ERR_INVALID_ARGUMENT;
   if (desc->num_seqs > 0 && (!q || !k || !v || !z || !beta || !state))
     return KDA_ERR_INVALID_ARGUMENT;
+  if (state && !aligned16(state)) return KDA_ERR_INVALID_ARGUMENT;  // float4 / bulk copies
   return KDA_OK;
 }
 }  // namespace

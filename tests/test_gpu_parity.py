@@ -379,6 +379,47 @@ def test_fused_replay_window_equals_replay_then_window():
     assert kda.get_device_error() == 0
 
 
+def test_speculative_decoding_many_units_streamed():
+    """Enough (request, head) units (40 x 16 = 640) for the persistent kernel
+    that streams the next unit's state in while applying the current one:
+    the fused call equals the separate calls bit for bit, sampled requests
+    equal the oracle, and a bad acceptance length leaves its request alone."""
+    B, W, H, dk, dv = 40, 4, 16, 128, 128
+    torch.manual_seed(2)
+    s_sep = torch.randn((B, H, dk, dv), device=DEV) * 0.1
+    s0 = s_sep.clone()
+    prev = _window_inputs(B, W, H, dk, dv, torch.bfloat16, 50)[:5]
+    nxt = _window_inputs(B, W, H, dk, dv, torch.bfloat16, 51)[:5]
+    acc_l = np.random.default_rng(3).integers(0, W + 1, size=B)
+    acc = torch.tensor(acc_l, dtype=torch.int32, device=DEV)
+    s_fused = s_sep.clone()
+    kda.decode_replay(*prev, acc, s_sep)
+    o_sep = kda.decode_window(*nxt, s_sep)
+    o_fused = kda.decode_replay_window(prev, acc, *nxt, s_fused)
+    torch.cuda.synchronize()
+    assert torch.equal(o_fused, o_sep) and torch.equal(s_fused, s_sep)
+    for b in (0, 17, 39):
+        n = int(acc_l[b])
+        if n:
+            cols = [x[b, :n].cpu() for x in prev]
+            _, fin, _ = oracle.recurrent(*cols, [0, n], s0[b:b + 1].cpu())
+            assert_close(s_sep[b], fin[0], torch.bfloat16, f"request {b} replayed state")
+        o, _, _ = oracle.recurrent(*[x[b].cpu() for x in nxt], [0, W], s_sep[b:b + 1].cpu())
+        assert_close(o_sep[b], o, torch.bfloat16, f"request {b} window outputs")
+    assert kda.get_device_error() == 0
+    bad = acc.clone()
+    bad[7] = W + 1
+    s_bad = s0.clone()
+    kda.decode_replay(*prev, bad, s_bad)
+    assert kda.get_device_error() == 5  # KDA_ERR_DEVICE_CHECK
+    assert torch.equal(s_bad[7], s0[7])
+    s_ref = s0.clone()
+    kda.decode_replay(*prev, acc, s_ref)  # the other requests as with a valid length
+    torch.cuda.synchronize()
+    assert torch.equal(s_bad[8], s_ref[8])
+    assert kda.get_device_error() == 0
+
+
 def test_decode_replay_bad_accept_length_sets_error_and_keeps_state():
     B, W, H = 3, 2, 2
     q, k, v, z, beta, state = _window_inputs(B, W, H, 64, 64, torch.float32, 23)
