@@ -599,7 +599,21 @@ def bench_e2e(kda, p, steps, device, groups=8):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    return ms, h2d, d2h
+    # the link itself: one 1 GiB pinned copy each way, timed alone
+    link = {}
+    big_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    for name, dst, src in (("h2d", big_d, big_h), ("d2h", big_h, big_d)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        link[name] = (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del big_h, big_d
+    return ms, h2d, d2h, link
 
 
 def main():
@@ -612,7 +626,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip", default="",
-                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv")
+                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv,prefill,tiny")
     ap.add_argument("--bwd-steps", type=int, default=3)
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
@@ -691,6 +705,72 @@ def main():
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
     }
+
+    # ---- the 4 x 4096-token, 16-head prefill (workspace offered: the planner
+    # decides whether splitting sequences across SMs pays) ----
+    if "prefill" not in skip and args.workload != "prefill":
+        p2 = workloads.prefill_workload("prefill", device=device, seed=rank)
+        torch.cuda.synchronize()
+        pclk = clock_sampler(gpu_uuid)
+        p2_ms, p2_launch = bench_prefill(kda, p2, args.steps, args.warmup, dist, device,
+                                         split=True, clk=pclk)
+        p2_ms = max_over_ranks(p2_ms, dist, device)
+        T2, H2, N2 = p2.total_tokens, p2.meta["num_heads"], p2.num_seqs
+        p2_bytes = T2 * H2 * PREFILL_BYTES_PER_HEAD_TOKEN + 4 * (N2 + 1) + N2 * H2 * STATE_BYTES
+        p2_launch_ms = statistics.mean(p2_launch)
+        p2_gbs = p2_bytes / (p2_launch_ms * 1e-3) / 1e9
+        p2_ws = kda.chunk_fwd_workspace_size(N2, T2, H2, 128, 128, p2.q.dtype, p2.cu_seqlens_host)
+        line["prefill"] = {
+            "value": round(weak_scaling_value(T2, world, p2_ms / 1e3 / args.steps), 3),
+            "unit": UNIT, "ms_per_step": round(p2_ms / args.steps, 4),
+            "workload": workloads.DESCRIPTIONS["prefill"],
+            "units": N2 * H2, "split_planned": bool(p2_ws),
+            "roofline": {"bound": "hbm", "achieved": round(p2_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(p2_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_launch": p2_bytes},
+            "clocks": pclk.summary(), "gpu_launches": args.steps * (3 if p2_ws else 1)}
+        del p2
+        torch.cuda.empty_cache()
+
+    # ---- the tiny fp32 call (B=1, H=1, T=64, d=32): launch-latency bound ----
+    if "tiny" not in skip:
+        pt = workloads.prefill_workload("tiny", device=device, seed=rank)
+        t_out = torch.empty_like(pt.v)
+        t_fin = torch.empty((1, 1, 32, 32), dtype=torch.float32, device=device)
+
+        def tiny_call():
+            kda.chunk_fwd(pt.q, pt.k, pt.v, pt.z, pt.beta, pt.cu_seqlens, None, out=t_out,
+                          final_state=t_fin, cu_seqlens_host=pt.cu_seqlens_host)
+
+        for _ in range(max(args.warmup, 10)):
+            tiny_call()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        single = []
+        for _ in range(50):  # one call between a synchronize and the next
+            a, b = event_time_ms(tiny_call, stream)
+            torch.cuda.synchronize()
+            single.append(a.elapsed_time(b))
+        n_b = 500
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(stream)
+        for _ in range(n_b):
+            tiny_call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        host_us = (time.perf_counter() - t0) / n_b * 1e6
+        if kda.get_device_error() != 0:
+            raise RuntimeError("device error word set after the tiny calls")
+        line["tiny"] = {
+            "value": round(statistics.median(single) * 1e3, 2), "unit": "us per call",
+            "higher_is_better": False, "workload": workloads.DESCRIPTIONS["tiny"],
+            "bound": "launch latency (41 KB of data)",
+            "device_us_per_call_back_to_back": round(a.elapsed_time(b) / n_b * 1e3, 2),
+            "host_us_per_call_back_to_back": round(host_us, 2),
+            "calls": 50 + n_b, "gpu_launches": 50 + n_b}
+        del pt
 
     # ---- reverse mode over the same workload ----
     if "bwd" not in skip:
@@ -810,11 +890,13 @@ def main():
         if p is None:
             p = workloads.prefill_workload(args.workload, device=device, seed=rank)
         groups = 8
-        ms, h2d, d2h = bench_e2e(kda, p, args.e2e_steps, device, groups=groups)
+        ms, h2d, d2h, link = bench_e2e(kda, p, args.e2e_steps, device, groups=groups)
         ms = max_over_ranks(ms, dist, device)
         line["e2e"] = {"value": round(weak_scaling_value(T, world, ms / 1e3), 3), "unit": UNIT,
                        "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                       "copy_gbs_effective": round((h2d + d2h) / (ms * 1e-3) / 1e9, 1),
+                       "link_gbs_1gib_pinned_copy": {k: round(v, 1) for k, v in link.items()},
                        "api": "kda_chunk_fwd_host (pinned host buffers, copies overlapped with "
                               f"the kernels over {groups} groups of sequences)",
                        "gpu_launches": groups * args.e2e_steps}

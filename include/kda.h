@@ -89,8 +89,10 @@ typedef struct {
    * it is checked and must equal the device copy. */
   const int32_t* cu_seqlens_host;
   /* Optional device scratch for splitting long sequences across SMs in
-   * kda_chunk_fwd (see kda_chunk_fwd_workspace_size).  NULL / 0 disables
-   * the split; results are the same either way. */
+   * kda_chunk_fwd (see kda_chunk_fwd_workspace_size), 256-byte aligned.
+   * NULL / 0 disables the split; an area smaller than the size query asks
+   * for limits the split to plans that fit in it.  Results are the same
+   * (within rounding) either way. */
   void* workspace;
   size_t workspace_bytes;
   /* Optional per-head log-scale A of the gate, DEVICE [H] fp32: the gate is
@@ -143,6 +145,16 @@ typedef struct {
  *
  * bf16 inputs run the tensor-core path (dk = dv = 128) or the CUDA-core
  * path (other sizes); fp32 inputs always run the fp32 CUDA-core path.
+ *
+ * Range limit of the tensor-core path: its dense products take fp16
+ * operands (11-bit significand, largest magnitude 65504), made from v, the
+ * state entering each 64-token chunk, S^T K+^T and the pseudo-values U.  A
+ * bf16 v or an fp32 state can exceed that range.  When any such operand
+ * reaches 65504 in magnitude the call's outputs are not valid and the
+ * kernel sets KDA_ERR_DEVICE_CHECK in the device error word (read it with
+ * kda_get_device_error); the following calls are unaffected.  Data of that
+ * magnitude must go through kda_recurrent_fwd (fp32 throughout) or fp32
+ * inputs.
  */
 kda_status_t kda_chunk_fwd(const kda_desc_t* desc, const void* q, const void* k,
                            const void* v, const float* z, const float* beta,
@@ -261,12 +273,14 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
  * loads libkda holds it until the process exits.  It calls no cudaMalloc,
  * no cudaFree and no allocating library routine.
  *
- *   - The first call on a device looks up the array's device address on
- *     that device (cudaGetSymbolAddress, with the device current); make that
- *     first call before any stream capture on the device.
- *   - A split that would need more scratch than KDA_NOALLOC_SCRATCH_BYTES
- *     (see kda_chunk_fwd_workspace_size) is rejected with
- *     KDA_ERR_INVALID_ARGUMENT and nothing is enqueued.
+ *   - Every call that may split looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress); the first such call on a device
+ *     also loads the library's module there, so make it before any stream
+ *     capture on that device.
+ *   - The split is the best plan whose segment summaries fit in
+ *     KDA_NOALLOC_SCRATCH_BYTES; when none fits (see
+ *     kda_chunk_fwd_workspace_size for what the best plan would need), the
+ *     sequences run unsplit, which needs no scratch at all.
  *   - All calls share the one array and it keeps the last call's contents;
  *     every byte a call reads is written earlier in that same call, so
  *     nothing needs clearing.  Calls whose work overlaps on the GPU (for

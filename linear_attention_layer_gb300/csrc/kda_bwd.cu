@@ -503,14 +503,15 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
                                  void* ws, cudaStream_t st) {
   using namespace bwd;
   if (p.num_seqs == 0) return cudaSuccess;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(bwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)sizeof(Smem));
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(bwd_kernel<__nv_bfloat16>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+  static PerDeviceInit attrs;
+  const cudaError_t attr = attrs.run([] {
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<float>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(Smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+    return e;
   });
   if (attr != cudaSuccess) return attr;
   static thread_local Params prm;  // large: keep off the stack

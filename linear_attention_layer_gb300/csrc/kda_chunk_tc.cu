@@ -1159,8 +1159,10 @@ constexpr int kMaxEntries = kMaxOrder / kEnt;
 thread_local int g_inject_wait_timeout = 0;
 
 // Choose a segment length by a waves-of-SMs cost model; split only when it
-// beats the unsplit launch by a clear margin.
-SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms) {
+// beats the unsplit launch by a clear margin.  Plans whose segment summaries
+// need more than max_bytes of scratch are not considered.
+SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms,
+                     size_t max_bytes = ~(size_t)0) {
   SplitPlan best;
   if (!cu || p.num_seqs == 0 || p.num_seqs > kMaxScanSeqs) return best;
   const long units = (long)p.num_seqs * p.num_heads;
@@ -1188,6 +1190,7 @@ SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms) {
       steps = std::max<long>(steps, k - 2);
     }
     if (e > kMaxEntries || u1 > kMaxEntries) continue;
+    if (3 * (size_t)e * p.num_heads * kD * kD * sizeof(float) > max_bytes) continue;
     u1 *= p.num_heads;
     u3 *= p.num_heads;
     const double cost = std::ceil((double)u1 / sms) * segc + std::ceil((double)u3 / sms) * segc +
@@ -1242,19 +1245,18 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   if (p.num_seqs == 0) return cudaSuccess;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(chunk_tc_kernel<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(chunk_tc_kernel<true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(state_scan_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)(2 * kD * kScanLd * sizeof(float)));
+  static PerDeviceInit attrs;
+  const cudaError_t attr_err = attrs.run([] {
+    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_tc_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(2 * kD * kScanLd * sizeof(float)));
+    return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
 
@@ -1306,11 +1308,8 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.use_order = 0;
   prm.mode = 0;
 
-  SplitPlan plan;
-  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0) {
-    plan = plan_split(p, cu_host, sms);
-    if (plan.use && ws_bytes < plan.bytes) plan.use = false;
-  }
+  SplitPlan plan;  // the best split whose summaries fit in the workspace, if any
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0) plan = plan_split(p, cu_host, sms, ws_bytes);
   if (!plan.use) {
     prm.num_units = p.num_seqs * p.num_heads;
     if (cu_host && p.num_seqs <= kMaxOrder) {

@@ -5,7 +5,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace kda {
+
+// Function attributes (such as the dynamic shared-memory limit) belong to a
+// device's context, so a launcher that sets them must do so on every device
+// it launches on.  run(fn) calls fn once per device -- the current one --
+// and remembers success; a failure is returned and retried on the next call.
+class PerDeviceInit {
+ public:
+  template <class F>
+  cudaError_t run(F&& fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return fn();  // beyond the table: every call
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev]) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
 
 struct Problem {
   int num_seqs;
@@ -72,8 +99,8 @@ cudaError_t launch_chunk_simt(const Problem& p, const Args& a, cudaStream_t stre
 
 // Chunked prefill on the tensor cores (bf16 io, dk = dv = 128, 16-byte
 // aligned buffers).  cu_host (optional) orders the work longest-first and,
-// with enough workspace (256-byte aligned), lets long sequences be split
-// across SMs.
+// with workspace (256-byte aligned), lets long sequences be split across SMs
+// by the best plan whose segment summaries fit in ws_bytes.
 bool chunk_tc_supported(const Problem& p, const Args& a);
 size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,

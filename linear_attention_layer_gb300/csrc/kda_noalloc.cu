@@ -11,8 +11,6 @@
 // module instead: nothing is allocated or freed at call time.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/kda.h"
 #include "kda_launch.h"
 
@@ -24,26 +22,16 @@ namespace {
 // from cudaGetSymbolAddress, per device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached; null on failure.
+// Device address of the scratch array on the current device, or null.  It is
+// looked up on every call (a cheap host query): a cached address would go
+// stale if the context were torn down and the module loaded again.
 void* scratch_on_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) {
-      cudaGetLastError();  // clear this thread's last-error state
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+    cudaGetLastError();  // clear this thread's last-error state
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  return p;
 }
 
 }  // namespace
@@ -63,15 +51,15 @@ extern "C" kda_status_t kda_chunk_fwd_noalloc(const kda_desc_t* desc, const void
     return kda::launch_chunk_simt(p, a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
                                                                              : KDA_ERR_CUDA;
   }
-  const size_t need = kda::chunk_tc_workspace_bytes(p, desc->cu_seqlens_host);
-  if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_INVALID_ARGUMENT;
+  // Any split plan at all?  The launcher then takes the best one whose
+  // segment summaries fit in the array, or runs unsplit when none fits.
   void* ws = nullptr;
-  if (need > 0) {
+  if (kda::chunk_tc_workspace_bytes(p, desc->cu_seqlens_host) > 0) {
     ws = scratch_on_current_device();
     if (!ws) return KDA_ERR_CUDA;
   }
   const cudaError_t e = kda::launch_chunk_tc(p, a, desc->cu_seqlens_host, ws,
-                                             need > 0 ? (size_t)KDA_NOALLOC_SCRATCH_BYTES : 0,
+                                             ws ? (size_t)KDA_NOALLOC_SCRATCH_BYTES : 0,
                                              (cudaStream_t)stream);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -94,3 +94,87 @@ def oracle_pairs(p, pairs, threads=0):
     for i, (n, h) in enumerate(pairs):
         res[(n, h)] = (out[cu2[i]:cu2[i + 1], 0], fin[i, 0])
     return res
+
+
+class WholeTensorError:
+    """Error statistics of one whole tensor, accumulated piece by piece.
+
+    The tensor has a head axis (axis `head_axis` of every piece added); the
+    sums of squared error and of squared reference values are kept per head,
+    so that both the whole-tensor relative L2 error and the worst per-head
+    value come out at the end, as do max |err| (after the storage half-ulp
+    discount) and the whole-tensor RMS of the reference."""
+
+    def __init__(self, num_heads, storage=None, roundings=1):
+        self.err2 = np.zeros(num_heads)
+        self.ref2 = np.zeros(num_heads)
+        self.max_err = 0.0
+        self.count = 0
+        self.storage = storage
+        self.roundings = roundings
+
+    def add(self, x, ref, head_axis, heads=None):
+        """x, ref: the same piece of the result and of the oracle; `heads` the
+        head indices the piece's head axis holds (default: all of them)."""
+        x, ref = as64(x), as64(ref)
+        assert x.shape == ref.shape, (x.shape, ref.shape)
+        d = x - ref
+        axes = tuple(i for i in range(x.ndim) if i != head_axis)
+        idx = np.arange(self.err2.size) if heads is None else np.asarray(heads)
+        self.err2[idx] += np.sum(d * d, axis=axes)
+        self.ref2[idx] += np.sum(ref * ref, axis=axes)
+        err = np.abs(d)
+        if self.storage is not None:
+            err = np.maximum(err - self.roundings * half_ulp(ref, self.storage), 0.0)
+        self.max_err = max(self.max_err, float(np.max(err, initial=0.0)))
+        self.count += ref.size
+
+    def rel_l2(self):
+        den = float(np.sum(self.ref2))
+        return float(np.sqrt(np.sum(self.err2) / den)) if den > 0 else float(np.sqrt(np.sum(self.err2)))
+
+    def worst_head(self):
+        with np.errstate(divide="ignore", invalid="ignore"):
+            per = np.where(self.ref2 > 0, np.sqrt(self.err2 / self.ref2), np.sqrt(self.err2))
+        h = int(np.argmax(per))
+        return h, float(per[h])
+
+    def max_over_rms(self):
+        rms = np.sqrt(np.sum(self.ref2) / self.count) if self.count else 0.0
+        return self.max_err / rms if rms > 0 else self.max_err
+
+    def report(self, what):
+        h, w = self.worst_head()
+        return (f"{what}: rel-L2 {self.rel_l2():.3e} (worst head {h}: {w:.3e}), "
+                f"max|err|/RMS {self.max_over_rms():.3e}")
+
+    def check(self, io_dtype, what):
+        """The tolerance rule of assert_close on the whole tensor."""
+        e = self.rel_l2()
+        if io_dtype == torch.float32:
+            assert e <= TOL_F32, self.report(what)
+        else:
+            assert e <= TOL_BF16_REL, self.report(what)
+            assert self.max_over_rms() <= TOL_BF16_MAX_RMS, self.report(what)
+        return self.report(what)
+
+
+def device_compare(x, ref, both_stored=False):
+    """(rel-L2, max|err|/RMS) of two same-shape device tensors, computed in
+    fp64 on their device (for comparisons too large to move to the host).
+    both_stored: each side is a bf16 result, so two half-ulps are discounted."""
+    xd, rd = x.double(), ref.double()
+    d = xd - rd
+    den = torch.linalg.vector_norm(rd)
+    rel = float(torch.linalg.vector_norm(d) / den) if float(den) > 0 else float(
+        torch.linalg.vector_norm(d))
+    err = d.abs()
+    if ref.dtype == torch.bfloat16 or x.dtype == torch.bfloat16:
+        a = rd.abs()
+        _, e = torch.frexp(a)
+        hu = torch.where(a > 0, torch.ldexp(torch.ones_like(a), (e - 9).to(a.dtype)),
+                         torch.zeros_like(a))
+        err = torch.clamp(err - (2 if both_stored else 1) * hu, min=0.0)
+    rms = torch.sqrt(torch.mean(rd * rd))
+    mx = float(err.max()) if err.numel() else 0.0
+    return rel, (mx / float(rms) if float(rms) > 0 else mx)

@@ -1,7 +1,7 @@
 """GPU parity: the libkda kernels (through the C ABI) against the fp64 oracle
 on the same seeded inputs, element by element, with the tolerances of
-tests/parity.py.  Small cases compare every output; the full-size workloads
-compare every output of a sample of (sequence, head) pairs."""
+tests/parity.py.  Small cases and the full-size workloads alike compare every output and every
+final state."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +9,7 @@ import torch
 import linear_attention_layer_gb300 as kda
 import oracle
 import workloads
-from tests.parity import assert_close, oracle_pairs, rel_l2
+from tests.parity import WholeTensorError, assert_close, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -492,60 +492,142 @@ def test_state_checkpoints_with_split_sequences():
 
 
 # ------------------------------------------------- full-size workloads -----
+#
+# Every (sequence, head) of each full workload against the oracle.  The oracle
+# runs piece by piece (groups of sequences, or of heads for a single long
+# sequence) on all host cores; the whole-tensor relative L2 error, the worst
+# per-head value and max|err| / RMS over the whole tensor are accumulated
+# across the pieces and checked at the end.
 
-def _sampled_prefill(name, pairs_fn, **kw):
-    p = workloads.prefill_workload(name, device=DEV)
+def _pieces(p, max_head_tokens=1 << 21):
+    """(sequence range, head range) pieces covering Problem p, each about
+    max_head_tokens head-tokens of oracle work."""
+    cu, H = p.cu_seqlens_host, p.meta["num_heads"]
+    if p.num_seqs == 1:
+        hs = max(1, min(H, max_head_tokens // max(cu[1], 1)))
+        return [((0, 1), (h, min(H, h + hs))) for h in range(0, H, hs)]
+    out, n0, tok = [], 0, 0
+    for n in range(p.num_seqs):
+        tok += (cu[n + 1] - cu[n]) * H
+        if tok >= max_head_tokens or n + 1 == p.num_seqs:
+            out.append(((n0, n + 1), (0, H)))
+            n0, tok = n + 1, 0
+    return out
+
+
+def _full_check(p, results, io_dtype=torch.bfloat16):
+    """results: {label: (out, final_state)} of GPU runs on Problem p; each is
+    compared with the oracle over every (sequence, head)."""
+    H = p.meta["num_heads"]
+    cu = p.cu_seqlens_host
+    acc = {lab: (WholeTensorError(H, io_dtype), WholeTensorError(H)) for lab in results}
+    for (n0, n1), (h0, h1) in _pieces(p):
+        a, b = cu[n0], cu[n1]
+        sl = lambda x: x[a:b, h0:h1].cpu()
+        s0 = None if p.initial_state is None else p.initial_state[n0:n1, h0:h1].cpu()
+        ro, rf, _ = oracle.recurrent(sl(p.q), sl(p.k), sl(p.v), sl(p.z), sl(p.beta),
+                                     [x - a for x in cu[n0:n1 + 1]], s0)
+        for lab, (out, fin) in results.items():
+            acc[lab][0].add(out[a:b, h0:h1].cpu(), ro, head_axis=1, heads=range(h0, h1))
+            acc[lab][1].add(fin[n0:n1, h0:h1].cpu(), rf, head_axis=1, heads=range(h0, h1))
+    for lab in results:
+        print(acc[lab][0].check(io_dtype, f"{p.name} {lab} out"))
+        print(acc[lab][1].check(io_dtype, f"{p.name} {lab} final state"))
+
+
+def _run_prefill(p, **kw):
     out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
                              cu_seqlens_host=p.cu_seqlens_host, **kw)
     torch.cuda.synchronize()
     assert kda.get_device_error() == 0
-    pairs = pairs_fn(p)
-    ref = oracle_pairs(p, pairs)
-    cu = p.cu_seqlens_host
-    for (n, h), (ro, rf) in ref.items():
-        assert_close(out[cu[n]:cu[n + 1], h], ro, torch.bfloat16, f"{name} out (n={n}, h={h})")
-        assert_close(fin[n, h], rf, torch.bfloat16, f"{name} final (n={n}, h={h})")
     assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
+    return out, fin
 
 
-def test_full_prefill_workload_sampled():
-    _sampled_prefill("prefill", lambda p: [(0, 0), (1, 7), (2, 15), (3, 3)])
+def test_full_prefill_workload():
+    """4 x 4096 tokens, 16 heads: every output and final state, unsplit and
+    with the split across SMs that scratch allows (64 units on 152 SMs)."""
+    p = workloads.prefill_workload("prefill", device=DEV)
+    res = {"unsplit": _run_prefill(p)}
+    if _ws_bytes(p) > 0:
+        res["split"] = _run_prefill(p, workspace="auto")
+    _full_check(p, res)
 
 
 @pytest.mark.parametrize("name", ["long", "long_slow"])
-def test_full_long_workload_sampled(name):
-    _sampled_prefill(name, lambda p: [(0, 0), (0, 13), (0, 31)])
+def test_full_long_workload(name):
+    """One 65536-token sequence, 32 heads, unsplit and split across SMs."""
+    p = workloads.prefill_workload(name, device=DEV)
+    assert _ws_bytes(p) > 0
+    _full_check(p, {"unsplit": _run_prefill(p), "split": _run_prefill(p, workspace="auto")})
 
 
-def test_full_varlen_workload_sampled():
-    def pairs(p):
-        lens = np.diff(p.cu_seqlens_host)
-        longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
-        return [(longest, 0), (shortest, 31), (5, 17), (63, 9)]
-    _sampled_prefill("varlen", pairs)
+def test_full_varlen_workload():
+    """The bench step: 64 sequences of 256..8192 tokens, 32 heads, initial
+    and final states -- every (sequence, head)."""
+    p = workloads.prefill_workload("varlen", device=DEV)
+    _full_check(p, {"chunk_fwd": _run_prefill(p)})
 
 
-def test_full_decode_workload_sampled():
-    """256 requests x 32 heads, 1000 steps in place; every step's output and
-    the final state of sampled (request, head) pairs against the oracle's
-    1000-token recurrence."""
-    steps = 1000
-    d = workloads.decode_workload(256, 32, 128, 128, steps=steps, device=DEV)
-    pairs = [(0, 0), (77, 5), (255, 31)]
-    s0 = {pr: d.state[pr[0], pr[1]].cpu().clone() for pr in pairs}
-    outs = {pr: [] for pr in pairs}
+def test_full_decode_workload():
+    """256 requests x 32 heads, 1000 steps in place: every step's output of
+    every (request, head) and every final state against the oracle's
+    1000-token recurrence per (request, head)."""
+    steps, N, H = 1000, 256, 32
+    d = workloads.decode_workload(N, H, 128, 128, steps=steps, device=DEV)
+    s0 = d.state.clone()
+    outs = torch.empty((steps, N, H, 128), dtype=torch.bfloat16, device=DEV)
     for t in range(steps):
-        o = kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state)
-        for (n, h) in pairs:
-            outs[(n, h)].append(o[n, h].clone())
+        kda.decode_step(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=outs[t])
     torch.cuda.synchronize()
     assert kda.get_device_error() == 0
-    for (n, h) in pairs:
-        ro, rf, _ = oracle.recurrent(d.q[:, n, h:h + 1], d.k[:, n, h:h + 1], d.v[:, n, h:h + 1],
-                                     d.z[:, n, h:h + 1], d.beta[:, n, h:h + 1], [0, steps],
-                                     s0[(n, h)][None, None])
-        assert_close(torch.stack(outs[(n, h)]), ro[:, 0], torch.bfloat16, f"decode out {n},{h}")
-        assert_close(d.state[n, h], rf[0, 0], torch.bfloat16, f"decode state {n},{h}")
+    acc_o, acc_s = WholeTensorError(H, torch.bfloat16), WholeTensorError(H)
+    per = 16  # requests per oracle piece (16 x 32 sequences of 1000 tokens)
+    for r0 in range(0, N, per):
+        r1 = min(N, r0 + per)
+        seq = lambda x: x[:, r0:r1].transpose(0, 1).reshape(-1, *x.shape[2:]).cpu()
+        cu = [i * steps for i in range(r1 - r0 + 1)]
+        ro, rf, _ = oracle.recurrent(seq(d.q), seq(d.k), seq(d.v), seq(d.z), seq(d.beta), cu,
+                                     s0[r0:r1].cpu())
+        acc_o.add(seq(outs), ro, head_axis=1)
+        acc_s.add(d.state[r0:r1].cpu(), rf, head_axis=1)
+    print(acc_o.check(torch.bfloat16, "decode 1000 steps out"))
+    print(acc_s.check(torch.bfloat16, "decode 1000 steps state"))
+
+
+def test_tensor_core_fp16_range_check():
+    """The tensor-core path's dense products take fp16 operands.  A bf16 v
+    beyond the fp16 range (|v| >= 65504, which bf16 holds) is flagged with
+    KDA_ERR_DEVICE_CHECK in the device error word, and the next call on the
+    same context is correct."""
+    p = workloads.random_problem([130, 70], 2, 128, 128, torch.bfloat16, init_std=0.1, seed=31,
+                                 device=DEV)
+    v_big = p.v.clone()
+    v_big[100, 1, 5] = 1.0e5
+    assert float(v_big[100, 1, 5]) >= 65504.0
+    assert kda.get_device_error() == 0
+    kda.chunk_fwd(p.q, p.k, v_big, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                  cu_seqlens_host=p.cu_seqlens_host)
+    assert kda.get_device_error() == 5  # KDA_ERR_DEVICE_CHECK
+    # an initial state beyond the range is flagged as well
+    s_big = p.initial_state.clone()
+    s_big[0, 0, 3, 3] = 7.0e4
+    kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, s_big,
+                  cu_seqlens_host=p.cu_seqlens_host)
+    assert kda.get_device_error() == 5
+    assert kda.get_device_error() == 0  # cleared by the read
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    _check_all(p, out, fin, torch.bfloat16)
+    # the fp32 recurrent path takes the same large v without complaint
+    o2, f2 = kda.recurrent_fwd(p.q, p.k, v_big, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    ro, rf, _ = oracle.recurrent(p.q, p.k, v_big, p.z, p.beta, p.cu_seqlens_host,
+                                 p.initial_state)
+    assert_close(o2, ro, torch.bfloat16, "recurrent out with |v| = 1e5")
 
 
 # ------------------------------------------- long sequences split across SMs --
@@ -585,15 +667,6 @@ def test_split_final_state_may_alias_initial_state():
     torch.cuda.synchronize()
     assert_close(out, ro, torch.bfloat16, "out")
     assert_close(fin, rf, torch.bfloat16, "final_state")
-
-
-@pytest.mark.parametrize("name", ["long", "long_slow"])
-def test_full_long_workload_split_sampled(name):
-    """The long-context workload (one 65536-token sequence, 32 heads) through
-    the split path."""
-    p = workloads.prefill_workload(name, device=DEV)
-    assert _ws_bytes(p) > 0
-    _sampled_prefill(name, lambda p: [(0, 0), (0, 19)], workspace="auto")
 
 
 def test_expired_device_wait_reports_timeout_and_recovers():
