@@ -421,6 +421,71 @@ kda_status_t kda_short_conv(const kda_desc_t* desc, int32_t width, const void* x
                             const int32_t* cu_seqlens, void* y, float* conv_state_out,
                             kda_stream_t stream);
 
+/*
+ * Context parallelism: one long sequence cut along its tokens across
+ * devices.  The state update is affine in the state (mhpq.cn/news/56770,
+ * section "KDA 到底在算什么"), so a piece of a sequence maps the state entering
+ * it to S_out = M S_in + S~.  The pages' context-parallel KDA (blog.higcp.com
+ * "猜想：K3 可能是最适合 TPU 的 MoE 架构", section "第二层") has each device
+ * summarise its piece by (M, S~), exchange the summaries in one all-gather,
+ * rebuild the state entering its piece by a prefix scan, and then run its
+ * piece from that state (kda_chunk_fwd with initial_state = that state).
+ *
+ * kda_chunk_fwd_summary -- the affine summary of every sequence of a packed
+ * batch (each rank's pieces):
+ *
+ *   desc               as for kda_chunk_fwd; bf16 io and dk = dv = 128 only
+ *                      (else KDA_ERR_UNSUPPORTED); cu_seqlens_host is
+ *                      REQUIRED; a_log and gate_per_head are honoured;
+ *                      workspace / workspace_bytes: optional device scratch
+ *                      (256-byte aligned) that lets long sequences be cut
+ *                      into segments summarised side by side and composed
+ *                      (kda_chunk_fwd_summary_workspace_size gives what the
+ *                      best plan needs; a smaller area limits the plan);
+ *                      checkpoint fields are ignored.
+ *   q, k, v, z, beta, cu_seqlens   device, as for kda_chunk_fwd (q, k, v, z
+ *                      16-byte aligned)
+ *   transition         device, [N, H, dk, dk] fp32, written: M, the product
+ *                      of the sequence's per-token transitions
+ *                      (I - beta k k^T) Diag(alpha), row = output key channel
+ *   offset_state       device, [N, H, dk, dv] fp32, written: S~, the state
+ *                      the sequence reaches from zeros
+ * An empty sequence gives M = I and S~ = 0.  Neither output may alias an
+ * input or the other.  In fp32, M's entries underflow to zero when the
+ * piece decays them below about e^-87; M S_in + S~ stays accurate.
+ */
+kda_status_t kda_chunk_fwd_summary(const kda_desc_t* desc, const void* q, const void* k,
+                                   const void* v, const float* z, const float* beta,
+                                   const int32_t* cu_seqlens, float* transition,
+                                   float* offset_state, kda_stream_t stream);
+
+/* Bytes of device scratch that let kda_chunk_fwd_summary split long
+ * sequences across SMs (0 when no split would be planned).  Needs
+ * desc->cu_seqlens_host. */
+kda_status_t kda_chunk_fwd_summary_workspace_size(const kda_desc_t* desc, size_t* bytes);
+
+/*
+ * kda_state_scan -- the prefix scan of the scheme above: starting from
+ * initial_state (zeros when NULL), applies S <- M_i S + S~_i for
+ * i = 0 .. count-1, in fp32, to every (sequence, head).  Rank r of a
+ * context-parallel run calls it with count = r on the gathered summaries
+ * of ranks 0 .. R-1 to get the state entering its pieces.
+ *
+ *   desc               num_seqs (N), num_heads (H), dk, dv (32, 64 or 128);
+ *                      other fields are ignored
+ *   count              >= 0; 0 copies initial_state (or writes zeros)
+ *   transitions        device, [count, N, H, dk, dk] fp32 (rank-major, as an
+ *                      all-gather of kda_chunk_fwd_summary's transition
+ *                      lays them out); may be NULL when count = 0
+ *   offsets            device, [count, N, H, dk, dv] fp32, likewise
+ *   initial_state      device, [N, H, dk, dv] fp32, or NULL for zeros
+ *   entry_state        device, [N, H, dk, dv] fp32, written; may alias
+ *                      initial_state exactly, not transitions or offsets
+ */
+kda_status_t kda_state_scan(const kda_desc_t* desc, int32_t count, const float* transitions,
+                            const float* offsets, const float* initial_state,
+                            float* entry_state, kda_stream_t stream);
+
 const char* kda_status_string(kda_status_t status);
 
 /* Synchronise `stream`, then read and clear the device error word of the

@@ -23,7 +23,8 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "get_device_error", "status_string", "KDAError", "load", "LIB_PATH",
            "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
            "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "chunk_fwd_host",
-           "chunk_fwd_host_workspace_size", "EXPORTED_SYMBOLS"]
+           "chunk_fwd_host_workspace_size", "chunk_fwd_summary",
+           "chunk_fwd_summary_workspace_size", "state_scan", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -38,7 +39,9 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_decode_replay_window", "kda_status_string", "kda_get_device_error",
                     "kda_chunk_fwd_noalloc", "kda_testing_inject_wait_timeout",
                     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "kda_short_conv",
-                    "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size")
+                    "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size",
+                    "kda_chunk_fwd_summary", "kda_chunk_fwd_summary_workspace_size",
+                    "kda_state_scan")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -95,6 +98,12 @@ def load() -> ctypes.CDLL:
         lib.kda_short_conv.argtypes = [dp, ctypes.c_int32] + [vp] * 7
         lib.kda_recurrent_bwd_workspace_size.restype = ctypes.c_int
         lib.kda_recurrent_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_chunk_fwd_summary.restype = ctypes.c_int
+        lib.kda_chunk_fwd_summary.argtypes = [dp] + [vp] * 9
+        lib.kda_chunk_fwd_summary_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_fwd_summary_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_state_scan.restype = ctypes.c_int
+        lib.kda_state_scan.argtypes = [dp, ctypes.c_int32] + [vp] * 5
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_testing_inject_wait_timeout.restype = None
@@ -590,3 +599,90 @@ def testing_inject_wait_timeout(launches: int = 1) -> None:
     """Make the next `launches` tensor-core prefill launches of this thread hit
     an expired device wait (``kda_testing_inject_wait_timeout``)."""
     load().kda_testing_inject_wait_timeout(int(launches))
+
+
+def chunk_fwd_summary_workspace_size(num_seqs, total_tokens, num_heads, dk, dv, dtype,
+                                     cu_seqlens_host):
+    """Bytes of device scratch that let ``chunk_fwd_summary`` split long
+    sequences across SMs (0: no split would be planned)."""
+    desc, keep = make_desc(num_seqs, total_tokens, num_heads, dk, dv, _io_code(dtype),
+                           cu_seqlens_host)
+    n = ctypes.c_size_t(0)
+    st = load().kda_chunk_fwd_summary_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_summary_workspace_size")
+    return int(n.value)
+
+
+def chunk_fwd_summary(q, k, v, z, beta, cu_seqlens, cu_seqlens_host, *, transition=None,
+                      offset_state=None, workspace="auto", stream=None, a_log=None):
+    """``kda_chunk_fwd_summary``: the affine map each sequence applies to its
+    entering state, S_out = transition @ S_in + offset_state.  Returns
+    (transition [N, H, dk, dk], offset_state [N, H, dk, dv]), fp32.
+    ``workspace``: device scratch of ``chunk_fwd_summary_workspace_size`` bytes
+    that lets long sequences split across SMs, "auto" (allocated here with
+    torch) or None."""
+    lib = load()
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (T, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (T, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (T, H, dv), dev)
+    per_head = z.dim() == 2
+    _check_tensor("z", z, torch.float32, (T, H) if per_head else (T, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (T, H), dev)
+    _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    if transition is None:
+        transition = torch.empty((N, H, dk, dk), dtype=torch.float32, device=dev)
+    if offset_state is None:
+        offset_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_tensor("transition", transition, torch.float32, (N, H, dk, dk), dev)
+    _check_tensor("offset_state", offset_state, torch.float32, (N, H, dk, dv), dev)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be a tensor, 'auto' or None")
+        nbytes = chunk_fwd_summary_workspace_size(N, T, H, dk, dv, q.dtype, cu_seqlens_host)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+    desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
+    desc.gate_per_head = 1 if per_head else 0
+    with torch.cuda.device(dev):
+        st = lib.kda_chunk_fwd_summary(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                       _ptr(beta), _ptr(cu_seqlens), _ptr(transition),
+                                       _ptr(offset_state), _stream_handle(stream))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_chunk_fwd_summary")
+    return transition, offset_state
+
+
+def state_scan(transitions, offsets, initial_state=None, *, count=None, out=None, stream=None):
+    """``kda_state_scan``: S <- transitions[i] @ S + offsets[i] for
+    i = 0 .. count-1 (default: all), from ``initial_state`` (zeros if None).
+    transitions [R, N, H, dk, dk], offsets [R, N, H, dk, dv] fp32 on the
+    device.  Returns the state [N, H, dk, dv] (``out`` may be initial_state)."""
+    lib = load()
+    R, N, H, dk, dv = offsets.shape
+    dev = offsets.device
+    count = R if count is None else int(count)
+    if not 0 <= count <= R:
+        raise ValueError(f"count must be in 0..{R}")
+    _check_tensor("transitions", transitions, torch.float32, (R, N, H, dk, dk), dev)
+    _check_tensor("offsets", offsets, torch.float32, (R, N, H, dk, dv), dev)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_tensor("out", out, torch.float32, (N, H, dk, dv), dev)
+    desc, keep = make_desc(N, 0, H, dk, dv, KDA_F32)
+    with torch.cuda.device(dev):
+        st = lib.kda_state_scan(ctypes.byref(desc), count, _ptr(transitions), _ptr(offsets),
+                                _ptr(initial_state), _ptr(out), _stream_handle(stream))
+    del keep
+    if st != KDA_OK:
+        raise KDAError(st, "kda_state_scan")
+    return out

@@ -129,6 +129,10 @@ kda_status_t check_bwd(const kda_desc_t* desc, const void* q, const void* k, con
 }  // namespace
 
 namespace kda {
+int* device_error() { return device_error_word(); }
+kda_status_t check_prefill_desc(const kda_desc_t* desc) { return check_desc(desc, false); }
+Problem problem_of(const kda_desc_t* desc) { return to_problem(desc); }
+
 // Host-side validation shared with kda_chunk_fwd_noalloc (kda_noalloc.cu).
 kda_status_t validate_prefill(const kda_desc_t* desc, const void* q, const void* k,
                               const void* v, const float* z, const float* beta,

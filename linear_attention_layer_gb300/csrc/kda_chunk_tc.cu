@@ -129,7 +129,9 @@ constexpr float kF16Max = 65504.0f;
 // caller's initial / final state of `seq`), kSlotNone for no output state;
 // flags & kFlagZeroV treats v as zero.
 constexpr int kEnt = 6;
-constexpr int kSlotNone = -1, kSlotZero = -1, kSlotIdentity = -2, kSlotUser = -3;
+// kSlotAux (out only): the caller's aux_state of `seq` (the transition M of an
+// affine summary).
+constexpr int kSlotNone = -1, kSlotZero = -1, kSlotIdentity = -2, kSlotUser = -3, kSlotAux = -4;
 constexpr int kFlagZeroV = 1;
 
 struct Params {
@@ -143,6 +145,7 @@ struct Params {
   const int32_t* cu;
   __nv_bfloat16* out;   // may be null (no output written)
   float* final_state;
+  float* aux_state;     // [N][H][dk][dk]: output slot kSlotAux (mode 1)
   float* ws;            // state slots [slot][H][dk][dv] (mode 1)
   int* err;
   int H, total, num_seqs, num_units, use_order, mode;
@@ -989,6 +992,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* dst = nullptr;
     if (out_slot == kSlotUser) {
       if (P.final_state) dst = P.final_state + ((size_t)seq * H + h) * kD * kD;
+    } else if (out_slot == kSlotAux) {
+      if (P.aux_state) dst = P.aux_state + ((size_t)seq * H + h) * kD * kD;
     } else if (out_slot >= 0) {
       dst = P.ws + ((size_t)out_slot * H + h) * kD * kD;
     }
@@ -1239,74 +1244,97 @@ size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host) {
   return plan.use ? (plan.bytes + 255) / 256 * 256 : 0;
 }
 
+namespace tcp {
+
+// What every tensor-core launch needs: the kernels' shared-memory limit set
+// on this device, the TMA maps of q, k, v and z, and the common parameters.
+struct TcLaunch {
+  CUtensorMap mq, mk, mv, mz;
+  bool per_head = false;
+  int sms = 0;
+  cudaStream_t st = nullptr;
+
+  cudaError_t init(const Problem& p, const Args& a, Params& prm, cudaStream_t stream) {
+    st = stream;
+    per_head = a.gate_per_head != 0;
+    sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    static PerDeviceInit attrs;
+    const cudaError_t attr_err = attrs.run([] {
+      cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_tc_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(2 * kD * kScanLd * sizeof(float)));
+      return e;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int T = std::max(p.total_tokens, 1);
+    if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (per_head) {
+      mz = mq;  // z is [T, H] and read directly; the z tile map is never used
+    } else if (!make_map(&mz, a.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.num_heads, T, 128,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      return cudaErrorInvalidValue;
+    }
+    prm.beta = a.beta;
+    prm.a_log = a.a_log;
+    prm.ckpt = a.ckpt;
+    prm.ckpt_off = a.ckpt_off;
+    prm.ckpt_every = a.ckpt_every;
+    prm.zh = per_head ? a.z : nullptr;
+    prm.initial_state = a.initial_state;
+    prm.cu = a.cu_seqlens;
+    prm.out = static_cast<__nv_bfloat16*>(a.out);
+    prm.final_state = a.final_state;
+    prm.aux_state = nullptr;
+    prm.ws = nullptr;
+    prm.err = a.err;
+    prm.H = p.num_heads;
+    prm.total = p.total_tokens;
+    prm.num_seqs = p.num_seqs;
+    prm.spin_cycles = 4000000000LL;  // ~2 s at 2 GHz
+    prm.inject_timeout = 0;
+    if (g_inject_wait_timeout > 0) {  // testing aid, see kda_testing_inject_wait_timeout
+      --g_inject_wait_timeout;
+      prm.inject_timeout = 1;
+      prm.spin_cycles = 20000000LL;  // ~10 ms
+    }
+    prm.use_order = 0;
+    prm.mode = 0;
+    return cudaSuccess;
+  }
+
+  void launch(const Params& prm, int grid) const {
+    if (per_head)
+      chunk_tc_kernel<true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    else
+      chunk_tc_kernel<false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+  }
+};
+
+}  // namespace tcp
+
 cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,
                             size_t ws_bytes, cudaStream_t st) {
   using namespace tcp;
   if (p.num_seqs == 0) return cudaSuccess;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  static PerDeviceInit attrs;
-  const cudaError_t attr_err = attrs.run([] {
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(chunk_tc_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(2 * kD * kScanLd * sizeof(float)));
-    return e;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-
-  CUtensorMap mq, mk, mv, mz;
-  const int T = std::max(p.total_tokens, 1);
-  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.num_heads, T, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  if (a.gate_per_head) {
-    mz = mq;  // z is [T, H] and read directly; the z tile map is never used
-  } else if (!make_map(&mz, a.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.num_heads, T, 128,
-                       CU_TENSOR_MAP_SWIZZLE_NONE)) {
-    return cudaErrorInvalidValue;
-  }
-
   static thread_local Params prm;  // large: keep off the stack
-  auto launch_tc = [&](int grid) {
-    if (a.gate_per_head)
-      chunk_tc_kernel<true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
-    else
-      chunk_tc_kernel<false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
-  };
-  prm.beta = a.beta;
-  prm.a_log = a.a_log;
-  prm.ckpt = a.ckpt;
-  prm.ckpt_off = a.ckpt_off;
-  prm.ckpt_every = a.ckpt_every;
-  prm.zh = a.gate_per_head ? a.z : nullptr;
-  prm.initial_state = a.initial_state;
-  prm.cu = a.cu_seqlens;
-  prm.out = static_cast<__nv_bfloat16*>(a.out);
-  prm.final_state = a.final_state;
-  prm.ws = nullptr;
-  prm.err = a.err;
-  prm.H = p.num_heads;
-  prm.total = p.total_tokens;
-  prm.num_seqs = p.num_seqs;
-  prm.spin_cycles = 4000000000LL;  // ~2 s at 2 GHz
-  prm.inject_timeout = 0;
-  if (g_inject_wait_timeout > 0) {  // testing aid, see kda_testing_inject_wait_timeout
-    --g_inject_wait_timeout;
-    prm.inject_timeout = 1;
-    prm.spin_cycles = 20000000LL;  // ~10 ms
-  }
-  prm.use_order = 0;
-  prm.mode = 0;
+  TcLaunch tl;
+  const cudaError_t se = tl.init(p, a, prm, st);
+  if (se != cudaSuccess) return se;
+  const int sms = tl.sms;
+  auto launch_tc = [&](int grid) { tl.launch(prm, grid); };
 
   SplitPlan plan;  // the best split whose summaries fit in the workspace, if any
   if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0) plan = plan_split(p, cu_host, sms, ws_bytes);
@@ -1393,6 +1421,125 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   prm.num_units = ne * p.num_heads;
   launch_tc(std::min(prm.num_units, sms));
   return cudaGetLastError();
+}
+
+// ------------------------------------------------- affine summaries --------
+//
+// The summary (M, S~) of a sequence is the final state of two runs of the
+// same kernel: from zeros (S~) and from the identity with v = 0 (M; its
+// "value" axis is the identity's column).  When there are fewer than one
+// such run per SM, each sequence is cut into k segments whose summaries run
+// side by side and are then composed in order,
+//   S~ = M_{k-1}(... (M_1 S~_0 + S~_1) ...) + S~_{k-1},   M = M_{k-1} ... M_0.
+
+namespace tcp {
+
+struct SummaryPlan {
+  bool use = false;
+  int seg_len = 0, E = 0;       // segment length (tokens); slots per summary part
+  std::vector<int> k, base;     // segments per sequence; first slot of a split sequence
+  size_t bytes = 0;
+};
+
+SummaryPlan plan_summary(const Problem& p, const int32_t* cu, int sms,
+                         size_t max_bytes = ~(size_t)0) {
+  SummaryPlan best;
+  if (!cu || p.num_seqs == 0) return best;
+  const long runs = 2L * p.num_seqs * p.num_heads;
+  if (runs >= sms) return best;
+  long maxc = 0;
+  for (int n = 0; n < p.num_seqs; ++n) maxc = std::max<long>(maxc, (cu[n + 1] - cu[n] + kC - 1) / kC);
+  for (long kmax = sms / runs; kmax >= 2; --kmax) {
+    const long segc = std::max<long>(4, (maxc + kmax - 1) / kmax);
+    if (segc >= maxc) break;  // nothing would split
+    SummaryPlan pl;
+    pl.k.resize(p.num_seqs);
+    pl.base.resize(p.num_seqs);
+    for (int n = 0; n < p.num_seqs; ++n) {
+      const long c = (cu[n + 1] - cu[n] + kC - 1) / kC;
+      pl.k[n] = (int)std::max<long>(1, (c + segc - 1) / segc);
+      pl.base[n] = pl.E;
+      if (pl.k[n] >= 2) pl.E += pl.k[n];
+    }
+    pl.bytes = 2 * (size_t)pl.E * p.num_heads * kD * kD * sizeof(float);
+    if (pl.bytes > max_bytes) continue;
+    pl.use = true;
+    pl.seg_len = (int)(segc * kC);
+    return pl;
+  }
+  return best;
+}
+
+}  // namespace tcp
+
+size_t chunk_tc_summary_workspace_bytes(const Problem& p, const int32_t* cu_host) {
+  if (!p.io_bf16 || p.dk != 128 || p.dv != 128) return 0;
+  const int sms = tcp::sm_count();
+  if (sms <= 0) return 0;
+  const tcp::SummaryPlan plan = tcp::plan_summary(p, cu_host, sms);
+  return plan.use ? (plan.bytes + 255) / 256 * 256 : 0;
+}
+
+cudaError_t launch_chunk_tc_summary(const Problem& p, const Args& a, const int32_t* cu_host,
+                                    float* m_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+  using namespace tcp;
+  if (p.num_seqs == 0) return cudaSuccess;
+  static thread_local Params prm;  // large: keep off the stack
+  TcLaunch tl;
+  cudaError_t e = tl.init(p, a, prm, st);
+  if (e != cudaSuccess) return e;
+  SummaryPlan plan;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0)
+    plan = plan_summary(p, cu_host, tl.sms, ws_bytes);
+  prm.mode = 1;
+  prm.out = nullptr;
+  prm.ckpt = nullptr;
+  prm.final_state = a.final_state;  // S~ of unsplit sequences
+  prm.aux_state = m_out;            // M of unsplit sequences
+  prm.ws = static_cast<float*>(ws);
+  const int E = plan.use ? plan.E : 0;
+  // every run, longest first: {length, seq, tb, te, in, out, flags}
+  std::vector<std::array<int, 7>> runs;
+  for (int n = 0; n < p.num_seqs; ++n) {
+    const int k = plan.use ? plan.k[n] : 1;
+    for (int q = 0; q < k; ++q) {
+      const int tb = k == 1 ? cu_host[n] : cu_host[n] + q * plan.seg_len;
+      const int te = k == 1 ? cu_host[n + 1] : std::min(cu_host[n + 1], tb + plan.seg_len);
+      const int s_slot = k == 1 ? kSlotUser : plan.base[n] + q;
+      const int m_slot = k == 1 ? kSlotAux : E + plan.base[n] + q;
+      runs.push_back({te - tb, n, tb, te, kSlotZero, s_slot, 0});
+      runs.push_back({te - tb, n, tb, te, kSlotIdentity, m_slot, kFlagZeroV});
+    }
+  }
+  std::stable_sort(runs.begin(), runs.end(),
+                   [](const std::array<int, 7>& x, const std::array<int, 7>& y) { return x[0] > y[0]; });
+  for (size_t r0 = 0; r0 < runs.size(); r0 += kMaxEntries) {
+    const int ne = (int)std::min<size_t>(kMaxEntries, runs.size() - r0);
+    for (int i = 0; i < ne; ++i) {
+      const auto& r = runs[r0 + i];
+      int* en = prm.list + kEnt * i;
+      en[0] = r[1]; en[1] = r[2]; en[2] = r[3]; en[3] = r[4]; en[4] = r[5]; en[5] = r[6];
+    }
+    prm.num_units = ne * p.num_heads;
+    tl.launch(prm, std::min(prm.num_units, tl.sms));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!plan.use) return cudaSuccess;
+  // compose the segments of every split sequence
+  std::vector<FoldEntry> fs, fm;
+  for (int n = 0; n < p.num_seqs; ++n) {
+    const int k = plan.k[n], b = plan.base[n];
+    if (k < 2) continue;
+    fs.push_back(FoldEntry{b, E + b + 1, b + 1, n, k - 1});
+    fm.push_back(FoldEntry{E + b, E + b + 1, 0, n, k - 1});
+  }
+  const float* w = static_cast<const float*>(ws);
+  e = launch_state_fold(kD, kD, p.num_heads, w, w, w, a.final_state, 1, fs.data(),
+                        (int)fs.size(), st);
+  if (e != cudaSuccess) return e;
+  return launch_state_fold(kD, kD, p.num_heads, w, w, nullptr, m_out, 1, fm.data(),
+                           (int)fm.size(), st);
 }
 
 }  // namespace kda

@@ -106,6 +106,28 @@ size_t chunk_tc_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_host, void* ws,
                             size_t ws_bytes, cudaStream_t stream);
 
+// Affine summary of every sequence on the tensor cores (bf16, dk = dv = 128):
+// m_out[n, h] = the transition M (state after the sequence = M S_in + S~) and
+// a.final_state[n, h] = S~, the state reached from zeros.  With workspace
+// (256-byte aligned) long sequences are cut into segments whose summaries
+// are computed side by side and then composed.
+size_t chunk_tc_summary_workspace_bytes(const Problem& p, const int32_t* cu_host);
+cudaError_t launch_chunk_tc_summary(const Problem& p, const Args& a, const int32_t* cu_host,
+                                    float* m_out, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// Chains of affine state maps S <- M_i S + b_i in fp32 (M_i [dk][dk]; S and b_i
+// [dk][dv]), one chain per (entry, head), H heads.  Entry e starts from
+// start + (start_idx * H + h) * dk * dv (start == nullptr: zeros); its step i
+// reads M at m + ((m_idx + i * stride) * H + h) * dk * dk and b at
+// b + ((b_idx + i * stride) * H + h) * dk * dv (b == nullptr: no offset); the
+// result goes to out + (out_idx * H + h) * dk * dv.  out may alias start.
+struct FoldEntry {
+  int start_idx, m_idx, b_idx, out_idx, count;
+};
+cudaError_t launch_state_fold(int dk, int dv, int H, const float* start, const float* m,
+                              const float* b, float* out, long long stride,
+                              const FoldEntry* entries, int n_entries, cudaStream_t st);
+
 // Reverse mode of the recurrence, token by token (fp32; dk = dv = 128).
 struct BwdArgs {
   const void* q;
@@ -167,6 +189,11 @@ cudaError_t launch_chunk_fwd_host(const Problem& p, const HostArgs& h, int group
 #include "../../include/kda.h"
 
 namespace kda {
+// The device error word of the current device (null if it cannot be found).
+int* device_error();
+// The descriptor checks shared by the prefill calls.
+kda_status_t check_prefill_desc(const kda_desc_t* desc);
+Problem problem_of(const kda_desc_t* desc);
 // Host validation of a prefill call (the checks of kda_chunk_fwd); fills a and p.
 kda_status_t validate_prefill(const kda_desc_t* desc, const void* q, const void* k,
                               const void* v, const float* z, const float* beta,

@@ -202,3 +202,46 @@ def decode_step(q, k, v, z, beta, state, *, eps: float = DEFAULT_EPS,
 
 # The Q/K preprocessing convolution + Swish (pure numpy, fp64).
 from .short_conv import short_conv, swish  # noqa: E402,F401
+
+
+def affine_summary(q, k, v, z, beta, cu_seqlens, *, a_log=None, eps: float = DEFAULT_EPS,
+                   threads: int = 0):
+    """The affine map a sequence applies to its entering state.
+
+    The state update is affine in S (mhpq.cn/news/56770, "KDA 到底在算什么"), so
+    the state after a sequence is S_out = M S_in + S~ with M [dk, dk] the
+    product of the per-token transitions (I - b k k^T) Diag(alpha) and S~
+    [dk, dv] the state reached from S_in = 0.  Here both come straight from
+    the recurrence: S~ is the final state from zeros, M the final state from
+    the identity with every v set to zero (blog.higcp.com "猜想：K3 可能是最适合
+    TPU 的 MoE 架构", section "第二层": each device summarises its segment by
+    such an affine map before the all-gather).
+
+    Returns ``(M [N, H, dk, dk], S~ [N, H, dk, dv])`` in float64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, dk = q.shape
+    cu = np.asarray(cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+                    dtype=np.int64)
+    N = cu.shape[0] - 1
+    _, s_tilde, _ = recurrent(q, k, v, z, beta, cu, None, eps=eps, threads=threads,
+                              a_log=a_log)
+    eye = np.broadcast_to(np.eye(dk), (N, H, dk, dk)).copy()
+    _, m, _ = recurrent(q, k, np.zeros((T, H, dk)), z, beta, cu, eye, eps=eps,
+                        threads=threads, a_log=a_log)
+    return m, s_tilde
+
+
+def state_scan(transitions, offsets, initial_state=None, count=None):
+    """Apply the first ``count`` affine maps in order to the initial state:
+    S <- M_i S + S~_i for i = 0 .. count-1 (blog.higcp.com "猜想：K3 可能是最适合
+    TPU 的 MoE 架构", section "第二层": the prefix scan that gives each device
+    the state entering its segment).  transitions [R, N, H, dk, dk], offsets
+    [R, N, H, dk, dv], initial_state [N, H, dk, dv] or None (zeros).
+    Returns float64 [N, H, dk, dv]."""
+    m, s = _f64(transitions), _f64(offsets)
+    count = m.shape[0] if count is None else int(count)
+    state = np.zeros(s.shape[1:]) if initial_state is None else _f64(initial_state).copy()
+    for i in range(count):
+        state = np.matmul(m[i], state) + s[i]
+    return state

@@ -232,3 +232,46 @@ def test_host_prefill_rejects_bad_arguments(lib):
     assert lib.kda_chunk_fwd_host_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     # q, k, v, out bf16 + z fp32 + beta, 8 tokens x 2 heads x 128, two states each way, cu
     assert n.value >= 8 * 2 * 128 * (2 * 4 + 4) + 8 * 2 * 4 + 2 * 2 * 2 * 128 * 128 * 4
+
+
+def _call_summary(lib, desc, q=FAKE, cu=FAKE, m=ctypes.c_void_p(0x5000),
+                  s=ctypes.c_void_p(0x6000)):
+    return lib.kda_chunk_fwd_summary(ctypes.byref(desc), q, FAKE, FAKE, FAKE, FAKE, cu, m, s,
+                                     None)
+
+
+def test_summary_rejects_bad_arguments(lib):
+    cu = [0, 3, 8]
+    d, keep = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16, cu)
+    assert _call_summary(lib, d, cu=None) == 1                        # device cu_seqlens
+    assert _call_summary(lib, d, q=None) == 1                         # q required
+    assert _call_summary(lib, d, m=None) == 1                         # outputs required
+    assert _call_summary(lib, d, s=ctypes.c_void_p(0x5000)) == 1      # outputs alias
+    assert _call_summary(lib, d, m=FAKE) == 1                         # output aliases q
+    assert _call_summary(lib, d, q=ctypes.c_void_p(0x1004)) == 1      # not 16-byte aligned
+    nohost, keep2 = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16)    # host copy required
+    assert _call_summary(lib, nohost) == 1
+    for dk, dv, io in ((64, 64, kda.KDA_BF16), (128, 128, kda.KDA_F32)):
+        other, keep3 = kda.make_desc(2, 8, 2, dk, dv, io, cu)
+        assert _call_summary(lib, other) == 2                         # KDA_ERR_UNSUPPORTED
+    bad_cu, keep4 = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16, [0, 9, 8])
+    assert _call_summary(lib, bad_cu) == 1
+    n = ctypes.c_size_t(7)
+    assert lib.kda_chunk_fwd_summary_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value % 256 == 0
+    assert lib.kda_chunk_fwd_summary_workspace_size(ctypes.byref(d), None) == 1
+
+
+def test_state_scan_rejects_bad_arguments(lib):
+    d, keep = kda.make_desc(3, 0, 2, 64, 32, kda.KDA_F32)
+    out = ctypes.c_void_p(0x7000)
+    scan = lambda dd, count, m=FAKE, s=ctypes.c_void_p(0x2000), o=out: lib.kda_state_scan(
+        ctypes.byref(dd), count, m, s, None, o, None)
+    assert scan(d, -1) == 1                    # negative count
+    assert scan(d, 2, o=None) == 1             # no output
+    assert scan(d, 2, m=None) == 1             # transitions needed when count > 0
+    assert scan(d, 2, o=FAKE) == 1             # output aliases the transitions
+    bad, keep2 = kda.make_desc(3, 0, 2, 48, 32, kda.KDA_F32)
+    assert scan(bad, 1) == 1                   # unsupported dk
+    empty, keep3 = kda.make_desc(0, 0, 2, 64, 32, kda.KDA_F32)
+    assert scan(empty, 2) == 0                 # nothing to do
