@@ -259,6 +259,68 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
                                       kda_stream_t stream);
 
 /*
+ * The decode-side calls with their surrounding per-token steps fused into the
+ * same pass.  The pages describe K3's replay kernel as one recurrent loop that
+ * fuses the short convolution, the input norm, the gating, the KDA recurrence
+ * and the output norm (blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架构",
+ * section "三条容易被忽略的代价" (1)); the pages define neither the
+ * convolution's nor the output norm's form, so this library reads them as:
+ *
+ *   convolution: the depthwise causal convolution + Swish of kda_short_conv,
+ *     applied to the raw q and k of every token before their L2 norm, the
+ *     positions before a token reading that request's convolution state (its
+ *     last W-1 raw inputs, oldest first);
+ *   output norm: a per-head RMS norm of each output row,
+ *     out = o / sqrt(mean_j o_j^2 + eps) * out_norm_weight[h].
+ *
+ * Options (NULL = none of them):
+ *   conv_width          W: 0 = no convolution (q, k used as given), 1..4
+ *                       (KDA_ERR_UNSUPPORTED above 4)
+ *   conv_weight_q/_k    device [H, dk, W] fp32 taps (tap j multiplies
+ *                       x[t - (W-1) + j]), required when W > 0
+ *   conv_state_q/_k     device [B, H, dk, W-1] fp32, required when W > 1:
+ *                       read, and advanced in place by the tokens that are
+ *                       committed to the state (not by a window's drafts)
+ *   out_norm_weight     device [H, dv] fp32, or NULL for no output norm
+ *   out_norm_eps        >= 0
+ */
+typedef struct {
+  int32_t conv_width;
+  const float* conv_weight_q;
+  const float* conv_weight_k;
+  float* conv_state_q;
+  float* conv_state_k;
+  const float* out_norm_weight;
+  float out_norm_eps;
+} kda_fusion_t;
+
+/* kda_decode_step with the options of `fusion`: q and k of each request
+ * pass through the convolution (its state advances by this token) and the
+ * outputs through the output norm.  Other arguments and errors as for
+ * kda_decode_step; state must be 16-byte aligned. */
+kda_status_t kda_decode_step_fused(const kda_desc_t* desc, const kda_fusion_t* fusion,
+                                   const void* q, const void* k, const void* v, const float* z,
+                                   const float* beta, float* state, void* out,
+                                   kda_stream_t stream);
+
+/* kda_decode_replay_window with the options of `fusion`, in one kernel: the
+ * accepted prefix of the previous window (prev_*, raw inputs) is replayed
+ * through convolution, norm, gate and recurrence, and the state and the
+ * convolution states are written once; then the new window's drafts (raw
+ * inputs) run from there, their outputs through the output norm, leaving
+ * both states as the replay left them.  prev_window = 0 skips the replay
+ * (prev_* and accept_len are not read); window = 0 computes no outputs (q ..
+ * beta and out are not read; desc->total_tokens = 0).  Not both 0.
+ * desc->total_tokens = B * window.  An accept_len outside 0 .. prev_window
+ * leaves that request's states alone, gives it no outputs and sets the
+ * device error word. */
+kda_status_t kda_decode_replay_window_fused(
+    const kda_desc_t* desc, const kda_fusion_t* fusion, int32_t prev_window, const void* prev_q,
+    const void* prev_k, const void* prev_v, const float* prev_z, const float* prev_beta,
+    const int32_t* accept_len, int32_t window, const void* q, const void* k, const void* v,
+    const float* z, const float* beta, float* state, void* out, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
  * device memory.  The pages describe no counterpart of this entry point.
  *

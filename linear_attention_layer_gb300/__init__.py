@@ -24,7 +24,8 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "checkpoint_offsets", "decode_window", "decode_replay", "decode_replay_window",
            "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "chunk_fwd_host",
            "chunk_fwd_host_workspace_size", "chunk_fwd_summary",
-           "chunk_fwd_summary_workspace_size", "state_scan", "EXPORTED_SYMBOLS"]
+           "chunk_fwd_summary_workspace_size", "state_scan", "decode_step_fused",
+           "decode_replay_window_fused", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -41,7 +42,8 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_recurrent_bwd", "kda_recurrent_bwd_workspace_size", "kda_short_conv",
                     "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size",
                     "kda_chunk_fwd_summary", "kda_chunk_fwd_summary_workspace_size",
-                    "kda_state_scan")
+                    "kda_state_scan", "kda_decode_step_fused",
+                    "kda_decode_replay_window_fused")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -62,6 +64,13 @@ class KdaDesc(ctypes.Structure):
                 ("a_log", ctypes.c_void_p), ("checkpoints", ctypes.c_void_p),
                 ("checkpoint_offsets", ctypes.c_void_p), ("checkpoint_every", ctypes.c_int32),
                 ("gate_per_head", ctypes.c_int32)]
+
+
+class KdaFusion(ctypes.Structure):
+    _fields_ = [("conv_width", ctypes.c_int32), ("conv_weight_q", ctypes.c_void_p),
+                ("conv_weight_k", ctypes.c_void_p), ("conv_state_q", ctypes.c_void_p),
+                ("conv_state_k", ctypes.c_void_p), ("out_norm_weight", ctypes.c_void_p),
+                ("out_norm_eps", ctypes.c_float)]
 
 
 _lib = None
@@ -104,6 +113,12 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_summary_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_state_scan.restype = ctypes.c_int
         lib.kda_state_scan.argtypes = [dp, ctypes.c_int32] + [vp] * 5
+        fp = ctypes.POINTER(KdaFusion)
+        lib.kda_decode_step_fused.restype = ctypes.c_int
+        lib.kda_decode_step_fused.argtypes = [dp, fp] + [vp] * 8
+        lib.kda_decode_replay_window_fused.restype = ctypes.c_int
+        lib.kda_decode_replay_window_fused.argtypes = (
+            [dp, fp, ctypes.c_int32] + [vp] * 6 + [ctypes.c_int32] + [vp] * 8)
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_testing_inject_wait_timeout.restype = None
@@ -587,6 +602,112 @@ def decode_replay_window(prev, accept_len, q, k, v, z, beta, state, *, out=None,
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_replay_window")
     return out
+
+
+def _fusion(H, dk, dv, B, dev, conv_weight_q, conv_weight_k, conv_state_q, conv_state_k,
+            out_norm_weight, out_norm_eps):
+    """The kda_fusion_t of the fused decode calls (None when nothing is fused)."""
+    f = KdaFusion()
+    if conv_weight_q is not None or conv_weight_k is not None:
+        W = conv_weight_q.shape[-1]
+        _check_tensor("conv_weight_q", conv_weight_q, torch.float32, (H, dk, W), dev)
+        _check_tensor("conv_weight_k", conv_weight_k, torch.float32, (H, dk, W), dev)
+        f.conv_width = W
+        f.conv_weight_q = ctypes.c_void_p(conv_weight_q.data_ptr())
+        f.conv_weight_k = ctypes.c_void_p(conv_weight_k.data_ptr())
+        if W > 1:
+            _check_tensor("conv_state_q", conv_state_q, torch.float32, (B, H, dk, W - 1), dev)
+            _check_tensor("conv_state_k", conv_state_k, torch.float32, (B, H, dk, W - 1), dev)
+            f.conv_state_q = ctypes.c_void_p(conv_state_q.data_ptr())
+            f.conv_state_k = ctypes.c_void_p(conv_state_k.data_ptr())
+    if out_norm_weight is not None:
+        _check_tensor("out_norm_weight", out_norm_weight, torch.float32, (H, dv), dev)
+        f.out_norm_weight = ctypes.c_void_p(out_norm_weight.data_ptr())
+        f.out_norm_eps = float(out_norm_eps)
+    return f
+
+
+def decode_step_fused(q, k, v, z, beta, state, *, conv_weight_q=None, conv_weight_k=None,
+                      conv_state_q=None, conv_state_k=None, out_norm_weight=None,
+                      out_norm_eps=1e-6, out=None, stream=None, a_log=None):
+    """``kda_decode_step_fused``: one decode step with raw q, k through the short
+    convolution + Swish (conv_weight_* [H, dk, W], conv_state_* [N, H, dk, W-1],
+    advanced in place) and the outputs through the per-head RMS norm
+    (out_norm_weight [H, dv]).  Returns out [N, H, dv]; ``state`` is updated."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    _check_tensor("q", q, q.dtype, (N, H, dk), dev)
+    _check_tensor("k", k, q.dtype, (N, H, dk), dev)
+    _check_tensor("v", v, q.dtype, (N, H, dv), dev)
+    per_head = z.dim() == 2
+    _check_tensor("z", z, torch.float32, (N, H) if per_head else (N, H, dk), dev)
+    _check_tensor("beta", beta, torch.float32, (N, H), dev)
+    _check_tensor("state", state, torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    _check_tensor("out", out, q.dtype, (N, H, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    f = _fusion(H, dk, dv, N, dev, conv_weight_q, conv_weight_k, conv_state_q, conv_state_k,
+                out_norm_weight, out_norm_eps)
+    desc, _ = make_desc(N, N, H, dk, dv, _io_code(q.dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_step_fused(ctypes.byref(desc), ctypes.byref(f), _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(z), _ptr(beta), _ptr(state), _ptr(out),
+                                       _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step_fused")
+    return out
+
+
+def decode_replay_window_fused(prev, accept_len, window, state, *, conv_weight_q=None,
+                               conv_weight_k=None, conv_state_q=None, conv_state_k=None,
+                               out_norm_weight=None, out_norm_eps=1e-6, out=None, stream=None,
+                               a_log=None):
+    """``kda_decode_replay_window_fused``: replay the first accept_len[b] raw
+    drafts of ``prev`` = (q, k, v, z, beta) [B, Wp, H, .] into ``state`` and the
+    convolution states (in place), then the outputs [B, W, H, dv] of ``window``
+    = (q, k, v, z, beta) [B, W, H, .] through the output norm.  ``prev`` or
+    ``window`` may be None (no replay / no outputs; returns None then)."""
+    lib = load()
+    ref = window if window is not None else prev
+    if ref is None:
+        raise ValueError("prev and window cannot both be None")
+    B, Wr, H, dk, dv, dev, per_head = _window_args(*ref, state)
+    W = 0
+    if window is not None:
+        W = Wr
+    Wp = 0
+    if prev is not None:
+        Bp, Wp, Hp, dkp, dvp, _, per_head_p = _window_args(*prev, state)
+        if (Bp, Hp, dkp, dvp, per_head_p) != (B, H, dk, dv, per_head) or \
+                prev[0].dtype != ref[0].dtype:
+            raise ValueError("the previous window must match the new one but for its length")
+        _check_tensor("accept_len", accept_len, torch.int32, (B,), dev)
+    if window is not None:
+        if out is None:
+            out = torch.empty((B, W, H, dv), dtype=ref[0].dtype, device=dev)
+        _check_tensor("out", out, ref[0].dtype, (B, W, H, dv), dev)
+    if a_log is not None:
+        _check_tensor("a_log", a_log, torch.float32, (H,), dev)
+    f = _fusion(H, dk, dv, B, dev, conv_weight_q, conv_weight_k, conv_state_q, conv_state_k,
+                out_norm_weight, out_norm_eps)
+    desc, _ = make_desc(B, B * W, H, dk, dv, _io_code(ref[0].dtype), a_log=a_log)
+    desc.gate_per_head = 1 if per_head else 0
+    pq = prev if prev is not None else (None,) * 5
+    wq = window if window is not None else (None,) * 5
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_replay_window_fused(
+            ctypes.byref(desc), ctypes.byref(f), ctypes.c_int32(Wp), *[_ptr(x) for x in pq],
+            _ptr(accept_len) if prev is not None else None, ctypes.c_int32(W),
+            *[_ptr(x) for x in wq], _ptr(state), _ptr(out) if window is not None else None,
+            _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_replay_window_fused")
+    return out if window is not None else None
 
 
 def get_device_error(stream=None) -> int:

@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <initializer_list>
+
 #include "../../include/kda.h"
 #include "kda_launch.h"
 
@@ -274,6 +276,107 @@ kda_status_t kda_decode_replay_window(const kda_desc_t* desc, int32_t prev_windo
   wn.q = q; wn.k = k; wn.v = v; wn.z = z; wn.beta = beta; wn.W = window;
   cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
                                      state, out, err, (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+namespace {
+// Checks of a kda_fusion_t (NULL = nothing fused); fills fa.
+kda_status_t check_fusion(const kda_fusion_t* f, kda::FusionArgs& fa) {
+  fa = kda::FusionArgs{0, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f};
+  if (!f) return KDA_OK;
+  if (f->conv_width < 0) return KDA_ERR_INVALID_ARGUMENT;
+  if (f->conv_width > 4) return KDA_ERR_UNSUPPORTED;
+  if (f->conv_width > 0) {
+    if (!f->conv_weight_q || !f->conv_weight_k) return KDA_ERR_INVALID_ARGUMENT;
+    if (f->conv_width > 1 && (!f->conv_state_q || !f->conv_state_k ||
+                              f->conv_state_q == f->conv_state_k))
+      return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (!(f->out_norm_eps >= 0.f)) return KDA_ERR_INVALID_ARGUMENT;  // also rejects NaN
+  fa.width = f->conv_width;
+  fa.wq = f->conv_weight_q;
+  fa.wk = f->conv_weight_k;
+  fa.sq = f->conv_width > 1 ? f->conv_state_q : nullptr;
+  fa.sk = f->conv_width > 1 ? f->conv_state_k : nullptr;
+  fa.onw = f->out_norm_weight;
+  fa.eps = f->out_norm_eps;
+  return KDA_OK;
+}
+
+bool any_equal(const void* x, std::initializer_list<const void*> ys) {
+  if (!x) return false;
+  for (const void* y : ys)
+    if (x == y) return true;
+  return false;
+}
+}  // namespace
+
+kda_status_t kda_decode_step_fused(const kda_desc_t* desc, const kda_fusion_t* fusion,
+                                   const void* q, const void* k, const void* v, const float* z,
+                                   const float* beta, float* state, void* out,
+                                   kda_stream_t stream) {
+  kda_status_t s = check_desc(desc, true);
+  if (s != KDA_OK) return s;
+  if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  kda::FusionArgs fa;
+  s = check_fusion(fusion, fa);
+  if (s != KDA_OK) return s;
+  if (desc->num_seqs > 0 && (!q || !k || !v || !z || !beta || !state || !out))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (any_equal(out, {q, k, v, state, z, beta, fa.sq, fa.sk}) ||
+      any_equal(fa.sq, {q, k, v, state, z, beta}) || any_equal(fa.sk, {q, k, v, state, z, beta}))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (state && !aligned16(state)) return KDA_ERR_INVALID_ARGUMENT;
+  cudaError_t e = kda::launch_decode_fused(to_problem(desc), q, k, v, z, beta, desc->a_log,
+                                           desc->gate_per_head, state, out, fa,
+                                           (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_replay_window_fused(
+    const kda_desc_t* desc, const kda_fusion_t* fusion, int32_t prev_window, const void* prev_q,
+    const void* prev_k, const void* prev_v, const float* prev_z, const float* prev_beta,
+    const int32_t* accept_len, int32_t window, const void* q, const void* k, const void* v,
+    const float* z, const float* beta, float* state, void* out, kda_stream_t stream) {
+  if (!desc) return KDA_ERR_INVALID_ARGUMENT;
+  kda_desc_t d = *desc;
+  d.cu_seqlens_host = nullptr;  // not used by the window calls
+  if (d.gate_per_head != 0 && d.gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status_t s = check_desc(&d, false);
+  if (s != KDA_OK) return s;
+  if (prev_window < 0 || window < 0 || (prev_window == 0 && window == 0))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)desc->num_seqs * window != desc->total_tokens) return KDA_ERR_INVALID_ARGUMENT;
+  kda::FusionArgs fa;
+  s = check_fusion(fusion, fa);
+  if (s != KDA_OK) return s;
+  const int B = desc->num_seqs;
+  if (B > 0) {
+    if (!state) return KDA_ERR_INVALID_ARGUMENT;
+    if (prev_window > 0 &&
+        (!prev_q || !prev_k || !prev_v || !prev_z || !prev_beta || !accept_len))
+      return KDA_ERR_INVALID_ARGUMENT;
+    if (window > 0 && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (state && !aligned16(state)) return KDA_ERR_INVALID_ARGUMENT;
+  const std::initializer_list<const void*> ins = {q, k, v, z, beta, prev_q, prev_k,
+                                                  prev_v, prev_z, prev_beta, state};
+  if ((window > 0 && any_equal(out, ins)) || any_equal(fa.sq, ins) || any_equal(fa.sk, ins) ||
+      (window > 0 && out && (out == fa.sq || out == fa.sk)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  int* err = device_error_word();
+  if (!err) return KDA_ERR_CUDA;
+  kda::WinInputs rp, wn;
+  if (prev_window > 0) {
+    rp.q = prev_q; rp.k = prev_k; rp.v = prev_v; rp.z = prev_z; rp.beta = prev_beta;
+    rp.W = prev_window; rp.accept = accept_len;
+  }
+  if (window > 0) {
+    wn.q = q; wn.k = k; wn.v = v; wn.z = z; wn.beta = beta; wn.W = window;
+  }
+  cudaError_t e = kda::launch_window(to_problem(desc), rp, wn, desc->a_log, desc->gate_per_head,
+                                     state, window > 0 ? out : nullptr, err,
+                                     (cudaStream_t)stream, &fa);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

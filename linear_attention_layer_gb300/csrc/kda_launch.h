@@ -87,9 +87,24 @@ struct WinInputs {
   int W = 0;
   const int32_t* accept = nullptr;
 };
+// Optional fused pre- and post-processing of the decode-side calls
+// (kda_fusion_t): width 0 = no convolution, onw null = no output norm.
+struct FusionArgs {
+  int width;
+  const float* wq;
+  const float* wk;
+  float* sq;
+  float* sk;
+  const float* onw;
+  float eps;
+};
 cudaError_t launch_window(const Problem& p, const WinInputs& rp, const WinInputs& wn,
                           const float* a_log, int gate_per_head, float* state, void* out,
-                          int* err, cudaStream_t stream);
+                          int* err, cudaStream_t stream, const FusionArgs* fusion = nullptr);
+cudaError_t launch_decode_fused(const Problem& p, const void* q, const void* k, const void* v,
+                                const float* z, const float* beta, const float* a_log,
+                                int gate_per_head, float* state, void* out,
+                                const FusionArgs& fusion, cudaStream_t stream);
 
 // Token-by-token prefill over a packed batch.
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);

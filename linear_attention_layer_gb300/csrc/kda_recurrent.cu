@@ -39,19 +39,86 @@ struct RecSmem {
   float vs[DV], es[DV];
   float red[2][RecShape<DK, DV>::RG][DV];
   float part[3][kNT / 32];
+  float onorm[kNT / 32];  // per-warp sums of o^2 (output norm)
 };
+
+// Optional pre- and post-processing fused into the decode-side kernels
+// (kda_fusion_t): the short causal convolution + Swish of q and k before their
+// L2 norm, and a per-head RMS norm of the outputs.
+struct Fusion {
+  int W;                 // convolution width, 0 = none
+  const float* wq;       // [H, DK, W] taps (tap j multiplies x[t - (W-1) + j])
+  const float* wk;
+  float* sq;             // [B, H, DK, W-1] last W-1 raw inputs, oldest first
+  float* sk;
+  const float* onw;      // [H, DV] output-norm weight, or null
+  float eps;
+};
+
+// The convolution of one channel (thread tid < DK) of q and of k: its taps
+// and its last three raw inputs, right-aligned so that any width 1..4 is the
+// same four-tap sum (unused taps are zero):
+//   u = t[0] h[0] + t[1] h[1] + t[2] h[2] + t[3] x,   y = u sigmoid(u).
+struct ConvRegs {
+  float hq[3], hk[3], tq[4], tk[4];
+};
+
+__device__ __forceinline__ float swish(float u) { return u / (1.f + __expf(-u)); }
+
+__device__ __forceinline__ float conv_step(float (&h)[3], const float (&t)[4], float x) {
+  const float u = fmaf(t[0], h[0], fmaf(t[1], h[1], fmaf(t[2], h[2], t[3] * x)));
+  h[0] = h[1];
+  h[1] = h[2];
+  h[2] = x;
+  return swish(u);
+}
+
+// Load channel c's taps and history of (unit = b * H + h).
+template <int DK>
+__device__ __forceinline__ void conv_load(ConvRegs& cr, const Fusion& f, size_t unit, int h,
+                                          int c) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int tj = j - (4 - f.W);  // tap index, < 0 for unused slots
+    cr.tq[j] = tj >= 0 ? __ldg(f.wq + ((size_t)h * DK + c) * f.W + tj) : 0.f;
+    cr.tk[j] = tj >= 0 ? __ldg(f.wk + ((size_t)h * DK + c) * f.W + tj) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int sj = j - (4 - f.W);  // history index (W-1 kept), < 0 for unused slots
+    cr.hq[j] = sj >= 0 ? f.sq[(unit * DK + c) * (f.W - 1) + sj] : 0.f;
+    cr.hk[j] = sj >= 0 ? f.sk[(unit * DK + c) * (f.W - 1) + sj] : 0.f;
+  }
+}
+
+template <int DK>
+__device__ __forceinline__ void conv_store(const ConvRegs& cr, const Fusion& f, size_t unit, int c) {
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int sj = j - (4 - f.W);
+    if (sj >= 0) {
+      f.sq[(unit * DK + c) * (f.W - 1) + sj] = cr.hq[j];
+      f.sk[(unit * DK + c) * (f.W - 1) + sj] = cr.hk[j];
+    }
+  }
+}
 
 // Stage one token's q, k, alpha = exp(g), v into shared memory and the
 // partial sums |q|^2, |k|^2, q.k per warp.
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, bool CONV = false>
 __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, const T* kp,
                                             const T* vp, const float* zp, float zscale,
-                                            bool zhead) {
+                                            bool zhead, ConvRegs* cr = nullptr,
+                                            bool conv_on = false) {
   const int tid = threadIdx.x;
   float qq = 0.f, kk = 0.f, kq = 0.f;
   if (tid < DK) {
-    const float a = IO<T>::ld(qp + tid);
-    const float b = IO<T>::ld(kp + tid);
+    float a = IO<T>::ld(qp + tid);
+    float b = IO<T>::ld(kp + tid);
+    if (CONV && conv_on) {  // raw inputs through this channel's convolution + Swish
+      a = conv_step(cr->hq, cr->tq, a);
+      b = conv_step(cr->hk, cr->tk, b);
+    }
     sm.qs[tid] = a;
     sm.ks[tid] = b;
     sm.as[tid] = __expf(log_decay(zscale * __ldg(zp + (zhead ? 0 : tid))));
@@ -74,9 +141,10 @@ __device__ __forceinline__ void stage_token(RecSmem<DK, DV>& sm, const T* qp, co
 
 // Apply one token to the register-resident state s.  Requires stage_token
 // followed by __syncthreads().  Writes o_t (when op != nullptr).
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, bool ONORM = false>
 __device__ __forceinline__ void apply_token(RecSmem<DK, DV>& sm, float4 (&s)[RecShape<DK, DV>::R],
-                                            float b, T* op) {
+                                            float b, T* op, const float* onw = nullptr,
+                                            float eps = 0.f) {
   using SH = RecShape<DK, DV>;
   const int tid = threadIdx.x;
   const int c4 = tid % SH::TPR, rg = tid / SH::TPR;
@@ -101,6 +169,7 @@ __device__ __forceinline__ void apply_token(RecSmem<DK, DV>& sm, float4 (&s)[Rec
   reinterpret_cast<float4*>(sm.red[0][rg])[c4] = pk;
   reinterpret_cast<float4*>(sm.red[1][rg])[c4] = pq;
   __syncthreads();
+  float o = 0.f;
   if (tid < DV) {
     float sk = 0.f, sq = 0.f;
 #pragma unroll
@@ -109,10 +178,21 @@ __device__ __forceinline__ void apply_token(RecSmem<DK, DV>& sm, float4 (&s)[Rec
       sq += sm.red[1][g][tid];
     }
     const float e = sm.vs[tid] - sk;
-    if (op) IO<T>::st(op + tid, sq + b * (kq * rk * rq) * e);
+    o = sq + b * (kq * rk * rq) * e;
+    if (op && !ONORM) IO<T>::st(op + tid, o);
     sm.es[tid] = b * e;
   }
+  if (ONORM && op && tid < DV) {  // per-warp sums of o^2 over the value channels
+    const float o2 = warp_sum(o * o);
+    if ((tid & 31) == 0) sm.onorm[tid >> 5] = o2;
+  }
   __syncthreads();
+  if (ONORM && op && tid < DV) {  // o / sqrt(mean(o^2) + eps) * weight
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < DV / 32; ++w) ss += sm.onorm[w];
+    IO<T>::st(op + tid, o * rsqrtf(ss * (1.f / DV) + eps) * __ldg(onw + tid));
+  }
   const float4 e4 = reinterpret_cast<const float4*>(sm.es)[c4];
 #pragma unroll
   for (int i = 0; i < SH::R; ++i) {
@@ -143,6 +223,41 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
 }
 
+// decode_kernel with the fused pre- and post-processing of kda_fusion_t:
+// q and k through the short convolution (whose state advances by this
+// token), the outputs through the per-head RMS norm.
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kNT, 2)
+decode_fused_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    const float* __restrict__ z, const float* __restrict__ beta,
+                    const float* __restrict__ a_log, int H, int zhead, float* __restrict__ state,
+                    T* __restrict__ out, const Fusion f) {
+  using SH = RecShape<DK, DV>;
+  __shared__ __align__(16) RecSmem<DK, DV> sm;
+  const size_t unit = blockIdx.x;  // n * H + h
+  const int h = (int)(unit % H);
+  const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
+  float4* S = reinterpret_cast<float4*>(state + unit * DK * DV);
+  float4 s[SH::R];
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
+  const bool conv = f.W > 0;
+  ConvRegs cr;
+  if (conv && threadIdx.x < DK) conv_load<DK>(cr, f, unit, h, threadIdx.x);
+  stage_token<DK, DV, T, true>(sm, q + unit * DK, k + unit * DK, v + unit * DV,
+                               z + unit * (zhead ? 1 : DK), gate_scale(a_log, h), zhead, &cr,
+                               conv);
+  __syncthreads();
+  if (f.onw)
+    apply_token<DK, DV, T, true>(sm, s, __ldg(beta + unit), out + unit * DV,
+                                 f.onw + (size_t)h * DV, f.eps);
+  else
+    apply_token<DK, DV, T>(sm, s, __ldg(beta + unit), out + unit * DV);
+#pragma unroll
+  for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
+  if (conv && threadIdx.x < DK) conv_store<DK>(cr, f, unit, threadIdx.x);
+}
+
 // Speculative decoding.  One CTA per (request, head).  A window's draft
 // tokens of request b are rows [b*W, b*W + W) of its [B*W, H, .] inputs.
 // With a replay part (rp.accept != null): the first accept[b] tokens of the
@@ -162,10 +277,10 @@ struct WinPart {
   const int32_t* accept;  // replay part only
 };
 
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, bool FUSED = false>
 __global__ void __launch_bounds__(kNT, 2)
 window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int H, int zhead,
-              float* __restrict__ state, T* __restrict__ out, int* err) {
+              float* __restrict__ state, T* __restrict__ out, int* err, const Fusion f) {
   using SH = RecShape<DK, DV>;
   __shared__ __align__(16) RecSmem<DK, DV> sm;
   const size_t unit = blockIdx.x;  // b * H + h
@@ -186,25 +301,37 @@ window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int
   for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
   const float zscale = gate_scale(a_log, h);
   const int zs = zhead ? 1 : DK;
+  // (fused) the convolution history of this thread's channel; the replayed
+  // tokens advance it and it is stored with the state, the window's drafts
+  // advance only this copy
+  const bool conv = FUSED && f.W > 0;
+  ConvRegs cr;
+  if (conv && threadIdx.x < DK) conv_load<DK>(cr, f, unit, h, threadIdx.x);
   for (int t = 0; t < nrep; ++t) {
     const size_t th = ((size_t)b * rp.W + t) * H + h;
     __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T>(sm, rp.q + th * DK, rp.k + th * DK, rp.v + th * DV, rp.z + th * zs,
-                           zscale, zhead);
+    stage_token<DK, DV, T, FUSED>(sm, rp.q + th * DK, rp.k + th * DK, rp.v + th * DV,
+                                  rp.z + th * zs, zscale, zhead, &cr, conv);
     __syncthreads();
     apply_token<DK, DV, T>(sm, s, __ldg(rp.beta + th), nullptr);
   }
   if (nrep > 0) {
 #pragma unroll
     for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
+    if (conv && threadIdx.x < DK) conv_store<DK>(cr, f, unit, threadIdx.x);
   }
+  const bool onorm = FUSED && f.onw != nullptr;
   for (int t = 0; t < wn.W; ++t) {
     const size_t th = ((size_t)b * wn.W + t) * H + h;
     __syncthreads();
-    stage_token<DK, DV, T>(sm, wn.q + th * DK, wn.k + th * DK, wn.v + th * DV, wn.z + th * zs,
-                           zscale, zhead);
+    stage_token<DK, DV, T, FUSED>(sm, wn.q + th * DK, wn.k + th * DK, wn.v + th * DV,
+                                  wn.z + th * zs, zscale, zhead, &cr, conv);
     __syncthreads();
-    apply_token<DK, DV, T>(sm, s, __ldg(wn.beta + th), out + th * DV);
+    if (onorm)
+      apply_token<DK, DV, T, FUSED>(sm, s, __ldg(wn.beta + th), out + th * DV,
+                                    f.onw + (size_t)h * DV, f.eps);
+    else
+      apply_token<DK, DV, T>(sm, s, __ldg(wn.beta + th), out + th * DV);
   }
 }
 
@@ -263,15 +390,32 @@ cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, cons
 }
 
 template <int DK, int DV, typename T>
+cudaError_t decode_fused_dispatch(const Problem& p, const void* q, const void* k, const void* v,
+                                  const float* z, const float* beta, const float* a_log,
+                                  int zhead, float* state, void* out, const Fusion& f,
+                                  cudaStream_t st) {
+  const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  decode_fused_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(
+      (const T*)q, (const T*)k, (const T*)v, z, beta, a_log, p.num_heads, zhead, state, (T*)out,
+      f);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename T>
 cudaError_t window_dispatch(const Problem& p, const WinInputs& rp, const WinInputs& wn,
                             const float* a_log, int zhead, float* state, void* out, int* err,
-                            cudaStream_t st) {
+                            const Fusion* f, cudaStream_t st) {
   auto part = [](const WinInputs& x) {
     return WinPart<T>{(const T*)x.q, (const T*)x.k, (const T*)x.v, x.z, x.beta, x.W, x.accept};
   };
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
-  window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(part(rp), part(wn), a_log, p.num_heads, zhead,
-                                                   state, (T*)out, err);
+  if (f)
+    window_kernel<DK, DV, T, true><<<blocks, kNT, 0, st>>>(part(rp), part(wn), a_log,
+                                                           p.num_heads, zhead, state, (T*)out,
+                                                           err, *f);
+  else
+    window_kernel<DK, DV, T><<<blocks, kNT, 0, st>>>(part(rp), part(wn), a_log, p.num_heads,
+                                                     zhead, state, (T*)out, err, Fusion{});
   return cudaGetLastError();
 }
 
@@ -317,13 +461,29 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
 
 cudaError_t launch_window(const Problem& p, const WinInputs& rp, const WinInputs& wn,
                           const float* a_log, int zhead, float* state, void* out, int* err,
-                          cudaStream_t st) {
+                          cudaStream_t st, const FusionArgs* fa) {
   if (p.num_seqs == 0 || (!rp.accept && wn.W == 0)) return cudaSuccess;
+  Fusion f{};
+  if (fa) f = Fusion{fa->width, fa->wq, fa->wk, fa->sq, fa->sk, fa->onw, fa->eps};
+  const Fusion* fp = fa ? &f : nullptr;
   return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
     return p.io_bf16 ? window_dispatch<DK, DV, __nv_bfloat16>(p, rp, wn, a_log, zhead, state, out,
-                                                              err, st)
+                                                              err, fp, st)
                      : window_dispatch<DK, DV, float>(p, rp, wn, a_log, zhead, state, out, err,
-                                                      st);
+                                                      fp, st);
+  });
+}
+
+cudaError_t launch_decode_fused(const Problem& p, const void* q, const void* k, const void* v,
+                                const float* z, const float* beta, const float* a_log, int zhead,
+                                float* state, void* out, const FusionArgs& fa, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  const Fusion f{fa.width, fa.wq, fa.wk, fa.sq, fa.sk, fa.onw, fa.eps};
+  return KDA_SIZE_SWITCH(p.dk, p.dv, [&] {
+    return p.io_bf16 ? decode_fused_dispatch<DK, DV, __nv_bfloat16>(p, q, k, v, z, beta, a_log,
+                                                                    zhead, state, out, f, st)
+                     : decode_fused_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, zhead,
+                                                            state, out, f, st);
   });
 }
 

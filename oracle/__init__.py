@@ -245,3 +245,4 @@ def state_scan(transitions, offsets, initial_state=None, count=None):
     for i in range(count):
         state = np.matmul(m[i], state) + s[i]
     return state
+from .output_norm import rms_norm  # noqa: E402,F401
