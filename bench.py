@@ -500,6 +500,53 @@ def bench_short_conv(kda, p, steps, warmup, device, width=4, clk=None):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs]
 
 
+def bench_spec_decode_fused(kda, B, H, W, steps, device, seed=0, clk=None, width=4):
+    """The speculative-decoding step with the short convolution of raw q, k
+    (width 4, states advanced by the replay) and the per-head RMS output norm
+    fused in: one kda_decode_replay_window_fused call per step.
+    Returns (ms per step, accepted tokens per step)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 1)
+    f32 = dict(dtype=torch.float32, device=device, generator=g)
+    q = torch.randn((B, W, H, 128), **f32).to(torch.bfloat16)
+    k = torch.randn((B, W, H, 128), **f32).to(torch.bfloat16)
+    v = torch.randn((B, W, H, 128), **f32).to(torch.bfloat16)
+    z = torch.randn((B, W, H, 128), **f32)
+    beta = torch.sigmoid(torch.randn((B, W, H), **f32))
+    state = torch.randn((B, H, 128, 128), **f32) * 0.1
+    fz = dict(conv_weight_q=torch.randn((H, 128, width), **f32) * 0.5,
+              conv_weight_k=torch.randn((H, 128, width), **f32) * 0.5,
+              conv_state_q=torch.randn((B, H, 128, width - 1), **f32),
+              conv_state_k=torch.randn((B, H, 128, width - 1), **f32),
+              out_norm_weight=torch.ones((H, 128), **f32), out_norm_eps=1e-6)
+    out = torch.empty((B, W, H, 128), dtype=torch.bfloat16, device=device)
+    acc = torch.randint(0, W + 1, (steps + 3, B), generator=g, device=device, dtype=torch.int32)
+    stream = torch.cuda.current_stream()
+    win = (q, k, v, z, beta)
+
+    def step(i):
+        kda.decode_replay_window_fused(win, acc[i], win, state, out=out, **fz)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
+    a.record(stream)
+    for i in range(steps):
+        step(3 + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
+    if kda.get_device_error() != 0:
+        raise RuntimeError("device error word set after the fused speculative-decoding steps")
+    return a.elapsed_time(b) / steps, float(acc[3:].sum().item()) / steps
+
+
 def bench_spec_decode(kda, B, H, W, steps, device, seed=0, clk=None):
     """Speculative decoding: per step one kda_decode_replay_window call -- the
     replay of the previous window's accepted prefix and the outputs of the
@@ -884,6 +931,27 @@ def main():
                          "unit": "GB/s", "frac": round(s_gbs / hbm_peak, 4),
                          "algorithmic_bytes_per_step": s_bytes},
             "clocks": sclk.summary(), "gpu_launches": ns}
+
+    # ---- the same step with the short convolution and the output norm fused in ----
+    if "spec" not in skip:
+        Bs, Hs, Ws, ns = 256, 32, 4, 200
+        fclk = clock_sampler(gpu_uuid)
+        f_ms, f_acc = bench_spec_decode_fused(kda, Bs, Hs, Ws, ns, device, seed=rank, clk=fclk)
+        tok_in = 3 * 256 + 512 + 4
+        conv_state = 2 * 128 * 3 * 4  # q and k convolution states of one (request, head)
+        f_bytes = int(Bs * Hs * (2 * STATE_BYTES + 2 * conv_state + Ws * (tok_in + 256)) +
+                      f_acc * Hs * tok_in)
+        f_gbs = f_bytes / (f_ms * 1e-3) / 1e9
+        line["spec_decode_fused"] = {
+            "value": round(f_acc * Hs / (f_ms * 1e-3) / 1e6, 3),
+            "unit": "M accepted head-tokens/s", "ms_per_step": round(f_ms, 5), "window": Ws,
+            "accepted_tokens_per_step": f_acc, "kernel": "kda_decode_replay_window_fused",
+            "fused": "short convolution (width 4) of raw q, k + per-head RMS output norm",
+            "workload": f"{Bs} requests x H={Hs}, dk=dv=128, window {Ws}, acceptance U{{0..{Ws}}}",
+            "roofline": {"bound": "hbm", "achieved": round(f_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(f_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_step": f_bytes},
+            "clocks": fclk.summary(), "gpu_launches": ns}
 
     # ---- end to end through host buffers ----
     if "e2e" not in skip:
