@@ -321,6 +321,35 @@ kda_status_t kda_decode_replay_window_fused(
     const float* z, const float* beta, float* state, void* out, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_fused -- kda_chunk_fwd over RAW q and k: the short
+ * convolution + Swish of `fusion` (the Q/K preprocessing of mhpq.cn/news/56770,
+ * section "KDA 到底在算什么", read as in kda_short_conv) runs inside the prefill
+ * kernel on the q and k tiles it has loaded, before their L2 norm, so the
+ * convolved q and k are never written to or read back from device memory.
+ * Each sequence's convolution states (conv_state_q / _k, [N, H, dk, W-1])
+ * are read as the raw inputs before its first token and, once every kernel
+ * of the call has read them, overwritten with its last W-1 raw inputs (in
+ * place; a sequence shorter than W-1 keeps the tail of its old state).
+ *
+ *   fusion             NULL or conv_width 0: exactly kda_chunk_fwd.
+ *                      conv_width 1..4 needs the tensor-core path (bf16 io,
+ *                      dk = dv = 128), else KDA_ERR_UNSUPPORTED; conv_state_*
+ *                      are required when W > 1 and must not alias any other
+ *                      buffer of the call.  out_norm_weight must be NULL
+ *                      (KDA_ERR_UNSUPPORTED): the output norm belongs to the
+ *                      decode-side calls.
+ * Other arguments, options (workspace split, checkpoints, a_log,
+ * gate_per_head) and errors as for kda_chunk_fwd.  The convolution's Swish
+ * uses the hardware tanh (sigmoid(u) = (1 + tanh(u/2)) / 2); its outputs are
+ * rounded to bf16 like the outputs of kda_short_conv.
+ */
+kda_status_t kda_chunk_fwd_fused(const kda_desc_t* desc, const kda_fusion_t* fusion,
+                                 const void* q, const void* k, const void* v, const float* z,
+                                 const float* beta, const float* initial_state,
+                                 const int32_t* cu_seqlens, void* out, float* final_state,
+                                 kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd for callers that cannot allocate
  * device memory.  The pages describe no counterpart of this entry point.
  *

@@ -25,7 +25,7 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "chunk_fwd_host",
            "chunk_fwd_host_workspace_size", "chunk_fwd_summary",
            "chunk_fwd_summary_workspace_size", "state_scan", "decode_step_fused",
-           "decode_replay_window_fused", "EXPORTED_SYMBOLS"]
+           "decode_replay_window_fused", "chunk_fwd_fused", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size",
                     "kda_chunk_fwd_summary", "kda_chunk_fwd_summary_workspace_size",
                     "kda_state_scan", "kda_decode_step_fused",
-                    "kda_decode_replay_window_fused")
+                    "kda_decode_replay_window_fused", "kda_chunk_fwd_fused")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -116,6 +116,8 @@ def load() -> ctypes.CDLL:
         fp = ctypes.POINTER(KdaFusion)
         lib.kda_decode_step_fused.restype = ctypes.c_int
         lib.kda_decode_step_fused.argtypes = [dp, fp] + [vp] * 8
+        lib.kda_chunk_fwd_fused.restype = ctypes.c_int
+        lib.kda_chunk_fwd_fused.argtypes = [dp, fp] + [vp] * 10
         lib.kda_decode_replay_window_fused.restype = ctypes.c_int
         lib.kda_decode_replay_window_fused.argtypes = (
             [dp, fp, ctypes.c_int32] + [vp] * 6 + [ctypes.c_int32] + [vp] * 8)
@@ -209,7 +211,7 @@ def checkpoint_offsets(cu_seqlens_host, every):
 
 def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state,
              output_final_state, cu_seqlens_host, workspace, stream, a_log=None,
-             checkpoint_every=0, checkpoints=None):
+             checkpoint_every=0, checkpoints=None, fusion=None):
     lib = load()
     if q.dim() != 3:
         raise ValueError("q must be [T_tot, H, dk]")
@@ -250,8 +252,9 @@ def _prefill(name, q, k, v, z, beta, cu_seqlens, initial_state, out, final_state
         desc.checkpoints = ctypes.c_void_p(checkpoints.data_ptr()) if offs[-1] else \
             ctypes.c_void_p(offs_dev.data_ptr())  # any valid pointer when there are none
         desc.checkpoint_offsets = ctypes.c_void_p(offs_dev.data_ptr())
+    pre = (ctypes.byref(desc),) if fusion is None else (ctypes.byref(desc), ctypes.byref(fusion))
     with torch.cuda.device(dev):
-        st = getattr(lib, name)(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+        st = getattr(lib, name)(*pre, _ptr(q), _ptr(k), _ptr(v), _ptr(z),
                                 _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
                                 _ptr(final_state), _stream_handle(stream))
     del keep
@@ -290,6 +293,33 @@ def chunk_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None, fin
     return _prefill("kda_chunk_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
                     final_state, output_final_state, cu_seqlens_host, workspace, stream, a_log,
                     checkpoint_every, checkpoints)
+
+
+def chunk_fwd_fused(q, k, v, z, beta, cu_seqlens, initial_state=None, *, conv_weight_q,
+                    conv_weight_k, conv_state_q=None, conv_state_k=None, out=None,
+                    final_state=None, output_final_state=True, cu_seqlens_host=None,
+                    workspace=None, stream=None, a_log=None, checkpoint_every=0,
+                    checkpoints=None):
+    """``kda_chunk_fwd_fused``: the chunked prefill over RAW q, k, with the short
+    convolution + Swish (conv_weight_* [H, dk, W]) fused into the kernel.
+    conv_state_* [N, H, dk, W-1] (required for W > 1) are read as each
+    sequence's inputs before its start and overwritten with its last W-1 raw
+    inputs.  Other arguments and the return value as ``chunk_fwd``."""
+    T, H, dk = q.shape
+    N = cu_seqlens.numel() - 1
+    f = _fusion(H, dk, v.shape[-1], N, q.device, conv_weight_q, conv_weight_k, conv_state_q,
+                conv_state_k, None, 0.0)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be a tensor, 'auto' or None")
+        workspace = None
+        if cu_seqlens_host is not None:
+            nbytes = chunk_fwd_workspace_size(N, T, H, dk, v.shape[-1], q.dtype, cu_seqlens_host)
+            if nbytes:
+                workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    return _prefill("kda_chunk_fwd_fused", q, k, v, z, beta, cu_seqlens, initial_state, out,
+                    final_state, output_final_state, cu_seqlens_host, workspace, stream, a_log,
+                    checkpoint_every, checkpoints, fusion=f)
 
 
 def recurrent_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,

@@ -380,6 +380,56 @@ kda_status_t kda_decode_replay_window_fused(
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_chunk_fwd_fused(const kda_desc_t* desc, const kda_fusion_t* fusion,
+                                 const void* q, const void* k, const void* v, const float* z,
+                                 const float* beta, const float* initial_state,
+                                 const int32_t* cu_seqlens, void* out, float* final_state,
+                                 kda_stream_t stream) {
+  kda::Args a;
+  kda_status_t s = prefill_common(desc, q, k, v, z, beta, initial_state, cu_seqlens, out,
+                                  final_state, a);
+  if (s != KDA_OK) return s;
+  kda::FusionArgs fa;
+  s = check_fusion(fusion, fa);
+  if (s != KDA_OK) return s;
+  if (fa.onw) return KDA_ERR_UNSUPPORTED;  // the output norm belongs to the decode side
+  const kda::Problem p = to_problem(desc);
+  const bool tc = kda::chunk_tc_supported(p, a);
+  if (fa.width > 0) {
+    if (!tc) return KDA_ERR_UNSUPPORTED;
+    const std::initializer_list<const void*> bufs = {q, k, v, z, beta, out, initial_state,
+                                                     final_state, cu_seqlens};
+    if (any_equal(fa.sq, bufs) || any_equal(fa.sk, bufs)) return KDA_ERR_INVALID_ARGUMENT;
+    a.conv_w = fa.width;
+    a.conv_wq = fa.wq;
+    a.conv_wk = fa.wk;
+    a.conv_sq = fa.sq;
+    a.conv_sk = fa.sk;
+  }
+  cudaError_t e = tc ? kda::launch_chunk_tc(p, a, desc->cu_seqlens_host, desc->workspace,
+                                            desc->workspace_bytes, (cudaStream_t)stream)
+                     : kda::launch_chunk_simt(p, a, (cudaStream_t)stream);
+  if (e == cudaSuccess && fa.width > 1) {
+    // each sequence's last W-1 raw inputs, once every reader of the incoming
+    // states is done (so the states may be updated in place)
+    kda::ConvArgs c{};
+    c.cu_seqlens = cu_seqlens;
+    c.width = fa.width;
+    c.err = a.err;
+    c.x = q;
+    c.state_in = fa.sq;
+    c.state_out = fa.sq;
+    e = kda::launch_short_conv_state(p, c, (cudaStream_t)stream);
+    if (e == cudaSuccess) {
+      c.x = k;
+      c.state_in = fa.sk;
+      c.state_out = fa.sk;
+      e = kda::launch_short_conv_state(p, c, (cudaStream_t)stream);
+    }
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* bytes) {
   if (!bytes || !desc) return KDA_ERR_INVALID_ARGUMENT;
   kda_status_t s = check_desc(desc, false);

@@ -106,7 +106,10 @@ constexpr uint32_t OFF_MISC = 212992;
 constexpr int M_BETA = 0, M_RQK = 64, M_DECAY = 192, M_TOT = 320,
               M_END = 320 + 4 * 128;
 constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
+// (fused convolution) the last three raw inputs before the chunk, fp32
+// [q, k][3 tokens, oldest first][128 channels]
+constexpr uint32_t OFF_HALO = OFF_BAR + 64;
+constexpr uint32_t SMEM_BYTES = OFF_HALO + 2 * 3 * 128 * 4 + 1024;  // + alignment slack
 
 // ---- Tensor Memory columns (all 128 lanes) ----
 constexpr uint32_t TS32 = 0;    // S^T fp32   [n][c]   128 cols
@@ -148,6 +151,16 @@ struct Params {
   float* aux_state;     // [N][H][dk][dk]: output slot kSlotAux (mode 1)
   float* ws;            // state slots [slot][H][dk][dv] (mode 1)
   int* err;
+  // fused Q/K convolution (kernel variant kConv): taps [H][128][W], incoming
+  // states [N][H][128][W-1] (null: zeros), and the raw q, k from which a
+  // segment that starts inside its sequence takes its first halo
+  const float* conv_wq;
+  const float* conv_wk;
+  const float* conv_sq;
+  const float* conv_sk;
+  const __nv_bfloat16* qraw;
+  const __nv_bfloat16* kraw;
+  int conv_w;
   int H, total, num_seqs, num_units, use_order, mode;
   long long spin_cycles;
   int inject_timeout;   // testing: make the first input wait of each unit unsatisfiable
@@ -307,8 +320,66 @@ __device__ __forceinline__ void prep_state(uint32_t my_lane, const float* dec, i
   tmem_st_wait();
 }
 
+// The fused short convolution + Swish of the chunk's raw q and k tiles (in
+// the input stages, 128-byte swizzled bf16), in place, before the token norms.
+// Warp w takes tensor w % 2 (q, k), 64-channel block (w / 2) % 2 and tokens
+// 16 (w / 4) .. + 15; lane l the channel pair 2l, 2l + 1 of the block.  The
+// three raw inputs before the chunk come from the halo area, which quarter 3
+// refills with the chunk's last three raw inputs for the next chunk.  All
+// threads take part (two block barriers).  Taps are right-aligned: width W
+// uses the last W of four (the others zero).
+__device__ __forceinline__ void conv_tiles(unsigned char* sm, const Params& P, int h, int warp,
+                                           int lane) {
+  const int tens = warp & 1, blk = (warp >> 1) & 1, qt = warp >> 2;
+  const int c0 = 64 * blk + 2 * lane;
+  unsigned char* tile = sm + (tens ? OFF_K : OFF_Q) + blk * 8192;
+  float* halo = reinterpret_cast<float*>(sm + OFF_HALO) + tens * 384;
+  const float* wsrc = (tens ? P.conv_wk : P.conv_wq) + ((size_t)h * kD + c0) * P.conv_w;
+  float ta[4], tb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int tj = j - (4 - P.conv_w);
+    ta[j] = tj >= 0 ? __ldg(wsrc + tj) : 0.f;
+    tb[j] = tj >= 0 ? __ldg(wsrc + P.conv_w + tj) : 0.f;
+  }
+  const uint32_t xo = (((uint32_t)lane & 3) << 2);
+  auto word = [&](int t) -> uint32_t* {
+    return reinterpret_cast<uint32_t*>(tile + t * 128 + (((((uint32_t)lane >> 2)) ^ (uint32_t)(t & 7)) << 4) + xo);
+  };
+  float xa[19], xb[19];  // raw inputs of tokens 16 qt - 3 .. 16 qt + 15
+#pragma unroll
+  for (int j = 0; j < 19; ++j) {
+    const int t = 16 * qt - 3 + j;
+    if (j < 3 && qt == 0) {
+      xa[j] = halo[j * 128 + c0];
+      xb[j] = halo[j * 128 + c0 + 1];
+    } else {
+      const uint32_t w = *word(t);
+      xa[j] = bf16_lo(w);
+      xb[j] = bf16_hi(w);
+    }
+  }
+  __syncthreads();  // every raw input is read before any is overwritten
+  if (qt == 3) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      halo[j * 128 + c0] = xa[16 + j];
+      halo[j * 128 + c0 + 1] = xb[16 + j];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float ua = fmaf(ta[0], xa[i], fmaf(ta[1], xa[i + 1], fmaf(ta[2], xa[i + 2], ta[3] * xa[i + 3])));
+    const float ub = fmaf(tb[0], xb[i], fmaf(tb[1], xb[i + 1], fmaf(tb[2], xb[i + 2], tb[3] * xb[i + 3])));
+    const __nv_bfloat162 y = __floats2bfloat162_rn(swish_tanh(ua), swish_tanh(ub));
+    *word(16 * qt + i) = *reinterpret_cast<const uint32_t*>(&y);
+  }
+  __syncthreads();  // the converted tiles are complete
+}
+
 // kZHead: one gate logit per (token, head) (P.zh) instead of z tiles per channel.
-template <bool kZHead>
+// kConv: q and k pass the fused short convolution + Swish first.
+template <bool kZHead, bool kConv>
 __global__ void __launch_bounds__(kNT, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -421,6 +492,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tmem_st_wait();
     }
+    if (kConv && tid < 256) {
+      // the halo before the unit's first chunk: raw inputs bos-3 .. bos-1 of the
+      // sequence where they exist (a segment starting inside it), else its
+      // incoming convolution state (last W-1 inputs before it), else zeros
+      const int tens = tid >> 7, c = tid & 127;
+      const __nv_bfloat16* raw = tens ? P.kraw : P.qraw;
+      const float* cst = tens ? P.conv_sk : P.conv_sq;
+      float* halo = reinterpret_cast<float*>(sm + OFF_HALO) + tens * 384;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int pos = bos - 3 + j;
+        float x = 0.f;
+        if (pos >= sbeg) {
+          x = __bfloat162float(raw[((size_t)pos * H + h) * kD + c]);
+        } else if (cst) {
+          const int si = pos - sbeg + (P.conv_w - 1);  // index into the W-1 kept inputs
+          if (si >= 0) x = __ldg(cst + (((size_t)seq * H + h) * kD + c) * (P.conv_w - 1) + si);
+        }
+        halo[j * 128 + c] = x;
+      }
+    }
     sync_tc();
 
     // ---------------- B: token norms and beta of the chunk at tc0 (lenc tokens) ----------------
@@ -485,6 +577,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           pend_qkz = false;
         }
         if (__syncthreads_or(!ok)) { aborted = true; break; }
+        if (kConv) conv_tiles(sm, P, h, warp, lane);
         norms_and_beta(t0, len);
       }
 
@@ -917,6 +1010,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // every lane runs it (its shuffles need the whole warp); after a timeout
         // the values are not used
+        if (kConv) conv_tiles(sm, P, h, warp, lane);
         norms_and_beta(t0 + kC, min(kC, eos - t0 - kC));
       }
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);
@@ -1261,12 +1355,15 @@ struct TcLaunch {
     if (sms <= 0) return cudaErrorInvalidDevice;
     static PerDeviceInit attrs;
     const cudaError_t attr_err = attrs.run([] {
-      cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<false>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)SMEM_BYTES);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_tc_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      cudaError_t e = cudaSuccess;
+      const void* kernels[] = {(const void*)chunk_tc_kernel<false, false>,
+                               (const void*)chunk_tc_kernel<true, false>,
+                               (const void*)chunk_tc_kernel<false, true>,
+                               (const void*)chunk_tc_kernel<true, true>};
+      for (const void* kf : kernels)
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SMEM_BYTES);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(2 * kD * kScanLd * sizeof(float)));
@@ -1310,16 +1407,29 @@ struct TcLaunch {
       prm.inject_timeout = 1;
       prm.spin_cycles = 20000000LL;  // ~10 ms
     }
+    prm.conv_w = a.conv_w;
+    prm.conv_wq = a.conv_wq;
+    prm.conv_wk = a.conv_wk;
+    prm.conv_sq = a.conv_sq;
+    prm.conv_sk = a.conv_sk;
+    prm.qraw = static_cast<const __nv_bfloat16*>(a.q);
+    prm.kraw = static_cast<const __nv_bfloat16*>(a.k);
     prm.use_order = 0;
     prm.mode = 0;
     return cudaSuccess;
   }
 
   void launch(const Params& prm, int grid) const {
-    if (per_head)
-      chunk_tc_kernel<true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
-    else
-      chunk_tc_kernel<false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    if (prm.conv_w > 0) {
+      if (per_head)
+        chunk_tc_kernel<true, true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+      else
+        chunk_tc_kernel<false, true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    } else if (per_head) {
+      chunk_tc_kernel<true, false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    } else {
+      chunk_tc_kernel<false, false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+    }
   }
 };
 

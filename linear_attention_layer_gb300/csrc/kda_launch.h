@@ -59,6 +59,13 @@ struct Args {
   const int32_t* ckpt_off;   // device [N + 1] prefix sums of checkpoints per sequence
   int ckpt_every;            // tokens between checkpoints (0: none)
   int gate_per_head;         // 1: z is [T, H], one gate per head (scalar alpha)
+  // fused short convolution of q and k (tensor-core path; conv_w = 0: none):
+  // taps [H][dk][W], incoming states [N][H][dk][W-1] (null: zeros)
+  int conv_w = 0;
+  const float* conv_wq = nullptr;
+  const float* conv_wk = nullptr;
+  const float* conv_sq = nullptr;
+  const float* conv_sk = nullptr;
 };
 
 // One work item of a chunked launch: a (sequence, head) pair, processed
@@ -179,6 +186,8 @@ struct ConvArgs {
   int* err;
 };
 cudaError_t launch_short_conv(const Problem& p, const ConvArgs& a, cudaStream_t stream);
+// Only its second step: each sequence's outgoing state (last W-1 inputs).
+cudaError_t launch_short_conv_state(const Problem& p, const ConvArgs& a, cudaStream_t stream);
 
 // The prefill over host buffers with copies overlapped (kda_host.cu).
 struct HostArgs {

@@ -229,6 +229,29 @@ cudaError_t launch_t(const Problem& p, const ConvArgs& a, cudaStream_t st) {
 
 }  // namespace conv
 
+cudaError_t launch_short_conv_state(const Problem& p, const ConvArgs& a, cudaStream_t st) {
+  if (!a.state_out || a.width < 2 || p.num_seqs == 0) return cudaSuccess;
+  const long long threads = (long long)p.num_seqs * p.num_heads * p.dk;
+  const unsigned blocks = (unsigned)((threads + conv::kNT - 1) / conv::kNT);
+  auto go = [&](auto tag) {
+    using T = decltype(tag);
+    switch (a.width) {
+      case 2: conv::state_kernel<T, 2><<<blocks, conv::kNT, 0, st>>>(
+          static_cast<const T*>(a.x), a.state_in, a.cu_seqlens, p.num_seqs, p.total_tokens,
+          p.num_heads, p.dk, a.state_out, a.err); break;
+      case 3: conv::state_kernel<T, 3><<<blocks, conv::kNT, 0, st>>>(
+          static_cast<const T*>(a.x), a.state_in, a.cu_seqlens, p.num_seqs, p.total_tokens,
+          p.num_heads, p.dk, a.state_out, a.err); break;
+      default: conv::state_kernel<T, 4><<<blocks, conv::kNT, 0, st>>>(
+          static_cast<const T*>(a.x), a.state_in, a.cu_seqlens, p.num_seqs, p.total_tokens,
+          p.num_heads, p.dk, a.state_out, a.err); break;
+    }
+    return cudaGetLastError();
+  };
+  if (a.width > 4) return cudaErrorInvalidValue;
+  return p.io_bf16 ? go(__nv_bfloat16{}) : go(float{});
+}
+
 cudaError_t launch_short_conv(const Problem& p, const ConvArgs& a, cudaStream_t st) {
   return p.io_bf16 ? conv::launch_t<__nv_bfloat16>(p, a, st) : conv::launch_t<float>(p, a, st);
 }
