@@ -500,6 +500,60 @@ def bench_short_conv(kda, p, steps, warmup, device, width=4, clk=None):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in evs]
 
 
+def bench_fused_prefill(kda, p, steps, warmup, device, width=4, clk=None):
+    """kda_chunk_fwd_fused (the short convolution of raw q, k inside the
+    prefill kernel) against the separate path (kda_short_conv of q and of k,
+    then kda_chunk_fwd) on the same workload.  Returns (fused ms per step,
+    separate ms per step)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(78)
+    H, N = p.meta["num_heads"], p.num_seqs
+    f32 = dict(dtype=torch.float32, device=device, generator=g)
+    wq = torch.randn((H, 128, width), **f32) * 0.5
+    wk = torch.randn((H, 128, width), **f32) * 0.5
+    sq = torch.randn((N, H, 128, width - 1), **f32)
+    sk = torch.randn((N, H, 128, width - 1), **f32)
+    out = torch.empty_like(p.v)
+    fin = torch.empty((N, H, 128, 128), dtype=torch.float32, device=device)
+    yq, yk = torch.empty_like(p.q), torch.empty_like(p.k)
+    fq, fk = torch.empty_like(sq), torch.empty_like(sk)
+    stream = torch.cuda.current_stream()
+
+    def fused():
+        kda.chunk_fwd_fused(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                            conv_weight_q=wq, conv_weight_k=wk, conv_state_q=sq,
+                            conv_state_k=sk, out=out, final_state=fin,
+                            cu_seqlens_host=p.cu_seqlens_host)
+
+    def separate():
+        kda.short_conv(p.q, wq, p.cu_seqlens, sq, out=yq, final_state=fq)
+        kda.short_conv(p.k, wk, p.cu_seqlens, sk, out=yk, final_state=fk)
+        kda.chunk_fwd(yq, yk, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, out=out,
+                      final_state=fin, cu_seqlens_host=p.cu_seqlens_host)
+
+    res = []
+    for fn, c in ((fused, clk), (separate, None)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        if c is not None:
+            c.start()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if c is not None:
+            c.stop()
+        res.append(a.elapsed_time(b) / steps)
+    if kda.get_device_error() != 0:
+        raise RuntimeError("device error word set after the fused prefill")
+    return res[0], res[1]
+
+
 def bench_spec_decode_fused(kda, B, H, W, steps, device, seed=0, clk=None, width=4):
     """The speculative-decoding step with the short convolution of raw q, k
     (width 4, states advanced by the replay) and the per-head RMS output norm
@@ -519,7 +573,8 @@ def bench_spec_decode_fused(kda, B, H, W, steps, device, seed=0, clk=None, width
               conv_weight_k=torch.randn((H, 128, width), **f32) * 0.5,
               conv_state_q=torch.randn((B, H, 128, width - 1), **f32),
               conv_state_k=torch.randn((B, H, 128, width - 1), **f32),
-              out_norm_weight=torch.ones((H, 128), **f32), out_norm_eps=1e-6)
+              out_norm_weight=torch.ones((H, 128), dtype=torch.float32, device=device),
+              out_norm_eps=1e-6)
     out = torch.empty((B, W, H, 128), dtype=torch.bfloat16, device=device)
     acc = torch.randint(0, W + 1, (steps + 3, B), generator=g, device=device, dtype=torch.int32)
     stream = torch.cuda.current_stream()
@@ -673,7 +728,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip", default="",
-                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv,prefill,tiny")
+                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv,prefill,tiny,fused")
     ap.add_argument("--bwd-steps", type=int, default=3)
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
@@ -752,6 +807,23 @@ def main():
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
     }
+
+    # ---- the short convolution fused into the prefill, against the separate calls ----
+    if "fused" not in skip:
+        fpclk = clock_sampler(gpu_uuid)
+        fu_ms, sep_ms = bench_fused_prefill(kda, p, args.steps, args.warmup, device, clk=fpclk)
+        fu_bytes = alg_bytes + 2 * 2 * N * H * 128 * 3 * 4  # + q, k convolution states in and out
+        fu_gbs = fu_bytes / (fu_ms * 1e-3) / 1e9
+        line["prefill_conv_fused"] = {
+            "value": round(weak_scaling_value(T, world, fu_ms / 1e3), 3), "unit": UNIT,
+            "ms_per_step": round(fu_ms, 4), "kernel": "kda_chunk_fwd_fused",
+            "separate_ms_per_step": round(sep_ms, 4),
+            "separate": "kda_short_conv (q), kda_short_conv (k), kda_chunk_fwd",
+            "workload": workloads.DESCRIPTIONS[args.workload] + "; raw q, k, convolution width 4",
+            "roofline": {"bound": "hbm", "achieved": round(fu_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(fu_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_launch": fu_bytes},
+            "clocks": fpclk.summary(), "gpu_launches": 3 * args.steps}
 
     # ---- the 4 x 4096-token, 16-head prefill (workspace offered: the planner
     # decides whether splitting sequences across SMs pays) ----

@@ -132,9 +132,10 @@ def test_context_parallel_emulated_matches_one_pass(world):
 
 
 def test_context_parallel_long_workload_four_ranks():
-    """The long-context workload (1 x 65536 tokens, 32 heads) cut over four
-    emulated ranks equals the single-GPU prefill of the whole sequence."""
-    p = workloads.prefill_workload("long", device=DEV)
+    """The slow-decay long-context workload (1 x 65536 tokens, 32 heads, z ~
+    N(-2, 1)) cut over four emulated ranks equals the single-GPU prefill of
+    the whole sequence."""
+    p = workloads.prefill_workload("long_slow", device=DEV)
     out, fin = _emulate(p, 4)
     ref_o, ref_f = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, None,
                                  cu_seqlens_host=p.cu_seqlens_host)
