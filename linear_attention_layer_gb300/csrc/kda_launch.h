@@ -115,6 +115,9 @@ cudaError_t launch_decode_fused(const Problem& p, const void* q, const void* k, 
 
 // Token-by-token prefill over a packed batch.
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t stream);
+// The same with one warp per (sequence, head) for small states (dv = 32, dk <= 64).
+bool recurrent_small_supported(const Problem& p);
+cudaError_t launch_recurrent_small(const Problem& p, const Args& a, cudaStream_t stream);
 
 // Chunked prefill on CUDA cores in fp32 (any supported size, fp32 or bf16 io).
 cudaError_t launch_chunk_simt(const Problem& p, const Args& a, cudaStream_t stream);

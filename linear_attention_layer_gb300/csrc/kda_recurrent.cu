@@ -379,6 +379,108 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
   }
 }
 
+// Small states (dv = 32, dk <= 64): one warp per (sequence, head), lane j
+// holding value column j of S (dk floats in registers), four warps per CTA.
+// A token costs no block barrier: its q, k and retentions go through the
+// warp's own shared-memory rows, both reductions over the key channels
+// (S^T k and S^T q) are per-lane sums, and the rank-one write is per lane.
+// Used for short latency-bound calls where a block per unit would spend its
+// time in barriers.
+constexpr int kSmallWarps = 4;
+
+template <int DK, typename T>
+__global__ void __launch_bounds__(32 * kSmallWarps)
+recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                       const float* __restrict__ z, const float* __restrict__ beta,
+                       const float* initial_state, const int32_t* __restrict__ cu,
+                       T* __restrict__ out, float* final_state, int H, int total, int units,
+                       int* err, const float* __restrict__ a_log, float* ckpt,
+                       const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
+  constexpr int DV = 32, CPL = DK / 32;  // channels staged per lane
+  __shared__ __align__(16) float sh[kSmallWarps][3][DK];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kSmallWarps + w;
+  if (unit >= units) return;
+  const int n = unit / H, h = unit % H;
+  int bos, eos;
+  if (!seq_range(cu, n, total, lane == 0 ? err : nullptr, bos, eos)) return;
+  const size_t sbase = (size_t)unit * DK * DV;
+  float s[DK];
+#pragma unroll
+  for (int c = 0; c < DK; ++c)
+    s[c] = initial_state ? __ldg(initial_state + sbase + (size_t)c * DV + lane) : 0.f;
+  const float zscale = gate_scale(a_log, h);
+  float* qs = sh[w][0];
+  float* ks = sh[w][1];
+  float* as = sh[w][2];
+  for (int t = bos; t < eos; ++t) {
+    const size_t th = (size_t)t * H + h;
+    float qq = 0.f, kk = 0.f, kq = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      const float a = IO<T>::ld(q + th * DK + c), b = IO<T>::ld(k + th * DK + c);
+      qs[c] = a;
+      ks[c] = b;
+      as[c] = __expf(log_decay(zscale * __ldg(z + th * (zhead ? 1 : DK) + (zhead ? 0 : c))));
+      qq += a * a;
+      kk += b * b;
+      kq += a * b;
+    }
+    const float vj = IO<T>::ld(v + th * DV + lane);
+    const float bt = __ldg(beta + th);
+    qq = warp_sum(qq);
+    kk = warp_sum(kk);
+    kq = warp_sum(kq);
+    __syncwarp();
+    const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
+    float ek[4] = {0.f, 0.f, 0.f, 0.f}, eq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < DK; c += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(as + c);
+      const float4 k4 = *reinterpret_cast<const float4*>(ks + c);
+      const float4 q4 = *reinterpret_cast<const float4*>(qs + c);
+      s[c] *= a4.x; s[c + 1] *= a4.y; s[c + 2] *= a4.z; s[c + 3] *= a4.w;
+      ek[0] = fmaf(s[c], k4.x, ek[0]); ek[1] = fmaf(s[c + 1], k4.y, ek[1]);
+      ek[2] = fmaf(s[c + 2], k4.z, ek[2]); ek[3] = fmaf(s[c + 3], k4.w, ek[3]);
+      eq[0] = fmaf(s[c], q4.x, eq[0]); eq[1] = fmaf(s[c + 1], q4.y, eq[1]);
+      eq[2] = fmaf(s[c + 2], q4.z, eq[2]); eq[3] = fmaf(s[c + 3], q4.w, eq[3]);
+    }
+    const float e = vj - (ek[0] + ek[1] + ek[2] + ek[3]) * rk;
+    const float o = (eq[0] + eq[1] + eq[2] + eq[3]) * rq + bt * (kq * rk * rq) * e;
+    IO<T>::st(out + th * DV + lane, o);
+    const float be = bt * e * rk;
+#pragma unroll
+    for (int c = 0; c < DK; c += 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(ks + c);
+      s[c] = fmaf(k4.x, be, s[c]); s[c + 1] = fmaf(k4.y, be, s[c + 1]);
+      s[c + 2] = fmaf(k4.z, be, s[c + 2]); s[c + 3] = fmaf(k4.w, be, s[c + 3]);
+    }
+    if (ckpt && (t + 1 - bos) % ckpt_every == 0) {
+      const size_t j = (size_t)__ldg(ckpt_off + n) + (t + 1 - bos) / ckpt_every - 1;
+      float* dst = ckpt + (j * H + h) * DK * DV;
+#pragma unroll
+      for (int c = 0; c < DK; ++c) dst[(size_t)c * DV + lane] = s[c];
+    }
+    __syncwarp();  // this token's rows are read before the next overwrites them
+  }
+  if (final_state) {
+#pragma unroll
+    for (int c = 0; c < DK; ++c) final_state[sbase + (size_t)c * DV + lane] = s[c];
+  }
+}
+
+template <int DK, typename T>
+cudaError_t small_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
+  const int units = p.num_seqs * p.num_heads;
+  const unsigned blocks = (unsigned)((units + kSmallWarps - 1) / kSmallWarps);
+  recurrent_small_kernel<DK, T><<<blocks, 32 * kSmallWarps, 0, st>>>(
+      (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
+      (T*)a.out, a.final_state, p.num_heads, p.total_tokens, units, a.err, a.a_log, a.ckpt,
+      a.ckpt_off, a.ckpt_every, a.gate_per_head);
+  return cudaGetLastError();
+}
+
 template <int DK, int DV, typename T>
 cudaError_t decode_dispatch(const Problem& p, const void* q, const void* k, const void* v,
                             const float* z, const float* beta, const float* a_log, int zhead,
@@ -485,6 +587,18 @@ cudaError_t launch_decode_fused(const Problem& p, const void* q, const void* k, 
                      : decode_fused_dispatch<DK, DV, float>(p, q, k, v, z, beta, a_log, zhead,
                                                             state, out, f, st);
   });
+}
+
+bool recurrent_small_supported(const Problem& p) { return p.dv == 32 && p.dk <= 64; }
+
+cudaError_t launch_recurrent_small(const Problem& p, const Args& a, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  if (p.dv != 32) return cudaErrorInvalidValue;
+  if (p.dk == 32)
+    return p.io_bf16 ? small_dispatch<32, __nv_bfloat16>(p, a, st) : small_dispatch<32, float>(p, a, st);
+  if (p.dk == 64)
+    return p.io_bf16 ? small_dispatch<64, __nv_bfloat16>(p, a, st) : small_dispatch<64, float>(p, a, st);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_recurrent(const Problem& p, const Args& a, cudaStream_t st) {

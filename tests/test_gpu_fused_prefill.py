@@ -36,11 +36,15 @@ def _conv_inputs(N, H, W, seed):
 
 
 def _oracle(p, wq, wk, sq, sk, z=None, a_log=None):
+    """The composition the fused call computes: the convolution (fp64) with its
+    output in the io dtype -- the form in which kda_short_conv hands q and k
+    to the prefill -- then the fp64 recurrence."""
     cu = p.cu_seqlens_host
     W = wq.shape[-1]
     qy, fq = oracle.short_conv(p.q, wq, cu, sq.cpu() if W > 1 else None)
     ky, fk = oracle.short_conv(p.k, wk, cu, sk.cpu() if W > 1 else None)
-    o, f, _ = oracle.recurrent(qy, ky, p.v, p.z if z is None else z, p.beta, cu,
+    io = lambda y: torch.from_numpy(y).to(p.q.dtype)
+    o, f, _ = oracle.recurrent(io(qy), io(ky), p.v, p.z if z is None else z, p.beta, cu,
                                p.initial_state, a_log=a_log)
     return o, f, fq, fk
 
@@ -119,9 +123,28 @@ def test_fused_prefill_continues_a_split_sequence():
     assert torch.equal(sq2, sq) and torch.equal(sk2, sk)
 
 
+def test_fused_prefill_full_prefill_workload():
+    """The 4 x 4096-token, 16-head workload through the fused call, every
+    output and final state against the oracle composition."""
+    p = workloads.prefill_workload("prefill", device=DEV)
+    wq, wk, sq, sk = _conv_inputs(p.num_seqs, 16, 4, 84)
+    sq0, sk0 = sq.clone(), sk.clone()
+    out, fin = kda.chunk_fwd_fused(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, None,
+                                   conv_weight_q=wq, conv_weight_k=wk, conv_state_q=sq,
+                                   conv_state_k=sk, cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    ro, rf, fq, fk = _oracle(p, wq, wk, sq0, sk0)
+    print("fused prefill 4x4096x16 out rel-L2", assert_close(out, ro, torch.bfloat16, "out"))
+    assert_close(fin, rf, torch.bfloat16, "final state")
+    assert torch.equal(sq.cpu(), torch.from_numpy(fq).float())
+
+
 def test_fused_prefill_equals_separate_calls_on_the_varlen_workload():
     """The bench workload (64 sequences, 32 heads): the fused call against
-    kda_short_conv of q and k followed by kda_chunk_fwd."""
+    kda_short_conv of q and k followed by kda_chunk_fwd.  Each path is within
+    the bf16 bounds of the oracle, so the two differ by at most their sum
+    (rel-L2 2e-2, max|err| 4e-2 RMS)."""
     p = workloads.prefill_workload("varlen", device=DEV)
     wq, wk, sq, sk = _conv_inputs(p.num_seqs, 32, 4, 89)
     sq_s, sk_s = sq.clone(), sk.clone()
@@ -137,5 +160,5 @@ def test_fused_prefill_equals_separate_calls_on_the_varlen_workload():
     for x, r, what, both in ((o_f, o_sep, "out", True), (f_f, f_sep, "final", False)):
         rel, mx = device_compare(x, r, both_stored=both)
         print(f"fused vs separate, varlen {what}: rel-L2 {rel:.3e}, max/RMS {mx:.3e}")
-        assert rel <= 1e-2 and mx <= 2e-2, (what, rel, mx)
+        assert rel <= 2e-2 and mx <= 4e-2, (what, rel, mx)
     assert torch.equal(sq, fq) and torch.equal(sk, fk)

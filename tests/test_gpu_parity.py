@@ -685,3 +685,37 @@ def test_expired_device_wait_reports_timeout_and_recovers():
     torch.cuda.synchronize()
     assert kda.get_device_error() == 0
     _check_all(p, out, fin, torch.bfloat16)
+
+
+# ------------------------------------------- small states, one warp per unit --
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk", [32, 64])
+def test_small_state_path(dtype, dk):
+    """dv = 32, dk <= 64 (the CUDA-core path runs one warp per (sequence,
+    head)): ragged lengths with a long one, checkpoints, the gate log-scale,
+    against the oracle."""
+    lens = [1, 0, 31, 64, 65, 2000]
+    p = workloads.random_problem(lens, 3, dk, 32, dtype, z_mean=-1.0, init_std=0.2, seed=33,
+                                 device=DEV)
+    A = torch.tensor([0.3, -0.4, 0.9])
+    out, fin, ck = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                 cu_seqlens_host=p.cu_seqlens_host, a_log=A.to(DEV),
+                                 checkpoint_every=64)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    ro, rf, _ = oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host,
+                                 p.initial_state, a_log=A)
+    assert_close(out, ro, dtype, "out")
+    assert_close(fin, rf, dtype, "final_state")
+    offs = kda.checkpoint_offsets(p.cu_seqlens_host, 64)
+    assert ck.shape[0] == offs[-1] == 1 + 1 + 31
+    assert torch.equal(ck[offs[4] - 1], fin[3])  # the 64-token sequence ends on a checkpoint
+    # and one gate per head
+    zh = p.z[:, :, 0].contiguous()
+    out2, fin2 = kda.chunk_fwd(p.q, p.k, p.v, zh, p.beta, p.cu_seqlens, p.initial_state)
+    torch.cuda.synchronize()
+    zb = zh.cpu()[:, :, None].expand(-1, -1, dk).contiguous()
+    ro2, rf2, _ = oracle.recurrent(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, p.initial_state)
+    assert_close(out2, ro2, dtype, "per-head gate out")
+    assert_close(fin2, rf2, dtype, "per-head gate final_state")
