@@ -442,8 +442,9 @@ kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* b
  * rebuilt forward from states the call itself keeps every 8 tokens in the
  * workspace.
  *
- *   desc               as for kda_chunk_fwd; dk = dv = 128 and
- *                      gate_per_head = 0 (else KDA_ERR_UNSUPPORTED);
+ *   desc               as for kda_chunk_fwd; dk = dv = 128 (else
+ *                      KDA_ERR_UNSUPPORTED); gate_per_head = 1 takes z [T_tot,
+ *                      H] and gives dz [T_tot, H] (the per-channel terms summed);
  *                      cu_seqlens_host is REQUIRED; workspace /
  *                      workspace_bytes must hold
  *                      kda_recurrent_bwd_workspace_size() bytes (16-byte
@@ -453,8 +454,9 @@ kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* b
  *                      the forward call's inputs (initial_state may be NULL)
  *   d_out              device, [T_tot, H, dv] io dtype: dL/d out
  *   d_final_state      device, [N, H, dk, dv] fp32, or NULL for zeros
- *   dq, dk, dv, dz     device, [T_tot, H, 128] fp32, written (dz is the
- *                      gradient w.r.t. the gate logits z as passed)
+ *   dq, dk, dv, dz     device, [T_tot, H, 128] fp32 (dz [T_tot, H] with one
+ *                      gate per head), written (dz is the gradient w.r.t. the
+ *                      gate logits z as passed)
  *   dbeta              device, [T_tot, H] fp32, written
  *   d_initial_state    device, [N, H, dk, dv] fp32, written, or NULL
  * Every pointer to per-token or state data must be 16-byte aligned, and no

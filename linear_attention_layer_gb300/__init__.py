@@ -472,8 +472,8 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     """Reverse mode of the prefill (``kda_recurrent_bwd``): given dL/d out and
     dL/d final_state (None: zeros), returns (dq, dk, dv, dz, dbeta,
     d_initial_state), fp32, for the inputs of the forward call (same q, k, v,
-    z, beta, cu_seqlens, initial_state and a_log; dk = dv = 128, one gate per
-    key channel).  ``cu_seqlens_host`` is required; ``workspace`` (a device
+    z, beta, cu_seqlens, initial_state and a_log; dk = dv = 128).  ``z`` [T, H]
+    (one gate per head) gives dz [T, H].  ``cu_seqlens_host`` is required; ``workspace`` (a device
     tensor of ``recurrent_bwd_workspace_size`` bytes) is allocated here when
     None; ``grads`` may give the six output tensors to fill."""
     lib = load()
@@ -484,7 +484,9 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     _check_tensor("q", q, q.dtype, (T, H, dk), dev)
     _check_tensor("k", k, q.dtype, (T, H, dk), dev)
     _check_tensor("v", v, q.dtype, (T, H, dv), dev)
-    _check_tensor("z", z, torch.float32, (T, H, dk), dev)
+    per_head = z.dim() == 2
+    zshape = (T, H) if per_head else (T, H, dk)
+    _check_tensor("z", z, torch.float32, zshape, dev)
     _check_tensor("beta", beta, torch.float32, (T, H), dev)
     _check_tensor("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
     _check_tensor("d_out", d_out, q.dtype, (T, H, dv), dev)
@@ -497,15 +499,16 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     if grads is None:
         f32 = dict(dtype=torch.float32, device=dev)
         grads = (torch.empty((T, H, dk), **f32), torch.empty((T, H, dk), **f32),
-                 torch.empty((T, H, dv), **f32), torch.empty((T, H, dk), **f32),
+                 torch.empty((T, H, dv), **f32), torch.empty(zshape, **f32),
                  torch.empty((T, H), **f32), torch.empty((N, H, dk, dv), **f32))
-    shapes = ((T, H, dk), (T, H, dk), (T, H, dv), (T, H, dk), (T, H), (N, H, dk, dv))
+    shapes = ((T, H, dk), (T, H, dk), (T, H, dv), zshape, (T, H), (N, H, dk, dv))
     for name, g, shp in zip(("dq", "dk", "dv", "dz", "dbeta", "d_initial"), grads, shapes):
         _check_tensor(name, g, torch.float32, shp, dev)
     if workspace is None:
         nbytes = recurrent_bwd_workspace_size(H, q.dtype, cu_seqlens_host)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
+    desc.gate_per_head = 1 if per_head else 0
     with torch.cuda.device(dev):
         st = lib.kda_recurrent_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
                                    _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),

@@ -112,7 +112,7 @@ kda_status_t check_bwd(const kda_desc_t* desc, const void* q, const void* k, con
   if (s != KDA_OK) return s;
   if (!desc->cu_seqlens_host || !cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
   if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
-  if (desc->dk != 128 || desc->dv != 128 || desc->gate_per_head != 0) return KDA_ERR_UNSUPPORTED;
+  if (desc->dk != 128 || desc->dv != 128) return KDA_ERR_UNSUPPORTED;
   if (desc->total_tokens > 0) {
     const void* need[] = {q, k, v, z, beta, d_out, dq, dk, dv, dz, dbeta};
     for (const void* x : need)
@@ -536,6 +536,7 @@ kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void
   a.a_log = desc->a_log;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dz = dz; a.dbeta = dbeta;
   a.d_initial = d_initial_state;
+  a.zhead = desc->gate_per_head;
   a.err = device_error_word();
   if (!a.err) return KDA_ERR_CUDA;
   cudaError_t e = kda::launch_recurrent_bwd(p, a, desc->cu_seqlens_host, desc->workspace,

@@ -71,6 +71,7 @@ struct Params {
   int num_seqs;
   int num_units;
   int use_order;
+  int zhead;  // 1: one gate logit per (token, head), z and dz [T, H]
   int order[kMaxOrder];
 };
 
@@ -86,6 +87,7 @@ struct Smem {
   float red3[2][3][4][kD];    // sums over n (dq^ of the token before, dk^, dalpha), per warp column (w & 3)
   float redq[4][kD];          // sums over n: dq^ of a sub-block's last token
   float beta[kBlk], rq[kBlk], rk[kBlk], db[kBlk];
+  float dzh[kBlk];  // one gate per head: dz of the block's tokens, summed over channels
 };
 
 template <typename T>
@@ -151,7 +153,13 @@ __device__ void stage_block(Smem& sm, const Params& P, int h, int t0, int len, f
     if (part == 0) (pass == 0 ? sm.rq : sm.rk)[t] = r;
   }
   // alpha = e^g, g = -5 sigmoid(s z)
-  if (live) Vec16<float>::ld(P.z + row, y);
+  if (live && P.zhead) {
+    const float zz = __ldg(P.z + (size_t)(t0 + t) * P.H + h);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = zz;
+  } else if (live) {
+    Vec16<float>::ld(P.z + row, y);
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) y[i] = live ? ex2_approx(log_decay_c(y[i], zc) * 1.4426950408889634f) : 1.f;
 #pragma unroll
@@ -307,6 +315,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
       const int b0 = bi * kBlk, bl = min(kBlk, len - b0);
       __syncthreads();
       stage_block<T>(sm, P, h, bos + b0, bl, zc, true);
+      if (P.zhead && tid < kBlk) sm.dzh[tid] = 0.f;
       __syncthreads();
       for (int j0 = ((bl - 1) / kSub) * kSub; j0 >= 0; j0 -= kSub) {
         const int sl = min(kSub, bl - j0);
@@ -430,7 +439,13 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
             if (i > 0) sm.dqh[t - 1][c] = dqh;
             sm.v[t][c] = dkh;  // this token's v is no longer read
             const float a = sm.al[t][c], g = __logf(a);
-            P.dz[((size_t)(bos + b0 + t) * P.H + h) * kD + c] = dal * a * g * (1.f + g / 5.f) * zs;
+            const float dzc = dal * a * g * (1.f + g / 5.f) * zs;
+            if (P.zhead) {  // the head's one logit feeds every channel: sum the terms
+              const float sum = warp_sum(dzc);
+              if ((tid & 31) == 0) atomicAdd(&sm.dzh[t], sum);
+            } else {
+              P.dz[((size_t)(bos + b0 + t) * P.H + h) * kD + c] = dzc;
+            }
           }
           par ^= 1;
         }
@@ -465,7 +480,10 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
                               r * (dxh[c0 + i + 2] - xh[c0 + i + 2] * dot),
                               r * (dxh[c0 + i + 3] - xh[c0 + i + 3] * dot)));
           }
-          if (live && part == 0) P.dbeta[(size_t)(bos + b0 + t) * P.H + h] = sm.db[t];
+          if (live && part == 0) {
+            P.dbeta[(size_t)(bos + b0 + t) * P.H + h] = sm.db[t];
+            if (P.zhead) P.dz[(size_t)(bos + b0 + t) * P.H + h] = sm.dzh[t];
+          }
         }
       }
     }
@@ -538,6 +556,7 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
   prm.total = p.total_tokens;
   prm.num_seqs = p.num_seqs;
   prm.num_units = p.num_seqs * p.num_heads;
+  prm.zhead = a.zhead;
   prm.use_order = 0;
   if (p.num_seqs <= kMaxOrder) {  // longest sequences first
     std::vector<int> idx(p.num_seqs);

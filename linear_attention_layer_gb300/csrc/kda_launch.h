@@ -172,6 +172,7 @@ struct BwdArgs {
   float* dbeta;
   float* d_initial;  // may be null
   int* err;
+  int zhead = 0;     // 1: one gate per head (z, dz [T, H])
 };
 size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,

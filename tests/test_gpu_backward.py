@@ -151,3 +151,25 @@ def test_backward_all_sequences_empty():
     got = _run(p, d_out, d_fin)
     assert torch.equal(got[5], d_fin)
     assert all(g.numel() == 0 for g in got[:5])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_backward_gate_per_head(dtype):
+    """One gate logit per (token, head) (the scalar-alpha case): z and dz are
+    [T, H].  The oracle runs the per-channel gate with the logit broadcast over
+    the key channels, so the head's dz is the sum of its channel terms."""
+    p = workloads.random_problem(RAGGED, 3, 128, 128, dtype, z_std=1.5, init_std=0.1, seed=27,
+                                 device=DEV)
+    zh = p.z[:, :, 0].contiguous()
+    A = torch.tensor([0.5, -0.4, 1.2])
+    d_out, d_fin = _cotangents(p, 7)
+    got = kda.recurrent_bwd(p.q, p.k, p.v, zh, p.beta, p.cu_seqlens, p.initial_state, d_out,
+                            d_fin, cu_seqlens_host=p.cu_seqlens_host, a_log=A.to(DEV))
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    assert got[3].shape == zh.shape
+    zb = zh.cpu()[:, :, None].expand(-1, -1, 128).contiguous()
+    ref = list(oracle.backward(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, p.initial_state,
+                               d_out, d_fin, a_log=A))
+    ref[3] = ref[3].sum(axis=-1)
+    _compare(got, ref)
