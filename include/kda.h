@@ -340,8 +340,10 @@ kda_status_t kda_decode_replay_window_fused(
  *                      decode-side calls.
  * Other arguments, options (workspace split, checkpoints, a_log,
  * gate_per_head) and errors as for kda_chunk_fwd.  The convolution's Swish
- * uses the hardware tanh (sigmoid(u) = (1 + tanh(u/2)) / 2); its outputs are
- * rounded to bf16 like the outputs of kda_short_conv.
+ * uses the hardware tanh (sigmoid(u) = (1 + tanh(u/2)) / 2) and its outputs
+ * stay in fp16 inside the kernel (finer than the bf16 that kda_short_conv
+ * writes); a convolved value of magnitude 65504 or more sets
+ * KDA_ERR_DEVICE_CHECK, like the tensor-core path's other fp16 operands.
  */
 kda_status_t kda_chunk_fwd_fused(const kda_desc_t* desc, const kda_fusion_t* fusion,
                                  const void* q, const void* k, const void* v, const float* z,

@@ -320,6 +320,19 @@ __device__ __forceinline__ void prep_state(uint32_t my_lane, const float* dec, i
   tmem_st_wait();
 }
 
+// q / k tile words: bf16 pairs as loaded, fp16 pairs once the fused
+// convolution has rewritten them (kConv).
+template <bool kF16>
+__device__ __forceinline__ float tile_lo(uint32_t x) {
+  if (kF16) return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
+  return bf16_lo(x);
+}
+template <bool kF16>
+__device__ __forceinline__ float tile_hi(uint32_t x) {
+  if (kF16) return __half2float(__ushort_as_half((unsigned short)(x >> 16)));
+  return bf16_hi(x);
+}
+
 // The fused short convolution + Swish of the chunk's raw q and k tiles (in
 // the input stages, 128-byte swizzled bf16), in place, before the token norms.
 // Warp w takes tensor w % 2 (q, k), 64-channel block (w / 2) % 2 and tokens
@@ -327,9 +340,11 @@ __device__ __forceinline__ void prep_state(uint32_t my_lane, const float* dec, i
 // three raw inputs before the chunk come from the halo area, which quarter 3
 // refills with the chunk's last three raw inputs for the next chunk.  All
 // threads take part (two block barriers).  Taps are right-aligned: width W
-// uses the last W of four (the others zero).
+// uses the last W of four (the others zero).  The results are stored as fp16
+// (11-bit significand; the raw inputs were bf16), so the tiles lose less than
+// an output stored in the io dtype would; absmax tracks the fp16 range.
 __device__ __forceinline__ void conv_tiles(unsigned char* sm, const Params& P, int h, int warp,
-                                           int lane) {
+                                           int lane, float& absmax) {
   const int tens = warp & 1, blk = (warp >> 1) & 1, qt = warp >> 2;
   const int c0 = 64 * blk + 2 * lane;
   unsigned char* tile = sm + (tens ? OFF_K : OFF_Q) + blk * 8192;
@@ -371,8 +386,9 @@ __device__ __forceinline__ void conv_tiles(unsigned char* sm, const Params& P, i
   for (int i = 0; i < 16; ++i) {
     const float ua = fmaf(ta[0], xa[i], fmaf(ta[1], xa[i + 1], fmaf(ta[2], xa[i + 2], ta[3] * xa[i + 3])));
     const float ub = fmaf(tb[0], xb[i], fmaf(tb[1], xb[i + 1], fmaf(tb[2], xb[i + 2], tb[3] * xb[i + 3])));
-    const __nv_bfloat162 y = __floats2bfloat162_rn(swish_tanh(ua), swish_tanh(ub));
-    *word(16 * qt + i) = *reinterpret_cast<const uint32_t*>(&y);
+    const float ya = swish_tanh(ua), yb = swish_tanh(ub);
+    absmax = fmaxf(absmax, fmaxf(fabsf(ya), fabsf(yb)));
+    *word(16 * qt + i) = pack_f16(ya, yb);
   }
   __syncthreads();  // the converted tiles are complete
 }
@@ -536,9 +552,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float u = bf16_lo(aw[i]), w = bf16_hi(aw[i]);
+          float u = tile_lo<kConv>(aw[i]), w = tile_hi<kConv>(aw[i]);
           sq += u * u + w * w;
-          u = bf16_lo(bw[i]); w = bf16_hi(bw[i]);
+          u = tile_lo<kConv>(bw[i]); w = tile_hi<kConv>(bw[i]);
           sk += u * u + w * w;
         }
       }
@@ -577,7 +593,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           pend_qkz = false;
         }
         if (__syncthreads_or(!ok)) { aborted = true; break; }
-        if (kConv) conv_tiles(sm, P, h, warp, lane);
+        if (kConv) conv_tiles(sm, P, h, warp, lane, absmax);
         norms_and_beta(t0, len);
       }
 
@@ -638,11 +654,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i = 0; i < 16; ++i) {
             const uint32_t off = 128u * i + ((x ^ (uint32_t)(i & 7)) << 4);
             const float2 rqk = *reinterpret_cast<const float2*>(misc + M_RQK + 2 * (16 * a + i));
-            const float q = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(qk + off)) *
-                            rqk.x;
-            const float k = __bfloat162float(
-                                *reinterpret_cast<const __nv_bfloat16*>(qk + OFF_K - OFF_Q + off)) *
-                            rqk.y;
+            const uint16_t qw = *reinterpret_cast<const uint16_t*>(qk + off);
+            const uint16_t kw = *reinterpret_cast<const uint16_t*>(qk + OFF_K - OFF_Q + off);
+            const float q = (kConv ? __half2float(__ushort_as_half(qw))
+                                   : __uint_as_float((uint32_t)qw << 16)) * rqk.x;
+            const float k = (kConv ? __half2float(__ushort_as_half(kw))
+                                   : __uint_as_float((uint32_t)kw << 16)) * rqk.y;
             qt[i] = q * F[i];
             kq[i] = k * F[i];
             kt[i] = k * E[i];
@@ -1010,7 +1027,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // every lane runs it (its shuffles need the whole warp); after a timeout
         // the values are not used
-        if (kConv) conv_tiles(sm, P, h, warp, lane);
+        if (kConv) conv_tiles(sm, P, h, warp, lane, absmax);
         norms_and_beta(t0 + kC, min(kC, eos - t0 - kC));
       }
       ok = wait_bar(bar_mma, ph_mma, P.spin_cycles);

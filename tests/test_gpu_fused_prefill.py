@@ -1,8 +1,8 @@
 """kda_chunk_fwd_fused: the chunked prefill over raw q, k with the short
 convolution + Swish fused into the tensor-core kernel, against the oracle
 composition (oracle.short_conv of q and k from each sequence's convolution
-state, then the fp64 recurrence on the results), and against the two
-separate calls (kda_short_conv, then kda_chunk_fwd).  The convolution states
+state, then the fp64 recurrence on its unrounded results), and against the
+two separate calls (kda_short_conv, then kda_chunk_fwd).  The convolution states
 left behind are each sequence's last raw inputs, compared bit for bit."""
 import numpy as np
 import pytest
@@ -36,15 +36,13 @@ def _conv_inputs(N, H, W, seed):
 
 
 def _oracle(p, wq, wk, sq, sk, z=None, a_log=None):
-    """The composition the fused call computes: the convolution (fp64) with its
-    output in the io dtype -- the form in which kda_short_conv hands q and k
-    to the prefill -- then the fp64 recurrence."""
+    """The composition the fused call computes: the convolution + Swish
+    (fp64), then the fp64 recurrence on its unrounded results."""
     cu = p.cu_seqlens_host
     W = wq.shape[-1]
     qy, fq = oracle.short_conv(p.q, wq, cu, sq.cpu() if W > 1 else None)
     ky, fk = oracle.short_conv(p.k, wk, cu, sk.cpu() if W > 1 else None)
-    io = lambda y: torch.from_numpy(y).to(p.q.dtype)
-    o, f, _ = oracle.recurrent(io(qy), io(ky), p.v, p.z if z is None else z, p.beta, cu,
+    o, f, _ = oracle.recurrent(qy, ky, p.v, p.z if z is None else z, p.beta, cu,
                                p.initial_state, a_log=a_log)
     return o, f, fq, fk
 
@@ -142,7 +140,8 @@ def test_fused_prefill_full_prefill_workload():
 
 def test_fused_prefill_equals_separate_calls_on_the_varlen_workload():
     """The bench workload (64 sequences, 32 heads): the fused call against
-    kda_short_conv of q and k followed by kda_chunk_fwd.  Each path is within
+    kda_short_conv of q and k followed by kda_chunk_fwd (which hands the
+    convolved q, k over in bf16, the fused call in fp16).  Each path is within
     the bf16 bounds of the oracle, so the two differ by at most their sum
     (rel-L2 2e-2, max|err| 4e-2 RMS)."""
     p = workloads.prefill_workload("varlen", device=DEV)
