@@ -123,7 +123,7 @@ __device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<floa
 
 // Stage the inputs of tokens [t0, t0 + len) of head h: eight threads per
 // token, 16 channels each.  Rows at or past len are zero.
-template <typename T>
+template <typename T, bool kZHead>
 __device__ void stage_block(Smem& sm, const Params& P, int h, int t0, int len, float zc,
                             bool with_q) {
   const int t = threadIdx.x >> 3, part = threadIdx.x & 7, c0 = 16 * part;
@@ -153,7 +153,7 @@ __device__ void stage_block(Smem& sm, const Params& P, int h, int t0, int len, f
     if (part == 0) (pass == 0 ? sm.rq : sm.rk)[t] = r;
   }
   // alpha = e^g, g = -5 sigmoid(s z)
-  if (live && P.zhead) {
+  if (live && kZHead) {
     const float zz = __ldg(P.z + (size_t)(t0 + t) * P.H + h);
 #pragma unroll
     for (int i = 0; i < 16; ++i) y[i] = zz;
@@ -254,7 +254,8 @@ __device__ __forceinline__ float4 fwd_token(Smem& sm, float (&s)[8][4], int t, i
   return e;
 }
 
-template <typename T>
+// kZHead: one gate logit per (token, head) (z and dz [T, H]).
+template <typename T, bool kZHead>
 __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Params P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
     for (int b0 = 0; b0 < len; b0 += kBlk) {
       const int bl = min(kBlk, len - b0);
       __syncthreads();  // the previous block's rows are no longer read
-      stage_block<T>(sm, P, h, bos + b0, bl, zc, false);
+      stage_block<T, kZHead>(sm, P, h, bos + b0, bl, zc, false);
       __syncthreads();
       for (int i = 0; i < bl; ++i) {
         const int t = b0 + i;
@@ -314,8 +315,8 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
     for (int bi = nblk - 1; bi >= 0; --bi) {
       const int b0 = bi * kBlk, bl = min(kBlk, len - b0);
       __syncthreads();
-      stage_block<T>(sm, P, h, bos + b0, bl, zc, true);
-      if (P.zhead && tid < kBlk) sm.dzh[tid] = 0.f;
+      stage_block<T, kZHead>(sm, P, h, bos + b0, bl, zc, true);
+      if (kZHead && tid < kBlk) sm.dzh[tid] = 0.f;
       __syncthreads();
       for (int j0 = ((bl - 1) / kSub) * kSub; j0 >= 0; j0 -= kSub) {
         const int sl = min(kSub, bl - j0);
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
             sm.v[t][c] = dkh;  // this token's v is no longer read
             const float a = sm.al[t][c], g = __logf(a);
             const float dzc = dal * a * g * (1.f + g / 5.f) * zs;
-            if (P.zhead) {  // the head's one logit feeds every channel: sum the terms
+            if (kZHead) {  // the head's one logit feeds every channel: sum the terms
               const float sum = warp_sum(dzc);
               if ((tid & 31) == 0) atomicAdd(&sm.dzh[t], sum);
             } else {
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
           }
           if (live && part == 0) {
             P.dbeta[(size_t)(bos + b0 + t) * P.H + h] = sm.db[t];
-            if (P.zhead) P.dz[(size_t)(bos + b0 + t) * P.H + h] = sm.dzh[t];
+            if (kZHead) P.dz[(size_t)(bos + b0 + t) * P.H + h] = sm.dzh[t];
           }
         }
       }
@@ -523,12 +524,15 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
   if (p.num_seqs == 0) return cudaSuccess;
   static PerDeviceInit attrs;
   const cudaError_t attr = attrs.run([] {
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<float>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(Smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+    cudaError_t e = cudaSuccess;
+    const void* kernels[] = {(const void*)bwd_kernel<float, false>,
+                             (const void*)bwd_kernel<__nv_bfloat16, false>,
+                             (const void*)bwd_kernel<float, true>,
+                             (const void*)bwd_kernel<__nv_bfloat16, true>};
+    for (const void* kf : kernels)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(Smem));
     return e;
   });
   if (attr != cudaSuccess) return attr;
@@ -569,9 +573,11 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
   }
   const int grid = grid_for(p);
   if (p.io_bf16)
-    bwd_kernel<__nv_bfloat16><<<grid, kNT, sizeof(Smem), st>>>(prm);
+    prm.zhead ? bwd_kernel<__nv_bfloat16, true><<<grid, kNT, sizeof(Smem), st>>>(prm)
+              : bwd_kernel<__nv_bfloat16, false><<<grid, kNT, sizeof(Smem), st>>>(prm);
   else
-    bwd_kernel<float><<<grid, kNT, sizeof(Smem), st>>>(prm);
+    prm.zhead ? bwd_kernel<float, true><<<grid, kNT, sizeof(Smem), st>>>(prm)
+              : bwd_kernel<float, false><<<grid, kNT, sizeof(Smem), st>>>(prm);
   return cudaGetLastError();
 }
 

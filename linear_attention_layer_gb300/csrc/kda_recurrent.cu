@@ -413,22 +413,40 @@ recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
   float* qs = sh[w][0];
   float* ks = sh[w][1];
   float* as = sh[w][2];
+  // this lane's inputs of the next token, loaded one token ahead so that a
+  // token's global-memory latency hides behind the previous token's work
+  float nq[CPL], nk[CPL], nz[CPL], nv = 0.f, nb = 0.f;
+  auto fetch = [&](int t) {
+    if (t >= eos) return;
+    const size_t th = (size_t)t * H + h;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      nq[i] = IO<T>::ld(q + th * DK + c);
+      nk[i] = IO<T>::ld(k + th * DK + c);
+      nz[i] = __ldg(z + th * (zhead ? 1 : DK) + (zhead ? 0 : c));
+    }
+    nv = IO<T>::ld(v + th * DV + lane);
+    nb = __ldg(beta + th);
+  };
+  fetch(bos);
   for (int t = bos; t < eos; ++t) {
     const size_t th = (size_t)t * H + h;
     float qq = 0.f, kk = 0.f, kq = 0.f;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int c = lane + 32 * i;
-      const float a = IO<T>::ld(q + th * DK + c), b = IO<T>::ld(k + th * DK + c);
+      const float a = nq[i], b = nk[i];
       qs[c] = a;
       ks[c] = b;
-      as[c] = __expf(log_decay(zscale * __ldg(z + th * (zhead ? 1 : DK) + (zhead ? 0 : c))));
+      as[c] = __expf(log_decay(zscale * nz[i]));
       qq += a * a;
       kk += b * b;
       kq += a * b;
     }
-    const float vj = IO<T>::ld(v + th * DV + lane);
-    const float bt = __ldg(beta + th);
+    const float vj = nv;
+    const float bt = nb;
+    fetch(t + 1);
     qq = warp_sum(qq);
     kk = warp_sum(kk);
     kq = warp_sum(kq);

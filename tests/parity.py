@@ -178,3 +178,20 @@ def device_compare(x, ref, both_stored=False):
     rms = torch.sqrt(torch.mean(rd * rd))
     mx = float(err.max()) if err.numel() else 0.0
     return rel, (mx / float(rms) if float(rms) > 0 else mx)
+
+
+def problem_pieces(p, max_head_tokens=1 << 21):
+    """(sequence range, head range) pieces covering a packed Problem p, each
+    about max_head_tokens head-tokens of oracle work: groups of whole
+    sequences, or groups of heads of a single sequence."""
+    cu, H = p.cu_seqlens_host, p.meta["num_heads"]
+    if p.num_seqs == 1:
+        hs = max(1, min(H, max_head_tokens // max(cu[1], 1)))
+        return [((0, 1), (h, min(H, h + hs))) for h in range(0, H, hs)]
+    out, n0, tok = [], 0, 0
+    for n in range(p.num_seqs):
+        tok += (cu[n + 1] - cu[n]) * H
+        if tok >= max_head_tokens or n + 1 == p.num_seqs:
+            out.append(((n0, n + 1), (0, H)))
+            n0, tok = n + 1, 0
+    return out

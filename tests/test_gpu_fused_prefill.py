@@ -11,7 +11,7 @@ import torch
 import linear_attention_layer_gb300 as kda
 import oracle
 import workloads
-from tests.parity import assert_close, device_compare
+from tests.parity import WholeTensorError, assert_close, problem_pieces, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -138,26 +138,39 @@ def test_fused_prefill_full_prefill_workload():
     assert torch.equal(sq.cpu(), torch.from_numpy(fq).float())
 
 
-def test_fused_prefill_equals_separate_calls_on_the_varlen_workload():
-    """The bench workload (64 sequences, 32 heads): the fused call against
-    kda_short_conv of q and k followed by kda_chunk_fwd (which hands the
-    convolved q, k over in bf16, the fused call in fp16).  Each path is within
-    the bf16 bounds of the oracle, so the two differ by at most their sum
-    (rel-L2 2e-2, max|err| 4e-2 RMS)."""
+def test_fused_prefill_full_varlen_workload():
+    """The bench workload (64 sequences of 256..8192 tokens, 32 heads, initial
+    states) through the fused call, every output and final state against the
+    oracle composition (run piece by piece), and against the separate calls:
+    kda_short_conv hands the convolved q, k over in bf16 where the fused call
+    keeps fp16, so the two are compared by relative L2 error only (the max
+    error of that comparison measures the bf16 rounding of q and k)."""
     p = workloads.prefill_workload("varlen", device=DEV)
-    wq, wk, sq, sk = _conv_inputs(p.num_seqs, 32, 4, 89)
-    sq_s, sk_s = sq.clone(), sk.clone()
-    yq, fq = kda.short_conv(p.q, wq, p.cu_seqlens, sq_s)
-    yk, fk = kda.short_conv(p.k, wk, p.cu_seqlens, sk_s)
-    o_sep, f_sep = kda.chunk_fwd(yq, yk, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
-                                 cu_seqlens_host=p.cu_seqlens_host)
+    H = p.meta["num_heads"]
+    wq, wk, sq, sk = _conv_inputs(p.num_seqs, H, 4, 89)
+    sq0, sk0 = sq.clone(), sk.clone()
     o_f, f_f = kda.chunk_fwd_fused(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
                                    conv_weight_q=wq, conv_weight_k=wk, conv_state_q=sq,
                                    conv_state_k=sk, cu_seqlens_host=p.cu_seqlens_host)
+    yq, fq = kda.short_conv(p.q, wq, p.cu_seqlens, sq0)
+    yk, fk = kda.short_conv(p.k, wk, p.cu_seqlens, sk0)
+    o_s, f_s = kda.chunk_fwd(yq, yk, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
     torch.cuda.synchronize()
     assert kda.get_device_error() == 0
-    for x, r, what, both in ((o_f, o_sep, "out", True), (f_f, f_sep, "final", False)):
-        rel, mx = device_compare(x, r, both_stored=both)
-        print(f"fused vs separate, varlen {what}: rel-L2 {rel:.3e}, max/RMS {mx:.3e}")
-        assert rel <= 2e-2 and mx <= 4e-2, (what, rel, mx)
     assert torch.equal(sq, fq) and torch.equal(sk, fk)
+    assert rel_l2(o_f, o_s) <= 1e-2 and rel_l2(f_f, f_s) <= 1e-2
+    cu = p.cu_seqlens_host
+    acc_o, acc_f = WholeTensorError(H, torch.bfloat16), WholeTensorError(H)
+    wqc, wkc = wq.cpu(), wk.cpu()
+    for (n0, n1), _ in problem_pieces(p):
+        a, b = cu[n0], cu[n1]
+        lcu = [x - a for x in cu[n0:n1 + 1]]
+        qy, _ = oracle.short_conv(p.q[a:b].cpu(), wqc, lcu, sq0[n0:n1].cpu())
+        ky, _ = oracle.short_conv(p.k[a:b].cpu(), wkc, lcu, sk0[n0:n1].cpu())
+        ro, rf, _ = oracle.recurrent(qy, ky, p.v[a:b].cpu(), p.z[a:b].cpu(), p.beta[a:b].cpu(),
+                                     lcu, p.initial_state[n0:n1].cpu())
+        acc_o.add(o_f[a:b].cpu(), ro, head_axis=1)
+        acc_f.add(f_f[n0:n1].cpu(), rf, head_axis=1)
+    print(acc_o.check(torch.bfloat16, "fused varlen out"))
+    print(acc_f.check(torch.bfloat16, "fused varlen final state"))

@@ -9,7 +9,7 @@ import torch
 import linear_attention_layer_gb300 as kda
 import oracle
 import workloads
-from tests.parity import WholeTensorError, assert_close, rel_l2
+from tests.parity import WholeTensorError, assert_close, problem_pieces, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -499,29 +499,13 @@ def test_state_checkpoints_with_split_sequences():
 # per-head value and max|err| / RMS over the whole tensor are accumulated
 # across the pieces and checked at the end.
 
-def _pieces(p, max_head_tokens=1 << 21):
-    """(sequence range, head range) pieces covering Problem p, each about
-    max_head_tokens head-tokens of oracle work."""
-    cu, H = p.cu_seqlens_host, p.meta["num_heads"]
-    if p.num_seqs == 1:
-        hs = max(1, min(H, max_head_tokens // max(cu[1], 1)))
-        return [((0, 1), (h, min(H, h + hs))) for h in range(0, H, hs)]
-    out, n0, tok = [], 0, 0
-    for n in range(p.num_seqs):
-        tok += (cu[n + 1] - cu[n]) * H
-        if tok >= max_head_tokens or n + 1 == p.num_seqs:
-            out.append(((n0, n + 1), (0, H)))
-            n0, tok = n + 1, 0
-    return out
-
-
 def _full_check(p, results, io_dtype=torch.bfloat16):
     """results: {label: (out, final_state)} of GPU runs on Problem p; each is
     compared with the oracle over every (sequence, head)."""
     H = p.meta["num_heads"]
     cu = p.cu_seqlens_host
     acc = {lab: (WholeTensorError(H, io_dtype), WholeTensorError(H)) for lab in results}
-    for (n0, n1), (h0, h1) in _pieces(p):
+    for (n0, n1), (h0, h1) in problem_pieces(p):
         a, b = cu[n0], cu[n1]
         sl = lambda x: x[a:b, h0:h1].cpu()
         s0 = None if p.initial_state is None else p.initial_state[n0:n1, h0:h1].cpu()
