@@ -339,8 +339,7 @@ kda_status_t kda_decode_replay_window_fused(
  *                      (KDA_ERR_UNSUPPORTED): the output norm belongs to the
  *                      decode-side calls.
  * Other arguments, options (workspace split, checkpoints, a_log,
- * gate_per_head) and errors as for kda_chunk_fwd.  The convolution's Swish
- * uses the hardware tanh (sigmoid(u) = (1 + tanh(u/2)) / 2) and its outputs
+ * gate_per_head) and errors as for kda_chunk_fwd.  The convolved q and k
  * stay in fp16 inside the kernel (finer than the bf16 that kda_short_conv
  * writes); a convolved value of magnitude 65504 or more sets
  * KDA_ERR_DEVICE_CHECK, like the tensor-core path's other fp16 operands.
@@ -444,9 +443,12 @@ kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* b
  * rebuilt forward from states the call itself keeps every 8 tokens in the
  * workspace.
  *
- *   desc               as for kda_chunk_fwd; dk = dv = 128 (else
- *                      KDA_ERR_UNSUPPORTED); gate_per_head = 1 takes z [T_tot,
- *                      H] and gives dz [T_tot, H] (the per-channel terms summed);
+ *   desc               as for kda_chunk_fwd; any supported dk, dv (below 128
+ *                      the inputs are zero-padded to 128 channels inside the
+ *                      workspace, which changes no gradient of the real
+ *                      channels and costs the work of dk = dv = 128);
+ *                      gate_per_head = 1 takes z [T_tot, H] and gives dz
+ *                      [T_tot, H] (the per-channel terms summed);
  *                      cu_seqlens_host is REQUIRED; workspace /
  *                      workspace_bytes must hold
  *                      kda_recurrent_bwd_workspace_size() bytes (16-byte
@@ -456,9 +458,10 @@ kda_status_t kda_chunk_fwd_host_workspace_size(const kda_desc_t* desc, size_t* b
  *                      the forward call's inputs (initial_state may be NULL)
  *   d_out              device, [T_tot, H, dv] io dtype: dL/d out
  *   d_final_state      device, [N, H, dk, dv] fp32, or NULL for zeros
- *   dq, dk, dv, dz     device, [T_tot, H, 128] fp32 (dz [T_tot, H] with one
+ *   dq, dk, dz         device, [T_tot, H, dk] fp32 (dz [T_tot, H] with one
  *                      gate per head), written (dz is the gradient w.r.t. the
  *                      gate logits z as passed)
+ *   dv                 device, [T_tot, H, dv] fp32, written
  *   dbeta              device, [T_tot, H] fp32, written
  *   d_initial_state    device, [N, H, dk, dv] fp32, written, or NULL
  * Every pointer to per-token or state data must be 16-byte aligned, and no
@@ -475,7 +478,8 @@ kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void
 
 /* Bytes of device workspace kda_recurrent_bwd needs for this descriptor
  * (needs desc->cu_seqlens_host): for every resident CTA (at most one per
- * SM) 64 KiB per 8 tokens of the longest sequence, plus 512 KiB. */
+ * SM) 64 KiB per 8 tokens of the longest sequence, plus 512 KiB; below
+ * dk = dv = 128 also the zero-padded copies of the inputs and gradients. */
 kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
 
 /*

@@ -454,10 +454,10 @@ def short_conv(x, weight, cu_seqlens, conv_state=None, *, out=None, final_state=
     return out, final_state
 
 
-def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host):
-    """Bytes of device workspace ``recurrent_bwd`` needs (dk = dv = 128)."""
+def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host, dk=128, dv=128):
+    """Bytes of device workspace ``recurrent_bwd`` needs."""
     N = len(cu_seqlens_host) - 1
-    desc, keep = make_desc(N, int(cu_seqlens_host[-1]), num_heads, 128, 128, _io_code(dtype),
+    desc, keep = make_desc(N, int(cu_seqlens_host[-1]), num_heads, dk, dv, _io_code(dtype),
                            cu_seqlens_host)
     n = ctypes.c_size_t(0)
     st = load().kda_recurrent_bwd_workspace_size(ctypes.byref(desc), ctypes.byref(n))
@@ -472,7 +472,7 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     """Reverse mode of the prefill (``kda_recurrent_bwd``): given dL/d out and
     dL/d final_state (None: zeros), returns (dq, dk, dv, dz, dbeta,
     d_initial_state), fp32, for the inputs of the forward call (same q, k, v,
-    z, beta, cu_seqlens, initial_state and a_log; dk = dv = 128).  ``z`` [T, H]
+    z, beta, cu_seqlens, initial_state and a_log; any supported dk, dv).  ``z`` [T, H]
     (one gate per head) gives dz [T, H].  ``cu_seqlens_host`` is required; ``workspace`` (a device
     tensor of ``recurrent_bwd_workspace_size`` bytes) is allocated here when
     None; ``grads`` may give the six output tensors to fill."""
@@ -505,7 +505,7 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     for name, g, shp in zip(("dq", "dk", "dv", "dz", "dbeta", "d_initial"), grads, shapes):
         _check_tensor(name, g, torch.float32, shp, dev)
     if workspace is None:
-        nbytes = recurrent_bwd_workspace_size(H, q.dtype, cu_seqlens_host)
+        nbytes = recurrent_bwd_workspace_size(H, q.dtype, cu_seqlens_host, dk, dv)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
     desc.gate_per_head = 1 if per_head else 0

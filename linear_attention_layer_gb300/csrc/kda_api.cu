@@ -112,7 +112,7 @@ kda_status_t check_bwd(const kda_desc_t* desc, const void* q, const void* k, con
   if (s != KDA_OK) return s;
   if (!desc->cu_seqlens_host || !cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
   if (desc->gate_per_head != 0 && desc->gate_per_head != 1) return KDA_ERR_INVALID_ARGUMENT;
-  if (desc->dk != 128 || desc->dv != 128) return KDA_ERR_UNSUPPORTED;
+
   if (desc->total_tokens > 0) {
     const void* need[] = {q, k, v, z, beta, d_out, dq, dk, dv, dz, dbeta};
     for (const void* x : need)

@@ -512,14 +512,162 @@ long long states_per_cta(const Problem& p, const int32_t* cu_host) {
 
 }  // namespace bwd
 
-size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host) {
+namespace bwd {
+
+// ---- dk or dv below 128: zero-padded to 128 channels around the kernel ----
+//
+// A key channel whose q, k are zero keeps a zero state row (its k never
+// reaches the rank-one updates, and its decay acts on zeros); a value channel
+// whose v is zero keeps a zero state column; zeros change no L2 norm.  So the
+// 128 x 128 reverse mode over zero-padded inputs gives exactly the gradients of
+// the real channels (those of the padded ones are zero and dropped).
+
+template <typename T>
+__global__ void pad_rows_kernel(T* __restrict__ dst, const T* __restrict__ src, long long rows,
+                                int d) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= rows * kD) return;
+  const long long r = i / kD;
+  const int c = (int)(i % kD);
+  dst[i] = c < d ? src[r * d + c] : T(0.f);
+}
+
+__global__ void unpad_rows_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                  long long rows, int d) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= rows * d) return;
+  dst[i] = src[(i / d) * kD + i % d];
+}
+
+// [NH][dk][dv] <-> [NH][128][128]
+__global__ void pad_state_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                 long long nh, int dk, int dv) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= nh * kD * kD) return;
+  const long long u = i / (kD * kD);
+  const int c = (int)((i / kD) % kD), n = (int)(i % kD);
+  dst[i] = (c < dk && n < dv) ? src[(u * dk + c) * dv + n] : 0.f;
+}
+
+__global__ void unpad_state_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                   long long nh, int dk, int dv) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= nh * dk * dv) return;
+  const long long u = i / ((long long)dk * dv);
+  const int c = (int)((i / dv) % dk), n = (int)(i % dv);
+  dst[i] = src[(u * kD + c) * kD + n];
+}
+
+inline unsigned blocks_for(long long n) { return (unsigned)((n + 255) / 256); }
+
+// Device layout of the padded inputs and outputs inside the workspace, ahead
+// of the 128 x 128 kernel's own workspace.
+struct PadLayout {
+  size_t q, k, v, dout, z, s0, dfin, dq, dk, dv, dz, dini, inner, total;
+};
+inline size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+PadLayout pad_layout(const Problem& p) {
+  const size_t th = (size_t)p.total_tokens * p.num_heads, es = p.io_bf16 ? 2 : 4;
+  const size_t st = (size_t)p.num_seqs * p.num_heads * kD * kD * 4;
+  PadLayout L;
+  size_t o = 0;
+  L.q = o; o += up256(th * kD * es);
+  L.k = o; o += up256(th * kD * es);
+  L.v = o; o += up256(th * kD * es);
+  L.dout = o; o += up256(th * kD * es);
+  L.z = o; o += up256(th * kD * 4);
+  L.s0 = o; o += up256(st);
+  L.dfin = o; o += up256(st);
+  L.dq = o; o += up256(th * kD * 4);
+  L.dk = o; o += up256(th * kD * 4);
+  L.dv = o; o += up256(th * kD * 4);
+  L.dz = o; o += up256(th * kD * 4);
+  L.dini = o; o += up256(st);
+  L.inner = o;
+  L.total = o;
+  return L;
+}
+
+}  // namespace bwd
+
+static size_t bwd_inner_bytes(const Problem& p, const int32_t* cu_host) {
   if (p.num_seqs == 0 || p.num_heads == 0) return 0;
   return (size_t)bwd::grid_for(p) * (size_t)bwd::states_per_cta(p, cu_host) * bwd::kState *
          sizeof(float);
 }
 
+size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host) {
+  if (p.num_seqs == 0 || p.num_heads == 0) return 0;
+  if (p.dk == bwd::kD && p.dv == bwd::kD) return bwd_inner_bytes(p, cu_host);
+  return bwd::pad_layout(p).total + bwd_inner_bytes(p, cu_host);
+}
+
+static cudaError_t launch_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                  void* ws, cudaStream_t st);
+
 cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
                                  void* ws, cudaStream_t st) {
+  using namespace bwd;
+  if (p.num_seqs == 0) return cudaSuccess;
+  if (p.dk == kD && p.dv == kD) return launch_bwd_128(p, a, cu_host, ws, st);
+  const PadLayout L = pad_layout(p);
+  unsigned char* W = static_cast<unsigned char*>(ws);
+  const long long th = (long long)p.total_tokens * p.num_heads;
+  const long long nh = (long long)p.num_seqs * p.num_heads;
+  Problem p128 = p;
+  p128.dk = p128.dv = kD;
+  BwdArgs b = a;
+  auto pad = [&](size_t off, const void* src, int d) {
+    if (p.io_bf16)
+      pad_rows_kernel<__nv_bfloat16><<<blocks_for(th * kD), 256, 0, st>>>(
+          reinterpret_cast<__nv_bfloat16*>(W + off), static_cast<const __nv_bfloat16*>(src), th, d);
+    else
+      pad_rows_kernel<float><<<blocks_for(th * kD), 256, 0, st>>>(
+          reinterpret_cast<float*>(W + off), static_cast<const float*>(src), th, d);
+    return reinterpret_cast<const void*>(W + off);
+  };
+  if (th > 0) {
+    b.q = pad(L.q, a.q, p.dk);
+    b.k = pad(L.k, a.k, p.dk);
+    b.v = pad(L.v, a.v, p.dv);
+    b.d_out = pad(L.dout, a.d_out, p.dv);
+    if (!a.zhead) {
+      pad_rows_kernel<float><<<blocks_for(th * kD), 256, 0, st>>>(
+          reinterpret_cast<float*>(W + L.z), a.z, th, p.dk);
+      b.z = reinterpret_cast<const float*>(W + L.z);
+    }
+  }
+  auto pad_state = [&](size_t off, const float* src) -> const float* {
+    if (!src) return nullptr;
+    pad_state_kernel<<<blocks_for(nh * kD * kD), 256, 0, st>>>(
+        reinterpret_cast<float*>(W + off), src, nh, p.dk, p.dv);
+    return reinterpret_cast<const float*>(W + off);
+  };
+  b.initial_state = pad_state(L.s0, a.initial_state);
+  b.d_final = pad_state(L.dfin, a.d_final);
+  b.dq = reinterpret_cast<float*>(W + L.dq);
+  b.dk = reinterpret_cast<float*>(W + L.dk);
+  b.dv = reinterpret_cast<float*>(W + L.dv);
+  if (!a.zhead) b.dz = reinterpret_cast<float*>(W + L.dz);  // one gate per head: [T, H] as is
+  b.d_initial = a.d_initial ? reinterpret_cast<float*>(W + L.dini) : nullptr;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_bwd_128(p128, b, cu_host, W + L.inner, st);
+  if (e != cudaSuccess) return e;
+  if (th > 0) {
+    unpad_rows_kernel<<<blocks_for(th * p.dk), 256, 0, st>>>(a.dq, b.dq, th, p.dk);
+    unpad_rows_kernel<<<blocks_for(th * p.dk), 256, 0, st>>>(a.dk, b.dk, th, p.dk);
+    unpad_rows_kernel<<<blocks_for(th * p.dv), 256, 0, st>>>(a.dv, b.dv, th, p.dv);
+    if (!a.zhead) unpad_rows_kernel<<<blocks_for(th * p.dk), 256, 0, st>>>(a.dz, b.dz, th, p.dk);
+  }
+  if (a.d_initial)
+    unpad_state_kernel<<<blocks_for(nh * p.dk * p.dv), 256, 0, st>>>(a.d_initial, b.d_initial,
+                                                                    nh, p.dk, p.dv);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                  void* ws, cudaStream_t st) {
   using namespace bwd;
   if (p.num_seqs == 0) return cudaSuccess;
   static PerDeviceInit attrs;

@@ -109,7 +109,10 @@ constexpr uint32_t OFF_BAR = OFF_MISC + M_END * 4;  // 3 mbarriers + tmem slot
 // (fused convolution) the last three raw inputs before the chunk, fp32
 // [q, k][3 tokens, oldest first][128 channels]
 constexpr uint32_t OFF_HALO = OFF_BAR + 64;
-constexpr uint32_t SMEM_BYTES = OFF_HALO + 2 * 3 * 128 * 4 + 1024;  // + alignment slack
+// (fused convolution) the head's taps, right-aligned: fp32 [q, k][128 channels][4]
+constexpr uint32_t OFF_TAPS = OFF_HALO + 2 * 3 * 128 * 4;
+constexpr uint32_t SMEM_BYTES = OFF_HALO + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES_CONV = OFF_TAPS + 2 * 128 * 4 * 4 + 1024;  // kConv variant
 
 // ---- Tensor Memory columns (all 128 lanes) ----
 constexpr uint32_t TS32 = 0;    // S^T fp32   [n][c]   128 cols
@@ -343,20 +346,19 @@ __device__ __forceinline__ float tile_hi(uint32_t x) {
 // uses the last W of four (the others zero).  The results are stored as fp16
 // (11-bit significand; the raw inputs were bf16), so the tiles lose less than
 // an output stored in the io dtype would; absmax tracks the fp16 range.
+// Swish is evaluated as u / (1 + e^-u): the form through tanh(u/2) costs one
+// multi-function op less but loses |u| 2^-12 absolutely to cancellation in
+// 1 + tanh for negative u.
 __device__ __forceinline__ void conv_tiles(unsigned char* sm, const Params& P, int h, int warp,
                                            int lane, float& absmax) {
   const int tens = warp & 1, blk = (warp >> 1) & 1, qt = warp >> 2;
   const int c0 = 64 * blk + 2 * lane;
   unsigned char* tile = sm + (tens ? OFF_K : OFF_Q) + blk * 8192;
   float* halo = reinterpret_cast<float*>(sm + OFF_HALO) + tens * 384;
-  const float* wsrc = (tens ? P.conv_wk : P.conv_wq) + ((size_t)h * kD + c0) * P.conv_w;
-  float ta[4], tb[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int tj = j - (4 - P.conv_w);
-    ta[j] = tj >= 0 ? __ldg(wsrc + tj) : 0.f;
-    tb[j] = tj >= 0 ? __ldg(wsrc + P.conv_w + tj) : 0.f;
-  }
+  const float4 t4a = reinterpret_cast<const float4*>(sm + OFF_TAPS)[tens * 128 + c0];
+  const float4 t4b = reinterpret_cast<const float4*>(sm + OFF_TAPS)[tens * 128 + c0 + 1];
+  const float ta[4] = {t4a.x, t4a.y, t4a.z, t4a.w};
+  const float tb[4] = {t4b.x, t4b.y, t4b.z, t4b.w};
   const uint32_t xo = (((uint32_t)lane & 3) << 2);
   auto word = [&](int t) -> uint32_t* {
     return reinterpret_cast<uint32_t*>(tile + t * 128 + (((((uint32_t)lane >> 2)) ^ (uint32_t)(t & 7)) << 4) + xo);
@@ -382,15 +384,22 @@ __device__ __forceinline__ void conv_tiles(unsigned char* sm, const Params& P, i
       halo[j * 128 + c0 + 1] = xb[16 + j];
     }
   }
+  __half2 hmax = __float2half2_rn(0.f);  // largest |y| of the pair, for the fp16 range check
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float ua = fmaf(ta[0], xa[i], fmaf(ta[1], xa[i + 1], fmaf(ta[2], xa[i + 2], ta[3] * xa[i + 3])));
     const float ub = fmaf(tb[0], xb[i], fmaf(tb[1], xb[i + 1], fmaf(tb[2], xb[i + 2], tb[3] * xb[i + 3])));
-    const float ya = swish_tanh(ua), yb = swish_tanh(ub);
-    absmax = fmaxf(absmax, fmaxf(fabsf(ya), fabsf(yb)));
-    *word(16 * qt + i) = pack_f16(ya, yb);
+    // swish u sigmoid(u) = u / (1 + e^-u)
+    const __half2 y2 = __floats2half2_rn(__fdividef(ua, 1.f + __expf(-ua)),
+                                         __fdividef(ub, 1.f + __expf(-ub)));
+    hmax = __hmax2(hmax, __habs2(y2));
+    *word(16 * qt + i) = *reinterpret_cast<const uint32_t*>(&y2);
   }
-  __syncthreads();  // the converted tiles are complete
+  absmax = fmaxf(absmax, fmaxf(__low2float(hmax), __high2float(hmax)));
+  // the converted tiles are complete for warps 0-7, which compute the token
+  // norms next; warps 8-15 only signal (the next block barrier orders them)
+  if (warp < 8) asm volatile("bar.sync 2, 512;" ::: "memory");
+  else asm volatile("bar.arrive 2, 512;" ::: "memory");
 }
 
 // kZHead: one gate logit per (token, head) (P.zh) instead of z tiles per channel.
@@ -509,6 +518,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_st_wait();
     }
     if (kConv && tid < 256) {
+      // the head's taps, right-aligned (width W uses the last W of four)
+      {
+        const int tens = tid >> 7, c = tid & 127;
+        const float* wsrc = (tens ? P.conv_wk : P.conv_wq) + ((size_t)h * kD + c) * P.conv_w;
+        float t4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tj = j - (4 - P.conv_w);
+          t4[j] = tj >= 0 ? __ldg(wsrc + tj) : 0.f;
+        }
+        reinterpret_cast<float4*>(sm + OFF_TAPS)[tens * 128 + c] =
+            make_float4(t4[0], t4[1], t4[2], t4[3]);
+      }
       // the halo before the unit's first chunk: raw inputs bos-3 .. bos-1 of the
       // sequence where they exist (a segment starting inside it), else its
       // incoming convolution state (last W-1 inputs before it), else zeros
@@ -1380,7 +1402,7 @@ struct TcLaunch {
       for (const void* kf : kernels)
         if (e == cudaSuccess)
           e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)SMEM_BYTES);
+                                   (int)SMEM_BYTES_CONV);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(2 * kD * kScanLd * sizeof(float)));
@@ -1439,9 +1461,9 @@ struct TcLaunch {
   void launch(const Params& prm, int grid) const {
     if (prm.conv_w > 0) {
       if (per_head)
-        chunk_tc_kernel<true, true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+        chunk_tc_kernel<true, true><<<grid, kNT, SMEM_BYTES_CONV, st>>>(mq, mk, mv, mz, prm);
       else
-        chunk_tc_kernel<false, true><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
+        chunk_tc_kernel<false, true><<<grid, kNT, SMEM_BYTES_CONV, st>>>(mq, mk, mv, mz, prm);
     } else if (per_head) {
       chunk_tc_kernel<true, false><<<grid, kNT, SMEM_BYTES, st>>>(mq, mk, mv, mz, prm);
     } else {

@@ -62,21 +62,6 @@ __device__ __forceinline__ float log_decay_c(float z, float c) {
   return __fdividef(kGateMin, 1.0f + ex2_approx(c * z));
 }
 
-// tanh by the hardware's approximate instruction (tanh.approx.f32, relative
-// error about 2^-11).
-__device__ __forceinline__ float tanh_approx(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Swish u sigmoid(u) through the identity sigmoid(u) = (1 + tanh(u/2)) / 2:
-// one multi-function instruction per value.
-__device__ __forceinline__ float swish_tanh(float u) {
-  const float h = 0.5f * u;
-  return fmaf(h, tanh_approx(h), h);
-}
-
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -173,3 +173,29 @@ def test_backward_gate_per_head(dtype):
                                d_out, d_fin, a_log=A))
     ref[3] = ref[3].sum(axis=-1)
     _compare(got, ref)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (64, 32)])
+def test_backward_small_dims(dk, dv):
+    """dk or dv below 128 (zero-padded to 128 channels around the kernel):
+    every gradient against the oracle, with the gate log-scale, and with one
+    gate per head."""
+    p = workloads.random_problem(RAGGED, 2, dk, dv, torch.bfloat16, z_std=1.5, init_std=0.1,
+                                 seed=40 + dk + dv, device=DEV)
+    A = torch.tensor([0.4, -0.7])
+    d_out, d_fin = _cotangents(p, 9)
+    got = kda.recurrent_bwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out,
+                            d_fin, cu_seqlens_host=p.cu_seqlens_host, a_log=A.to(DEV))
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    ref = oracle.backward(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state,
+                          d_out, d_fin, a_log=A)
+    _compare(got, ref)
+    zh = p.z[:, :, 0].contiguous()
+    got = kda.recurrent_bwd(p.q, p.k, p.v, zh, p.beta, p.cu_seqlens, None, d_out, None,
+                            cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    zb = zh.cpu()[:, :, None].expand(-1, -1, dk).contiguous()
+    ref = list(oracle.backward(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, None, d_out, None))
+    ref[3] = ref[3].sum(axis=-1)
+    _compare(got, ref)

@@ -703,3 +703,18 @@ def test_small_state_path(dtype, dk):
     ro2, rf2, _ = oracle.recurrent(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, p.initial_state)
     assert_close(out2, ro2, dtype, "per-head gate out")
     assert_close(fin2, rf2, dtype, "per-head gate final_state")
+
+
+def test_many_short_sequences():
+    """More sequences than the tensor-core launcher's longest-first order
+    table holds (6144): 7000 sequences of 0..12 tokens, unsplit and with the
+    workspace offered, against the oracle."""
+    lens = np.random.default_rng(3).integers(0, 13, size=7000).tolist()
+    p = workloads.random_problem(lens, 2, 128, 128, torch.bfloat16, init_std=0.1, seed=34,
+                                 device=DEV)
+    for ws in (None, "auto"):
+        out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                 cu_seqlens_host=p.cu_seqlens_host, workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        _check_all(p, out, fin, torch.bfloat16)
