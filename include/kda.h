@@ -147,9 +147,10 @@ typedef struct {
  * path (other sizes); fp32 inputs always run the fp32 CUDA-core path.
  *
  * Range limit of the tensor-core path: its dense products take fp16
- * operands (11-bit significand, largest magnitude 65504), made from v, the
- * state entering each 64-token chunk, S^T K+^T and the pseudo-values U.  A
- * bf16 v or an fp32 state can exceed that range.  When any such operand
+ * operands (11-bit significand, largest magnitude 65504), made from the
+ * state entering each 64-token chunk, the corrections v - S^T k+ and the
+ * pseudo-values U.  A bf16 v or an fp32 state can exceed that range.  When
+ * any such operand
  * reaches 65504 in magnitude the call's outputs are not valid and the
  * kernel sets KDA_ERR_DEVICE_CHECK in the device error word (read it with
  * kda_get_device_error); the following calls are unaffected.  Data of that

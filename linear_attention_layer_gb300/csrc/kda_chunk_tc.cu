@@ -29,10 +29,12 @@
 // Everything else is kept in the transposed orientation so that the dense
 // tcgen05 GEMMs have M = 128 and the state and U can feed the tensor core
 // straight from Tensor Memory:
-//   W^T = K+^T T'^T,  U~^T = V^T T'^T,  U^T = U~^T - S^T W^T,
+//   Y^T = S^T K+^T,  D^T = V^T - Y^T,  U^T = D^T T'^T,
 //   O^T = S^T Q+^T + U^T P^T,  S^T <- S^T Diag(e^{G_C}) + U^T Khat.
 // S^T (fp32, 128 lanes = value channel) stays resident in TMEM across
-// chunks; its fp16 copy and U^T's are A operands read from TMEM.
+// chunks; its fp16 copy, D^T and U^T are A operands read from TMEM.  D is
+// formed in fp32 before its one rounding: v - S^T k cancels when a key
+// already holds its value.
 //
 // Precision: the Gram products run as tcgen05 kind::tf32 on operands rounded
 // to tf32 once (the e^80 range rules out fp16 there); the dense products
@@ -79,7 +81,7 @@ constexpr int kMaxOrder = 6144;
 constexpr uint32_t OFF_Q = 0;         // q stage: [2 c-blk][64 t][64 c] bf16, SW128 (TMA)
 constexpr uint32_t OFF_K = 16384;     // k stage, same
 constexpr uint32_t OFF_Z = 32768;     // z stage: [64 t][128 c] fp32 (TMA); then G in place
-constexpr uint32_t OFF_V = 65536;     // v stage: [2 n-blk][64 j][64 n] SW128; fp16 in place = MN-major A
+constexpr uint32_t OFF_V = 65536;     // v stage: [2 n-blk][64 j][64 n] bf16 SW128 (TMA); read for D = V - Y
 constexpr uint32_t OFF_G = 81920;     // 80K: Gram A operand, later A / T / T' / P / W^T
 // Gram operands (tf32, K-major, 128-byte swizzle; one region per 32-channel atom):
 //   G_M (A operand, M = 128) over the q / k / z stages: [4 atoms][128 rows][32 c],
@@ -98,6 +100,7 @@ constexpr uint32_t S_AKK = OFF_G;             // A   fp32 [64][kLS]
 constexpr uint32_t S_T32 = OFF_G + 17408;     // T   fp32 [64][kLS]
 constexpr uint32_t S_TP = OFF_G + 34816;      // T'  fp16 [64 t][64 j] SW128: K-major B
 constexpr uint32_t G_P = OFF_G + 43008;       // P   fp16 [64 t][64 j] SW128: K-major B
+constexpr uint32_t S_TPL = OFF_G + 51200;     // T' - fp16(T'), fp16, same layout as S_TP
 constexpr uint32_t OFF_QPT = 163840;  // Q+^T  fp16 [128 c][64 t] SW128: MN-major B
 constexpr uint32_t OFF_KPT = 180224;  // K+^T  fp16 [128 c][64 j] SW128: K-major A
 constexpr uint32_t OFF_KH = 196608;   // Khat^T fp16 [128 c][64 t] SW128: K-major B
@@ -118,9 +121,10 @@ constexpr uint32_t SMEM_BYTES_CONV = OFF_TAPS + 2 * 128 * 4 * 4 + 1024;  // kCon
 constexpr uint32_t TS32 = 0;    // S^T fp32   [n][c]   128 cols
 constexpr uint32_t TS16 = 128;  // S^T fp16   [n][c/2]  64 cols (A operand)
 constexpr uint32_t TG = 192;    // Gram [Q~; K~q] K^(a)^T  [t][key row] 160 cols, until read back
-constexpr uint32_t TY16 = 192;  // Y^T fp16   [n][t/2]  32 cols (A operand), after the Gram
+constexpr uint32_t TY16 = 192;  // D^T = V^T - Y^T fp16 [n][t/2] 32 cols (A operand), after the Gram
 constexpr uint32_t TU = 256;    // U~^T / U^T [n][t]    64 cols
 constexpr uint32_t TU16 = 320;  // U^T fp16   [n][t/2]  32 cols (A operand)
+constexpr uint32_t TU16L = 352; // U^T - fp16(U^T), fp16 [n][t/2] 32 cols (A operand)
 constexpr uint32_t TO = 384;    // O^T fp32   [n][t]    64 cols
 constexpr uint32_t TY = 448;    // Y^T = S^T K+^T fp32 [n][t] 64 cols
 
@@ -804,20 +808,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           ok = ok && okv;
         }
-        // v stage bf16 -> fp16 in place (same layout: the MN-major A operand of U~^T)
-        uint4* vv = reinterpret_cast<uint4*>(sm + OFF_V) + tid * 2;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint4 x = zero_v || !ok ? make_uint4(0u, 0u, 0u, 0u) : vv[i];
-          uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-            absmax = fmaxf(absmax, fmaxf(fabsf(lo), fabsf(hi)));
-            w[j] = pack_f16(lo, hi);
-          }
-          vv[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
         const bool okg = wait_bar(bar_mma, ph_mma, P.spin_cycles);
         if (okg) ph_mma ^= 1;
         pend_mma = !okg;
@@ -893,6 +883,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const float v[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
                               x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
           st_row8_f16(sm + S_TP, t, j0, v);
+          float lo[8];  // what the fp16 rounding of T' dropped
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lo[i] = v[i] - __half2float(__float2half_rn(v[i]));
+          st_row8_f16(sm + S_TPL, t, j0, lo);
         };
         // Warps 0-11 invert.  Meanwhile warps 12-15 run the state products
         // O^T = S^T Q+^T and Y^T = S^T K+^T (M=128 value channels, N=64 tokens,
@@ -932,11 +926,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const bool okm = wait_bar(bar_mma2, ph_mma2, P.spin_cycles);
           tc_fence_after();
           if (okm) {
+            // D^T = V^T - Y^T (lane n = value channel, column t = token), formed in
+            // fp32 and rounded to fp16 once: the delta rule's correction v - S^T k
+            // cancels when a key already holds its value, so rounding Y first
+            // would cost 2^-12 |Y| rather than 2^-12 |D|.  V[t][n] is read from
+            // the bf16 stage (row t, 16-byte chunk (n % 64) / 8 XOR t % 8).
+            const int n = row;
+            const unsigned char* vb = sm + OFF_V + (n >> 6) * 8192 + ((n & 7) << 1);
+            const uint32_t xn = ((uint32_t)n & 63) >> 3;
 #pragma unroll
             for (int col = 0; col < kC; col += 16) {
               float v[16];
               tmem_ld16(my_lane + TY + col, v);
               tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int t = col + i;
+                const float vt = zero_v ? 0.f
+                                        : __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                              vb + t * 128 + ((xn ^ (uint32_t)(t & 7)) << 4))
+                                                          << 16);
+                v[i] = vt - v[i];
+              }
               uint32_t hp[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
@@ -1024,17 +1035,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ph_mma2 ^= 1;
       pend_mma2 = false;
 
-      // ---------------- G: U^T = V^T T'^T - Y^T T'^T ----------------
+      // ---------------- G: U^T = D^T T'^T,  D = V - Y ----------------
       if (tid == 256) {  // warp 8: no norm work below
-        const uint32_t id_u = make_idesc_f16(128, kC, true, false);
-        const uint32_t id_n = make_idesc_f16(128, kC, false, false, true);
+        const uint32_t id_u = make_idesc_f16(128, kC, false, false);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16_ss(tmem + TU, desc_mn(dbase, OFF_V + kk * 2048), desc_k(dbase, S_TP + kk * 32),
-                      id_u, kk > 0);
+          mma_ts(tmem + TU, tmem + TY16 + kk * 8, desc_k(dbase, S_TP + kk * 32), id_u, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          mma_ts(tmem + TU, tmem + TY16 + kk * 8, desc_k(dbase, S_TP + kk * 32), id_n, true);
+        for (int kk = 0; kk < kC / 16; ++kk)  // + the part of T' its fp16 rounding dropped
+          mma_ts(tmem + TU, tmem + TY16 + kk * 8, desc_k(dbase, S_TPL + kk * 32), id_u, true);
         mma_commit(bar_mma);
       }
       pend_mma = true;
@@ -1067,18 +1076,21 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       pend_v = (ci + 1 < nchunks) && !zero_v;
 
-      // ---------------- J: U^T -> fp16 in TMEM ----------------
+      // ---------------- J: U^T -> fp16 in TMEM, and what that rounding drops ----------------
       {
         float v[16];
         tmem_ld16(my_lane + TU + 16 * cq, v);
         tmem_ld_wait();
-        uint32_t hp[8];
+        uint32_t hp[8], lp[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           hp[i] = pack_f16(v[2 * i], v[2 * i + 1]);
           absmax = fmaxf(absmax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+          const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&hp[i]));
+          lp[i] = pack_f16(v[2 * i] - h2.x, v[2 * i + 1] - h2.y);
         }
         tmem_st8(my_lane + TU16 + 8 * cq, hp);
+        tmem_st8(my_lane + TU16L + 8 * cq, lp);
         tmem_st_wait();
       }
       sync_tc();
@@ -1089,9 +1101,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t id_s = make_idesc_f16(128, kD, false, false);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint32_t au = tmem + TU16 + kk * 8;
+          const uint32_t au = tmem + TU16 + kk * 8, al = tmem + TU16L + kk * 8;
           mma_ts(tmem + TO, au, desc_k(dbase, G_P + kk * 32), id_o, true);
           mma_ts(tmem + TS32, au, desc_k(dbase, OFF_KH + kk * 32), id_s, true);
+          mma_ts(tmem + TO, al, desc_k(dbase, G_P + kk * 32), id_o, true);
+          mma_ts(tmem + TS32, al, desc_k(dbase, OFF_KH + kk * 32), id_s, true);
         }
         mma_commit(bar_mma);
       }
