@@ -163,3 +163,34 @@ def test_fused_bad_accept_length_keeps_both_states():
     assert torch.equal(state[2], before[0][2]) and torch.equal(fz["conv_state_k"][2], before[2][2])
     assert not torch.equal(state[0], before[0][0])
     assert kda.get_device_error() == 0
+
+
+def test_fused_decode_gate_log_scale_and_per_head_gate():
+    """The fused decode step honours the gate log-scale A and one gate per
+    head, like the plain decode step."""
+    g = torch.Generator(device=DEV).manual_seed(73)
+    B, H, dk, dv, steps = 4, 3, 128, 128, 3
+    toks = _tokens((steps, B), H, dk, dv, torch.bfloat16, g)
+    A = torch.tensor([0.4, -0.6, 1.1], device=DEV)
+    for per_head in (False, True):
+        state = torch.randn((B, H, dk, dv), device=DEV, generator=g) * 0.1
+        fz = _fusion_tensors(B, H, dk, dv, 4, g, True)
+        s0, cq0, ck0 = state.clone(), fz["conv_state_q"].clone(), fz["conv_state_k"].clone()
+        zs = toks[3][..., 0].contiguous() if per_head else toks[3]
+        outs = [kda.decode_step_fused(toks[0][t], toks[1][t], toks[2][t], zs[t], toks[4][t], state,
+                                      a_log=A, **fz) for t in range(steps)]
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        fz_cpu = {kk: vv.cpu() for kk, vv in fz.items() if torch.is_tensor(vv)}
+        for b in range(B):
+            zb = zs[:, b].cpu()
+            if per_head:
+                zb = zb[:, :, None].expand(-1, -1, dk).contiguous()
+            T = steps
+            qy, _ = oracle.short_conv(toks[0][:, b].cpu(), fz_cpu["conv_weight_q"], [0, T], cq0[b:b + 1].cpu())
+            ky, _ = oracle.short_conv(toks[1][:, b].cpu(), fz_cpu["conv_weight_k"], [0, T], ck0[b:b + 1].cpu())
+            ro, rf, _ = oracle.recurrent(qy, ky, toks[2][:, b].cpu(), zb, toks[4][:, b].cpu(), [0, T],
+                                         s0[b:b + 1].cpu(), a_log=A.cpu())
+            ro = oracle.rms_norm(ro, fz_cpu["out_norm_weight"], EPS)
+            assert_close(torch.stack([o[b] for o in outs]), ro, torch.bfloat16, f"b={b} out")
+            assert_close(state[b], rf[0], torch.bfloat16, f"b={b} state")

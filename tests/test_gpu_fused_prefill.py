@@ -174,3 +174,31 @@ def test_fused_prefill_full_varlen_workload():
         acc_f.add(f_f[n0:n1].cpu(), rf, head_axis=1)
     print(acc_o.check(torch.bfloat16, "fused varlen out"))
     print(acc_f.check(torch.bfloat16, "fused varlen final state"))
+
+
+def test_fused_prefill_checkpoints():
+    """State checkpoints every 64 tokens through the fused call: each equals
+    the oracle composition's final state of that prefix."""
+    lens = [64, 200, 0, 130]
+    p = workloads.random_problem(lens, 2, 128, 128, torch.bfloat16, init_std=0.1, seed=91,
+                                 device=DEV, normalize_qk=False)
+    wq, wk, sq, sk = _conv_inputs(len(lens), 2, 4, 92)
+    sq0, sk0 = sq.clone(), sk.clone()
+    out, fin, ck = kda.chunk_fwd_fused(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                                       conv_weight_q=wq, conv_weight_k=wk, conv_state_q=sq,
+                                       conv_state_k=sk, cu_seqlens_host=p.cu_seqlens_host,
+                                       checkpoint_every=64)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    assert ck.shape[0] == 1 + 3 + 0 + 2
+    cu = p.cu_seqlens_host
+    i = 0
+    for n in range(len(lens)):
+        for j in range(1, lens[n] // 64 + 1):
+            a, b = cu[n], cu[n] + 64 * j
+            qy, _ = oracle.short_conv(p.q[a:b].cpu(), wq.cpu(), [0, b - a], sq0[n:n + 1].cpu())
+            ky, _ = oracle.short_conv(p.k[a:b].cpu(), wk.cpu(), [0, b - a], sk0[n:n + 1].cpu())
+            _, rf, _ = oracle.recurrent(qy, ky, p.v[a:b].cpu(), p.z[a:b].cpu(), p.beta[a:b].cpu(),
+                                        [0, b - a], p.initial_state[n:n + 1].cpu())
+            assert_close(ck[i], rf[0], torch.bfloat16, f"checkpoint {i}")
+            i += 1
