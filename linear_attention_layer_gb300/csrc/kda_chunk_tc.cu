@@ -137,12 +137,13 @@ constexpr float kF16Max = 65504.0f;
 // of kEnt ints {seq, token begin, token end, in, out, flags}; in / out are
 // state slots of `ws` (>= 0), or kSlotZero / kSlotIdentity / kSlotUser (the
 // caller's initial / final state of `seq`), kSlotNone for no output state;
-// flags & kFlagZeroV treats v as zero.
+// flags & kFlagZeroV treats v as zero; flags & kFlagNoOut writes no outputs and
+// no checkpoints (a run from a stand-in entry state).
 constexpr int kEnt = 6;
 // kSlotAux (out only): the caller's aux_state of `seq` (the transition M of an
 // affine summary).
 constexpr int kSlotNone = -1, kSlotZero = -1, kSlotIdentity = -2, kSlotUser = -3, kSlotAux = -4;
-constexpr int kFlagZeroV = 1;
+constexpr int kFlagZeroV = 1, kFlagNoOut = 2;
 
 struct Params {
   const float* beta;
@@ -467,6 +468,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       seq = e[0]; bos = e[1]; eos = e[2]; in_slot = e[3]; out_slot = e[4]; flags = e[5];
     }
     const bool zero_v = (flags & kFlagZeroV) != 0;
+    const bool no_out = (flags & kFlagNoOut) != 0;
     const int sbeg = P.mode == 0 ? bos : __ldg(P.cu + seq);  // start of the sequence
     const float zcoef = gate_coef(gate_scale(P.a_log, h));  // -e^{A_h} log2(e)
     if (bos < 0 || eos < bos || eos > P.total) {
@@ -791,7 +793,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // products) and S^T <- S^T Diag(e^{G_C}) ahead of this chunk's update.
       if (ok) {
         if (pend_l) {
-          if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
+          if (P.out && !no_out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
           if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
         }
         prep_state(my_lane, misc + M_DECAY, cq, absmax);
@@ -1115,7 +1117,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       l_t0 = t0;
       l_len = len;
       l_ck = -1;
-      if (P.ckpt && (t0 + len - sbeg) % P.ckpt_every == 0)
+      if (P.ckpt && !no_out && (t0 + len - sbeg) % P.ckpt_every == 0)
         l_ck = (long long)__ldg(P.ckpt_off + seq) + (t0 + len - sbeg) / P.ckpt_every - 1;
     }
     if (aborted) break;
@@ -1126,7 +1128,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ph_mma ^= 1;
         pend_mma = false;
         tc_fence_after();
-        if (P.out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
+        if (P.out && !no_out) write_o(P.out, H, h, l_t0, l_len, my_lane, row, cq);
         if (l_ck >= 0) write_state(P.ckpt + ((size_t)l_ck * H + h) * kD * kD, my_lane, row, cq);
       }
       pend_l = false;
@@ -1212,10 +1214,11 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize
 // before it, S_out = M S_in + S~, with M the product of the segment's
 // per-token transitions (the final state of the segment run from S_in = I
 // with v = 0) and S~ the final state run from S_in = 0.  Pass 1 computes
-// (S~, M) for the inner segments (the first segment runs from the true
-// initial state), a prefix scan S_in(p+1) = M_p S_in(p) + S~_p yields every
-// segment's entry state, and pass 2 reruns each segment from its entry state,
-// writing the outputs and, for the last segment, the final state.
+// (S~, M) for the inner segments, while the first segment runs from the true
+// initial state and writes its outputs; a prefix scan S_in(p+1) = M_p S_in(p)
+// + S~_p yields every segment's entry state, and pass 2 runs every other
+// segment from its entry state, writing the outputs and, for the last
+// segment, the final state.
 
 constexpr int kScanThreads = 256;
 constexpr int kMaxScanSeqs = 512;
@@ -1337,7 +1340,7 @@ SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms,
       const int k = (int)std::max<long>(1, (c + segc - 1) / segc);
       ns[n] = k;
       e += k;
-      u3 += k;
+      u3 += k >= 2 ? k - 1 : 1;  // a split sequence's segment 0 finishes in pass 1
       if (k >= 2) u1 += 1 + 2 * (k - 2);
       steps = std::max<long>(steps, k - 2);
     }
@@ -1538,12 +1541,14 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     }
     for (int q = 1; q + 1 < k; ++q) {
       seg(n, q, tb, te);
-      put(n, tb, te, kSlotZero, E + b + q, 0);
-      put(n, tb, te, kSlotIdentity, 2 * E + b + q, kFlagZeroV);
+      put(n, tb, te, kSlotZero, E + b + q, kFlagNoOut);
+      put(n, tb, te, kSlotIdentity, 2 * E + b + q, kFlagZeroV | kFlagNoOut);
     }
   }
-  prm.out = nullptr;
-  prm.ckpt = nullptr;  // pass 1 runs segments from stand-in entry states
+  // segment 0 runs from the true initial state, so it writes its outputs and
+  // checkpoints here; the inner segments' runs from stand-in states do not
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.ckpt = a.ckpt;
   if (ne > 0) {
     prm.num_units = ne * p.num_heads;
     launch_tc(std::min(prm.num_units, sms));
@@ -1563,10 +1568,10 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // ---- pass 2: every segment from its entry state, longest first ----
+  // ---- pass 2: every other segment from its entry state, longest first ----
   std::vector<std::array<int, 4>> segs;  // {len, n, q, k}
   for (int n = 0; n < p.num_seqs; ++n)
-    for (int q = 0; q < plan.nseg[n]; ++q) {
+    for (int q = plan.nseg[n] >= 2 ? 1 : 0; q < plan.nseg[n]; ++q) {
       int tb, te;
       seg(n, q, tb, te);
       segs.push_back({te - tb, n, q, plan.nseg[n]});

@@ -413,40 +413,46 @@ recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
   float* qs = sh[w][0];
   float* ks = sh[w][1];
   float* as = sh[w][2];
-  // this lane's inputs of the next token, loaded one token ahead so that a
-  // token's global-memory latency hides behind the previous token's work
-  float nq[CPL], nk[CPL], nz[CPL], nv = 0.f, nb = 0.f;
-  auto fetch = [&](int t) {
+  // this lane's inputs of the next two tokens, loaded ahead so that a token's
+  // global-memory latency hides behind the work of the tokens before it
+  struct In {
+    float q[CPL], k[CPL], z[CPL], v, b;
+  };
+  In n1{}, n2{};
+  auto fetch = [&](In& x, int t) {
     if (t >= eos) return;
     const size_t th = (size_t)t * H + h;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int c = lane + 32 * i;
-      nq[i] = IO<T>::ld(q + th * DK + c);
-      nk[i] = IO<T>::ld(k + th * DK + c);
-      nz[i] = __ldg(z + th * (zhead ? 1 : DK) + (zhead ? 0 : c));
+      x.q[i] = IO<T>::ld(q + th * DK + c);
+      x.k[i] = IO<T>::ld(k + th * DK + c);
+      x.z[i] = __ldg(z + th * (zhead ? 1 : DK) + (zhead ? 0 : c));
     }
-    nv = IO<T>::ld(v + th * DV + lane);
-    nb = __ldg(beta + th);
+    x.v = IO<T>::ld(v + th * DV + lane);
+    x.b = __ldg(beta + th);
   };
-  fetch(bos);
+  fetch(n1, bos);
+  fetch(n2, bos + 1);
   for (int t = bos; t < eos; ++t) {
     const size_t th = (size_t)t * H + h;
+    const In cur = n1;
+    n1 = n2;
+    fetch(n2, t + 2);
     float qq = 0.f, kk = 0.f, kq = 0.f;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int c = lane + 32 * i;
-      const float a = nq[i], b = nk[i];
+      const float a = cur.q[i], b = cur.k[i];
       qs[c] = a;
       ks[c] = b;
-      as[c] = __expf(log_decay(zscale * nz[i]));
+      as[c] = __expf(log_decay(zscale * cur.z[i]));
       qq += a * a;
       kk += b * b;
       kq += a * b;
     }
-    const float vj = nv;
-    const float bt = nb;
-    fetch(t + 1);
+    const float vj = cur.v;
+    const float bt = cur.b;
     qq = warp_sum(qq);
     kk = warp_sum(kk);
     kq = warp_sum(kq);

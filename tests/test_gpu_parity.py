@@ -718,3 +718,18 @@ def test_many_short_sequences():
         torch.cuda.synchronize()
         assert kda.get_device_error() == 0
         _check_all(p, out, fin, torch.bfloat16)
+
+
+def test_split_with_a_workspace_smaller_than_the_best_plan():
+    """A workspace below what the best split needs: kda_chunk_fwd takes the
+    best plan that fits (fewer, longer segments) and stays exact."""
+    p = workloads.random_problem([6000, 900], 2, 128, 128, torch.bfloat16, init_std=0.1,
+                                 seed=35, device=DEV)
+    need = _ws_bytes(p)
+    assert need > 0
+    small = torch.empty((need // 3) // 256 * 256, dtype=torch.uint8, device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host, workspace=small)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    _check_all(p, out, fin, torch.bfloat16)
