@@ -669,6 +669,42 @@ def bench_decode(kda, d, steps, device, clk=None):
     return a.elapsed_time(b)
 
 
+def bench_decode_fused(kda, d, steps, device, width=4, clk=None):
+    """kda_decode_step_fused over the decode workload: raw q, k through the
+    short convolution (width 4, states advanced in place) and the outputs
+    through the per-head RMS norm, one launch per step."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(79)
+    N, H = d.meta["num_requests"], d.meta["num_heads"]
+    f32 = dict(dtype=torch.float32, device=device, generator=g)
+    fz = dict(conv_weight_q=torch.randn((H, 128, width), **f32) * 0.5,
+              conv_weight_k=torch.randn((H, 128, width), **f32) * 0.5,
+              conv_state_q=torch.randn((N, H, 128, width - 1), **f32),
+              conv_state_k=torch.randn((N, H, 128, width - 1), **f32),
+              out_norm_weight=torch.ones((H, 128), dtype=torch.float32, device=device),
+              out_norm_eps=1e-6)
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(d.v[0])
+    for t in range(3):
+        kda.decode_step_fused(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=out, **fz)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start()
+    a.record(stream)
+    for t in range(steps):
+        kda.decode_step_fused(d.q[t], d.k[t], d.v[t], d.z[t], d.beta[t], d.state, out=out, **fz)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.stop()
+    if kda.get_device_error() != 0:
+        raise RuntimeError("device error word set after the fused decode steps")
+    return a.elapsed_time(b)
+
+
 def bench_e2e(kda, p, steps, device, groups=8):
     """End to end through kda_chunk_fwd_host: inputs and outputs in pinned host
     memory, every step copies the batch in, computes and copies out and the
@@ -998,6 +1034,21 @@ def main():
                          "kernel": "kda_decode_step", "algorithmic_bytes_per_launch": dec_bytes,
                          "peak_source": f"{peak_src} hbm_gbs"},
             "clocks": dclk.summary(), "gpu_launches": args.decode_steps}
+        # the same steps with the convolution of raw q, k and the output norm fused in
+        fdclk = clock_sampler(gpu_uuid)
+        fdec_ms = bench_decode_fused(kda, d, args.decode_steps, device, clk=fdclk)
+        f_step_ms = fdec_ms / args.decode_steps
+        f_bytes = dec_bytes + Nq * Hq * 2 * 2 * 128 * 3 * 4  # + q, k convolution states in and out
+        f_gbs = f_bytes / (f_step_ms * 1e-3) / 1e9
+        line["decode_fused"] = {
+            "value": round(f_gbs, 1), "unit": "GB/s", "ms_per_step": round(f_step_ms, 5),
+            "steps": args.decode_steps, "kernel": "kda_decode_step_fused",
+            "fused": "short convolution (width 4) of raw q, k + per-head RMS output norm",
+            "workload": workloads.DESCRIPTIONS["decode"],
+            "roofline": {"bound": "hbm", "achieved": round(f_gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(f_gbs / hbm_peak, 4),
+                         "algorithmic_bytes_per_launch": f_bytes},
+            "clocks": fdclk.summary(), "gpu_launches": args.decode_steps}
         del d
         torch.cuda.empty_cache()
 
