@@ -42,6 +42,26 @@ FLOPS_PER_HEAD_TOKEN = 10 * CHUNK * 128 + 6 * 128 * 128
 # flops per state element (decay, the e reduction, the rank-1 write) and the
 # reverse step at 16 (read-out, y, dq^, dk^, dalpha and the decayed dS).
 BWD_FLOPS_PER_HEAD_TOKEN = (2 * 5 + 16) * 128 * 128
+# Chunked reverse mode (kda_chunk_bwd), tf32 tensor-core products, per 16-token
+# chunk (C = 16, d = 128): the forward chunk products that rebuild the states
+# (C x C x d Gram, C x d x d for K+S, C x C x d for T'R, d x d x C state update)
+# and the reverse step's products (the two C x C x d Grams and T'R again, then
+# C x C x d + C x d x d for dU, C x C x d for dR, three C x d x d for dK~, dO S^T
+# and dR S^T, two C x C x d for dT' and dP, d x d x 2C for dS, four C x C x d
+# for the rest of dQ+, dK+, dK-, and two C^3 for the UT transform); 2 flops per
+# multiply-add.
+def _chunk_bwd_macs(C=16, d=128):
+    fwd = C * C * d + C * d * d + C * C * d + d * d * C
+    rev_common = 2 * C * C * d + C * d * d + C * C * d
+    rev = (C * C * d + C * d * d) + C * C * d + 3 * C * d * d + 2 * C * C * d \
+        + d * d * 2 * C + 4 * C * C * d + 2 * C ** 3
+    return fwd + rev_common + rev
+
+
+CBWD_FLOPS_PER_HEAD_TOKEN = 2 * _chunk_bwd_macs() // 16
+# tf32 tensor-core peak: the measured bf16 peak times the nominal tf32 / bf16
+# ratio (1.1 / 2.25 PFLOP/s dense).
+TF32_PER_BF16 = 1.1 / 2.25
 # Bytes a reverse pass cannot avoid per head-token: q, k, v, d out (bf16),
 # z (fp32) and beta read; dq, dk, dv, dz (fp32) and dbeta written.
 BWD_BYTES_PER_HEAD_TOKEN = 4 * 256 + 512 + 4 + 4 * 512 + 4
@@ -417,16 +437,19 @@ def bench_prefill(kda, p, steps, warmup, dist, device, split=False, clk=None):
     return total_ms, per_launch
 
 
-def bench_backward(kda, p, steps, warmup, device, clk=None):
-    """kda_recurrent_bwd over the prefill workload with random cotangents
-    (d out bf16, d final state fp32).  Returns (total ms, per-launch ms)."""
+def bench_backward(kda, p, steps, warmup, device, clk=None, chunked=False):
+    """kda_recurrent_bwd (chunked: kda_chunk_bwd) over the prefill workload
+    with random cotangents (d out bf16, d final state fp32).  Returns (total
+    ms, per-launch ms)."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(99)
     H = p.meta["num_heads"]
     d_out = torch.randn(p.v.shape, device=device, generator=g).to(p.q.dtype)
     d_fin = torch.randn((p.num_seqs, H, 128, 128), device=device, generator=g)
-    nbytes = kda.recurrent_bwd_workspace_size(H, p.q.dtype, p.cu_seqlens_host)
+    size_fn = kda.chunk_bwd_workspace_size if chunked else kda.recurrent_bwd_workspace_size
+    bwd_fn = kda.chunk_bwd if chunked else kda.recurrent_bwd
+    nbytes = size_fn(H, p.q.dtype, p.cu_seqlens_host)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
     T = p.total_tokens
     f32 = dict(dtype=torch.float32, device=device)
@@ -436,8 +459,8 @@ def bench_backward(kda, p, steps, warmup, device, clk=None):
     stream = torch.cuda.current_stream()
 
     def step():
-        kda.recurrent_bwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out,
-                          d_fin, cu_seqlens_host=p.cu_seqlens_host, workspace=ws, grads=grads)
+        bwd_fn(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out, d_fin,
+               cu_seqlens_host=p.cu_seqlens_host, workspace=ws, grads=grads)
 
     for _ in range(warmup):
         step()
@@ -770,7 +793,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--skip", default="",
-                    help="comma list of: decode,e2e,cpu,long,spec,bwd,conv,prefill,tiny,fused")
+                    help="comma list of: decode,e2e,cpu,long,spec,bwd,cbwd,conv,prefill,tiny,fused")
     ap.add_argument("--bwd-steps", type=int, default=3)
     ap.add_argument("--workload", default="varlen", choices=["varlen", "long", "prefill"])
     ap.add_argument("--split", action="store_true",
@@ -966,6 +989,32 @@ def main():
             "hbm": {"achieved": round(b_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(b_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": b_bytes},
             "clocks": bclk.summary(), "gpu_launches": args.bwd_steps}
+
+    # ---- the chunked tensor-core reverse mode over the same workload ----
+    if "cbwd" not in skip:
+        cbclk = clock_sampler(gpu_uuid)
+        c_ms, c_launch = bench_backward(kda, p, args.bwd_steps, args.warmup, device, clk=cbclk,
+                                        chunked=True)
+        c_launch_ms = statistics.mean(c_launch)
+        c_flops = T * H * CBWD_FLOPS_PER_HEAD_TOKEN
+        c_tf = c_flops / (c_launch_ms * 1e-3) / 1e12
+        tf32_peak = peaks["bf16_tflops_sustained"] * TF32_PER_BF16
+        c_bytes = T * H * BWD_BYTES_PER_HEAD_TOKEN + 3 * N * H * STATE_BYTES
+        c_gbs = c_bytes / (c_launch_ms * 1e-3) / 1e9
+        line["backward_chunked"] = {
+            "value": round(weak_scaling_value(T, world, c_ms / 1e3 / args.bwd_steps), 3),
+            "unit": UNIT, "ms_per_step": round(c_ms / args.bwd_steps, 3),
+            "steps": args.bwd_steps, "kernel": "kda_chunk_bwd",
+            "workload": workloads.DESCRIPTIONS[args.workload] + "; random d out and d final state",
+            "roofline": {"bound": "tensor", "achieved": round(c_tf, 2),
+                         "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(c_tf / tf32_peak, 4), "traffic": None,
+                         "flops_per_head_token": CBWD_FLOPS_PER_HEAD_TOKEN,
+                         "peak_source": f"{peak_src} bf16_tflops_sustained x nominal "
+                                        "tf32/bf16 ratio 1.1/2.25"},
+            "hbm": {"achieved": round(c_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(c_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": c_bytes},
+            "clocks": cbclk.summary(), "gpu_launches": args.bwd_steps}
 
     # ---- the Q/K short convolution + Swish over the same workload ----
     if "conv" not in skip:

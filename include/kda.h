@@ -484,6 +484,37 @@ kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void
 kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
 
 /*
+ * kda_chunk_bwd -- the same gradients as kda_recurrent_bwd from the chunked
+ * (WY / UT) form of the recurrence (mhpq.cn/news/56770, section "KDA 到底在算
+ * 什么", evaluated chunkwise; the chunked forward with a custom reverse mode
+ * is the training kernel of blog.higcp.com "猜想：K3 可能是最适合 TPU 的 MoE 架
+ * 构", section "第二层").  Per 16-token chunk the state products (dO S^T,
+ * dR S^T, U dS'^T, K~ dS', Q+^T dO - K+^T dR, ...) and the chunk's own 16 x 16
+ * products run on the tensor cores (bf16 MMAs, fp32 accumulation); states
+ * and their gradients stay fp32.  States are kept every
+ * 64 tokens in the workspace and each block's chunk-entry states rebuilt.
+ * Arguments, layouts, dtypes, alignment and errors exactly as for
+ * kda_recurrent_bwd (any supported dk, dv; per-channel or per-head gate;
+ * a_log honoured; cu_seqlens_host REQUIRED); the workspace must hold
+ * kda_chunk_bwd_workspace_size() bytes.  Accuracy: every tensor-core operand
+ * is split into a high and a low bf16 part (16 significant bits, three
+ * multiplies per product, fp32 accumulation), and the gradient of the
+ * log-decay is summed without cancelling terms, so the gradients agree with
+ * an fp64 evaluation to about 1e-5 relative L2, like kda_recurrent_bwd.
+ */
+kda_status_t kda_chunk_bwd(const kda_desc_t* desc, const void* q, const void* k, const void* v,
+                           const float* z, const float* beta, const float* initial_state,
+                           const int32_t* cu_seqlens, const void* d_out,
+                           const float* d_final_state, float* dq, float* dk, float* dv,
+                           float* dz, float* dbeta, float* d_initial_state, kda_stream_t stream);
+
+/* Bytes of device workspace kda_chunk_bwd needs (needs desc->cu_seqlens_host):
+ * for every resident CTA (at most one per SM) 64 KiB per 64 tokens of the
+ * longest sequence, plus 256 KiB; below dk = dv = 128 also the zero-padded
+ * copies of the inputs and gradients. */
+kda_status_t kda_chunk_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
+
+/*
  * kda_short_conv -- the Q/K preprocessing before the recurrence
  * (mhpq.cn/news/56770, section "KDA 到底在算什么", the Q/K preprocessing
  * paragraph: a short causal convolution over the most recent few positions,

@@ -25,7 +25,8 @@ __all__ = ["chunk_fwd", "chunk_fwd_noalloc", "recurrent_fwd", "decode_step",
            "recurrent_bwd", "recurrent_bwd_workspace_size", "short_conv", "chunk_fwd_host",
            "chunk_fwd_host_workspace_size", "chunk_fwd_summary",
            "chunk_fwd_summary_workspace_size", "state_scan", "decode_step_fused",
-           "decode_replay_window_fused", "chunk_fwd_fused", "EXPORTED_SYMBOLS"]
+           "decode_replay_window_fused", "chunk_fwd_fused", "chunk_bwd",
+           "chunk_bwd_workspace_size", "EXPORTED_SYMBOLS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkda.so")
 
@@ -43,7 +44,8 @@ EXPORTED_SYMBOLS = ("kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurr
                     "kda_chunk_fwd_host", "kda_chunk_fwd_host_workspace_size",
                     "kda_chunk_fwd_summary", "kda_chunk_fwd_summary_workspace_size",
                     "kda_state_scan", "kda_decode_step_fused",
-                    "kda_decode_replay_window_fused", "kda_chunk_fwd_fused")
+                    "kda_decode_replay_window_fused", "kda_chunk_fwd_fused", "kda_chunk_bwd",
+                    "kda_chunk_bwd_workspace_size")
 
 #: Size of the library's own scratch array used by chunk_fwd_noalloc
 #: (KDA_NOALLOC_SCRATCH_BYTES in include/kda.h).
@@ -97,16 +99,18 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
         lib.kda_chunk_fwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
-        lib.kda_recurrent_bwd.restype = ctypes.c_int
-        lib.kda_recurrent_bwd.argtypes = [dp] + [vp] * 16
+        for f in (lib.kda_recurrent_bwd, lib.kda_chunk_bwd):
+            f.restype = ctypes.c_int
+            f.argtypes = [dp] + [vp] * 16
         lib.kda_chunk_fwd_host.restype = ctypes.c_int
         lib.kda_chunk_fwd_host.argtypes = [dp, ctypes.c_int32] + [vp] * 10
         lib.kda_chunk_fwd_host_workspace_size.restype = ctypes.c_int
         lib.kda_chunk_fwd_host_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_short_conv.restype = ctypes.c_int
         lib.kda_short_conv.argtypes = [dp, ctypes.c_int32] + [vp] * 7
-        lib.kda_recurrent_bwd_workspace_size.restype = ctypes.c_int
-        lib.kda_recurrent_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        for f in (lib.kda_recurrent_bwd_workspace_size, lib.kda_chunk_bwd_workspace_size):
+            f.restype = ctypes.c_int
+            f.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_chunk_fwd_summary.restype = ctypes.c_int
         lib.kda_chunk_fwd_summary.argtypes = [dp] + [vp] * 9
         lib.kda_chunk_fwd_summary_workspace_size.restype = ctypes.c_int
@@ -454,28 +458,32 @@ def short_conv(x, weight, cu_seqlens, conv_state=None, *, out=None, final_state=
     return out, final_state
 
 
-def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host, dk=128, dv=128):
-    """Bytes of device workspace ``recurrent_bwd`` needs."""
+def _bwd_workspace_size(fn, num_heads, dtype, cu_seqlens_host, dk, dv):
     N = len(cu_seqlens_host) - 1
     desc, keep = make_desc(N, int(cu_seqlens_host[-1]), num_heads, dk, dv, _io_code(dtype),
                            cu_seqlens_host)
     n = ctypes.c_size_t(0)
-    st = load().kda_recurrent_bwd_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    st = getattr(load(), fn)(ctypes.byref(desc), ctypes.byref(n))
     del keep
     if st != KDA_OK:
-        raise KDAError(st, "kda_recurrent_bwd_workspace_size")
+        raise KDAError(st, fn)
     return int(n.value)
 
 
-def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=None, *,
-                  cu_seqlens_host, a_log=None, workspace=None, grads=None, stream=None):
-    """Reverse mode of the prefill (``kda_recurrent_bwd``): given dL/d out and
-    dL/d final_state (None: zeros), returns (dq, dk, dv, dz, dbeta,
-    d_initial_state), fp32, for the inputs of the forward call (same q, k, v,
-    z, beta, cu_seqlens, initial_state and a_log; any supported dk, dv).  ``z`` [T, H]
-    (one gate per head) gives dz [T, H].  ``cu_seqlens_host`` is required; ``workspace`` (a device
-    tensor of ``recurrent_bwd_workspace_size`` bytes) is allocated here when
-    None; ``grads`` may give the six output tensors to fill."""
+def recurrent_bwd_workspace_size(num_heads, dtype, cu_seqlens_host, dk=128, dv=128):
+    """Bytes of device workspace ``recurrent_bwd`` needs."""
+    return _bwd_workspace_size("kda_recurrent_bwd_workspace_size", num_heads, dtype,
+                               cu_seqlens_host, dk, dv)
+
+
+def chunk_bwd_workspace_size(num_heads, dtype, cu_seqlens_host, dk=128, dv=128):
+    """Bytes of device workspace ``chunk_bwd`` needs."""
+    return _bwd_workspace_size("kda_chunk_bwd_workspace_size", num_heads, dtype,
+                               cu_seqlens_host, dk, dv)
+
+
+def _bwd(fn, ws_size, q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final,
+         cu_seqlens_host, a_log, workspace, grads, stream):
     lib = load()
     T, H, dk = q.shape
     dv = v.shape[-1]
@@ -505,19 +513,40 @@ def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=No
     for name, g, shp in zip(("dq", "dk", "dv", "dz", "dbeta", "d_initial"), grads, shapes):
         _check_tensor(name, g, torch.float32, shp, dev)
     if workspace is None:
-        nbytes = recurrent_bwd_workspace_size(H, q.dtype, cu_seqlens_host, dk, dv)
+        nbytes = ws_size(H, q.dtype, cu_seqlens_host, dk, dv)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     desc, keep = make_desc(N, T, H, dk, dv, _io_code(q.dtype), cu_seqlens_host, workspace, a_log)
     desc.gate_per_head = 1 if per_head else 0
     with torch.cuda.device(dev):
-        st = lib.kda_recurrent_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
-                                   _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
-                                   _ptr(d_out), _ptr(d_final), *[_ptr(g) for g in grads],
-                                   _stream_handle(stream))
+        st = getattr(lib, fn)(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                              _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(d_out),
+                              _ptr(d_final), *[_ptr(g) for g in grads], _stream_handle(stream))
     del keep
     if st != KDA_OK:
-        raise KDAError(st, "kda_recurrent_bwd")
+        raise KDAError(st, fn)
     return grads
+
+
+def recurrent_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=None, *,
+                  cu_seqlens_host, a_log=None, workspace=None, grads=None, stream=None):
+    """Reverse mode of the prefill (``kda_recurrent_bwd``): given dL/d out and
+    dL/d final_state (None: zeros), returns (dq, dk, dv, dz, dbeta,
+    d_initial_state), fp32, for the inputs of the forward call (same q, k, v,
+    z, beta, cu_seqlens, initial_state and a_log; any supported dk, dv).  ``z`` [T, H]
+    (one gate per head) gives dz [T, H].  ``cu_seqlens_host`` is required; ``workspace`` (a device
+    tensor of ``recurrent_bwd_workspace_size`` bytes) is allocated here when
+    None; ``grads`` may give the six output tensors to fill."""
+    return _bwd("kda_recurrent_bwd", recurrent_bwd_workspace_size, q, k, v, z, beta, cu_seqlens,
+                initial_state, d_out, d_final, cu_seqlens_host, a_log, workspace, grads, stream)
+
+
+def chunk_bwd(q, k, v, z, beta, cu_seqlens, initial_state, d_out, d_final=None, *,
+              cu_seqlens_host, a_log=None, workspace=None, grads=None, stream=None):
+    """The same gradients as ``recurrent_bwd`` from the chunked form on the
+    tensor cores (``kda_chunk_bwd``; tf32 products, fp32 states): arguments and
+    results as for ``recurrent_bwd``, workspace ``chunk_bwd_workspace_size``."""
+    return _bwd("kda_chunk_bwd", chunk_bwd_workspace_size, q, k, v, z, beta, cu_seqlens,
+                initial_state, d_out, d_final, cu_seqlens_host, a_log, workspace, grads, stream)
 
 
 def decode_step(q, k, v, z, beta, state, *, out=None, stream=None, a_log=None):

@@ -128,6 +128,40 @@ kda_status_t check_bwd(const kda_desc_t* desc, const void* q, const void* k, con
     if (x && !aligned16(x)) return KDA_ERR_INVALID_ARGUMENT;
   return KDA_OK;
 }
+
+// Both reverse modes: validation, workspace check, launch.
+kda_status_t run_bwd(bool chunked, const kda_desc_t* desc, const void* q, const void* k,
+                     const void* v, const float* z, const float* beta,
+                     const float* initial_state, const int32_t* cu_seqlens, const void* d_out,
+                     const float* d_final_state, float* dq, float* dk, float* dv, float* dz,
+                     float* dbeta, float* d_initial_state, kda_stream_t stream) {
+  kda_status_t s = check_bwd(desc, q, k, v, z, beta, initial_state, cu_seqlens, d_out,
+                             d_final_state, dq, dk, dv, dz, dbeta, d_initial_state);
+  if (s != KDA_OK) return s;
+  const kda::Problem p = to_problem(desc);
+  const size_t need = chunked ? kda::chunk_bwd_workspace_bytes(p, desc->cu_seqlens_host)
+                              : kda::recurrent_bwd_workspace_bytes(p, desc->cu_seqlens_host);
+  if (need > 0 && (!desc->workspace || desc->workspace_bytes < need || !aligned16(desc->workspace)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  kda::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.z = z; a.beta = beta;
+  a.initial_state = initial_state;
+  a.cu_seqlens = cu_seqlens;
+  a.d_out = d_out;
+  a.d_final = d_final_state;
+  a.a_log = desc->a_log;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dz = dz; a.dbeta = dbeta;
+  a.d_initial = d_initial_state;
+  a.zhead = desc->gate_per_head;
+  a.err = device_error_word();
+  if (!a.err) return KDA_ERR_CUDA;
+  const cudaError_t e =
+      chunked ? kda::launch_chunk_bwd(p, a, desc->cu_seqlens_host, desc->workspace,
+                                      (cudaStream_t)stream)
+              : kda::launch_recurrent_bwd(p, a, desc->cu_seqlens_host, desc->workspace,
+                                          (cudaStream_t)stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 }  // namespace
 
 namespace kda {
@@ -514,34 +548,32 @@ kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* by
   return KDA_OK;
 }
 
+kda_status_t kda_chunk_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes) {
+  if (!bytes || !desc) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status_t s = check_desc(desc, false);
+  if (s != KDA_OK) return s;
+  if (!desc->cu_seqlens_host) return KDA_ERR_INVALID_ARGUMENT;
+  *bytes = kda::chunk_bwd_workspace_bytes(to_problem(desc), desc->cu_seqlens_host);
+  return KDA_OK;
+}
+
 kda_status_t kda_recurrent_bwd(const kda_desc_t* desc, const void* q, const void* k,
                                const void* v, const float* z, const float* beta,
                                const float* initial_state, const int32_t* cu_seqlens,
                                const void* d_out, const float* d_final_state, float* dq,
                                float* dk, float* dv, float* dz, float* dbeta,
                                float* d_initial_state, kda_stream_t stream) {
-  kda_status_t s = check_bwd(desc, q, k, v, z, beta, initial_state, cu_seqlens, d_out,
-                             d_final_state, dq, dk, dv, dz, dbeta, d_initial_state);
-  if (s != KDA_OK) return s;
-  const kda::Problem p = to_problem(desc);
-  const size_t need = kda::recurrent_bwd_workspace_bytes(p, desc->cu_seqlens_host);
-  if (need > 0 && (!desc->workspace || desc->workspace_bytes < need || !aligned16(desc->workspace)))
-    return KDA_ERR_INVALID_ARGUMENT;
-  kda::BwdArgs a;
-  a.q = q; a.k = k; a.v = v; a.z = z; a.beta = beta;
-  a.initial_state = initial_state;
-  a.cu_seqlens = cu_seqlens;
-  a.d_out = d_out;
-  a.d_final = d_final_state;
-  a.a_log = desc->a_log;
-  a.dq = dq; a.dk = dk; a.dv = dv; a.dz = dz; a.dbeta = dbeta;
-  a.d_initial = d_initial_state;
-  a.zhead = desc->gate_per_head;
-  a.err = device_error_word();
-  if (!a.err) return KDA_ERR_CUDA;
-  cudaError_t e = kda::launch_recurrent_bwd(p, a, desc->cu_seqlens_host, desc->workspace,
-                                            (cudaStream_t)stream);
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return run_bwd(false, desc, q, k, v, z, beta, initial_state, cu_seqlens, d_out, d_final_state,
+                 dq, dk, dv, dz, dbeta, d_initial_state, stream);
+}
+
+kda_status_t kda_chunk_bwd(const kda_desc_t* desc, const void* q, const void* k, const void* v,
+                           const float* z, const float* beta, const float* initial_state,
+                           const int32_t* cu_seqlens, const void* d_out,
+                           const float* d_final_state, float* dq, float* dk, float* dv,
+                           float* dz, float* dbeta, float* d_initial_state, kda_stream_t stream) {
+  return run_bwd(true, desc, q, k, v, z, beta, initial_state, cu_seqlens, d_out, d_final_state,
+                 dq, dk, dv, dz, dbeta, d_initial_state, stream);
 }
 
 const char* kda_status_string(kda_status_t status) {

@@ -602,14 +602,25 @@ size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host) {
   return bwd::pad_layout(p).total + bwd_inner_bytes(p, cu_host);
 }
 
+size_t chunk_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host) {
+  if (p.num_seqs == 0 || p.num_heads == 0) return 0;
+  if (p.dk == bwd::kD && p.dv == bwd::kD) return chunk_bwd_inner_bytes(p, cu_host);
+  return bwd::pad_layout(p).total + chunk_bwd_inner_bytes(p, cu_host);
+}
+
 static cudaError_t launch_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
                                   void* ws, cudaStream_t st);
 
-cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
-                                 void* ws, cudaStream_t st) {
+using Bwd128 = cudaError_t (*)(const Problem&, const BwdArgs&, const int32_t*, void*,
+                               cudaStream_t);
+
+// Either reverse mode (token by token or chunked) over inputs zero-padded to
+// dk = dv = 128 when they are narrower.
+static cudaError_t launch_bwd_padded(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                     void* ws, cudaStream_t st, Bwd128 launch_128) {
   using namespace bwd;
   if (p.num_seqs == 0) return cudaSuccess;
-  if (p.dk == kD && p.dv == kD) return launch_bwd_128(p, a, cu_host, ws, st);
+  if (p.dk == kD && p.dv == kD) return launch_128(p, a, cu_host, ws, st);
   const PadLayout L = pad_layout(p);
   unsigned char* W = static_cast<unsigned char*>(ws);
   const long long th = (long long)p.total_tokens * p.num_heads;
@@ -652,7 +663,7 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
   b.d_initial = a.d_initial ? reinterpret_cast<float*>(W + L.dini) : nullptr;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_bwd_128(p128, b, cu_host, W + L.inner, st);
+  e = launch_128(p128, b, cu_host, W + L.inner, st);
   if (e != cudaSuccess) return e;
   if (th > 0) {
     unpad_rows_kernel<<<blocks_for(th * p.dk), 256, 0, st>>>(a.dq, b.dq, th, p.dk);
@@ -664,6 +675,16 @@ cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32
     unpad_state_kernel<<<blocks_for(nh * p.dk * p.dv), 256, 0, st>>>(a.d_initial, b.d_initial,
                                                                     nh, p.dk, p.dv);
   return cudaGetLastError();
+}
+
+cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                 void* ws, cudaStream_t st) {
+  return launch_bwd_padded(p, a, cu_host, ws, st, launch_bwd_128);
+}
+
+cudaError_t launch_chunk_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host, void* ws,
+                             cudaStream_t st) {
+  return launch_bwd_padded(p, a, cu_host, ws, st, launch_chunk_bwd_128);
 }
 
 static cudaError_t launch_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,

@@ -177,6 +177,14 @@ struct BwdArgs {
 size_t recurrent_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host);
 cudaError_t launch_recurrent_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
                                  void* ws, cudaStream_t stream);
+// The same gradients from the chunked form (16-token chunks, tf32 tensor-core
+// products); BwdArgs as above.
+size_t chunk_bwd_workspace_bytes(const Problem& p, const int32_t* cu_host);
+cudaError_t launch_chunk_bwd(const Problem& p, const BwdArgs& a, const int32_t* cu_host, void* ws,
+                             cudaStream_t stream);
+size_t chunk_bwd_inner_bytes(const Problem& p, const int32_t* cu_host);  // dk = dv = 128
+cudaError_t launch_chunk_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,
+                                 void* ws, cudaStream_t stream);
 
 // The Q/K preprocessing convolution (depthwise, causal, width 1..4) + Swish.
 struct ConvArgs {

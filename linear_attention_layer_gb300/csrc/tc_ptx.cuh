@@ -272,6 +272,15 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32
                : "r"(saddr));
 }
 
+// The same, transposed: lane l's register j holds the 16-bit elements of
+// rows 2 (l % 4) and 2 (l % 4) + 1, column l / 4, of matrix j.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(saddr));
+}
+
 // Four 8x8 matrices of 16-bit pairs to shared memory: lane l's register j is
 // word l % 4 of row l / 4 of matrix j; lane 8 j + r gives the address of row r
 // of matrix j (16 bytes).  Used for 32-bit data as well: it only moves bits.

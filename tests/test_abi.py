@@ -159,30 +159,33 @@ def test_workspace_size_query(lib):
     assert lib.kda_chunk_fwd_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
 
 
-def _call_bwd(lib, desc, q=FAKE, dq=ctypes.c_void_p(0x2000), d_out=FAKE, cu=FAKE):
+def _call_bwd(lib, desc, q=FAKE, dq=ctypes.c_void_p(0x2000), d_out=FAKE, cu=FAKE,
+              fn="kda_recurrent_bwd"):
     outs = [dq] + [ctypes.c_void_p(0x3000 + 0x1000 * i) for i in range(4)]
-    return lib.kda_recurrent_bwd(ctypes.byref(desc), q, FAKE, FAKE, FAKE, FAKE, None, cu, d_out,
-                                 None, *outs, None, None)
+    return getattr(lib, fn)(ctypes.byref(desc), q, FAKE, FAKE, FAKE, FAKE, None, cu, d_out,
+                            None, *outs, None, None)
 
 
-def test_backward_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("fn", ["kda_recurrent_bwd", "kda_chunk_bwd"])
+def test_backward_rejects_bad_arguments(lib, fn):
+    _call = lambda *a, **k: _call_bwd(*a, fn=fn, **k)
     cu = [0, 3, 8]
     d, keep = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16, cu)
-    assert _call_bwd(lib, d) == 1                                   # no workspace
-    assert _call_bwd(lib, d, cu=None) == 1                          # cu_seqlens required
-    assert _call_bwd(lib, d, q=None) == 1                           # q required
-    assert _call_bwd(lib, d, d_out=None) == 1                       # d_out required
-    assert _call_bwd(lib, d, dq=None) == 1                          # dq required
-    assert _call_bwd(lib, d, dq=FAKE) == 1                          # dq aliases q
-    assert _call_bwd(lib, d, q=ctypes.c_void_p(0x1004)) == 1        # not 16-byte aligned
+    assert _call(lib, d) == 1                                   # no workspace
+    assert _call(lib, d, cu=None) == 1                          # cu_seqlens required
+    assert _call(lib, d, q=None) == 1                           # q required
+    assert _call(lib, d, d_out=None) == 1                       # d_out required
+    assert _call(lib, d, dq=None) == 1                          # dq required
+    assert _call(lib, d, dq=FAKE) == 1                          # dq aliases q
+    assert _call(lib, d, q=ctypes.c_void_p(0x1004)) == 1        # not 16-byte aligned
     nohost, keep2 = kda.make_desc(2, 8, 2, 128, 128, kda.KDA_BF16)  # no host cu_seqlens
-    assert _call_bwd(lib, nohost) == 1
+    assert _call(lib, nohost) == 1
     small, keep3 = kda.make_desc(2, 8, 2, 64, 64, kda.KDA_BF16, cu)
-    assert _call_bwd(lib, small) == 1                               # supported; no workspace
+    assert _call(lib, small) == 1                               # supported; no workspace
     d.gate_per_head = 1
-    assert _call_bwd(lib, d) == 1  # one gate per head is accepted; the workspace is missing
+    assert _call(lib, d) == 1  # one gate per head is accepted; the workspace is missing
     d.gate_per_head = 3
-    assert _call_bwd(lib, d) == 1
+    assert _call(lib, d) == 1
 
 
 def test_backward_workspace_size_query(lib):
@@ -194,6 +197,22 @@ def test_backward_workspace_size_query(lib):
     assert n.value > 0 and n.value % (16 * 64 * 1024) == 0
     nohost, keep2 = kda.make_desc(2, 100, 4, 128, 128, kda.KDA_BF16)
     assert lib.kda_recurrent_bwd_workspace_size(ctypes.byref(nohost), ctypes.byref(n)) == 1
+
+
+def test_chunk_backward_workspace_size_query(lib):
+    d, keep = kda.make_desc(2, 100, 4, 128, 128, kda.KDA_BF16, [0, 60, 100])
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    # per resident CTA (at most 8 units here): one 64 KiB state per 64 tokens of
+    # the longest sequence (ceil(60 / 64) = 1) plus a ring of 4
+    assert n.value > 0 and n.value % (5 * 64 * 1024) == 0
+    assert n.value <= 8 * 5 * 64 * 1024
+    small, keep3 = kda.make_desc(2, 100, 4, 64, 32, kda.KDA_BF16, [0, 60, 100])
+    m = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(small), ctypes.byref(m)) == 0
+    assert m.value > n.value  # the zero-padded copies come on top
+    nohost, keep2 = kda.make_desc(2, 100, 4, 128, 128, kda.KDA_BF16)
+    assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(nohost), ctypes.byref(n)) == 1
 
 
 def test_short_conv_rejects_bad_arguments(lib):
