@@ -40,9 +40,9 @@
 // Schedule: one CTA of 16 warps per (sequence, head), persistent over units
 // longest first.  S and dS stay fp32 in registers (each warp a 32 x 32 block),
 // with bf16 hi / lo copies in shared memory as MMA operands.  A forward sweep
-// keeps the state entering every 64-token block in the workspace; the reverse
-// sweep rebuilds a block's four chunk-entry states into a ring (L2-resident)
-// and walks the chunks backwards.
+// writes the state entering every chunk to the workspace; the reverse sweep
+// walks the chunks backwards from those states, each chunk's inputs and state
+// prefetched toward L2 one chunk ahead.
 #include <algorithm>
 #include <numeric>
 #include <vector>
@@ -62,8 +62,6 @@ using tc::smem_u32;
 
 constexpr int kD = 128;    // key and value channels
 constexpr int kC = 16;     // tokens per chunk
-constexpr int kBlk = 64;   // tokens between stored states
-constexpr int kSubs = kBlk / kC;
 constexpr int kNT = 512;
 constexpr int kMaxOrder = 2048;
 constexpr size_t kState = (size_t)kD * kD;
@@ -123,7 +121,7 @@ struct Params {
   float* dz;
   float* dbeta;
   float* d_initial;
-  float* ws;            // per CTA: ws_states states (kSubs ring slots, then the block states)
+  float* ws;            // per CTA: ws_states states, one per chunk of the longest sequence
   long long ws_states;
   int* err;
   int H;
@@ -251,6 +249,18 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4],
   mma_16816(d, ah, bl0, bl1);
   mma_16816(d, ah, bh0, bh1);
 }
+// ... when A is exact in bf16 (al = 0)
+__device__ __forceinline__ void mma2a(float (&d)[4], const uint32_t (&ah)[4], uint32_t bh0,
+                                      uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+  mma_16816(d, ah, bl0, bl1);
+  mma_16816(d, ah, bh0, bh1);
+}
+// ... when B is exact in bf16 (bl = 0)
+__device__ __forceinline__ void mma2b(float (&d)[4], const uint32_t (&ah)[4],
+                                      const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1) {
+  mma_16816(d, al, bh0, bh1);
+  mma_16816(d, ah, bh0, bh1);
+}
 __device__ __forceinline__ void negate(uint32_t (&a)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) a[i] ^= 0x80008000u;
@@ -314,8 +324,39 @@ __device__ __forceinline__ void block_planes(const Block& s, unsigned char* sm, 
 // zero log-decay, so they change nothing).  The S planes hold the entering
 // state.  On return (after a block barrier): EG, K+, K-, K~, EC, beta, rk,
 // Araw, T, T', R, U, and with kBack also q^, Q+, dO, rq and P.
+// Lines of the inputs of tokens [ts, ts + 16) of head h toward L2 (k, v, z,
+// and q, dO when kBack): one 128-byte line per thread.
+template <typename T, bool kZHead>
+__device__ __forceinline__ void prefetch_chunk(const Params& P, int h, int ts, bool back) {
+  constexpr int L = (int)sizeof(T) * kD / 128;  // lines per io row
+  const int t = threadIdx.x >> 5, li = threadIdx.x & 31;
+  const int tok = ts + t;
+  if (ts < 0 || tok >= P.total) return;
+  const size_t row = (size_t)tok * P.H + h;
+  const char* a = nullptr;
+  if (li < 4) {
+    if (!kZHead) a = reinterpret_cast<const char*>(P.z + row * kD) + 128 * li;
+  } else if (li < 4 + L) {
+    a = static_cast<const char*>(P.k) + row * kD * sizeof(T) + 128 * (li - 4);
+  } else if (li < 4 + 2 * L) {
+    a = static_cast<const char*>(P.v) + row * kD * sizeof(T) + 128 * (li - 4 - L);
+  } else if (back && li < 4 + 3 * L) {
+    a = static_cast<const char*>(P.q) + row * kD * sizeof(T) + 128 * (li - 4 - 2 * L);
+  } else if (back && li < 4 + 4 * L) {
+    a = static_cast<const char*>(P.d_out) + row * kD * sizeof(T) + 128 * (li - 4 - 3 * L);
+  }
+  if (a) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// Tokens [ts, ts + n) of head h; `s_src`, when given, is the entering state
+// (global [dk][dv]) to load into S and its planes (its loads overlap the
+// staging); `ts_next` / `next_back` name the chunk processed next, whose
+// inputs (and state `s_next`, when given) are prefetched toward L2
+// (ts_next < 0: none).
 template <typename T, bool kZHead, bool kBack>
-__device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, int n, float zc) {
+__device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, int n, float zc,
+                             const float* s_src, const float* s_next, Block& S, int ts_next,
+                             bool next_back) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, q = l & 3;
   const uint32_t sb = smem_u32(sm);
   float* const QH = reinterpret_cast<float*>(sm + OFF_QH);
@@ -327,6 +368,10 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   float* const KHs = reinterpret_cast<float*>(sm + OFF_DR);  // scratch
   float* const Vs = reinterpret_cast<float*>(sm + OFF_DU);   // scratch
   __syncthreads();  // the previous chunk no longer reads any chunk array
+  if (s_src) block_load(S, s_src);
+  prefetch_chunk<T, kZHead>(P, h, ts_next, next_back);
+  if (s_next)  // the next chunk's entering state toward L2: one 128-byte line per thread
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(s_next + 32 * threadIdx.x));
   {  // staging: one warp per token, four channels per lane
     const int t = w, c = 4 * l;
     const bool live = t < n;
@@ -368,25 +413,30 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       vec[64 + t] = 0.f; // dzh
     }
     if (tid < kD) reinterpret_cast<float*>(sm + OFF_DEC)[tid] = 0.f;
-  }
-  __syncthreads();
-  {  // cumulative log-decay and the decayed operands: two channels, two tokens per thread
-    float* const part = reinterpret_cast<float*>(sm + OFF_R);  // scratch [8][128]
-    const int c = 2 * (tid & 63), p = tid >> 6, t0 = 2 * p;
-    const float2 g0 = ld2(Gs + swz(t0, c)), g1 = ld2(Gs + swz(t0 + 1, c));
-    st2(part + p * kD + c, make_float2(g0.x + g1.x, g0.y + g1.y));
-    __syncthreads();
-    float gx = 0.f, gy = 0.f, cx = 0.f, cy = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 v = ld2(part + i * kD + c);
-      if (i < p) {
-        gx += v.x;
-        gy += v.y;
-      }
-      cx += v.x;
-      cy += v.y;
+    if (tid < kC * kC) {  // accumulated by atomics below
+      reinterpret_cast<float*>(sm + OFF_ARAW)[tid] = 0.f;
+      reinterpret_cast<float*>(sm + OFF_DPF)[tid] = 0.f;
+      reinterpret_cast<float*>(sm + OFF_DTP)[tid] = 0.f;
     }
+  }
+  if (s_src) block_planes(S, sm, OFF_S);
+  __syncthreads();
+  {  // cumulative log-decay and the decayed operands: two channels, two tokens
+     // per thread; the eight threads of a channel pair are adjacent lanes
+    const int c = 2 * (tid >> 3), p = tid & 7, t0 = 2 * p;
+    const float2 g0 = ld2(Gs + swz(t0, c)), g1 = ld2(Gs + swz(t0 + 1, c));
+    float sx = g0.x + g1.x, sy = g0.y + g1.y;  // inclusive prefix over the parts
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const float ux = __shfl_up_sync(0xffffffffu, sx, o, 8);
+      const float uy = __shfl_up_sync(0xffffffffu, sy, o, 8);
+      if (p >= o) {
+        sx += ux;
+        sy += uy;
+      }
+    }
+    const float cx = __shfl_sync(0xffffffffu, sx, 7, 8), cy = __shfl_sync(0xffffffffu, sy, 7, 8);
+    float gx = sx - (g0.x + g1.x), gy = sy - (g0.y + g1.y);
     const float ecx = ex2_approx(cx), ecy = ex2_approx(cy);
     if (p == 0) st2(EC + c, make_float2(ecx, ecy));
 #pragma unroll
@@ -410,40 +460,34 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
     }
   }
   __syncthreads();
-  // strict_lower(K+ K-^T) on warps 0-1, lower(Q+ K-^T) on warps 2-3 (one 16 x 8
-  // tile each, K = 128 channels)
-  if (w < 2 || (kBack && w < 4)) {
-    const int nt = w & 1;
-    const uint32_t ao = sb + (w < 2 ? OFF_KP : OFF_QP);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int k0 = 0; k0 < kD; k0 += 16) {
+  // K+ K-^T on warps 0-3 and Q+ K-^T on warps 4-7: each warp one 16 x 8 tile
+  // over half of the 128 channels, summed into fp32 by shared atomics (the
+  // masks are applied where the products are read)
+  if (w < 4 || (kBack && w < 8)) {
+    const int nt = w & 1, kh0 = 64 * ((w >> 1) & 1);
+    const uint32_t ao = sb + (w < 4 ? OFF_KP : OFF_QP);
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = kh0; k0 < kh0 + 64; k0 += 32) {
       uint32_t ah[4], al[4], b[4];
       lda<true>(ao, 0, k0, ah);
       lda<true>(ao + kPlane, 0, k0, al);
       ldb_nk_hl(sb + OFF_KM, sb + OFF_KM + kPlane, k0, 8 * nt, b);
-      mma3(acc, ah, al, b[0], b[1], b[2], b[3]);
+      mma3(acc0, ah, al, b[0], b[1], b[2], b[3]);
+      lda<true>(ao, 0, k0 + 16, ah);
+      lda<true>(ao + kPlane, 0, k0 + 16, al);
+      ldb_nk_hl(sb + OFF_KM, sb + OFF_KM + kPlane, k0 + 16, 8 * nt, b);
+      mma3(acc1, ah, al, b[0], b[1], b[2], b[3]);
     }
-    if (w < 2) {
-      float* const Araw = reinterpret_cast<float*>(sm + OFF_ARAW);
+    float* const M = reinterpret_cast<float*>(sm + (w < 4 ? OFF_ARAW : OFF_DPF));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = g + 8 * (e >> 1), cc = 8 * nt + 2 * q + (e & 1);
-        Araw[r * kC + cc] = cc < r ? acc[e] : 0.f;
-      }
-    } else {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = g + 8 * hf, cc = 8 * nt + 2 * q;
-        st_split(sm + OFF_P, sm + OFF_P + kPlane16, boff16(r, cc), cc <= r ? acc[2 * hf] : 0.f,
-                 cc + 1 <= r ? acc[2 * hf + 1] : 0.f);
-      }
-    }
+    for (int e = 0; e < 4; ++e)
+      atomicAdd(M + (g + 8 * (e >> 1)) * kC + 8 * nt + 2 * q + (e & 1), acc0[e] + acc1[e]);
   }
   // Y = K+ S on this warp's 8 value columns; R = v - Y
   {
     const int n0 = 8 * w;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 32) {
       uint32_t bh[4], bl[4];
@@ -454,20 +498,21 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
         uint32_t ah[4], al[4];
         lda<true>(sb + OFF_KP, 0, k0 + 16 * s, ah);
         lda<true>(sb + OFF_KP + kPlane, 0, k0 + 16 * s, al);
-        mma3(acc, ah, al, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+        mma3(acc[s], ah, al, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
       }
     }
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       const int r = g + 8 * hf, c = n0 + 2 * q;
       const float2 v = ld2(Vs + swz(r, c));
-      st_split(sm + OFF_R, sm + OFF_R + kPlane, boff(r, c), v.x - acc[2 * hf],
-               v.y - acc[2 * hf + 1]);
+      st_split(sm + OFF_R, sm + OFF_R + kPlane, boff(r, c), v.x - acc[0][2 * hf] - acc[1][2 * hf],
+               v.y - acc[0][2 * hf + 1] - acc[1][2 * hf + 1]);
     }
   }
-  // T = (I + A)^{-1} by forward substitution, one lane per column (warp 0,
-  // once warps 0-1 have written A); T' = T diag(beta)
-  if (w < 2) asm volatile("bar.sync 1, 64;" ::: "memory");
+  // T = (I + A)^{-1} (A = diag(beta) strict_lower(K+ K-^T)) by forward
+  // substitution, one lane per column, column entries updated right-looking
+  // (warp 0, once warps 0-3 have added their parts of A); T' = T diag(beta)
+  if (w < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
   if (w == 0) {
     const float* const Araw = reinterpret_cast<const float*>(sm + OFF_ARAW);
     float* const Tm = reinterpret_cast<float*>(sm + OFF_T);
@@ -476,11 +521,10 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
 #pragma unroll
     for (int t = 0; t < kC; ++t) col[t] = t == j ? 1.f : 0.f;
 #pragma unroll
-    for (int t = 1; t < kC; ++t) {
-      float acc = 0.f;
+    for (int m = 0; m < kC - 1; ++m) {
+      const float cm = col[m];
 #pragma unroll
-      for (int m = 0; m < t; ++m) acc = fmaf(Araw[t * kC + m], col[m], acc);
-      if (t > j) col[t] = -beta[t] * acc;
+      for (int u = m + 1; u < kC; ++u) col[u] = fmaf(-beta[u] * Araw[u * kC + m], cm, col[u]);
     }
     if (l < kC) {
       const float bj = beta[j];
@@ -506,12 +550,18 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       st_split(sm + OFF_U, sm + OFF_U + kPlane, boff(g + 8 * hf, n0 + 2 * q), acc[2 * hf],
                acc[2 * hf + 1]);
   }
+  if (kBack && tid < kC * kC) {  // P = lower(Q+ K-^T) to its planes; the sum area back to zero
+    float* const PF = reinterpret_cast<float*>(sm + OFF_DPF);
+    const int a = tid >> 4, b = tid & 15;
+    st_split1(sm + OFF_P, sm + OFF_P + kPlane16, boff16(a, b), b <= a ? PF[tid] : 0.f);
+    PF[tid] = 0.f;
+  }
   __syncthreads();
 }
 
 // S <- Diag(e^{G_C}) S + K~^T U (registers, this warp's block), its planes
-// rewritten, and the block written to `out` (global [dk][dv]) when given.
-__device__ void advance_state(unsigned char* sm, Block& S, float* out) {
+// rewritten.
+__device__ void advance_state(unsigned char* sm, Block& S) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2;
   const uint32_t sb = smem_u32(sm);
   const float* const EC = reinterpret_cast<const float*>(sm + OFF_EC);
@@ -539,15 +589,16 @@ __device__ void advance_state(unsigned char* sm, Block& S, float* out) {
     }
   }
   block_planes(S, sm, OFF_S);
-  if (out) block_store(S, out);
 }
 
 // The reverse step of one chunk (after chunk_common<kBack = true>): the
 // chunk's gradients to global memory; dS (registers) updated to the gradient
 // w.r.t. the state entering the chunk, and its planes rewritten.
-template <bool kZHead>
+template <typename T, bool kZHead>
 __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts, int n, float zs,
                               float zc, Block& dS) {
+  // dO is exact in bf16 for bf16 inputs: its low planes are zero
+  constexpr bool kExactDO = sizeof(T) == 2;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, q = l & 3;
   const uint32_t sb = smem_u32(sm);
   const int n0 = 8 * w;  // this warp's 8 columns of the 16-row products
@@ -567,7 +618,8 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
       lda_t<false>(sb + OFF_P, 0, 0, ah);
       lda_t<false>(sb + OFF_P + kPlane16, 0, 0, al);
       ldb_kn_hl(sb + OFF_DO, sb + OFF_DO + kPlane, n0, b);
-      mma3(acc, ah, al, b[0], b[1], b[2], b[3]);
+      if (kExactDO) mma2b(acc, ah, al, b[0], b[1]);
+      else mma3(acc, ah, al, b[0], b[1], b[2], b[3]);
     }
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 32) {
@@ -624,8 +676,12 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
     for (int s = 0; s < 2; ++s) {
       uint32_t ah[4], al[4];
       lda<true>(sb + OFF_DO, 0, k0 + 16 * s, ah);
-      lda<true>(sb + OFF_DO + kPlane, 0, k0 + 16 * s, al);
-      mma3(dqp, ah, al, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+      if (kExactDO) {
+        mma2a(dqp, ah, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+      } else {
+        lda<true>(sb + OFF_DO + kPlane, 0, k0 + 16 * s, al);
+        mma3(dqp, ah, al, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+      }
     }
   }
   // rowsum(S o dS') over this warp's block, into DEC
@@ -666,32 +722,30 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
       mma3(dkp, ah, al, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
     }
   }
-  // dT' = dU R^T (warps 0-1) and dP = lower(dO U^T) (warps 2-3): 16 x 8 tiles
-  if (w < 4) {
-    const int nt = w & 1;
-    const uint32_t ao = sb + (w < 2 ? OFF_DU : OFF_DO), bo = sb + (w < 2 ? OFF_R : OFF_U);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int k0 = 0; k0 < kD; k0 += 16) {
+  // dT' = dU R^T (warps 0-3) and dO U^T (warps 4-7): each warp one 16 x 8 tile
+  // over half of the 128 value channels, summed into fp32 by shared atomics
+  if (w < 8) {
+    const int nt = w & 1, kh0 = 64 * ((w >> 1) & 1);
+    const bool dp = w >= 4;
+    const uint32_t ao = sb + (dp ? OFF_DO : OFF_DU), bo = sb + (dp ? OFF_U : OFF_R);
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = kh0; k0 < kh0 + 64; k0 += 16) {
       uint32_t ah[4], al[4], b[4];
       lda<true>(ao, 0, k0, ah);
-      lda<true>(ao + kPlane, 0, k0, al);
       ldb_nk_hl(bo, bo + kPlane, k0, 8 * nt, b);
-      mma3(acc, ah, al, b[0], b[1], b[2], b[3]);
-    }
-    float* const M = reinterpret_cast<float*>(sm + (w < 2 ? OFF_DTP : OFF_DPF));
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int r = g + 8 * hf, cc = 8 * nt + 2 * q;
-      float v0 = acc[2 * hf], v1 = acc[2 * hf + 1];
-      if (w >= 2) {
-        v0 = cc <= r ? v0 : 0.f;
-        v1 = cc + 1 <= r ? v1 : 0.f;
-        st_split(sm + OFF_DP, sm + OFF_DP + kPlane16, boff16(r, cc), v0, v1);
+      float (&acc)[4] = (k0 & 16) ? acc1 : acc0;
+      if (kExactDO && dp) {
+        mma2a(acc, ah, b[0], b[1], b[2], b[3]);
+      } else {
+        lda<true>(ao + kPlane, 0, k0, al);
+        mma3(acc, ah, al, b[0], b[1], b[2], b[3]);
       }
-      M[r * kC + cc] = v0;
-      M[r * kC + cc + 1] = v1;
     }
+    float* const M = reinterpret_cast<float*>(sm + (dp ? OFF_DPF : OFF_DTP));
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      atomicAdd(M + (g + 8 * (e >> 1)) * kC + 8 * nt + 2 * q + (e & 1), acc0[e] + acc1[e]);
   }
   // dS <- Diag(e^{G_C}) dS' + Q+^T dO - K+^T dR (registers), then its planes
 #pragma unroll
@@ -709,14 +763,15 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
     for (int np = 0; np < 2; ++np) {
       uint32_t oh[4], ol[4], rh[4], rl[4];
       ldb_kn_2n(sb + OFF_DO, 0, vb + 16 * np, oh);
-      ldb_kn_2n(sb + OFF_DO + kPlane, 0, vb + 16 * np, ol);
+      if (!kExactDO) ldb_kn_2n(sb + OFF_DO + kPlane, 0, vb + 16 * np, ol);
       ldb_kn_2n(sb + OFF_DR, 0, vb + 16 * np, rh);
       ldb_kn_2n(sb + OFF_DR + kPlane, 0, vb + 16 * np, rl);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         float* x = dS.x[mt][2 * np + i];
         float acc[4] = {e_lo * x[0], e_lo * x[1], e_hi * x[2], e_hi * x[3]};
-        mma3(acc, qh_, ql_, oh[2 * i], oh[2 * i + 1], ol[2 * i], ol[2 * i + 1]);
+        if (kExactDO) mma2b(acc, qh_, ql_, oh[2 * i], oh[2 * i + 1]);
+        else mma3(acc, qh_, ql_, oh[2 * i], oh[2 * i + 1], ol[2 * i], ol[2 * i + 1]);
         mma3(acc, kh_, kl_, rh[2 * i], rh[2 * i + 1], rl[2 * i], rl[2 * i + 1]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = acc[e];
@@ -744,6 +799,10 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
       }
       X[a * kC + b] = x * beta[b];
       if (a == 0) db[b] = d1;  // from T' = T diag(beta)
+      float* const dPF = reinterpret_cast<float*>(sm + OFF_DPF);
+      const float dpv = b <= a ? dPF[tid] : 0.f;  // dP = lower(dO U^T)
+      dPF[tid] = dpv;
+      st_split1(sm + OFF_DP, sm + OFF_DP + kPlane16, boff16(a, b), dpv);
     }
     __syncthreads();
     if (tid < 256) {
@@ -869,6 +928,13 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
   float* const dzs = reinterpret_cast<float*>(sm + OFF_DO);  // scratch: dO is no longer read
   {
     const int ch = tid >> 2, p = tid & 3;
+    float zrow[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // the gate logits of rows 4 p + i, early
+      const int r = min(4 * p + i, n - 1);
+      zrow[i] = kZHead ? __ldg(P.z + (size_t)(ts + r) * P.H + h)
+                       : __ldg(P.z + ((size_t)(ts + r) * P.H + h) * kD + ch);
+    }
     const float* const dPF = reinterpret_cast<const float*>(sm + OFF_DPF);
     const float* const dArF = reinterpret_cast<const float*>(sm + OFF_R) + kC * kC;
     float qp[kC], kp[kC], rs[kC];
@@ -929,11 +995,7 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
       for (int t = 0; t < kC; ++t)
         if (t == r) dgv = qp[t] + kp[t] + rs[t];
       dgv += base;
-      float zz = 0.f;
-      if (r < n)
-        zz = kZHead ? __ldg(P.z + (size_t)(ts + r) * P.H + h)
-                    : __ldg(P.z + ((size_t)(ts + r) * P.H + h) * kD + ch);
-      const float gd = log_decay_c(zz, zc);
+      const float gd = log_decay_c(zrow[i], zc);
       const float dzv = r < n ? dgv * gd * (1.f + gd * (1.f / 5.f)) * zs : 0.f;
       if (kZHead) {
         float sum = dzv;
@@ -960,8 +1022,7 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
 template <typename T, bool kZHead>
 __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant__ Params P) {
   extern __shared__ __align__(128) unsigned char sm[];
-  float* const ring = P.ws + (size_t)blockIdx.x * P.ws_states * kState;  // kSubs slots
-  float* const blk = ring + kSubs * kState;                              // every kBlk tokens
+  float* const states = P.ws + (size_t)blockIdx.x * P.ws_states * kState;  // one per chunk
 
   for (int unit = blockIdx.x; unit < P.num_units; unit += gridDim.x) {
     const int si = unit / P.H, h = unit % P.H;
@@ -969,51 +1030,39 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
     int bos, eos;
     if (!seq_range(P.cu, seq, P.total, P.err, bos, eos)) continue;
     const int len = eos - bos;
-    const int nblk = (len + kBlk - 1) / kBlk;
-    if (nblk + kSubs > P.ws_states) {  // workspace planned for shorter sequences
+    const int nch = (len + kC - 1) / kC;
+    if (nch > P.ws_states) {  // workspace planned for shorter sequences
       report_error(P.err, kErrDeviceCheck);
       continue;
     }
     const float zs = gate_scale(P.a_log, h), zc = gate_coef(zs);
     const size_t st_off = ((size_t)seq * P.H + h) * kState;
 
-    // ---- forward: the state entering every 64-token block ----
+    // ---- forward: the state entering every chunk ----
     __syncthreads();  // the previous unit no longer reads any plane
     Block S;
     block_load(S, P.initial_state ? P.initial_state + st_off : nullptr);
     block_planes(S, sm, OFF_S);
-    for (int b = 0; b < nblk; ++b) {
-      block_store(S, blk + (size_t)b * kState);
-      if (b == nblk - 1) break;  // the last block is rebuilt in the reverse sweep
-      for (int j = 0; j < kSubs; ++j) {
-        chunk_common<T, kZHead, false>(sm, P, h, bos + b * kBlk + j * kC, kC, zc);
-        advance_state(sm, S, nullptr);
-      }
+    for (int j = 0; j < nch; ++j) {
+      block_store(S, states + (size_t)j * kState);
+      if (j == nch - 1) break;  // the last chunk's state is not needed
+      const int ts = bos + j * kC;
+      // next: the following chunk (after the last forward one, the reverse sweep's first)
+      chunk_common<T, kZHead, false>(sm, P, h, ts, kC, zc, nullptr, nullptr, S, ts + kC,
+                                     j + 2 == nch);
+      advance_state(sm, S);
     }
 
-    // ---- reverse sweep ----
+    // ---- reverse sweep: each chunk from its stored entering state ----
     Block dS;
     block_load(dS, P.d_final ? P.d_final + st_off : nullptr);
     block_planes(dS, sm, OFF_DS);
-    for (int b = nblk - 1; b >= 0; --b) {
-      const int b0 = b * kBlk, bl = min(kBlk, len - b0), ns = (bl + kC - 1) / kC;
-      __syncthreads();  // the previous chunk no longer reads the S planes
-      block_load(S, blk + (size_t)b * kState);
-      block_planes(S, sm, OFF_S);
-      // rebuild the block's chunk-entry states: slot j holds the state entering chunk j
-      for (int j = 0; j + 1 < ns; ++j) {
-        chunk_common<T, kZHead, false>(sm, P, h, bos + b0 + j * kC, kC, zc);
-        advance_state(sm, S, ring + (size_t)(j + 1) * kState);
-      }
-      for (int j = ns - 1; j >= 0; --j) {
-        if (j < ns - 1) {
-          __syncthreads();
-          block_load(S, j == 0 ? blk + (size_t)b * kState : ring + (size_t)j * kState);
-          block_planes(S, sm, OFF_S);
-        }
-        chunk_common<T, kZHead, true>(sm, P, h, bos + b0 + j * kC, min(kC, bl - j * kC), zc);
-        chunk_reverse<kZHead>(sm, P, h, bos + b0 + j * kC, min(kC, bl - j * kC), zs, zc, dS);
-      }
+    for (int j = nch - 1; j >= 0; --j) {
+      const int ts = bos + j * kC, n = min(kC, len - j * kC);
+      chunk_common<T, kZHead, true>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
+                                    j > 0 ? states + (size_t)(j - 1) * kState : nullptr, S,
+                                    j > 0 ? ts - kC : -1, true);
+      chunk_reverse<T, kZHead>(sm, P, h, ts, n, zs, zc, dS);
     }
     if (P.d_initial) block_store(dS, P.d_initial + st_off);
   }
@@ -1033,7 +1082,7 @@ int grid_for(const Problem& p) {
 long long states_per_cta(const Problem& p, const int32_t* cu_host) {
   int max_len = 0;
   for (int n = 0; n < p.num_seqs; ++n) max_len = std::max(max_len, cu_host[n + 1] - cu_host[n]);
-  return (long long)(max_len + kBlk - 1) / kBlk + kSubs;
+  return std::max<long long>(1, (max_len + kC - 1) / kC);
 }
 
 }  // namespace cbwd
