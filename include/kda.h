@@ -492,7 +492,7 @@ kda_status_t kda_recurrent_bwd_workspace_size(const kda_desc_t* desc, size_t* by
  * dR S^T, U dS'^T, K~ dS', Q+^T dO - K+^T dR, ...) and the chunk's own 16 x 16
  * products run on the tensor cores (bf16 MMAs, fp32 accumulation); states
  * and their gradients stay fp32.  A forward sweep keeps the state entering
- * every chunk in the workspace.
+ * every chunk, and the chunk's R = V - K+ S, U, A and T, in the workspace.
  * Arguments, layouts, dtypes, alignment and errors exactly as for
  * kda_recurrent_bwd (any supported dk, dv; per-channel or per-head gate;
  * a_log honoured; cu_seqlens_host REQUIRED); the workspace must hold
@@ -509,9 +509,10 @@ kda_status_t kda_chunk_bwd(const kda_desc_t* desc, const void* q, const void* k,
                            float* dz, float* dbeta, float* d_initial_state, kda_stream_t stream);
 
 /* Bytes of device workspace kda_chunk_bwd needs (needs desc->cu_seqlens_host):
- * for every resident CTA (at most one per SM) 64 KiB per 16 tokens of the
- * longest sequence; below dk = dv = 128 also the zero-padded copies of the
- * inputs and gradients. */
+ * for every resident CTA (at most one per SM) 84 KiB per 16 tokens of the
+ * longest sequence (the state entering each chunk and 20 KiB of the chunk's
+ * own products); below dk = dv = 128 also the zero-padded copies of the inputs
+ * and gradients. */
 kda_status_t kda_chunk_bwd_workspace_size(const kda_desc_t* desc, size_t* bytes);
 
 /*

@@ -40,9 +40,10 @@
 // Schedule: one CTA of 16 warps per (sequence, head), persistent over units
 // longest first.  S and dS stay fp32 in registers (each warp a 32 x 32 block),
 // with bf16 hi / lo copies in shared memory as MMA operands.  A forward sweep
-// writes the state entering every chunk to the workspace; the reverse sweep
-// walks the chunks backwards from those states, each chunk's inputs and state
-// prefetched toward L2 one chunk ahead.
+// writes the state entering every chunk to the workspace, with the chunk's R,
+// U, A and T; the reverse sweep walks the chunks backwards from those records
+// (recomputing only what involves q and dO), each chunk's inputs, state and
+// record prefetched toward L2 one chunk ahead.
 #include <algorithm>
 #include <numeric>
 #include <vector>
@@ -99,6 +100,15 @@ constexpr int OFF_DEC = OFF_EC + 512;           // rowsum(S o dS') [128]
 constexpr int OFF_VEC = OFF_DEC + 512;          // beta, rq, rk, db, dzh [16] each
 constexpr int SMEM_BYTES = OFF_VEC + 5 * 64;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+// What the forward sweep keeps of each chunk besides its state, copied verbatim
+// from / to shared memory: the R and U planes, A and T (fp32), the T' planes.
+constexpr int kKeptRU = 4 * kPlane;          // R hi, lo, U hi, lo
+constexpr int kKeptAT = 2048;                // A, T fp32
+constexpr int kKeptTP = 2 * kPlane16;        // T' hi, lo
+constexpr int kKeptBytes = kKeptRU + kKeptAT + kKeptTP;
+constexpr int kKeptStride = 20480;
+static_assert(OFF_U == OFF_R + 2 * kPlane && OFF_T == OFF_ARAW + 1024, "kept regions");
+static_assert(kKeptBytes <= kKeptStride && kKeptBytes % (16 * 4) == 0, "kept layout");
 // fp32 scratch laid over operands that are dead at the time:
 //   staging: g (log2 units) on U, k^ on dR, v on dU, the scan's partial sums on R
 //   reverse: the dg state terms on dU and dR, T^T dT and dAr (fp32) on R,
@@ -121,7 +131,8 @@ struct Params {
   float* dz;
   float* dbeta;
   float* d_initial;
-  float* ws;            // per CTA: ws_states states, one per chunk of the longest sequence
+  float* ws;            // per CTA: ws_states states, one per chunk of the longest
+                        // sequence, then as many kept records (kKeptStride bytes each)
   long long ws_states;
   int* err;
   int H;
@@ -319,6 +330,14 @@ __device__ __forceinline__ void block_planes(const Block& s, unsigned char* sm, 
       }
 }
 
+// byte i (multiple of 16) of a kept record <-> its place in shared memory
+__device__ __forceinline__ int kept_smem_off(int i) {
+  return i < kKeptRU ? OFF_R + i
+                     : (i < kKeptRU + kKeptAT ? OFF_ARAW + (i - kKeptRU)
+                                              : OFF_TP + (i - kKeptRU - kKeptAT));
+}
+constexpr int kKeptPerThread = (kKeptBytes / 16 + kNT - 1) / kNT;
+
 // ---- steps shared by the forward rebuild and the reverse step of a chunk ----
 // Tokens [ts, ts + n) of head h (n <= 16; rows at or past n are zero, with a
 // zero log-decay, so they change nothing).  The S planes hold the entering
@@ -353,10 +372,11 @@ __device__ __forceinline__ void prefetch_chunk(const Params& P, int h, int ts, b
 // staging); `ts_next` / `next_back` name the chunk processed next, whose
 // inputs (and state `s_next`, when given) are prefetched toward L2
 // (ts_next < 0: none).
-template <typename T, bool kZHead, bool kBack>
+template <typename T, bool kZHead, bool kBack, bool kKept = false>
 __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, int n, float zc,
                              const float* s_src, const float* s_next, Block& S, int ts_next,
-                             bool next_back) {
+                             bool next_back, const unsigned char* kept = nullptr,
+                             const unsigned char* kept_next = nullptr) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, q = l & 3;
   const uint32_t sb = smem_u32(sm);
   float* const QH = reinterpret_cast<float*>(sm + OFF_QH);
@@ -364,7 +384,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   float* const EC = reinterpret_cast<float*>(sm + OFF_EC);
   float* const vec = reinterpret_cast<float*>(sm + OFF_VEC);
   float* const beta = vec;
-  float* const Gs = reinterpret_cast<float*>(sm + OFF_U);    // scratch
+  float* const Gs = reinterpret_cast<float*>(sm + (kKept ? OFF_DU : OFF_U));  // scratch
   float* const KHs = reinterpret_cast<float*>(sm + OFF_DR);  // scratch
   float* const Vs = reinterpret_cast<float*>(sm + OFF_DU);   // scratch
   __syncthreads();  // the previous chunk no longer reads any chunk array
@@ -372,6 +392,16 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   prefetch_chunk<T, kZHead>(P, h, ts_next, next_back);
   if (s_next)  // the next chunk's entering state toward L2: one 128-byte line per thread
     asm volatile("prefetch.global.L2 [%0];" ::"l"(s_next + 32 * threadIdx.x));
+  if (kept_next && tid * 128 < kKeptBytes)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(kept_next + 128 * tid));
+  uint4 kv[kKeptPerThread];
+  if (kKept) {  // this chunk's kept record, in flight during the staging
+#pragma unroll
+    for (int i = 0; i < kKeptPerThread; ++i) {
+      const int b = 16 * (tid + i * kNT);
+      if (b < kKeptBytes) kv[i] = __ldcg(reinterpret_cast<const uint4*>(kept + b));
+    }
+  }
   {  // staging: one warp per token, four channels per lane
     const int t = w, c = 4 * l;
     const bool live = t < n;
@@ -391,7 +421,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c), x.x, x.y);
       st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c + 2), x.z, x.w);
     }
-    st4(Vs + swz(t, c), live ? ld4_io<T>(static_cast<const T*>(P.v) + row) : zero4);
+    if (!kKept) st4(Vs + swz(t, c), live ? ld4_io<T>(static_cast<const T*>(P.v) + row) : zero4);
     float4 zz = zero4;
     if (live) {
       if (kZHead) {
@@ -414,12 +444,19 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
     }
     if (tid < kD) reinterpret_cast<float*>(sm + OFF_DEC)[tid] = 0.f;
     if (tid < kC * kC) {  // accumulated by atomics below
-      reinterpret_cast<float*>(sm + OFF_ARAW)[tid] = 0.f;
+      if (!kKept) reinterpret_cast<float*>(sm + OFF_ARAW)[tid] = 0.f;
       reinterpret_cast<float*>(sm + OFF_DPF)[tid] = 0.f;
       reinterpret_cast<float*>(sm + OFF_DTP)[tid] = 0.f;
     }
   }
   if (s_src) block_planes(S, sm, OFF_S);
+  if (kKept) {
+#pragma unroll
+    for (int i = 0; i < kKeptPerThread; ++i) {
+      const int b = 16 * (tid + i * kNT);
+      if (b < kKeptBytes) *reinterpret_cast<uint4*>(sm + kept_smem_off(b)) = kv[i];
+    }
+  }
   __syncthreads();
   {  // cumulative log-decay and the decayed operands: two channels, two tokens
      // per thread; the eight threads of a channel pair are adjacent lanes
@@ -463,7 +500,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   // K+ K-^T on warps 0-3 and Q+ K-^T on warps 4-7: each warp one 16 x 8 tile
   // over half of the 128 channels, summed into fp32 by shared atomics (the
   // masks are applied where the products are read)
-  if (w < 4 || (kBack && w < 8)) {
+  if ((!kKept && w < 4) || (kBack && w >= 4 && w < 8)) {
     const int nt = w & 1, kh0 = 64 * ((w >> 1) & 1);
     const uint32_t ao = sb + (w < 4 ? OFF_KP : OFF_QP);
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -485,7 +522,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       atomicAdd(M + (g + 8 * (e >> 1)) * kC + 8 * nt + 2 * q + (e & 1), acc0[e] + acc1[e]);
   }
   // Y = K+ S on this warp's 8 value columns; R = v - Y
-  {
+  if (!kKept) {
     const int n0 = 8 * w;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 2
@@ -512,8 +549,8 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   // T = (I + A)^{-1} (A = diag(beta) strict_lower(K+ K-^T)) by forward
   // substitution, one lane per column, column entries updated right-looking
   // (warp 0, once warps 0-3 have added their parts of A); T' = T diag(beta)
-  if (w < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
-  if (w == 0) {
+  if (!kKept && w < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (!kKept && w == 0) {
     const float* const Araw = reinterpret_cast<const float*>(sm + OFF_ARAW);
     float* const Tm = reinterpret_cast<float*>(sm + OFF_T);
     const int j = l & 15;
@@ -537,7 +574,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   }
   __syncthreads();
   // U = T' R on this warp's 8 value columns
-  {
+  if (!kKept) {
     const int n0 = 8 * w;
     uint32_t ah[4], al[4], b[4];
     lda<false>(sb + OFF_TP, 0, 0, ah);
@@ -1022,7 +1059,9 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
 template <typename T, bool kZHead>
 __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant__ Params P) {
   extern __shared__ __align__(128) unsigned char sm[];
-  float* const states = P.ws + (size_t)blockIdx.x * P.ws_states * kState;  // one per chunk
+  float* const states =
+      P.ws + (size_t)blockIdx.x * P.ws_states * (kState + kKeptStride / 4);  // one per chunk
+  unsigned char* const kept = reinterpret_cast<unsigned char*>(states + P.ws_states * kState);
 
   for (int unit = blockIdx.x; unit < P.num_units; unit += gridDim.x) {
     const int si = unit / P.H, h = unit % P.H;
@@ -1050,6 +1089,13 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
       // next: the following chunk (after the last forward one, the reverse sweep's first)
       chunk_common<T, kZHead, false>(sm, P, h, ts, kC, zc, nullptr, nullptr, S, ts + kC,
                                      j + 2 == nch);
+#pragma unroll
+      for (int i = 0; i < kKeptPerThread; ++i) {  // the chunk's kept record
+        const int b = 16 * (threadIdx.x + i * kNT);
+        if (b < kKeptBytes)
+          __stcg(reinterpret_cast<uint4*>(kept + (size_t)j * kKeptStride + b),
+                 *reinterpret_cast<const uint4*>(sm + kept_smem_off(b)));
+      }
       advance_state(sm, S);
     }
 
@@ -1059,9 +1105,16 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
     block_planes(dS, sm, OFF_DS);
     for (int j = nch - 1; j >= 0; --j) {
       const int ts = bos + j * kC, n = min(kC, len - j * kC);
-      chunk_common<T, kZHead, true>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
-                                    j > 0 ? states + (size_t)(j - 1) * kState : nullptr, S,
-                                    j > 0 ? ts - kC : -1, true);
+      const float* const s_next = j > 0 ? states + (size_t)(j - 1) * kState : nullptr;
+      const unsigned char* const k_next = j > 0 ? kept + (size_t)(j - 1) * kKeptStride : nullptr;
+      if (j == nch - 1)  // the last chunk has no kept record: computed in full
+        chunk_common<T, kZHead, true, false>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
+                                             s_next, S, j > 0 ? ts - kC : -1, true, nullptr,
+                                             k_next);
+      else
+        chunk_common<T, kZHead, true, true>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
+                                            s_next, S, j > 0 ? ts - kC : -1, true,
+                                            kept + (size_t)j * kKeptStride, k_next);
       chunk_reverse<T, kZHead>(sm, P, h, ts, n, zs, zc, dS);
     }
     if (P.d_initial) block_store(dS, P.d_initial + st_off);
@@ -1089,8 +1142,8 @@ long long states_per_cta(const Problem& p, const int32_t* cu_host) {
 
 size_t chunk_bwd_inner_bytes(const Problem& p, const int32_t* cu_host) {
   if (p.num_seqs == 0 || p.num_heads == 0) return 0;
-  return (size_t)cbwd::grid_for(p) * (size_t)cbwd::states_per_cta(p, cu_host) * cbwd::kState *
-         sizeof(float);
+  return (size_t)cbwd::grid_for(p) * (size_t)cbwd::states_per_cta(p, cu_host) *
+         (cbwd::kState * sizeof(float) + cbwd::kKeptStride);
 }
 
 cudaError_t launch_chunk_bwd_128(const Problem& p, const BwdArgs& a, const int32_t* cu_host,

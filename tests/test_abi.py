@@ -203,10 +203,10 @@ def test_chunk_backward_workspace_size_query(lib):
     d, keep = kda.make_desc(2, 100, 4, 128, 128, kda.KDA_BF16, [0, 60, 100])
     n = ctypes.c_size_t(0)
     assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    # per resident CTA (at most 8 units here): one 64 KiB state per 16 tokens of
-    # the longest sequence (ceil(60 / 16) = 4)
-    assert n.value > 0 and n.value % (4 * 64 * 1024) == 0
-    assert n.value <= 8 * 4 * 64 * 1024
+    # per resident CTA (at most 8 units here): per 16 tokens of the longest
+    # sequence (ceil(60 / 16) = 4) one 64 KiB state and a 20 KiB chunk record
+    assert n.value > 0 and n.value % (4 * 84 * 1024) == 0
+    assert n.value <= 8 * 4 * 84 * 1024
     small, keep3 = kda.make_desc(2, 100, 4, 64, 32, kda.KDA_BF16, [0, 60, 100])
     m = ctypes.c_size_t(0)
     assert lib.kda_chunk_bwd_workspace_size(ctypes.byref(small), ctypes.byref(m)) == 0
