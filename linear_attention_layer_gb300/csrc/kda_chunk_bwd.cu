@@ -40,10 +40,12 @@
 // Schedule: one CTA of 16 warps per (sequence, head), persistent over units
 // longest first.  S and dS stay fp32 in registers (each warp a 32 x 32 block),
 // with bf16 hi / lo copies in shared memory as MMA operands.  A forward sweep
-// writes the state entering every chunk to the workspace, with the chunk's R,
-// U, A and T; the reverse sweep walks the chunks backwards from those records
-// (recomputing only what involves q and dO), each chunk's inputs, state and
-// record prefetched toward L2 one chunk ahead.
+// writes the state entering every chunk to the workspace (as its hi / lo
+// planes, the only form the reverse step reads), with the chunk's R, U, A and
+// T; the reverse sweep walks the chunks backwards, copying each chunk's planes
+// and record straight into shared memory (cp.async) and recomputing only what
+// involves q and dO; each chunk's inputs, state and record are prefetched
+// toward L2 one chunk ahead.
 #include <algorithm>
 #include <numeric>
 #include <vector>
@@ -131,8 +133,8 @@ struct Params {
   float* dz;
   float* dbeta;
   float* d_initial;
-  float* ws;            // per CTA: ws_states states, one per chunk of the longest
-                        // sequence, then as many kept records (kKeptStride bytes each)
+  float* ws;            // per CTA: ws_states state plane images (64 KiB), one per chunk
+                        // of the longest sequence, then as many kept records
   long long ws_states;
   int* err;
   int H;
@@ -330,6 +332,24 @@ __device__ __forceinline__ void block_planes(const Block& s, unsigned char* sm, 
       }
 }
 
+// 16 bytes global -> shared without registers (cp.async; completed by cp_async_wait)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+// The S planes (hi and lo, 64 KiB, as laid out in shared memory) to global memory
+__device__ __forceinline__ void planes_out(const unsigned char* sm, float* dst) {
+#pragma unroll
+  for (int i = 0; i < 2 * kPlaneS / 16 / kNT; ++i) {
+    const int b = 16 * (threadIdx.x + i * kNT);
+    __stcg(reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(dst) + b),
+           *reinterpret_cast<const uint4*>(sm + OFF_S + b));
+  }
+}
+
 // byte i (multiple of 16) of a kept record <-> its place in shared memory
 __device__ __forceinline__ int kept_smem_off(int i) {
   return i < kKeptRU ? OFF_R + i
@@ -367,15 +387,15 @@ __device__ __forceinline__ void prefetch_chunk(const Params& P, int h, int ts, b
   if (a) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
 
-// Tokens [ts, ts + n) of head h; `s_src`, when given, is the entering state
-// (global [dk][dv]) to load into S and its planes (its loads overlap the
-// staging); `ts_next` / `next_back` name the chunk processed next, whose
-// inputs (and state `s_next`, when given) are prefetched toward L2
-// (ts_next < 0: none).
+// Tokens [ts, ts + n) of head h; `s_src`, when given, is the entering
+// state's planes as kept in global memory, copied into the S planes under the
+// staging (`s_out`, when given: the S planes are written there);
+// `ts_next` / `next_back` name the chunk processed next, whose inputs (and
+// state `s_next`, when given) are prefetched toward L2 (ts_next < 0: none).
 template <typename T, bool kZHead, bool kBack, bool kKept = false>
 __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, int n, float zc,
-                             const float* s_src, const float* s_next, Block& S, int ts_next,
-                             bool next_back, const unsigned char* kept = nullptr,
+                             const float* s_src, const float* s_next, float* s_out,
+                             int ts_next, bool next_back, const unsigned char* kept = nullptr,
                              const unsigned char* kept_next = nullptr) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31, g = l >> 2, q = l & 3;
   const uint32_t sb = smem_u32(sm);
@@ -388,18 +408,24 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
   float* const KHs = reinterpret_cast<float*>(sm + OFF_DR);  // scratch
   float* const Vs = reinterpret_cast<float*>(sm + OFF_DU);   // scratch
   __syncthreads();  // the previous chunk no longer reads any chunk array
-  if (s_src) block_load(S, s_src);
+  if (s_src) {
+#pragma unroll
+    for (int i = 0; i < 2 * kPlaneS / 16 / kNT; ++i) {
+      const int b = 16 * (tid + i * kNT);
+      cp_async16(sm + OFF_S + b, reinterpret_cast<const unsigned char*>(s_src) + b);
+    }
+  }
+  if (s_out) planes_out(sm, s_out);
   prefetch_chunk<T, kZHead>(P, h, ts_next, next_back);
   if (s_next)  // the next chunk's entering state toward L2: one 128-byte line per thread
     asm volatile("prefetch.global.L2 [%0];" ::"l"(s_next + 32 * threadIdx.x));
   if (kept_next && tid * 128 < kKeptBytes)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(kept_next + 128 * tid));
-  uint4 kv[kKeptPerThread];
   if (kKept) {  // this chunk's kept record, in flight during the staging
 #pragma unroll
     for (int i = 0; i < kKeptPerThread; ++i) {
       const int b = 16 * (tid + i * kNT);
-      if (b < kKeptBytes) kv[i] = __ldcg(reinterpret_cast<const uint4*>(kept + b));
+      if (b < kKeptBytes) cp_async16(sm + kept_smem_off(b), kept + b);
     }
   }
   {  // staging: one warp per token, four channels per lane
@@ -449,14 +475,7 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       reinterpret_cast<float*>(sm + OFF_DTP)[tid] = 0.f;
     }
   }
-  if (s_src) block_planes(S, sm, OFF_S);
-  if (kKept) {
-#pragma unroll
-    for (int i = 0; i < kKeptPerThread; ++i) {
-      const int b = 16 * (tid + i * kNT);
-      if (b < kKeptBytes) *reinterpret_cast<uint4*>(sm + kept_smem_off(b)) = kv[i];
-    }
-  }
+  if (s_src || kKept) cp_async_wait();
   __syncthreads();
   {  // cumulative log-decay and the decayed operands: two channels, two tokens
      // per thread; the eight threads of a channel pair are adjacent lanes
@@ -1082,13 +1101,12 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
     Block S;
     block_load(S, P.initial_state ? P.initial_state + st_off : nullptr);
     block_planes(S, sm, OFF_S);
-    for (int j = 0; j < nch; ++j) {
-      block_store(S, states + (size_t)j * kState);
-      if (j == nch - 1) break;  // the last chunk's state is not needed
+    for (int j = 0; j + 1 < nch; ++j) {
       const int ts = bos + j * kC;
-      // next: the following chunk (after the last forward one, the reverse sweep's first)
-      chunk_common<T, kZHead, false>(sm, P, h, ts, kC, zc, nullptr, nullptr, S, ts + kC,
-                                     j + 2 == nch);
+      // next: the following chunk (after the last forward one, the reverse sweep's first);
+      // the entering state's planes are kept
+      chunk_common<T, kZHead, false>(sm, P, h, ts, kC, zc, nullptr, nullptr,
+                                     states + (size_t)j * kState, ts + kC, j + 2 == nch);
 #pragma unroll
       for (int i = 0; i < kKeptPerThread; ++i) {  // the chunk's kept record
         const int b = 16 * (threadIdx.x + i * kNT);
@@ -1097,6 +1115,10 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
                  *reinterpret_cast<const uint4*>(sm + kept_smem_off(b)));
       }
       advance_state(sm, S);
+    }
+    if (nch > 0) {  // the last chunk's entering state
+      __syncthreads();
+      planes_out(sm, states + (size_t)(nch - 1) * kState);
     }
 
     // ---- reverse sweep: each chunk from its stored entering state ----
@@ -1109,11 +1131,11 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
       const unsigned char* const k_next = j > 0 ? kept + (size_t)(j - 1) * kKeptStride : nullptr;
       if (j == nch - 1)  // the last chunk has no kept record: computed in full
         chunk_common<T, kZHead, true, false>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
-                                             s_next, S, j > 0 ? ts - kC : -1, true, nullptr,
-                                             k_next);
+                                             s_next, nullptr, j > 0 ? ts - kC : -1, true,
+                                             nullptr, k_next);
       else
         chunk_common<T, kZHead, true, true>(sm, P, h, ts, n, zc, states + (size_t)j * kState,
-                                            s_next, S, j > 0 ? ts - kC : -1, true,
+                                            s_next, nullptr, j > 0 ? ts - kC : -1, true,
                                             kept + (size_t)j * kKeptStride, k_next);
       chunk_reverse<T, kZHead>(sm, P, h, ts, n, zs, zc, dS);
     }
