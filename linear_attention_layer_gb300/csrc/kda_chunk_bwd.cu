@@ -428,27 +428,18 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
       if (b < kKeptBytes) cp_async16(sm + kept_smem_off(b), kept + b);
     }
   }
-  {  // staging: one warp per token, four channels per lane
+  {  // staging: one warp per token, four channels per lane; every load issued first
     const int t = w, c = 4 * l;
     const bool live = t < n;
     const size_t row = ((size_t)(ts + t) * P.H + h) * kD + c;
     const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 x = live ? ld4_io<T>(static_cast<const T*>(P.k) + row) : zero4;
-    float r = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
-    const float rk = live ? rsqrtf(r + kNormEps) : 0.f;
-    st4(KHs + swz(t, c), make_float4(x.x * rk, x.y * rk, x.z * rk, x.w * rk));
-    float rq = 0.f;
-    if (kBack) {
-      x = live ? ld4_io<T>(static_cast<const T*>(P.q) + row) : zero4;
-      r = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
-      rq = live ? rsqrtf(r + kNormEps) : 0.f;
-      st4(QH + swz(t, c), make_float4(x.x * rq, x.y * rq, x.z * rq, x.w * rq));
-      x = live ? ld4_io<T>(static_cast<const T*>(P.d_out) + row) : zero4;
-      st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c), x.x, x.y);
-      st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c + 2), x.z, x.w);
+    const float4 xk = live ? ld4_io<T>(static_cast<const T*>(P.k) + row) : zero4;
+    float4 xq = zero4, xo = zero4, xv = zero4, zz = zero4;
+    if (kBack && live) {
+      xq = ld4_io<T>(static_cast<const T*>(P.q) + row);
+      xo = ld4_io<T>(static_cast<const T*>(P.d_out) + row);
     }
-    if (!kKept) st4(Vs + swz(t, c), live ? ld4_io<T>(static_cast<const T*>(P.v) + row) : zero4);
-    float4 zz = zero4;
+    if (!kKept && live) xv = ld4_io<T>(static_cast<const T*>(P.v) + row);
     if (live) {
       if (kZHead) {
         const float z1 = __ldg(P.z + (size_t)(ts + t) * P.H + h);
@@ -457,12 +448,25 @@ __device__ void chunk_common(unsigned char* sm, const Params& P, int h, int ts, 
         zz = __ldg(reinterpret_cast<const float4*>(P.z + row));
       }
     }
+    const float bt = (live && l == 0) ? __ldg(P.beta + (size_t)(ts + t) * P.H + h) : 0.f;
+    float r = warp_sum(xk.x * xk.x + xk.y * xk.y + xk.z * xk.z + xk.w * xk.w);
+    const float rk = live ? rsqrtf(r + kNormEps) : 0.f;
+    st4(KHs + swz(t, c), make_float4(xk.x * rk, xk.y * rk, xk.z * rk, xk.w * rk));
+    float rq = 0.f;
+    if (kBack) {
+      r = warp_sum(xq.x * xq.x + xq.y * xq.y + xq.z * xq.z + xq.w * xq.w);
+      rq = live ? rsqrtf(r + kNormEps) : 0.f;
+      st4(QH + swz(t, c), make_float4(xq.x * rq, xq.y * rq, xq.z * rq, xq.w * rq));
+      st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c), xo.x, xo.y);
+      st_split(sm + OFF_DO, sm + OFF_DO + kPlane, boff(t, c + 2), xo.z, xo.w);
+    }
+    if (!kKept) st4(Vs + swz(t, c), xv);
     st4(Gs + swz(t, c),
         live ? make_float4(log_decay_c(zz.x, zc) * kLog2e, log_decay_c(zz.y, zc) * kLog2e,
                            log_decay_c(zz.z, zc) * kLog2e, log_decay_c(zz.w, zc) * kLog2e)
              : zero4);
     if (l == 0) {
-      beta[t] = live ? __ldg(P.beta + (size_t)(ts + t) * P.H + h) : 0.f;
+      beta[t] = bt;
       vec[32 + t] = rk;  // rk
       vec[16 + t] = rq;  // rq
       vec[48 + t] = 0.f; // db
