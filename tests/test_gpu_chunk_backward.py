@@ -213,3 +213,31 @@ def test_chunk_backward_matches_recurrent_on_prefill_workload():
                               sl(d_out), d_fin[n:n + 1, h:h + 1].cpu())
         mine = [g[a:b, h:h + 1] for g in got[:5]] + [got[5][n:n + 1, h:h + 1]]
         _compare(mine, ref, f"prefill workload ({n}, {h})")
+
+
+def test_chunk_backward_matches_recurrent_on_varlen_workload():
+    """The bench's varlen workload (64 sequences of 256..8192 tokens, 32 heads,
+    initial state) in one launch: every gradient tensor against the per-token
+    fp32 reverse mode on the GPU (itself held to the oracle at 1e-4), with the
+    cotangents the bench draws."""
+    p = workloads.prefill_workload("varlen", device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(99)
+    H = p.meta["num_heads"]
+    d_out = torch.randn(p.v.shape, device=DEV, generator=g).to(p.q.dtype)
+    d_fin = torch.randn((p.num_seqs, H, 128, 128), device=DEV, generator=g)
+    got = _run(p, d_out, d_fin)
+    ref = kda.recurrent_bwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out,
+                            d_fin, cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    for name, x, r in zip(NAMES, got, ref):
+        diff = (x - r).double()
+        rel = float(torch.linalg.vector_norm(diff) / torch.linalg.vector_norm(r.double()))
+        rms = float(torch.sqrt(torch.mean(r.double() ** 2)))
+        mx = float(diff.abs().max()) / rms
+        print(f"varlen workload vs recurrent_bwd, {name}: rel-L2 {rel:.2e}, max/RMS {mx:.2e}")
+        assert rel <= TOL_REL and mx <= TOL_MAX, (name, rel, mx)
+        del diff
+    del got, ref
+    torch.cuda.empty_cache()
