@@ -241,3 +241,28 @@ def test_chunk_backward_matches_recurrent_on_varlen_workload():
         del diff
     del got, ref
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fn", ["recurrent_bwd", "chunk_bwd"])
+def test_backward_device_lengths_beyond_the_host_plan(fn):
+    """The workspace is planned from the host copy of cu_seqlens; a device copy
+    with a longer sequence than planned makes the kernel skip that sequence
+    (no workspace access past the plan), record KDA_ERR_DEVICE_CHECK, and leave
+    the context usable: the next call with matching offsets is correct."""
+    p = workloads.random_problem([20, 20], 1, 128, 128, torch.bfloat16, init_std=0.1, seed=31,
+                                 device=DEV)
+    d_out, d_fin = _cotangents(p, 12)
+    f = getattr(kda, fn)
+    bad = torch.tensor([0, 5, 40], dtype=torch.int32, device=DEV)  # sequence 1: 35 > 20 tokens
+    assert kda.get_device_error() == 0
+    f(p.q, p.k, p.v, p.z, p.beta, bad, p.initial_state, d_out, d_fin,
+      cu_seqlens_host=p.cu_seqlens_host)
+    assert kda.get_device_error() == 5
+    assert kda.get_device_error() == 0  # cleared by the read
+    got = f(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state, d_out, d_fin,
+            cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    ref = oracle.backward(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state,
+                          d_out, d_fin)
+    _compare(got, ref, f"{fn} after a device check")
