@@ -31,9 +31,12 @@ def _unit(x, eps):
     return x * r, r
 
 
-def chunked_backward(q, k, v, z, beta, s0, d_out, d_fin, chunk=8, a_log=0.0, eps=1e-6):
+def chunked_backward(q, k, v, z, beta, s0, d_out, d_fin, chunk=8, a_log=0.0, eps=1e-6,
+                     dg_form="plain"):
     """One sequence, one head.  q, k, z: [T, dk]; v, d_out: [T, dv]; beta: [T];
-    s0, d_fin: [dk, dv] (None for zeros).  Returns (dq, dk, dv, dz, dbeta, ds0)."""
+    s0, d_fin: [dk, dv] (None for zeros).  Returns (dq, dk, dv, dz, dbeta, ds0).
+    dg_form "crossing": the gradient of the log-decay summed without cancelling
+    terms (see _chunk_backward), the form the tensor-core kernel evaluates."""
     q, k, v, z = (np.asarray(x, dtype=np.float64) for x in (q, k, v, z))
     beta = np.asarray(beta, dtype=np.float64)
     d_out = np.asarray(d_out, dtype=np.float64)
@@ -60,7 +63,7 @@ def chunked_backward(q, k, v, z, beta, s0, d_out, d_fin, chunk=8, a_log=0.0, eps
         c0 = starts[ci]
         c1 = min(c0 + chunk, T)
         grads = _chunk_backward(qh[c0:c1], kh[c0:c1], v[c0:c1], g[c0:c1], beta[c0:c1],
-                                entering[ci], d_out[c0:c1], dS)
+                                entering[ci], d_out[c0:c1], dS, dg_form)
         dqh[c0:c1], dkh[c0:c1], dv[c0:c1], dg[c0:c1], dbeta[c0:c1], dS = grads
     # gate: g = GMIN sigmoid(s z)  ->  dg/dz = GMIN s sigmoid (1 - sigmoid)
     dz = dg * GMIN * s * sig * (1.0 - sig)
@@ -87,7 +90,7 @@ def _chunk_forward(qh, kh, v, g, beta, S):
     return Qp @ S + P @ U, eC[:, None] * S + Kt.T @ U
 
 
-def _chunk_backward(qh, kh, v, g, beta, S, dO, dS1):
+def _chunk_backward(qh, kh, v, g, beta, S, dO, dS1, dg_form="plain"):
     C = qh.shape[0]
     _, Qp, Kp, Km, Kt, eC = _operands(qh, kh, g)
     Ls = np.tril(np.ones((C, C)), -1)
@@ -128,4 +131,17 @@ def _chunk_backward(qh, kh, v, g, beta, S, dO, dS1):
     dG = dQp * Qp + dKp * Kp - dKm * Km - dKt * Kt
     dG[-1] += np.sum(dKt * Kt, axis=0) + deC * eC
     dg = np.cumsum(dG[::-1], axis=0)[::-1]           # G = cumsum(g)
+    if dg_form == "crossing":
+        # The same sum without the terms that cancel in it: the state parts of
+        # dQ+ o Q+ and dK+ o K+ from row r on, the K~ parts before row r, and
+        # only those (t, s) pairs of the chunk-internal products with
+        # t >= r > s, plus rowsum(S o dS') e^{G_C}:
+        #   dg_r = e^{G_C} rowsum(S o dS') + sum_{t>=r} a_t + sum_{t<r} b_t
+        #          + sum_{t>=r>s} (dP_ts Q+_t + dAr_ts K+_t) K-_s
+        a = (dO @ S.T) * Qp - (dR @ S.T) * Kp
+        b = dKt * Kt
+        M = (dP[:, :, None] * Qp[:, None, :] + dAr[:, :, None] * Kp[:, None, :]) * Km[None, :, :]
+        dg = np.zeros_like(dG)
+        for r in range(C):
+            dg[r] = deC * eC + a[r:].sum(0) + b[:r].sum(0) + M[r:, :r].sum((0, 1))
     return dqh, dkh, dv, dg, dbeta, dS

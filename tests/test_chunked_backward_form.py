@@ -50,3 +50,22 @@ def test_chunked_reverse_mode_with_gate_scale_and_strong_decay():
     refs = [ref[0][:, 0], ref[1][:, 0], ref[2][:, 0], ref[3][:, 0], ref[4][:, 0], ref[5][0, 0]]
     for x, r in zip(got, refs):
         assert np.linalg.norm(x - r) <= 1e-9 * np.linalg.norm(r)
+
+
+@pytest.mark.parametrize("z_mean", [0.0, 6.0, -3.0])
+def test_cancellation_free_log_decay_gradient(z_mean):
+    """The log-decay gradient the tensor-core kernel sums (only crossing pairs
+    of the chunk-internal products, the state terms split at r) equals the
+    plain reverse cumulative sum of dG, and the oracle, to 1e-9: slow decay
+    (z mean 6), fast decay (z mean -3) and the plain workload spread."""
+    rng = np.random.default_rng(31 + int(z_mean))
+    T, D, E = 37, 6, 5
+    q, k, v, z, b, s0, do, dfin = _case(rng, T, D, E, True)
+    z = z + z_mean
+    ref = oracle.backward(q, k, v, z, b, [0, T], s0, do, dfin)
+    args = (q[:, 0], k[:, 0], v[:, 0], z[:, 0], b[:, 0], s0[0, 0], do[:, 0], dfin[0, 0])
+    plain = chunked_backward(*args, chunk=16)
+    cross = chunked_backward(*args, chunk=16, dg_form="crossing")
+    for x, y in zip(plain, cross):
+        assert np.linalg.norm(x - y) <= 1e-12 * max(np.linalg.norm(y), 1e-300)
+    assert np.linalg.norm(cross[3] - ref[3][:, 0]) <= 1e-9 * np.linalg.norm(ref[3][:, 0])
