@@ -275,14 +275,189 @@ struct WinPart {
   const float* beta;
   int W;
   const int32_t* accept;  // replay part only
+  bool vec;               // q, k, v (and per-channel z) 16-byte aligned: bulk copies
 };
+
+// The window kernel's thread layout: a thread holds four adjacent value
+// columns (a column quad) of R consecutive key rows, and the RG threads of a
+// quad are lanes of one warp (lane = g * QPW + quad within the warp), so the
+// two sums over the key rows (Sbar^T k, Sbar^T q) are warp shuffles and each
+// thread gets e for its own columns: a token needs one block barrier, with
+// the next token staged into the other half of a double buffer meanwhile.
+//
+// The registers hold S~ = Gamma^{-1} S, Gamma = Diag of the decays' running
+// product since the last renormalisation, so the decay costs no pass over
+// the state: with K_G = Gamma_t k, Q_G = Gamma_t q (row scalings of the
+// staged vectors), Sbar_t^T k = S~^T K_G, Sbar_t^T q = S~^T Q_G and the update
+// is S~ += (Gamma_t^{-1} k) (beta e)^T.  S = Gamma S~ is formed every
+// kWinRenorm tokens of a part (the decay of one token is at least e^{-5}, so
+// Gamma stays above e^{-40}) and where the replayed state is stored; a part
+// starts from Gamma = I, so the replay and the window give the same results
+// in one call as in two.
+template <int DK, int DV>
+struct WinShape {
+  static constexpr int QPW = DV / 32;  // column quads per warp
+  static constexpr int RG = 32 / QPW;  // threads per quad
+  static constexpr int R = DK / RG;    // key rows per thread
+  static_assert(DV % 32 == 0 && kNT / 32 * QPW * 4 == DV && DK % RG == 0 && R >= 1,
+                "unsupported shape");
+};
+
+template <int DK, int DV>
+struct WinSmem {
+  float kg[2][DK], qg[2][DK], ki[2][DK], gm[2][DK];  // Gamma k, Gamma q, Gamma^{-1} k, Gamma
+  float vs[2][DV];
+  float part[2][3][kNT / 32];  // per staging warp: |q|^2, |k|^2, q.k
+  float onorm[2][kNT / 32];    // per warp: the sum of o^2 over its columns
+  float os[2][DV];             // raw outputs awaiting the output norm
+  float beta[2];
+};
+
+// A token's inputs as they are in global memory, copied into shared memory
+// by cp.async three tokens ahead (no registers held meanwhile).
+template <int DK, int DV, typename T>
+struct WinRaw {
+  T q[DK], k[DK], v[DV];
+  float z[DK];
+  float beta, zh;
+  float pad[2];
+};
+constexpr int kWinSlots = 4;
+constexpr int kWinRenorm = 8;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ float ld_raw(const float* p) { return *p; }
+__device__ __forceinline__ float ld_raw(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ void cp_async_b16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_b4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The copies of token row th of part p into slot x: one 16-byte piece (or a
+// 4-byte scalar) per thread.
+template <int DK, int DV, typename T>
+__device__ __forceinline__ void win_copy(WinRaw<DK, DV, T>& x, const WinPart<T>& p, size_t th,
+                                         bool zhead) {
+  constexpr int QB = DK * (int)sizeof(T) / 16, VB = DV * (int)sizeof(T) / 16, ZB = DK / 4;
+  constexpr int QE = 16 / (int)sizeof(T);  // elements per piece
+  int t = threadIdx.x;
+  if (!p.vec) {  // element by element
+    if (t < DK) {
+      x.q[t] = p.q[th * DK + t];
+      x.k[t] = p.k[th * DK + t];
+      if (!zhead) x.z[t] = __ldg(p.z + th * DK + t);
+    }
+    if (t < DV) x.v[t] = p.v[th * DV + t];
+    if (t == 0) {
+      x.beta = __ldg(p.beta + th);
+      if (zhead) x.zh = __ldg(p.z + th);
+    }
+    return;
+  }
+  if (t < QB) {
+    cp_async_b16(x.q + QE * t, p.q + th * DK + QE * t);
+  } else if ((t -= QB) < QB) {
+    cp_async_b16(x.k + QE * t, p.k + th * DK + QE * t);
+  } else if ((t -= QB) < VB) {
+    cp_async_b16(x.v + QE * t, p.v + th * DV + QE * t);
+  } else if ((t -= VB) < ZB) {
+    if (!zhead) cp_async_b16(x.z + 4 * t, p.z + th * DK + 4 * t);
+  } else if ((t -= ZB) == 0) {
+    cp_async_b4(&x.beta, p.beta + th);
+  } else if (t == 1 && zhead) {
+    cp_async_b4(&x.zh, p.z + th);
+  }
+}
+
+// The fused convolution of one channel: its history in registers, its taps
+// (q then k, right-aligned as in ConvRegs) in shared memory.
+struct ConvHist {
+  float hq[3], hk[3];
+};
+__device__ __forceinline__ float conv_step_s(float (&h)[3], const float* t, float x) {
+  const float u = fmaf(t[0], h[0], fmaf(t[1], h[1], fmaf(t[2], h[2], t[3] * x)));
+  h[0] = h[1];
+  h[1] = h[2];
+  h[2] = x;
+  return swish(u);
+}
+
+// Token j of the unit (whose part starts afresh when `fresh`): q, k (through
+// the fused convolution), the decay's running product gam (this channel's,
+// kept by its thread), v and beta from the raw slot into buffer `bf`, with
+// the per-warp partial sums |q|^2, |k|^2, q.k of the convolved q, k.
+template <int DK, int DV, typename T, bool CONV>
+__device__ __forceinline__ void win_stage(WinSmem<DK, DV>& sm, int bf, const WinRaw<DK, DV, T>& x,
+                                          float zscale, bool zhead, bool fresh, float& gam,
+                                          ConvHist& ch, const float (*taps)[8], bool conv_on) {
+  const int tid = threadIdx.x;
+  if (tid < DK) {
+    float a = ld_raw(x.q + tid), b = ld_raw(x.k + tid);
+    if (CONV && conv_on) {
+      a = conv_step_s(ch.hq, taps[tid], a);
+      b = conv_step_s(ch.hk, taps[tid] + 4, b);
+    }
+    const float al = __expf(log_decay(zscale * (zhead ? x.zh : x.z[tid])));
+    gam = fresh ? al : gam * al;
+    sm.kg[bf][tid] = b * gam;
+    sm.qg[bf][tid] = a * gam;
+    sm.ki[bf][tid] = b / gam;
+    sm.gm[bf][tid] = gam;
+    const float qq = warp_sum(a * a), kk = warp_sum(b * b), kq = warp_sum(a * b);
+    if ((tid & 31) == 0) {
+      sm.part[bf][0][tid >> 5] = qq;
+      sm.part[bf][1][tid >> 5] = kk;
+      sm.part[bf][2][tid >> 5] = kq;
+    }
+  }
+  if (tid < DV) sm.vs[bf][tid] = ld_raw(x.v + tid);
+  if (tid == 0) sm.beta[bf] = x.beta;
+}
+
+// V consecutive floats of shared memory (V = 4, 2 or 1, aligned to V floats)
+template <int V>
+__device__ __forceinline__ void lds_v(float (&d)[V], const float* p) {
+  if constexpr (V == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
+  } else if constexpr (V == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    d[0] = t.x; d[1] = t.y;
+  } else {
+    d[0] = *p;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void st4_io(T* p, float4 o) {
+  IO<T>::st(p, o.x);
+  IO<T>::st(p + 1, o.y);
+  IO<T>::st(p + 2, o.z);
+  IO<T>::st(p + 3, o.w);
+}
 
 template <int DK, int DV, typename T, bool FUSED = false>
 __global__ void __launch_bounds__(kNT, 2)
 window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int H, int zhead,
               float* __restrict__ state, T* __restrict__ out, int* err, const Fusion f) {
-  using SH = RecShape<DK, DV>;
-  __shared__ __align__(16) RecSmem<DK, DV> sm;
+  using SH = WinShape<DK, DV>;
+  __shared__ __align__(16) WinSmem<DK, DV> sm;
+  __shared__ __align__(16) WinRaw<DK, DV, T> raw[kWinSlots];
+  __shared__ __align__(16) float taps[FUSED ? DK : 1][8];
   const size_t unit = blockIdx.x;  // b * H + h
   const int b = (int)(unit / H), h = (int)(unit % H);
   int nrep = 0;
@@ -293,45 +468,176 @@ window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int
       return;
     }
   }
-  if (nrep == 0 && wn.W == 0) return;
-  const int c4 = threadIdx.x % SH::TPR, rg = threadIdx.x / SH::TPR;
+  const int ntok = nrep + wn.W;
+  if (ntok == 0) return;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane / SH::QPW;                        // row group: rows [g R, g R + R)
+  const int c = 4 * (w * SH::QPW + lane % SH::QPW);    // first of this thread's columns
+  // token i (the replayed tokens first, then the window's) into its raw slot;
+  // one commit group per token, empty past the last
+  auto fetch = [&](int i) {
+    if (i < nrep)
+      win_copy<DK, DV, T>(raw[i % kWinSlots], rp, ((size_t)b * rp.W + i) * H + h, zhead);
+    else if (i < ntok)
+      win_copy<DK, DV, T>(raw[i % kWinSlots], wn, ((size_t)b * wn.W + (i - nrep)) * H + h, zhead);
+    cp_async_commit();
+  };
+  fetch(0);
+  fetch(1);
+  fetch(2);
   float4* S = reinterpret_cast<float4*>(state + unit * DK * DV);
   float4 s[SH::R];
 #pragma unroll
-  for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4);
+  for (int i = 0; i < SH::R; ++i) s[i] = ld_stream(S + ((size_t)(g * SH::R + i) * DV + c) / 4);
   const float zscale = gate_scale(a_log, h);
-  const int zs = zhead ? 1 : DK;
   // (fused) the convolution history of this thread's channel; the replayed
   // tokens advance it and it is stored with the state, the window's drafts
   // advance only this copy
   const bool conv = FUSED && f.W > 0;
-  ConvRegs cr;
-  if (conv && threadIdx.x < DK) conv_load<DK>(cr, f, unit, h, threadIdx.x);
-  for (int t = 0; t < nrep; ++t) {
-    const size_t th = ((size_t)b * rp.W + t) * H + h;
-    __syncthreads();  // previous token finished reading shared memory
-    stage_token<DK, DV, T, FUSED>(sm, rp.q + th * DK, rp.k + th * DK, rp.v + th * DV,
-                                  rp.z + th * zs, zscale, zhead, &cr, conv);
-    __syncthreads();
-    apply_token<DK, DV, T>(sm, s, __ldg(rp.beta + th), nullptr);
-  }
-  if (nrep > 0) {
+  ConvHist ch;
+  if (conv && threadIdx.x < DK) {
+    ConvRegs cr;
+    conv_load<DK>(cr, f, unit, h, threadIdx.x);
 #pragma unroll
-    for (int i = 0; i < SH::R; ++i) st_stream(S + (size_t)(rg + i * SH::RG) * SH::TPR + c4, s[i]);
-    if (conv && threadIdx.x < DK) conv_store<DK>(cr, f, unit, threadIdx.x);
+    for (int j = 0; j < 4; ++j) {
+      taps[threadIdx.x][j] = cr.tq[j];
+      taps[threadIdx.x][4 + j] = cr.tk[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      ch.hq[j] = cr.hq[j];
+      ch.hk[j] = cr.hk[j];
+    }
   }
+  auto conv_save = [&]() {  // the history after the replayed tokens
+    if (conv && threadIdx.x < DK) {
+      ConvRegs cr;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        cr.hq[j] = ch.hq[j];
+        cr.hk[j] = ch.hk[j];
+      }
+      conv_store<DK>(cr, f, unit, threadIdx.x);
+    }
+  };
+  // a part (replay, window) starts afresh, and renormalises every kWinRenorm tokens
+  auto fresh = [&](int j) { return j == nrep || (j < nrep ? j : j - nrep) % kWinRenorm == 0; };
+  float gam = 1.f;  // (staging threads) this channel's running decay product
   const bool onorm = FUSED && f.onw != nullptr;
-  for (int t = 0; t < wn.W; ++t) {
-    const size_t th = ((size_t)b * wn.W + t) * H + h;
+  // (output norm) token i's raw outputs wait in sm.os[i & 1] for the next barrier
+  auto finish = [&](int i) {
+    if (g != 0) return;
+    float ss = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < kNT / 32; ++ww) ss += sm.onorm[i & 1][ww];
+    const float r = rsqrtf(ss * (1.f / DV) + f.eps);
+    const float4 o = *reinterpret_cast<const float4*>(&sm.os[i & 1][c]);
+    const float4 gm = __ldg(reinterpret_cast<const float4*>(f.onw + (size_t)h * DV + c));
+    st4_io(out + (((size_t)b * wn.W + (i - nrep)) * H + h) * DV + c,
+           make_float4(o.x * r * gm.x, o.y * r * gm.y, o.z * r * gm.z, o.w * r * gm.w));
+  };
+
+  cp_async_wait_pending<2>();  // token 0's copies (this thread's)
+  __syncthreads();             // ... and every thread's
+  win_stage<DK, DV, T, FUSED>(sm, 0, raw[0], zscale, zhead, true, gam, ch, taps, conv);
+  if (nrep == 1) conv_save();
+  cp_async_wait_pending<1>();  // token 1's
+  for (int i = 0; i < ntok; ++i) {
+    const int bf = i & 1;
+    __syncthreads();  // token i staged; token i - 1's buffer read by every thread
+    if (onorm && i > nrep) finish(i - 1);  // the previous token's outputs, normalised
+    if (i + 1 < ntok) {  // token i + 1 into the other buffer
+      win_stage<DK, DV, T, FUSED>(sm, bf ^ 1, raw[(i + 1) % kWinSlots], zscale, zhead,
+                                  fresh(i + 1), gam, ch, taps, conv);
+      if (i + 2 == nrep) conv_save();
+    }
+    fetch(i + 3);  // into the slot of token i - 1, staged before the barrier above
+    // token i
+    float qq = 0.f, kk = 0.f, kq = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < (DK + 31) / 32; ++ww) {
+      qq += sm.part[bf][0][ww];
+      kk += sm.part[bf][1][ww];
+      kq += sm.part[bf][2][ww];
+    }
+    const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
+    const float bt = sm.beta[bf];
+    constexpr int V = SH::R % 4 == 0 ? 4 : (SH::R % 2 == 0 ? 2 : 1);
+    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+    for (int j0 = 0; j0 < SH::R; j0 += V) {
+      float kv[V], qv[V];
+      lds_v<V>(kv, &sm.kg[bf][g * SH::R + j0]);
+      lds_v<V>(qv, &sm.qg[bf][g * SH::R + j0]);
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const float4 x = s[j0 + u];
+        pk.x += kv[u] * x.x; pk.y += kv[u] * x.y; pk.z += kv[u] * x.z; pk.w += kv[u] * x.w;
+        pq.x += qv[u] * x.x; pq.y += qv[u] * x.y; pq.z += qv[u] * x.z; pq.w += qv[u] * x.w;
+      }
+    }
+#pragma unroll
+    for (int o = SH::QPW; o < 32; o <<= 1) {  // over the row groups of this quad
+      pk.x += __shfl_xor_sync(0xffffffffu, pk.x, o);
+      pk.y += __shfl_xor_sync(0xffffffffu, pk.y, o);
+      pk.z += __shfl_xor_sync(0xffffffffu, pk.z, o);
+      pk.w += __shfl_xor_sync(0xffffffffu, pk.w, o);
+      pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o);
+      pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+      pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o);
+      pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+    }
+    const float4 v4 = *reinterpret_cast<const float4*>(&sm.vs[bf][c]);
+    // e = v - Sbar^T k^ ; o = Sbar^T q^ + beta (k^ . q^) e ; S~ += Gamma^{-1} k^ beta e^T
+    const float4 e = make_float4(v4.x - pk.x * rk, v4.y - pk.y * rk, v4.z - pk.z * rk,
+                                 v4.w - pk.w * rk);
+    if (i >= nrep) {
+      const float m = bt * (kq * rk * rq);
+      const float4 o = make_float4(pq.x * rq + m * e.x, pq.y * rq + m * e.y,
+                                   pq.z * rq + m * e.z, pq.w * rq + m * e.w);
+      if (onorm) {  // normalised after the next barrier, when every warp's sum is in
+        float ss = g == 0 ? o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w : 0.f;
+#pragma unroll
+        for (int q = 1; q < SH::QPW; q <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, q);
+        if (lane == 0) sm.onorm[bf][w] = ss;
+        if (g == 0) *reinterpret_cast<float4*>(&sm.os[bf][c]) = o;
+      } else if (g == 0) {
+        st4_io(out + (((size_t)b * wn.W + (i - nrep)) * H + h) * DV + c, o);
+      }
+    }
+    const float bk = bt * rk;
+    const float4 be = make_float4(bk * e.x, bk * e.y, bk * e.z, bk * e.w);
+#pragma unroll
+    for (int j0 = 0; j0 < SH::R; j0 += V) {
+      float kv[V];
+      lds_v<V>(kv, &sm.ki[bf][g * SH::R + j0]);
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        float4& x = s[j0 + u];
+        x.x += kv[u] * be.x; x.y += kv[u] * be.y; x.z += kv[u] * be.z; x.w += kv[u] * be.w;
+      }
+    }
+    if (i + 1 < ntok ? fresh(i + 1) : i + 1 == nrep) {  // S = Gamma S~
+#pragma unroll
+      for (int j0 = 0; j0 < SH::R; j0 += V) {
+        float gv[V];
+        lds_v<V>(gv, &sm.gm[bf][g * SH::R + j0]);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float4& x = s[j0 + u];
+          x.x *= gv[u]; x.y *= gv[u]; x.z *= gv[u]; x.w *= gv[u];
+        }
+      }
+    }
+    if (i + 1 == nrep) {  // the replayed state, written once
+#pragma unroll
+      for (int j = 0; j < SH::R; ++j) st_stream(S + ((size_t)(g * SH::R + j) * DV + c) / 4, s[j]);
+    }
+    cp_async_wait_pending<1>();  // token i + 2's copies, staged after the next barrier
+  }
+  if (onorm && ntok > nrep) {  // the last token's outputs
     __syncthreads();
-    stage_token<DK, DV, T, FUSED>(sm, wn.q + th * DK, wn.k + th * DK, wn.v + th * DV,
-                                  wn.z + th * zs, zscale, zhead, &cr, conv);
-    __syncthreads();
-    if (onorm)
-      apply_token<DK, DV, T, FUSED>(sm, s, __ldg(wn.beta + th), out + th * DV,
-                                    f.onw + (size_t)h * DV, f.eps);
-    else
-      apply_token<DK, DV, T>(sm, s, __ldg(wn.beta + th), out + th * DV);
+    finish(ntok - 1);
   }
 }
 
@@ -531,8 +837,11 @@ template <int DK, int DV, typename T>
 cudaError_t window_dispatch(const Problem& p, const WinInputs& rp, const WinInputs& wn,
                             const float* a_log, int zhead, float* state, void* out, int* err,
                             const Fusion* f, cudaStream_t st) {
-  auto part = [](const WinInputs& x) {
-    return WinPart<T>{(const T*)x.q, (const T*)x.k, (const T*)x.v, x.z, x.beta, x.W, x.accept};
+  auto part = [zhead](const WinInputs& x) {
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    const bool vec = a16(x.q) && a16(x.k) && a16(x.v) && (zhead || a16(x.z));
+    return WinPart<T>{(const T*)x.q, (const T*)x.k, (const T*)x.v, x.z, x.beta, x.W, x.accept,
+                      vec};
   };
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   if (f)

@@ -297,7 +297,9 @@ def _oracle_window(q, k, v, z, beta, state, ntok, a_log=None):
     return outs, np.stack(fins)
 
 
-@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 32)])
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 32),
+                                         (torch.float32, 32, 64), (torch.bfloat16, 128, 64),
+                                         (torch.bfloat16, 32, 128), (torch.float32, 128, 32)])
 def test_decode_window_outputs_and_state_untouched(dtype, dk, dv):
     B, W, H = 5, 4, 3
     q, k, v, z, beta, state = _window_inputs(B, W, H, dk, dv, dtype, 21)
@@ -322,6 +324,34 @@ def test_decode_replay_applies_accepted_prefix(dtype):
     _, ref = _oracle_window(q, k, v, z, beta, before, acc)
     assert torch.equal(state[0], before[0])   # nothing accepted: state untouched
     assert_close(state, ref, dtype, "replayed states")
+    assert kda.get_device_error() == 0
+
+
+def _misaligned(x, elems=1):
+    """x's values in a contiguous tensor whose data starts `elems` elements
+    past an allocation's start (not 16-byte aligned)."""
+    buf = torch.empty(x.numel() + elems, dtype=x.dtype, device=x.device)
+    y = buf[elems:].view(x.shape)
+    y.copy_(x)
+    return y
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_window_inputs_not_16_byte_aligned(dtype):
+    """q, k, v, z that start off a 16-byte boundary (element-wise input
+    copies) give the results of the aligned call bit for bit."""
+    B, W, H, dk, dv = 4, 3, 2, 128, 128
+    q, k, v, z, beta, state = _window_inputs(B, W, H, dk, dv, dtype, 27)
+    acc = torch.tensor([0, 3, 1, 2], dtype=torch.int32, device=DEV)
+    s1, s2 = state.clone(), state.clone()
+    o1 = kda.decode_replay_window((q, k, v, z, beta), acc, q, k, v, z, beta, s1)
+    mq, mk, mv, mz = (_misaligned(x) for x in (q, k, v, z))
+    assert all(x.data_ptr() % 16 for x in (mq, mk, mv, mz))
+    o2 = kda.decode_replay_window((mq, mk, mv, mz, beta), acc, mq, mk, mv, mz, beta, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    ref, fins = _oracle_window(q, k, v, z, beta, state, acc.tolist())
+    assert_close(s2, fins, dtype, "replayed states")
     assert kda.get_device_error() == 0
 
 
