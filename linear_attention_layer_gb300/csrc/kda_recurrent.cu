@@ -63,7 +63,7 @@ struct ConvRegs {
   float hq[3], hk[3], tq[4], tk[4];
 };
 
-__device__ __forceinline__ float swish(float u) { return u / (1.f + __expf(-u)); }
+__device__ __forceinline__ float swish(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
 __device__ __forceinline__ float conv_step(float (&h)[3], const float (&t)[4], float x) {
   const float u = fmaf(t[0], h[0], fmaf(t[1], h[1], fmaf(t[2], h[2], t[3] * x)));

@@ -64,6 +64,39 @@ def test_short_conv_ragged(dtype, W):
     assert kda.get_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype,H,D", [(torch.bfloat16, 4, 128), (torch.float32, 2, 128),
+                                       (torch.bfloat16, 1, 64), (torch.float32, 1, 32),
+                                       (torch.bfloat16, 1, 32)])
+@pytest.mark.parametrize("W", [2, 4])
+def test_short_conv_row_widths(dtype, H, D, W):
+    """Rows of 1024, 256, 128 and 64 bytes: tiles cut from 512-, 256- and
+    128-byte slabs of each row, and (64 bytes) the register-only kernel;
+    sequence starts inside, at and just after tile starts (tiles of 32, 64
+    and 128 tokens)."""
+    lengths = [1, 2, 0, 31, 32, 33, 3, 61, 66, 1, 127, 129, 5]
+    x, w, st, cu, cu_h = _inputs(lengths, H, D, W, dtype, seed=40 + W + D)
+    y, fin = kda.short_conv(x, w, cu, st)
+    torch.cuda.synchronize()
+    ry, rfin = oracle.short_conv(x, w, cu_h, st)
+    _check(y, ry, dtype)
+    assert np.array_equal(as64(fin), rfin)
+    assert kda.get_device_error() == 0
+
+
+def test_short_conv_many_tiles_per_cta():
+    """About 10 K tokens x 32 heads x 128 channels: more tiles than the
+    persistent CTAs' four-stage rings hold at once, so every ring stage is
+    reused several times; every output against the oracle."""
+    lengths = [4000, 1, 3000, 0, 2500, 700]
+    x, w, st, cu, cu_h = _inputs(lengths, 32, 128, 4, torch.bfloat16, seed=77)
+    y, fin = kda.short_conv(x, w, cu, st)
+    torch.cuda.synchronize()
+    ry, rfin = oracle.short_conv(x, w, cu_h, st)
+    _check(y, ry, torch.bfloat16)
+    assert np.array_equal(as64(fin), rfin)
+    assert kda.get_device_error() == 0
+
+
 @pytest.mark.parametrize("D", [32, 64])
 def test_short_conv_small_channels_no_state(D):
     x, w, _, cu, cu_h = _inputs([5, 70], 2, D, 4, torch.bfloat16, seed=3, with_state=False)
