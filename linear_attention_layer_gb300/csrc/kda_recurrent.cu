@@ -415,7 +415,7 @@ __device__ __forceinline__ void win_stage(WinSmem<DK, DV>& sm, int bf, const Win
     gam = fresh ? al : gam * al;
     sm.kg[bf][tid] = b * gam;
     sm.qg[bf][tid] = a * gam;
-    sm.ki[bf][tid] = b / gam;
+    sm.ki[bf][tid] = __fdividef(b, gam);
     sm.gm[bf][tid] = gam;
     const float qq = warp_sum(a * a), kk = warp_sum(b * b), kq = warp_sum(a * b);
     if ((tid & 31) == 0) {
