@@ -905,8 +905,8 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
     st2(As + swz(t, c), make_float2(dqp[2 * hf] * q2.x * e2.x - dkp[2 * hf] * kh[2 * hf] * e2.x,
                                     dqp[2 * hf + 1] * q2.y * e2.y -
                                         dkp[2 * hf + 1] * kh[2 * hf + 1] * e2.y));
-    st2(Bs + swz(t, c), make_float2(dkt[2 * hf] * kh[2 * hf] * ec0 / e2.x,
-                                    dkt[2 * hf + 1] * kh[2 * hf + 1] * ec1 / e2.y));
+    st2(Bs + swz(t, c), make_float2(dkt[2 * hf] * km.x * ec0,  // k^ / e^{G} = K-
+                                    dkt[2 * hf + 1] * km.y * ec1));
   }
   float dkm[4] = {0.f, 0.f, 0.f, 0.f};
   {
@@ -937,7 +937,7 @@ __device__ void chunk_reverse(unsigned char* sm, const Params& P, int h, int ts,
     for (int e = 0; e < 4; ++e) {
       const float ec = EC[c + (e & 1)];
       dqh[e] = dqp[e] * eg[e];
-      dkh[e] = -dkp[e] * eg[e] + (dkm[e] + dkt[e] * ec) / eg[e];
+      dkh[e] = -dkp[e] * eg[e] + __fdividef(dkm[e] + dkt[e] * ec, eg[e]);
     }
     float pq[2], pk[2];
 #pragma unroll
