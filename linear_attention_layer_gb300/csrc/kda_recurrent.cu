@@ -800,6 +800,142 @@ recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
   }
 }
 
+// Small states (dv = 32, dk <= 64) with few (sequence, head) units: one
+// 128-thread CTA per unit, the sequence in blocks of BLK tokens.  First all
+// threads stage the block -- q and k normalised, the decays, beta, (q^.k^) and
+// v, none of which depends on the state -- in shared memory; then each warp
+// runs the token loop for its own eight value columns, lane (rg, col) holding
+// key rows [rg R, rg R + R) of its column, the two sums over the key rows by
+// warp shuffles: no block barrier inside the token loop, and only the state
+// chain left on it.
+constexpr int kCtaNT = 128;
+constexpr long long kCtaUnitsMax = 1024;  // (sequence, head) units for a CTA each
+
+template <int DK>
+struct CtaShape {
+  static constexpr int BLK = DK == 64 ? 32 : 64;  // tokens per block
+  static constexpr int TPK = kCtaNT / BLK;        // staging threads per token
+  static constexpr int CH = DK / TPK;             // channels each stages
+  static constexpr int R = DK / 4;                // key rows per thread
+};
+
+template <int DK, typename T>
+__global__ void __launch_bounds__(kCtaNT)
+recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                     const float* __restrict__ z, const float* __restrict__ beta,
+                     const float* initial_state, const int32_t* __restrict__ cu,
+                     T* __restrict__ out, float* final_state, int H, int total, int* err,
+                     const float* __restrict__ a_log, float* ckpt,
+                     const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
+  using CS = CtaShape<DK>;
+  constexpr int DV = 32, BLK = CS::BLK, R = CS::R;
+  __shared__ __align__(16) float qs[BLK][DK], ks[BLK][DK], as[BLK][DK];
+  __shared__ __align__(16) float vs[BLK][DV];
+  __shared__ float bs[BLK], kqs[BLK];
+  const int n = blockIdx.x / H, h = blockIdx.x % H;
+  int bos, eos;
+  if (!seq_range(cu, n, total, threadIdx.x == 0 ? err : nullptr, bos, eos)) return;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = 8 * w + (lane & 7), rg = lane >> 3;
+  const size_t sbase = (size_t)blockIdx.x * DK * DV;
+  float s[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    s[i] = initial_state ? __ldg(initial_state + sbase + (size_t)(rg * R + i) * DV + col) : 0.f;
+  const float zscale = gate_scale(a_log, h);
+  for (int b0 = bos; b0 < eos; b0 += BLK) {
+    const int nb = min(BLK, eos - b0);
+    __syncthreads();  // the previous block's rows are read
+    {  // stage: CS::TPK adjacent threads per token, CS::CH channels each
+      const int t = threadIdx.x / CS::TPK, part = threadIdx.x % CS::TPK, c0 = part * CS::CH;
+      float qq = 0.f, kk = 0.f, kq = 0.f;
+      const bool live = t < nb;
+      const size_t th = (size_t)(b0 + t) * H + h;
+      if (live) {
+#pragma unroll
+        for (int c = 0; c < CS::CH; ++c) {
+          const float a = IO<T>::ld(q + th * DK + c0 + c), b = IO<T>::ld(k + th * DK + c0 + c);
+          qs[t][c0 + c] = a;
+          ks[t][c0 + c] = b;
+          as[t][c0 + c] = __expf(log_decay(zscale * __ldg(z + (zhead ? th : th * DK + c0 + c))));
+          qq += a * a;
+          kk += b * b;
+          kq += a * b;
+        }
+#pragma unroll
+        for (int c = part; c < DV; c += CS::TPK) vs[t][c] = IO<T>::ld(v + th * DV + c);
+      }
+#pragma unroll
+      for (int o = 1; o < CS::TPK; o <<= 1) {  // over the token's staging threads
+        qq += __shfl_xor_sync(0xffffffffu, qq, o);
+        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        kq += __shfl_xor_sync(0xffffffffu, kq, o);
+      }
+      if (live) {
+        const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
+#pragma unroll
+        for (int c = 0; c < CS::CH; ++c) {  // this thread's own values: no barrier needed
+          qs[t][c0 + c] *= rq;
+          ks[t][c0 + c] *= rk;
+        }
+        if (part == 0) {
+          bs[t] = __ldg(beta + th);
+          kqs[t] = kq * rq * rk;
+        }
+      }
+    }
+    __syncthreads();
+    for (int t = 0; t < nb; ++t) {  // e = v - Sbar^T k^, o = Sbar^T q^ + beta (k^.q^) e
+      float pk = 0.f, pq = 0.f;
+#pragma unroll
+      for (int i0 = 0; i0 < R; i0 += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(&as[t][rg * R + i0]);
+        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t][rg * R + i0]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&qs[t][rg * R + i0]);
+        s[i0] *= a4.x; s[i0 + 1] *= a4.y; s[i0 + 2] *= a4.z; s[i0 + 3] *= a4.w;
+        pk = fmaf(k4.x, s[i0], pk); pk = fmaf(k4.y, s[i0 + 1], pk);
+        pk = fmaf(k4.z, s[i0 + 2], pk); pk = fmaf(k4.w, s[i0 + 3], pk);
+        pq = fmaf(q4.x, s[i0], pq); pq = fmaf(q4.y, s[i0 + 1], pq);
+        pq = fmaf(q4.z, s[i0 + 2], pq); pq = fmaf(q4.w, s[i0 + 3], pq);
+      }
+      pk += __shfl_xor_sync(0xffffffffu, pk, 8);
+      pq += __shfl_xor_sync(0xffffffffu, pq, 8);
+      pk += __shfl_xor_sync(0xffffffffu, pk, 16);
+      pq += __shfl_xor_sync(0xffffffffu, pq, 16);
+      const float bt = bs[t];
+      const float e = vs[t][col] - pk;
+      if (rg == 0) IO<T>::st(out + ((size_t)(b0 + t) * H + h) * DV + col, pq + bt * kqs[t] * e);
+      const float be = bt * e;
+#pragma unroll
+      for (int i0 = 0; i0 < R; i0 += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t][rg * R + i0]);
+        s[i0] = fmaf(k4.x, be, s[i0]); s[i0 + 1] = fmaf(k4.y, be, s[i0 + 1]);
+        s[i0 + 2] = fmaf(k4.z, be, s[i0 + 2]); s[i0 + 3] = fmaf(k4.w, be, s[i0 + 3]);
+      }
+      if (ckpt && (b0 + t + 1 - bos) % ckpt_every == 0) {  // state after a multiple of ckpt_every
+        const size_t j = (size_t)__ldg(ckpt_off + n) + (b0 + t + 1 - bos) / ckpt_every - 1;
+        float* dst = ckpt + (j * H + h) * DK * DV;
+#pragma unroll
+        for (int i = 0; i < R; ++i) dst[(size_t)(rg * R + i) * DV + col] = s[i];
+      }
+    }
+  }
+  if (final_state) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) final_state[sbase + (size_t)(rg * R + i) * DV + col] = s[i];
+  }
+}
+
+template <int DK, typename T>
+cudaError_t cta_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
+  const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  recurrent_cta_kernel<DK, T><<<blocks, kCtaNT, 0, st>>>(
+      (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
+      (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt, a.ckpt_off,
+      a.ckpt_every, a.gate_per_head);
+  return cudaGetLastError();
+}
+
 template <int DK, typename T>
 cudaError_t small_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   const int units = p.num_seqs * p.num_heads;
@@ -927,6 +1063,15 @@ bool recurrent_small_supported(const Problem& p) { return p.dv == 32 && p.dk <= 
 cudaError_t launch_recurrent_small(const Problem& p, const Args& a, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   if (p.dv != 32) return cudaErrorInvalidValue;
+  // few units: a CTA each (the token chain shortened by staging each block
+  // first); many: a warp each, four to a CTA
+  if ((long long)p.num_seqs * p.num_heads <= kCtaUnitsMax) {
+    if (p.dk == 32)
+      return p.io_bf16 ? cta_dispatch<32, __nv_bfloat16>(p, a, st) : cta_dispatch<32, float>(p, a, st);
+    if (p.dk == 64)
+      return p.io_bf16 ? cta_dispatch<64, __nv_bfloat16>(p, a, st) : cta_dispatch<64, float>(p, a, st);
+    return cudaErrorInvalidValue;
+  }
   if (p.dk == 32)
     return p.io_bf16 ? small_dispatch<32, __nv_bfloat16>(p, a, st) : small_dispatch<32, float>(p, a, st);
   if (p.dk == 64)

@@ -701,14 +701,14 @@ def test_expired_device_wait_reports_timeout_and_recovers():
     _check_all(p, out, fin, torch.bfloat16)
 
 
-# ------------------------------------------- small states, one warp per unit --
+# ----------------------- small states (a CTA per unit, or a warp when many) --
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("dk", [32, 64])
 def test_small_state_path(dtype, dk):
-    """dv = 32, dk <= 64 (the CUDA-core path runs one warp per (sequence,
-    head)): ragged lengths with a long one, checkpoints, the gate log-scale,
-    against the oracle."""
+    """dv = 32, dk <= 64 (the CUDA-core path runs a CTA per (sequence, head)
+    here): ragged lengths with a long one (many token blocks), checkpoints,
+    the gate log-scale, against the oracle."""
     lens = [1, 0, 31, 64, 65, 2000]
     p = workloads.random_problem(lens, 3, dk, 32, dtype, z_mean=-1.0, init_std=0.2, seed=33,
                                  device=DEV)
@@ -733,6 +733,20 @@ def test_small_state_path(dtype, dk):
     ro2, rf2, _ = oracle.recurrent(p.q, p.k, p.v, zb, p.beta, p.cu_seqlens_host, p.initial_state)
     assert_close(out2, ro2, dtype, "per-head gate out")
     assert_close(fin2, rf2, dtype, "per-head gate final_state")
+
+
+def test_small_state_many_units():
+    """More (sequence, head) units than the small-state path gives a CTA each
+    (1,024): 600 sequences x 2 heads run one warp per unit, against the
+    oracle."""
+    lens = np.random.default_rng(5).integers(0, 40, size=600).tolist()
+    p = workloads.random_problem(lens, 2, 32, 32, torch.float32, init_std=0.2, seed=35,
+                                 device=DEV)
+    out, fin = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state,
+                             cu_seqlens_host=p.cu_seqlens_host)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    _check_all(p, out, fin, torch.float32)
 
 
 def test_many_short_sequences():
