@@ -802,12 +802,12 @@ recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
 
 // Small states (dv = 32, dk <= 64) with few (sequence, head) units: one
 // 128-thread CTA per unit, the sequence in blocks of BLK tokens.  First all
-// threads stage the block -- q and k normalised, the decays, beta, (q^.k^) and
-// v, none of which depends on the state -- in shared memory; then each warp
-// runs the token loop for its own eight value columns, lane (rg, col) holding
-// key rows [rg R, rg R + R) of its column, the two sums over the key rows by
-// warp shuffles: no block barrier inside the token loop, and only the state
-// chain left on it.
+// threads stage the block -- q and k normalised, the decays, beta, (q^.k^), v
+// and the products below, none of which depends on the state -- in shared
+// memory; then each warp runs the token loop for its own eight value columns,
+// lane (rg, col) holding key rows [rg R, rg R + R) of its column, the sums
+// over the key rows by warp shuffles: no block barrier inside the token loop,
+// and only the state chain left on it.
 constexpr int kCtaNT = 128;
 constexpr long long kCtaUnitsMax = 1024;  // (sequence, head) units for a CTA each
 
@@ -819,19 +819,39 @@ struct CtaShape {
   static constexpr int R = DK / 4;                // key rows per thread
 };
 
+// The token loop takes four tokens at a time.  For a group j = 0..3 entered
+// with state S, A_j the decays' running product over the group's tokens
+// 0..j (per key row) and x_i = beta_i e_i:
+//     Sbar_j^T k_j = K_j + sum_{i<j} c_ji x_i,   K_j = S^T (A_j k_j),
+//     Sbar_j^T q_j = Q_j + sum_{i<j} d_ji x_i,   Q_j = S^T (A_j q_j),
+//     c_ji = k_j . (A_j / A_i) k_i,  d_ji = q_j . (A_j / A_i) k_i,
+//     e_j = v_j - Sbar_j^T k_j,  o_j = Sbar_j^T q_j + (q_j . k_j) x_j,
+//     S' = A_3 S + sum_i (A_3 / A_i) k_i x_i^T,
+// so one pass over the state gives the eight sums of a group (reduced by one
+// round of shuffles), the e_j follow from a 4 x 4 triangular solve on
+// scalars, and one more pass applies the group: the state chain is a quarter
+// as long.  (k, q normalised; every ratio A_j / A_i is a product of decays,
+// so nothing leaves the fp32 range.)  The c, d and the scaled key and query
+// rows are staged with the block.  Checkpoints fall on group ends (the call
+// takes checkpoint intervals in multiples of 64 tokens).
 template <int DK, typename T>
-__global__ void __launch_bounds__(kCtaNT)
+__global__ void __launch_bounds__(kCtaNT, 1)
 recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                     const float* __restrict__ z, const float* __restrict__ beta,
-                     const float* initial_state, const int32_t* __restrict__ cu,
-                     T* __restrict__ out, float* final_state, int H, int total, int* err,
-                     const float* __restrict__ a_log, float* ckpt,
-                     const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
+                      const float* __restrict__ z, const float* __restrict__ beta,
+                      const float* initial_state, const int32_t* __restrict__ cu,
+                      T* __restrict__ out, float* final_state, int H, int total, int* err,
+                      const float* __restrict__ a_log, float* ckpt,
+                      const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
   using CS = CtaShape<DK>;
-  constexpr int DV = 32, BLK = CS::BLK, R = CS::R;
+  constexpr int DV = 32, BLK = CS::BLK, R = CS::R, NG = BLK / 4;
+  constexpr int TPG = kCtaNT / NG;  // group-staging threads per group
+  static_assert(DK / TPG == 4, "four channels per group-staging thread");
+  // per token: q^ then A_j q^, k^ then A_j k^, alpha then (A_3 / A_j) k^
   __shared__ __align__(16) float qs[BLK][DK], ks[BLK][DK], as[BLK][DK];
+  __shared__ __align__(16) float a3s[NG][DK];
   __shared__ __align__(16) float vs[BLK][DV];
   __shared__ float bs[BLK], kqs[BLK];
+  __shared__ float cds[NG][12];  // c10 c20 c21 c30 c31 c32, then d in the same order
   const int n = blockIdx.x / H, h = blockIdx.x % H;
   int bos, eos;
   if (!seq_range(cu, n, total, threadIdx.x == 0 ? err : nullptr, bos, eos)) return;
@@ -846,74 +866,150 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   for (int b0 = bos; b0 < eos; b0 += BLK) {
     const int nb = min(BLK, eos - b0);
     __syncthreads();  // the previous block's rows are read
-    {  // stage: CS::TPK adjacent threads per token, CS::CH channels each
+    {  // stage the tokens (rows past the sequence: k = q = v = 0, alpha = 1, beta = 0)
       const int t = threadIdx.x / CS::TPK, part = threadIdx.x % CS::TPK, c0 = part * CS::CH;
       float qq = 0.f, kk = 0.f, kq = 0.f;
       const bool live = t < nb;
       const size_t th = (size_t)(b0 + t) * H + h;
-      if (live) {
 #pragma unroll
-        for (int c = 0; c < CS::CH; ++c) {
-          const float a = IO<T>::ld(q + th * DK + c0 + c), b = IO<T>::ld(k + th * DK + c0 + c);
-          qs[t][c0 + c] = a;
-          ks[t][c0 + c] = b;
-          as[t][c0 + c] = __expf(log_decay(zscale * __ldg(z + (zhead ? th : th * DK + c0 + c))));
-          qq += a * a;
-          kk += b * b;
-          kq += a * b;
-        }
-#pragma unroll
-        for (int c = part; c < DV; c += CS::TPK) vs[t][c] = IO<T>::ld(v + th * DV + c);
+      for (int c = 0; c < CS::CH; ++c) {
+        const float a = live ? IO<T>::ld(q + th * DK + c0 + c) : 0.f;
+        const float b = live ? IO<T>::ld(k + th * DK + c0 + c) : 0.f;
+        qs[t][c0 + c] = a;
+        ks[t][c0 + c] = b;
+        as[t][c0 + c] =
+            live ? __expf(log_decay(zscale * __ldg(z + (zhead ? th : th * DK + c0 + c)))) : 1.f;
+        qq += a * a;
+        kk += b * b;
+        kq += a * b;
       }
 #pragma unroll
-      for (int o = 1; o < CS::TPK; o <<= 1) {  // over the token's staging threads
+      for (int c = part; c < DV; c += CS::TPK) vs[t][c] = live ? IO<T>::ld(v + th * DV + c) : 0.f;
+#pragma unroll
+      for (int o = 1; o < CS::TPK; o <<= 1) {
         qq += __shfl_xor_sync(0xffffffffu, qq, o);
         kk += __shfl_xor_sync(0xffffffffu, kk, o);
         kq += __shfl_xor_sync(0xffffffffu, kq, o);
       }
-      if (live) {
-        const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
+      const float rq = rsqrtf(qq + kNormEps), rk = rsqrtf(kk + kNormEps);
 #pragma unroll
-        for (int c = 0; c < CS::CH; ++c) {  // this thread's own values: no barrier needed
-          qs[t][c0 + c] *= rq;
-          ks[t][c0 + c] *= rk;
-        }
-        if (part == 0) {
-          bs[t] = __ldg(beta + th);
-          kqs[t] = kq * rq * rk;
-        }
+      for (int c = 0; c < CS::CH; ++c) {
+        qs[t][c0 + c] *= rq;
+        ks[t][c0 + c] *= rk;
+      }
+      if (part == 0) {
+        bs[t] = live ? __ldg(beta + th) : 0.f;
+        kqs[t] = kq * rq * rk;
       }
     }
     __syncthreads();
-    for (int t = 0; t < nb; ++t) {  // e = v - Sbar^T k^, o = Sbar^T q^ + beta (k^.q^) e
-      float pk = 0.f, pq = 0.f;
+    {  // per group: A_j, the scaled rows (in place) and c, d (TPG threads, 4 channels each)
+      const int gi = threadIdx.x / TPG, p = threadIdx.x % TPG, c0 = 4 * p, t0 = 4 * gi;
+      float kh[4][4], qh[4][4], al[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t0 + j][c0]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&qs[t0 + j][c0]);
+        const float4 a4 = *reinterpret_cast<const float4*>(&as[t0 + j][c0]);
+        kh[j][0] = k4.x; kh[j][1] = k4.y; kh[j][2] = k4.z; kh[j][3] = k4.w;
+        qh[j][0] = q4.x; qh[j][1] = q4.y; qh[j][2] = q4.z; qh[j][3] = q4.w;
+        al[j][0] = a4.x; al[j][1] = a4.y; al[j][2] = a4.z; al[j][3] = a4.w;
+      }
+      float cd[12];
+#pragma unroll
+      for (int m = 0; m < 12; ++m) cd[m] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // channel c0 + u
+        float A[4];
+        A[0] = al[0][u];
+#pragma unroll
+        for (int j = 1; j < 4; ++j) A[j] = A[j - 1] * al[j][u];
+        // rho(j, i) = A_j / A_i as products of the decays in between
+        const float r10 = al[1][u], r21 = al[2][u], r32 = al[3][u];
+        const float r20 = r21 * r10, r31 = r32 * r21, r30 = r31 * r10;
+        cd[0] += kh[1][u] * r10 * kh[0][u];
+        cd[1] += kh[2][u] * r20 * kh[0][u];
+        cd[2] += kh[2][u] * r21 * kh[1][u];
+        cd[3] += kh[3][u] * r30 * kh[0][u];
+        cd[4] += kh[3][u] * r31 * kh[1][u];
+        cd[5] += kh[3][u] * r32 * kh[2][u];
+        cd[6] += qh[1][u] * r10 * kh[0][u];
+        cd[7] += qh[2][u] * r20 * kh[0][u];
+        cd[8] += qh[2][u] * r21 * kh[1][u];
+        cd[9] += qh[3][u] * r30 * kh[0][u];
+        cd[10] += qh[3][u] * r31 * kh[1][u];
+        cd[11] += qh[3][u] * r32 * kh[2][u];
+        const float e3[4] = {r30, r31, r32, 1.f};  // A_3 / A_j
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ks[t0 + j][c0 + u] = A[j] * kh[j][u];
+          qs[t0 + j][c0 + u] = A[j] * qh[j][u];
+          as[t0 + j][c0 + u] = e3[j] * kh[j][u];
+        }
+        a3s[gi][c0 + u] = A[3];
+      }
+#pragma unroll
+      for (int o = 1; o < TPG; o <<= 1)
+#pragma unroll
+        for (int m = 0; m < 12; ++m) cd[m] += __shfl_xor_sync(0xffffffffu, cd[m], o);
+      if (p == 0)
+#pragma unroll
+        for (int m = 0; m < 12; ++m) cds[gi][m] = cd[m];
+    }
+    __syncthreads();
+    const int ngr = (nb + 3) / 4;
+    for (int gi = 0; gi < ngr; ++gi) {
+      const int t0 = 4 * gi;
+      float K[4] = {0.f, 0.f, 0.f, 0.f}, Q[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i0 = 0; i0 < R; i0 += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(&as[t][rg * R + i0]);
-        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t][rg * R + i0]);
-        const float4 q4 = *reinterpret_cast<const float4*>(&qs[t][rg * R + i0]);
-        s[i0] *= a4.x; s[i0 + 1] *= a4.y; s[i0 + 2] *= a4.z; s[i0 + 3] *= a4.w;
-        pk = fmaf(k4.x, s[i0], pk); pk = fmaf(k4.y, s[i0 + 1], pk);
-        pk = fmaf(k4.z, s[i0 + 2], pk); pk = fmaf(k4.w, s[i0 + 3], pk);
-        pq = fmaf(q4.x, s[i0], pq); pq = fmaf(q4.y, s[i0 + 1], pq);
-        pq = fmaf(q4.z, s[i0 + 2], pq); pq = fmaf(q4.w, s[i0 + 3], pq);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 k4 = *reinterpret_cast<const float4*>(&ks[t0 + j][rg * R + i0]);
+          const float4 q4 = *reinterpret_cast<const float4*>(&qs[t0 + j][rg * R + i0]);
+          K[j] = fmaf(k4.x, s[i0], K[j]); K[j] = fmaf(k4.y, s[i0 + 1], K[j]);
+          K[j] = fmaf(k4.z, s[i0 + 2], K[j]); K[j] = fmaf(k4.w, s[i0 + 3], K[j]);
+          Q[j] = fmaf(q4.x, s[i0], Q[j]); Q[j] = fmaf(q4.y, s[i0 + 1], Q[j]);
+          Q[j] = fmaf(q4.z, s[i0 + 2], Q[j]); Q[j] = fmaf(q4.w, s[i0 + 3], Q[j]);
+        }
       }
-      pk += __shfl_xor_sync(0xffffffffu, pk, 8);
-      pq += __shfl_xor_sync(0xffffffffu, pq, 8);
-      pk += __shfl_xor_sync(0xffffffffu, pk, 16);
-      pq += __shfl_xor_sync(0xffffffffu, pq, 16);
-      const float bt = bs[t];
-      const float e = vs[t][col] - pk;
-      if (rg == 0) IO<T>::st(out + ((size_t)(b0 + t) * H + h) * DV + col, pq + bt * kqs[t] * e);
-      const float be = bt * e;
+#pragma unroll
+      for (int o = 8; o < 32; o <<= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          K[j] += __shfl_xor_sync(0xffffffffu, K[j], o);
+          Q[j] += __shfl_xor_sync(0xffffffffu, Q[j], o);
+        }
+      const float* const cd = cds[gi];
+      float x[4];
+      x[0] = bs[t0] * (vs[t0][col] - K[0]);
+      x[1] = bs[t0 + 1] * (vs[t0 + 1][col] - K[1] - cd[0] * x[0]);
+      x[2] = bs[t0 + 2] * (vs[t0 + 2][col] - K[2] - cd[1] * x[0] - cd[2] * x[1]);
+      x[3] = bs[t0 + 3] * (vs[t0 + 3][col] - K[3] - cd[3] * x[0] - cd[4] * x[1] - cd[5] * x[2]);
+      if (rg == 0) {
+        const float o[4] = {Q[0] + kqs[t0] * x[0],
+                            Q[1] + cd[6] * x[0] + kqs[t0 + 1] * x[1],
+                            Q[2] + cd[7] * x[0] + cd[8] * x[1] + kqs[t0 + 2] * x[2],
+                            Q[3] + cd[9] * x[0] + cd[10] * x[1] + cd[11] * x[2] +
+                                kqs[t0 + 3] * x[3]};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (t0 + j < nb) IO<T>::st(out + ((size_t)(b0 + t0 + j) * H + h) * DV + col, o[j]);
+      }
 #pragma unroll
       for (int i0 = 0; i0 < R; i0 += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t][rg * R + i0]);
-        s[i0] = fmaf(k4.x, be, s[i0]); s[i0 + 1] = fmaf(k4.y, be, s[i0 + 1]);
-        s[i0 + 2] = fmaf(k4.z, be, s[i0 + 2]); s[i0 + 3] = fmaf(k4.w, be, s[i0 + 3]);
+        const float4 a4 = *reinterpret_cast<const float4*>(&a3s[gi][rg * R + i0]);
+        float4 e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e[j] = *reinterpret_cast<const float4*>(&as[t0 + j][rg * R + i0]);
+        s[i0] = fmaf(e[3].x, x[3], fmaf(e[2].x, x[2], fmaf(e[1].x, x[1], fmaf(e[0].x, x[0], a4.x * s[i0]))));
+        s[i0 + 1] = fmaf(e[3].y, x[3], fmaf(e[2].y, x[2], fmaf(e[1].y, x[1], fmaf(e[0].y, x[0], a4.y * s[i0 + 1]))));
+        s[i0 + 2] = fmaf(e[3].z, x[3], fmaf(e[2].z, x[2], fmaf(e[1].z, x[1], fmaf(e[0].z, x[0], a4.z * s[i0 + 2]))));
+        s[i0 + 3] = fmaf(e[3].w, x[3], fmaf(e[2].w, x[2], fmaf(e[1].w, x[1], fmaf(e[0].w, x[0], a4.w * s[i0 + 3]))));
       }
-      if (ckpt && (b0 + t + 1 - bos) % ckpt_every == 0) {  // state after a multiple of ckpt_every
-        const size_t j = (size_t)__ldg(ckpt_off + n) + (b0 + t + 1 - bos) / ckpt_every - 1;
+      const int done = min(t0 + 4, nb);  // tokens of the block applied
+      if (ckpt && (b0 + done - bos) % ckpt_every == 0) {  // a checkpoint ends this group
+        const size_t j = (size_t)__ldg(ckpt_off + n) + (b0 + done - bos) / ckpt_every - 1;
         float* dst = ckpt + (j * H + h) * DK * DV;
 #pragma unroll
         for (int i = 0; i < R; ++i) dst[(size_t)(rg * R + i) * DV + col] = s[i];
@@ -929,6 +1025,7 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 template <int DK, typename T>
 cudaError_t cta_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
+  if (a.ckpt && a.ckpt_every % 4 != 0) return cudaErrorInvalidValue;  // the API takes 64s
   recurrent_cta_kernel<DK, T><<<blocks, kCtaNT, 0, st>>>(
       (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
       (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt, a.ckpt_off,
