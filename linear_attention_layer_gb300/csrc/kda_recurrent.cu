@@ -841,7 +841,8 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
                       const float* initial_state, const int32_t* __restrict__ cu,
                       T* __restrict__ out, float* final_state, int H, int total, int* err,
                       const float* __restrict__ a_log, float* ckpt,
-                      const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead) {
+                      const int32_t* __restrict__ ckpt_off, int ckpt_every, int zhead,
+                      int vec) {
   using CS = CtaShape<DK>;
   constexpr int DV = 32, BLK = CS::BLK, R = CS::R, NG = BLK / 4;
   constexpr int TPG = kCtaNT / NG;  // group-staging threads per group
@@ -852,6 +853,14 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   __shared__ __align__(16) float vs[BLK][DV];
   __shared__ float bs[BLK], kqs[BLK];
   __shared__ float cds[NG][12];  // c10 c20 c21 c30 c31 c32, then d in the same order
+  __shared__ float zh[BLK];      // (one gate per head) the block's logits
+  // (16-byte aligned inputs) the block's raw q, k, v rows, copied in by cp.async
+  // (fp32: straight into qs, ks, vs; bf16: here, then widened)
+  constexpr bool kNarrow = sizeof(T) == 2;
+  __shared__ __align__(16) T rawbuf[kNarrow ? BLK * (2 * DK + DV) : 8];
+  T* const rq = kNarrow ? rawbuf : reinterpret_cast<T*>(&qs[0][0]);
+  T* const rkk = kNarrow ? rawbuf + BLK * DK : reinterpret_cast<T*>(&ks[0][0]);
+  T* const rv = kNarrow ? rawbuf + 2 * BLK * DK : reinterpret_cast<T*>(&vs[0][0]);
   const int n = blockIdx.x / H, h = blockIdx.x % H;
   int bos, eos;
   if (!seq_range(cu, n, total, threadIdx.x == 0 ? err : nullptr, bos, eos)) return;
@@ -866,6 +875,34 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   for (int b0 = bos; b0 < eos; b0 += BLK) {
     const int nb = min(BLK, eos - b0);
     __syncthreads();  // the previous block's rows are read
+    if (vec) {  // the block's rows in one round trip: 16-byte pieces, every thread
+      constexpr int QP = DK * (int)sizeof(T) / 16, VP = DV * (int)sizeof(T) / 16, ZP = DK / 4;
+      constexpr int QE = 16 / (int)sizeof(T);  // elements per piece
+      for (int i = threadIdx.x; i < nb * QP; i += kCtaNT) {
+        const int t = i / QP, j = i % QP;
+        const size_t th = (size_t)(b0 + t) * H + h;
+        cp_async_b16(rq + t * DK + QE * j, q + th * DK + QE * j);
+        cp_async_b16(rkk + t * DK + QE * j, k + th * DK + QE * j);
+      }
+      for (int i = threadIdx.x; i < nb * VP; i += kCtaNT) {
+        const int t = i / VP, j = i % VP;
+        cp_async_b16(rv + t * DV + QE * j, v + ((size_t)(b0 + t) * H + h) * DV + QE * j);
+      }
+      if (!zhead) {
+        for (int i = threadIdx.x; i < nb * ZP; i += kCtaNT) {
+          const int t = i / ZP, j = i % ZP;
+          cp_async_b16(&as[t][4 * j], z + ((size_t)(b0 + t) * H + h) * DK + 4 * j);
+        }
+      }
+      for (int t = threadIdx.x; t < nb; t += kCtaNT) {
+        const size_t th = (size_t)(b0 + t) * H + h;
+        cp_async_b4(&bs[t], beta + th);
+        if (zhead) cp_async_b4(&zh[t], z + th);
+      }
+      cp_async_commit();
+      cp_async_wait_pending<0>();
+      __syncthreads();
+    }
     {  // stage the tokens (rows past the sequence: k = q = v = 0, alpha = 1, beta = 0)
       const int t = threadIdx.x / CS::TPK, part = threadIdx.x % CS::TPK, c0 = part * CS::CH;
       float qq = 0.f, kk = 0.f, kq = 0.f;
@@ -873,18 +910,28 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
       const size_t th = (size_t)(b0 + t) * H + h;
 #pragma unroll
       for (int c = 0; c < CS::CH; ++c) {
-        const float a = live ? IO<T>::ld(q + th * DK + c0 + c) : 0.f;
-        const float b = live ? IO<T>::ld(k + th * DK + c0 + c) : 0.f;
+        float a = 0.f, b = 0.f, zz = 0.f;
+        if (live) {
+          if (vec) {
+            a = ld_raw(rq + t * DK + c0 + c);
+            b = ld_raw(rkk + t * DK + c0 + c);
+            zz = zhead ? zh[t] : as[t][c0 + c];
+          } else {
+            a = IO<T>::ld(q + th * DK + c0 + c);
+            b = IO<T>::ld(k + th * DK + c0 + c);
+            zz = __ldg(z + (zhead ? th : th * DK + c0 + c));
+          }
+        }
         qs[t][c0 + c] = a;
         ks[t][c0 + c] = b;
-        as[t][c0 + c] =
-            live ? __expf(log_decay(zscale * __ldg(z + (zhead ? th : th * DK + c0 + c)))) : 1.f;
+        as[t][c0 + c] = live ? __expf(log_decay(zscale * zz)) : 1.f;
         qq += a * a;
         kk += b * b;
         kq += a * b;
       }
 #pragma unroll
-      for (int c = part; c < DV; c += CS::TPK) vs[t][c] = live ? IO<T>::ld(v + th * DV + c) : 0.f;
+      for (int c = part; c < DV; c += CS::TPK)
+        vs[t][c] = live ? (vec ? ld_raw(rv + t * DV + c) : IO<T>::ld(v + th * DV + c)) : 0.f;
 #pragma unroll
       for (int o = 1; o < CS::TPK; o <<= 1) {
         qq += __shfl_xor_sync(0xffffffffu, qq, o);
@@ -898,7 +945,7 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         ks[t][c0 + c] *= rk;
       }
       if (part == 0) {
-        bs[t] = live ? __ldg(beta + th) : 0.f;
+        bs[t] = live ? (vec ? bs[t] : __ldg(beta + th)) : 0.f;
         kqs[t] = kq * rq * rk;
       }
     }
@@ -1026,10 +1073,12 @@ template <int DK, typename T>
 cudaError_t cta_dispatch(const Problem& p, const Args& a, cudaStream_t st) {
   const unsigned blocks = (unsigned)p.num_seqs * (unsigned)p.num_heads;
   if (a.ckpt && a.ckpt_every % 4 != 0) return cudaErrorInvalidValue;  // the API takes 64s
+  auto a16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  const int vec = a16(a.q) && a16(a.k) && a16(a.v) && (a.gate_per_head || a16(a.z));
   recurrent_cta_kernel<DK, T><<<blocks, kCtaNT, 0, st>>>(
       (const T*)a.q, (const T*)a.k, (const T*)a.v, a.z, a.beta, a.initial_state, a.cu_seqlens,
       (T*)a.out, a.final_state, p.num_heads, p.total_tokens, a.err, a.a_log, a.ckpt, a.ckpt_off,
-      a.ckpt_every, a.gate_per_head);
+      a.ckpt_every, a.gate_per_head, vec);
   return cudaGetLastError();
 }
 

@@ -735,6 +735,23 @@ def test_small_state_path(dtype, dk):
     assert_close(fin2, rf2, dtype, "per-head gate final_state")
 
 
+@pytest.mark.parametrize("dtype,dk", [(torch.float32, 32), (torch.bfloat16, 64)])
+def test_small_state_inputs_not_16_byte_aligned(dtype, dk):
+    """q, k, v, z that start off a 16-byte boundary take the small-state
+    path's element-wise staging (aligned inputs are copied in by cp.async):
+    the same results bit for bit."""
+    p = workloads.random_problem([70, 5, 130], 2, dk, 32, dtype, init_std=0.2, seed=37,
+                                 device=DEV)
+    o1, f1 = kda.chunk_fwd(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens, p.initial_state)
+    mq, mk, mv, mz = (_misaligned(x) for x in (p.q, p.k, p.v, p.z))
+    assert all(x.data_ptr() % 16 for x in (mq, mk, mv, mz))
+    o2, f2 = kda.chunk_fwd(mq, mk, mv, mz, p.beta, p.cu_seqlens, p.initial_state)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    _check_all(p, o1, f1, dtype)
+
+
 def test_small_state_many_units():
     """More (sequence, head) units than the small-state path gives a CTA each
     (1,024): 600 sequences x 2 heads run one warp per unit, against the
