@@ -335,26 +335,9 @@ __global__ void __launch_bounds__(kNT, 2) conv_tile_kernel(const __grid_constant
         report_error(err, kErrDeviceCheck);
       } else {
         fill(ta);
-        for (int t = ta; t < tb; ++t) {
-          if (t >= eos) {  // the next non-empty sequence starts at t
-            bool bad = false;
-            while (eos <= t) {
-              ++n;
-              bos = __ldg(cu + n);
-              eos = __ldg(cu + n + 1);
-              if (eos < bos || bos > t) {
-                bad = true;
-                break;
-              }
-            }
-            if (bad) {
-              report_error(err, kErrDeviceCheck);
-              break;
-            }
-            fill(t);
-          }
-          float xt[kVec], out[kVec];
-          ld4_smem(rows + (size_t)(t - t0 + kHalo) * CS + 4 * q, xt);
+        // one token: y_t from the window and x_t, then x_t enters the window
+        auto token = [&](int t, const float (&xt)[kVec]) {
+          float out[kVec];
 #pragma unroll
           for (int c = 0; c < kVec; ++c) {
             float acc = wr[W - 1][c] * xt[c];
@@ -370,6 +353,38 @@ __global__ void __launch_bounds__(kNT, 2) conv_tile_kernel(const __grid_constant
           if (W > 1)
 #pragma unroll
             for (int c = 0; c < kVec; ++c) win[W > 1 ? W - 2 : 0][c] = xt[c];
+        };
+        if (tb - ta == TS::TPT && eos >= tb) {  // a whole run inside one sequence: unrolled
+          const T* const rr = rows + (size_t)(ta - t0 + kHalo) * CS + 4 * q;
+#pragma unroll
+          for (int u = 0; u < TS::TPT; ++u) {
+            float xt[kVec];
+            ld4_smem(rr + u * CS, xt);
+            token(ta + u, xt);
+          }
+        } else {
+          for (int t = ta; t < tb; ++t) {
+            if (t >= eos) {  // the next non-empty sequence starts at t
+              bool bad = false;
+              while (eos <= t) {
+                ++n;
+                bos = __ldg(cu + n);
+                eos = __ldg(cu + n + 1);
+                if (eos < bos || bos > t) {
+                  bad = true;
+                  break;
+                }
+              }
+              if (bad) {
+                report_error(err, kErrDeviceCheck);
+                break;
+              }
+              fill(t);
+            }
+            float xt[kVec];
+            ld4_smem(rows + (size_t)(t - t0 + kHalo) * CS + 4 * q, xt);
+            token(t, xt);
+          }
         }
       }
     }
