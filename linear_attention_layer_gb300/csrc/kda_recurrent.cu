@@ -801,14 +801,14 @@ recurrent_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
 }
 
 // Small states (dv = 32, dk <= 64) with few (sequence, head) units: one
-// 128-thread CTA per unit, the sequence in blocks of BLK tokens.  First all
+// 256-thread CTA per unit, the sequence in blocks of BLK tokens.  First all
 // threads stage the block -- q and k normalised, the decays, beta, (q^.k^), v
 // and the products below, none of which depends on the state -- in shared
-// memory; then each warp runs the token loop for its own eight value columns,
+// memory; then each warp runs the token loop for its own four value columns,
 // lane (rg, col) holding key rows [rg R, rg R + R) of its column, the sums
 // over the key rows by warp shuffles: no block barrier inside the token loop,
 // and only the state chain left on it.
-constexpr int kCtaNT = 128;
+constexpr int kCtaNT = 256;
 constexpr long long kCtaUnitsMax = 1024;  // (sequence, head) units for a CTA each
 
 template <int DK>
@@ -816,7 +816,7 @@ struct CtaShape {
   static constexpr int BLK = DK == 64 ? 32 : 64;  // tokens per block
   static constexpr int TPK = kCtaNT / BLK;        // staging threads per token
   static constexpr int CH = DK / TPK;             // channels each stages
-  static constexpr int R = DK / 4;                // key rows per thread
+  static constexpr int R = DK / 8;                // key rows per thread
 };
 
 // The token loop takes four tokens at a time.  For a group j = 0..3 entered
@@ -846,7 +846,8 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   using CS = CtaShape<DK>;
   constexpr int DV = 32, BLK = CS::BLK, R = CS::R, NG = BLK / 4;
   constexpr int TPG = kCtaNT / NG;  // group-staging threads per group
-  static_assert(DK / TPG == 4, "four channels per group-staging thread");
+  constexpr int CPT = DK / TPG;  // channels per group-staging thread
+  static_assert(CPT == 2, "two channels per group-staging thread");
   // per token: q^ then A_j q^, k^ then A_j k^, alpha then (A_3 / A_j) k^
   __shared__ __align__(16) float qs[BLK][DK], ks[BLK][DK], as[BLK][DK];
   __shared__ __align__(16) float a3s[NG][DK];
@@ -865,7 +866,7 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   int bos, eos;
   if (!seq_range(cu, n, total, threadIdx.x == 0 ? err : nullptr, bos, eos)) return;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = 8 * w + (lane & 7), rg = lane >> 3;
+  const int col = 4 * w + (lane & 3), rg = lane >> 2;
   const size_t sbase = (size_t)blockIdx.x * DK * DV;
   float s[R];
 #pragma unroll
@@ -950,23 +951,23 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
       }
     }
     __syncthreads();
-    {  // per group: A_j, the scaled rows (in place) and c, d (TPG threads, 4 channels each)
-      const int gi = threadIdx.x / TPG, p = threadIdx.x % TPG, c0 = 4 * p, t0 = 4 * gi;
-      float kh[4][4], qh[4][4], al[4][4];
+    {  // per group: A_j, the scaled rows (in place) and c, d (TPG threads, CPT channels each)
+      const int gi = threadIdx.x / TPG, p = threadIdx.x % TPG, c0 = CPT * p, t0 = 4 * gi;
+      float kh[4][CPT], qh[4][CPT], al[4][CPT];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 k4 = *reinterpret_cast<const float4*>(&ks[t0 + j][c0]);
-        const float4 q4 = *reinterpret_cast<const float4*>(&qs[t0 + j][c0]);
-        const float4 a4 = *reinterpret_cast<const float4*>(&as[t0 + j][c0]);
-        kh[j][0] = k4.x; kh[j][1] = k4.y; kh[j][2] = k4.z; kh[j][3] = k4.w;
-        qh[j][0] = q4.x; qh[j][1] = q4.y; qh[j][2] = q4.z; qh[j][3] = q4.w;
-        al[j][0] = a4.x; al[j][1] = a4.y; al[j][2] = a4.z; al[j][3] = a4.w;
+        const float2 k2 = *reinterpret_cast<const float2*>(&ks[t0 + j][c0]);
+        const float2 q2 = *reinterpret_cast<const float2*>(&qs[t0 + j][c0]);
+        const float2 a2 = *reinterpret_cast<const float2*>(&as[t0 + j][c0]);
+        kh[j][0] = k2.x; kh[j][1] = k2.y;
+        qh[j][0] = q2.x; qh[j][1] = q2.y;
+        al[j][0] = a2.x; al[j][1] = a2.y;
       }
       float cd[12];
 #pragma unroll
       for (int m = 0; m < 12; ++m) cd[m] = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // channel c0 + u
+      for (int u = 0; u < CPT; ++u) {  // channel c0 + u
         float A[4];
         A[0] = al[0][u];
 #pragma unroll
@@ -1021,7 +1022,7 @@ recurrent_cta_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         }
       }
 #pragma unroll
-      for (int o = 8; o < 32; o <<= 1)
+      for (int o = 4; o < 32; o <<= 1)  // over the row groups of this column
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           K[j] += __shfl_xor_sync(0xffffffffu, K[j], o);
