@@ -1303,7 +1303,9 @@ state_scan_kernel(const __grid_constant__ ScanParams Q) {
 
 struct SplitPlan {
   bool use = false;
-  int seg_len = 0, E = 0;
+  int seg_len = 0, seg0_len = 0, E = 0;  // tokens of segments 1, 2, .. and of segment 0
+  int s0_at = -1;  // pass 1: position of the block of segment-0 entries among the inner
+                   // entries, or -1 for each before its own sequence's
   std::vector<int> nseg, base;
   size_t bytes = 0;
 };
@@ -1313,61 +1315,219 @@ constexpr int kMaxEntries = kMaxOrder / kEnt;
 // launches (from this host thread) that still get an unsatisfiable input wait
 thread_local int g_inject_wait_timeout = 0;
 
-// Choose a segment length by a waves-of-SMs cost model; split only when it
-// beats the unsplit launch by a clear margin.  Plans whose segment summaries
-// need more than max_bytes of scratch are not considered.
-SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms,
-                     size_t max_bytes = ~(size_t)0) {
+// Token range of segment q of sequence n.
+void seg_range(const SplitPlan& pl, const int32_t* cu, int n, int q, int& tb, int& te) {
+  tb = q == 0 ? cu[n] : cu[n] + pl.seg0_len + (q - 1) * pl.seg_len;
+  te = std::min(cu[n + 1], tb + (q == 0 ? pl.seg0_len : pl.seg_len));
+}
+
+struct RunEntry {
+  int n, tb, te, in, out, flags;
+};
+
+// Pass 1: segment 0 of every split sequence, from the true initial state, and
+// the two runs (S~ from zero, M from the identity) of every inner segment.
+std::vector<RunEntry> pass1_entries(const SplitPlan& pl, const int32_t* cu, int num_seqs) {
+  std::vector<RunEntry> inner, first, all;
+  for (int n = 0; n < num_seqs; ++n) {
+    const int k = pl.nseg[n], b = pl.base[n];
+    if (k < 2) continue;
+    int tb, te;
+    seg_range(pl, cu, n, 0, tb, te);
+    const RunEntry e0{n, tb, te, kSlotUser, b + 1, 0};
+    if (pl.s0_at < 0) all.push_back(e0);
+    else first.push_back(e0);
+    for (int q = 1; q + 1 < k; ++q) {
+      seg_range(pl, cu, n, q, tb, te);
+      const RunEntry es{n, tb, te, kSlotZero, pl.E + b + q, kFlagNoOut};
+      const RunEntry em{n, tb, te, kSlotIdentity, 2 * pl.E + b + q, kFlagZeroV | kFlagNoOut};
+      if (pl.s0_at < 0) {
+        all.push_back(es);
+        all.push_back(em);
+      } else {
+        inner.push_back(es);
+        inner.push_back(em);
+      }
+    }
+  }
+  if (pl.s0_at < 0) return all;
+  const size_t at = std::min<size_t>((size_t)pl.s0_at, inner.size());
+  all.assign(inner.begin(), inner.begin() + at);
+  all.insert(all.end(), first.begin(), first.end());
+  all.insert(all.end(), inner.begin() + at, inner.end());
+  return all;
+}
+
+// Pass 2: every segment but a split sequence's first (and every unsplit
+// sequence), from its entry state, longest first.
+std::vector<RunEntry> pass2_entries(const SplitPlan& pl, const int32_t* cu, int num_seqs) {
+  std::vector<std::array<int, 4>> segs;  // {len, n, q, k}
+  for (int n = 0; n < num_seqs; ++n)
+    for (int q = pl.nseg[n] >= 2 ? 1 : 0; q < pl.nseg[n]; ++q) {
+      int tb, te;
+      seg_range(pl, cu, n, q, tb, te);
+      segs.push_back({te - tb, n, q, pl.nseg[n]});
+    }
+  std::stable_sort(segs.begin(), segs.end(),
+                   [](const std::array<int, 4>& x, const std::array<int, 4>& y) { return x[0] > y[0]; });
+  std::vector<RunEntry> all;
+  for (const auto& sg : segs) {
+    int tb, te;
+    seg_range(pl, cu, sg[1], sg[2], tb, te);
+    all.push_back({sg[1], tb, te, pl.base[sg[1]] + sg[2], sg[2] + 1 == sg[3] ? kSlotUser : kSlotNone,
+                   0});
+  }
+  return all;
+}
+
+// Chunk-times until the last of a launch's units ends, given its entries'
+// lengths in chunks: unit u is entry u / H, and CTA b of the min(units, sms)
+// runs units b, b + grid, ...
+double static_makespan(const std::vector<int>& len, int H, int sms, std::vector<double>& t) {
+  const long units = (long)len.size() * H;
+  if (units == 0) return 0.0;
+  const long grid = std::min<long>(units, sms);
+  t.assign(grid, 0.0);
+  long b = 0;  // the CTA of unit i * H + h
+  for (size_t i = 0; i < len.size(); ++i)
+    for (int h = 0; h < H; ++h) {
+      t[b] += len[i];
+      if (++b == grid) b = 0;
+    }
+  return *std::max_element(t.begin(), t.end());
+}
+
+double static_makespan(const std::vector<RunEntry>& es, int H, int sms) {
+  std::vector<int> len(es.size());
+  for (size_t i = 0; i < es.size(); ++i) len[i] = (es[i].te - es[i].tb + kC - 1) / kC;
+  std::vector<double> t;
+  return static_makespan(len, H, sms, t);
+}
+
+// Choose the segment lengths by the launches' makespans; split only when it
+// beats the unsplit launch by a clear margin.  Segment 0 runs once (in pass 1,
+// beside the inner segments' two runs each), every later segment also runs
+// in pass 2, so segment 0 may be longer than the rest; where the block of
+// segment-0 entries goes in pass 1 is chosen so that no CTA holding one gets a
+// second entry.  Plans whose segment summaries need more than max_bytes of
+// scratch are not considered.  (The entry lengths below follow the order of
+// pass1_entries and pass2_entries.)
+SplitPlan plan_split_search(const Problem& p, const int32_t* cu, int sms, size_t max_bytes) {
   SplitPlan best;
   if (!cu || p.num_seqs == 0 || p.num_seqs > kMaxScanSeqs) return best;
   const long units = (long)p.num_seqs * p.num_heads;
   if (units >= 2L * sms) return best;
+  std::vector<long> cs(p.num_seqs);
   long maxc = 0, sumc = 0;
   for (int n = 0; n < p.num_seqs; ++n) {
-    const long c = (cu[n + 1] - cu[n] + kC - 1) / kC;
-    maxc = std::max(maxc, c);
-    sumc += c;
+    cs[n] = (cu[n + 1] - cu[n] + kC - 1) / kC;
+    maxc = std::max(maxc, cs[n]);
+    sumc += cs[n];
   }
   const double unsplit = std::max<double>(maxc, std::ceil((double)sumc * p.num_heads / sms));
   double best_cost = 0.85 * unsplit;
+  static const double kFirst[] = {1.0, 1.5, 2.0, 2.5, 3.0};  // segment 0 / the rest
+  std::vector<int> nat, inner, first, order, p2;
+  std::vector<double> t;
   for (int target = 2; target <= 64; ++target) {
-    const long segc = (maxc + target - 1) / target;  // chunks per segment
-    if (segc < 4) break;
-    long e = 0, u1 = 0, u3 = 0, steps = 0;
-    std::vector<int> ns(p.num_seqs);
-    for (int n = 0; n < p.num_seqs; ++n) {
-      const long c = (cu[n + 1] - cu[n] + kC - 1) / kC;
-      const int k = (int)std::max<long>(1, (c + segc - 1) / segc);
-      ns[n] = k;
-      e += k;
-      u3 += k >= 2 ? k - 1 : 1;  // a split sequence's segment 0 finishes in pass 1
-      if (k >= 2) u1 += 1 + 2 * (k - 2);
-      steps = std::max<long>(steps, k - 2);
-    }
-    if (e > kMaxEntries || u1 > kMaxEntries) continue;
-    if (3 * (size_t)e * p.num_heads * kD * kD * sizeof(float) > max_bytes) continue;
-    u1 *= p.num_heads;
-    u3 *= p.num_heads;
-    const double cost = std::ceil((double)u1 / sms) * segc + std::ceil((double)u3 / sms) * segc +
-                        (double)steps;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best.use = true;
-      best.seg_len = (int)(segc * kC);
-      best.E = (int)e;
-      best.nseg = ns;
+    for (double f : kFirst) {
+      const long segc = (long)std::ceil((double)maxc / (f + target - 1));  // chunks per segment
+      if (segc < 4) continue;
+      const long seg0c = std::min<long>(maxc, (long)std::lround(f * segc));
+      nat.clear();
+      inner.clear();
+      first.clear();
+      p2.clear();
+      long steps = 0, e = 0;
+      for (int n = 0; n < p.num_seqs; ++n) {
+        const long c = cs[n];
+        const int k = c <= seg0c ? 1 : (int)(1 + (c - seg0c + segc - 1) / segc);
+        e += k;
+        steps = std::max<long>(steps, k - 2);
+        if (k < 2) {
+          p2.push_back((int)c);
+          continue;
+        }
+        nat.push_back((int)seg0c);
+        first.push_back((int)seg0c);
+        for (int q = 1; q + 1 < k; ++q) {
+          nat.push_back((int)segc);
+          nat.push_back((int)segc);
+          inner.push_back((int)segc);
+          inner.push_back((int)segc);
+          p2.push_back((int)segc);
+        }
+        p2.push_back((int)(c - seg0c - (k - 2) * segc));  // the last segment
+      }
+      if (e > kMaxEntries || nat.empty() || (long)nat.size() > kMaxEntries ||
+          (long)p2.size() > kMaxEntries)
+        continue;
+      if (3 * (size_t)e * p.num_heads * kD * kD * sizeof(float) > max_bytes) continue;
+      if ((long)nat.size() * p.num_heads > 4L * sms) continue;  // pass 1 in more than 4 waves
+      // pass 1 in the order with the smallest makespan: natural, or the
+      // segment-0 block first, last, or where its units end the first wave
+      // on CTAs that get no second unit
+      double ms1 = static_makespan(nat, p.num_heads, sms, t);
+      int best_at = -1;
+      const int n_inner = (int)inner.size();
+      const long u1 = (long)nat.size() * p.num_heads, grid = std::min<long>(u1, sms);
+      const int ideal = (int)std::min<long>(
+          n_inner, (std::max<long>(0, u1 - grid) + p.num_heads - 1) / p.num_heads);
+      for (int at : {0, n_inner, ideal}) {
+        order.assign(inner.begin(), inner.begin() + at);
+        order.insert(order.end(), first.begin(), first.end());
+        order.insert(order.end(), inner.begin() + at, inner.end());
+        const double m = static_makespan(order, p.num_heads, sms, t);
+        if (m < ms1) {
+          ms1 = m;
+          best_at = at;
+        }
+      }
+      std::sort(p2.begin(), p2.end(), std::greater<int>());  // pass 2 runs longest first
+      const double cost = ms1 + static_makespan(p2, p.num_heads, sms, t) + (double)steps;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best.use = true;
+        best.seg_len = (int)(segc * kC);
+        best.seg0_len = (int)(seg0c * kC);
+        best.s0_at = best_at;
+        best.E = (int)e;
+      }
     }
   }
   if (best.use) {
+    const long segc = best.seg_len / kC, seg0c = best.seg0_len / kC;
+    best.nseg.resize(p.num_seqs);
     best.base.resize(p.num_seqs);
     int b = 0;
     for (int n = 0; n < p.num_seqs; ++n) {
+      best.nseg[n] = cs[n] <= seg0c ? 1 : (int)(1 + (cs[n] - seg0c + segc - 1) / segc);
       best.base[n] = b;
       b += best.nseg[n];
     }
     best.bytes = 3 * (size_t)best.E * p.num_heads * kD * kD * sizeof(float);
   }
   return best;
+}
+
+// plan_split_search for the last arguments seen on this host thread (a
+// workspace query and the launch that follows ask for the same plan).
+SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms,
+                     size_t max_bytes = ~(size_t)0) {
+  thread_local std::vector<int32_t> key_cu;
+  thread_local int key[3] = {-1, -1, -1};
+  thread_local size_t key_bytes = 0;
+  thread_local SplitPlan plan;
+  if (!cu || p.num_seqs == 0 || p.num_seqs > kMaxScanSeqs) return SplitPlan{};
+  const int k3[3] = {p.num_seqs, p.num_heads, sms};
+  if (std::equal(k3, k3 + 3, key) && key_bytes == max_bytes &&
+      key_cu.size() == (size_t)p.num_seqs + 1 && std::equal(cu, cu + p.num_seqs + 1, key_cu.begin()))
+    return plan;
+  plan = plan_split_search(p, cu, sms, max_bytes);
+  std::copy(k3, k3 + 3, key);
+  key_bytes = max_bytes;
+  key_cu.assign(cu, cu + p.num_seqs + 1);
+  return plan;
 }
 
 int sm_count() {
@@ -1523,28 +1683,12 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
   const int E = plan.E;
   prm.ws = static_cast<float*>(ws);
   prm.mode = 1;
-  auto seg = [&](int n, int q, int& tb, int& te) {
-    tb = cu_host[n] + q * plan.seg_len;
-    te = std::min(cu_host[n + 1], tb + plan.seg_len);
-  };
   int ne = 0;
-  auto put = [&](int n, int tb, int te, int in, int out, int flags) {
+  auto put = [&](const RunEntry& r) {
     int* e = prm.list + kEnt * ne++;
-    e[0] = n; e[1] = tb; e[2] = te; e[3] = in; e[4] = out; e[5] = flags;
+    e[0] = r.n; e[1] = r.tb; e[2] = r.te; e[3] = r.in; e[4] = r.out; e[5] = r.flags;
   };
-  for (int n = 0; n < p.num_seqs; ++n) {
-    const int k = plan.nseg[n], b = plan.base[n];
-    int tb, te;
-    if (k >= 2) {
-      seg(n, 0, tb, te);
-      put(n, tb, te, kSlotUser, b + 1, 0);
-    }
-    for (int q = 1; q + 1 < k; ++q) {
-      seg(n, q, tb, te);
-      put(n, tb, te, kSlotZero, E + b + q, kFlagNoOut);
-      put(n, tb, te, kSlotIdentity, 2 * E + b + q, kFlagZeroV | kFlagNoOut);
-    }
-  }
+  for (const RunEntry& r : pass1_entries(plan, cu_host, p.num_seqs)) put(r);
   // segment 0 runs from the true initial state, so it writes its outputs and
   // checkpoints here; the inner segments' runs from stand-in states do not
   prm.out = static_cast<__nv_bfloat16*>(a.out);
@@ -1569,21 +1713,8 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     if (e != cudaSuccess) return e;
   }
   // ---- pass 2: every other segment from its entry state, longest first ----
-  std::vector<std::array<int, 4>> segs;  // {len, n, q, k}
-  for (int n = 0; n < p.num_seqs; ++n)
-    for (int q = plan.nseg[n] >= 2 ? 1 : 0; q < plan.nseg[n]; ++q) {
-      int tb, te;
-      seg(n, q, tb, te);
-      segs.push_back({te - tb, n, q, plan.nseg[n]});
-    }
-  std::stable_sort(segs.begin(), segs.end(),
-                   [](const std::array<int, 4>& x, const std::array<int, 4>& y) { return x[0] > y[0]; });
   ne = 0;
-  for (const auto& sgi : segs) {
-    int tb, te;
-    seg(sgi[1], sgi[2], tb, te);
-    put(sgi[1], tb, te, plan.base[sgi[1]] + sgi[2], sgi[2] + 1 == sgi[3] ? kSlotUser : kSlotNone, 0);
-  }
+  for (const RunEntry& r : pass2_entries(plan, cu_host, p.num_seqs)) put(r);
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.ckpt = a.ckpt;
   prm.num_units = ne * p.num_heads;
