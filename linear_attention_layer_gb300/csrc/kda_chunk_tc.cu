@@ -61,6 +61,7 @@
 #include <cmath>
 #include <mutex>
 #include <numeric>
+#include <queue>
 #include <vector>
 
 #include "kda_common.cuh"
@@ -132,7 +133,9 @@ constexpr uint32_t TY = 448;    // Y^T = S^T K+^T fp32 [n][t] 64 cols
 constexpr float kF16Max = 65504.0f;
 
 // Work list.  mode 0: units are (sequence, head) pairs, list[i] = the i-th
-// sequence to process (longest first) when use_order, token ranges from the
+// sequence to process (longest first) when use_order == 1, or list[u] =
+// seq * H + head of unit u (-1: none) when use_order == 2 (a schedule built on
+// the host: CTA b runs list[b], list[b + grid], ...); token ranges from the
 // device cu_seqlens.  mode 1 (splitting long sequences): list holds entries
 // of kEnt ints {seq, token begin, token end, in, out, flags}; in / out are
 // state slots of `ws` (>= 0), or kSlotZero / kSlotIdentity / kSlotUser (the
@@ -457,10 +460,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   float absmax = 0.f;  // largest |value| this thread converted to fp16
 
   for (int u = blockIdx.x; u < P.num_units && !aborted; u += gridDim.x) {
-    const int si = u / H, h = u % H;
+    int si = u / H, h = u % H;
     int seq, bos, eos, in_slot = kSlotUser, out_slot = kSlotUser, flags = 0;
     if (P.mode == 0) {
-      seq = P.use_order ? P.list[si] : si;
+      if (P.use_order == 2) {  // the host's schedule
+        const int pk = P.list[u];
+        if (pk < 0) continue;  // this CTA has no unit at this position
+        si = pk / H;
+        h = pk % H;
+        seq = si;
+      } else {
+        seq = P.use_order ? P.list[si] : si;
+      }
       bos = P.cu[seq];
       eos = P.cu[seq + 1];
     } else {
@@ -1530,6 +1541,38 @@ SplitPlan plan_split(const Problem& p, const int32_t* cu, int sms,
   return plan;
 }
 
+// The (sequence, head) units of an unsplit launch, longest first, each given
+// to the CTA with the least work so far (chunks), written so that CTA b's
+// k-th unit is list[b + k * grid] (use_order 2).  False when the schedule
+// does not fit the list (the caller keeps the plain longest-first order).
+bool unit_schedule(const std::vector<int>& by_len, const int32_t* cu, int H, int grid,
+                   Params& prm) {
+  if (grid <= 0) return false;
+  std::vector<long> load(grid, 0);
+  std::vector<std::vector<int>> mine(grid);
+  using Slot = std::pair<long, int>;  // (chunks so far, CTA)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_first;
+  for (int b = 0; b < grid; ++b) free_first.push({0, b});
+  for (int seq : by_len) {
+    const long c = std::max<long>(1, (cu[seq + 1] - cu[seq] + kC - 1) / kC);
+    for (int h = 0; h < H; ++h) {
+      const Slot sl = free_first.top();
+      free_first.pop();
+      mine[sl.second].push_back(seq * H + h);
+      free_first.push({sl.first + c, sl.second});
+    }
+  }
+  size_t depth = 0;
+  for (const auto& m : mine) depth = std::max(depth, m.size());
+  if (depth * (size_t)grid > (size_t)kMaxOrder) return false;
+  for (size_t k = 0; k < depth; ++k)
+    for (int b = 0; b < grid; ++b)
+      prm.list[k * grid + b] = k < mine[b].size() ? mine[b][k] : -1;
+  prm.num_units = (int)(depth * grid);
+  prm.use_order = 2;
+  return true;
+}
+
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1672,8 +1715,11 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
       std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
         return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
       });
-      for (int i = 0; i < p.num_seqs; ++i) prm.list[i] = idx[i];
-      prm.use_order = 1;
+      const int grid = std::min(prm.num_units, sms);
+      if (!unit_schedule(idx, cu_host, p.num_heads, grid, prm)) {
+        for (int i = 0; i < p.num_seqs; ++i) prm.list[i] = idx[i];
+        prm.use_order = 1;
+      }
     }
     launch_tc(std::min(prm.num_units, sms));
     return cudaGetLastError();
