@@ -35,6 +35,7 @@
 
 #include "kda_common.cuh"
 #include "kda_launch.h"
+#include "kda_schedule.h"
 
 namespace kda {
 namespace bwd {
@@ -43,7 +44,7 @@ constexpr int kD = 128;
 constexpr int kNT = 512;
 constexpr int kBlk = 64;  // tokens whose inputs are staged in shared memory at once
 constexpr int kSub = 8;   // tokens between stored states
-constexpr int kMaxOrder = 2048;
+constexpr int kMaxOrder = 4096;
 constexpr size_t kState = (size_t)kD * kD;  // floats per state
 
 struct Params {
@@ -265,8 +266,14 @@ __global__ void __launch_bounds__(kNT, 1) bwd_kernel(const __grid_constant__ Par
   float* const subck = ring + kSub * kState;                             // every kSub tokens
 
   for (int unit = blockIdx.x; unit < P.num_units; unit += gridDim.x) {
-    const int si = unit / P.H, h = unit % P.H;
-    const int seq = P.use_order ? P.order[si] : si;
+    int si = unit / P.H, h = unit % P.H;
+    if (P.use_order == 2) {  // the host's schedule: order[unit] = seq * H + head, or -1
+      const int pk = P.order[unit];
+      if (pk < 0) continue;
+      si = pk / P.H;
+      h = pk % P.H;
+    }
+    const int seq = P.use_order == 1 ? P.order[si] : si;
     int bos, eos;
     if (!seq_range(P.cu, seq, P.total, P.err, bos, eos)) continue;
     const int len = eos - bos;
@@ -731,16 +738,23 @@ static cudaError_t launch_bwd_128(const Problem& p, const BwdArgs& a, const int3
   prm.num_units = p.num_seqs * p.num_heads;
   prm.zhead = a.zhead;
   prm.use_order = 0;
-  if (p.num_seqs <= kMaxOrder) {  // longest sequences first
+  const int grid = grid_for(p);
+  if (p.num_seqs <= kMaxOrder) {  // longest sequences first, each unit to the least-loaded CTA
     std::vector<int> idx(p.num_seqs);
     std::iota(idx.begin(), idx.end(), 0);
     std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
       return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
     });
-    for (int i = 0; i < p.num_seqs; ++i) prm.order[i] = idx[i];
-    prm.use_order = 1;
+    auto tokens = [&](int sq) { return (long long)(cu_host[sq + 1] - cu_host[sq]); };
+    const int n = build_unit_schedule(idx, p.num_heads, grid, tokens, prm.order, kMaxOrder);
+    if (n > 0) {
+      prm.num_units = n;
+      prm.use_order = 2;
+    } else {
+      for (int i = 0; i < p.num_seqs; ++i) prm.order[i] = idx[i];
+      prm.use_order = 1;
+    }
   }
-  const int grid = grid_for(p);
   if (p.io_bf16)
     prm.zhead ? bwd_kernel<__nv_bfloat16, true><<<grid, kNT, sizeof(Smem), st>>>(prm)
               : bwd_kernel<__nv_bfloat16, false><<<grid, kNT, sizeof(Smem), st>>>(prm);

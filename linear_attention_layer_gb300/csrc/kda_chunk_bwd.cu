@@ -52,6 +52,7 @@
 
 #include "kda_common.cuh"
 #include "kda_launch.h"
+#include "kda_schedule.h"
 #include "tc_ptx.cuh"
 
 namespace kda {
@@ -66,7 +67,7 @@ using tc::smem_u32;
 constexpr int kD = 128;    // key and value channels
 constexpr int kC = 16;     // tokens per chunk
 constexpr int kNT = 512;
-constexpr int kMaxOrder = 2048;
+constexpr int kMaxOrder = 4096;
 constexpr size_t kState = (size_t)kD * kD;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -1087,8 +1088,14 @@ __global__ void __launch_bounds__(kNT, 1) chunk_bwd_kernel(const __grid_constant
   unsigned char* const kept = reinterpret_cast<unsigned char*>(states + P.ws_states * kState);
 
   for (int unit = blockIdx.x; unit < P.num_units; unit += gridDim.x) {
-    const int si = unit / P.H, h = unit % P.H;
-    const int seq = P.use_order ? P.order[si] : si;
+    int si = unit / P.H, h = unit % P.H;
+    if (P.use_order == 2) {  // the host's schedule: order[unit] = seq * H + head, or -1
+      const int pk = P.order[unit];
+      if (pk < 0) continue;
+      si = pk / P.H;
+      h = pk % P.H;
+    }
+    const int seq = P.use_order == 1 ? P.order[si] : si;
     int bos, eos;
     if (!seq_range(P.cu, seq, P.total, P.err, bos, eos)) continue;
     const int len = eos - bos;
@@ -1214,16 +1221,23 @@ cudaError_t launch_chunk_bwd_128(const Problem& p, const BwdArgs& a, const int32
   prm.num_seqs = p.num_seqs;
   prm.num_units = p.num_seqs * p.num_heads;
   prm.use_order = 0;
-  if (p.num_seqs <= kMaxOrder) {  // longest sequences first
+  const int grid = grid_for(p);
+  if (p.num_seqs <= kMaxOrder) {  // longest sequences first, each unit to the least-loaded CTA
     std::vector<int> idx(p.num_seqs);
     std::iota(idx.begin(), idx.end(), 0);
     std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) {
       return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
     });
-    for (int i = 0; i < p.num_seqs; ++i) prm.order[i] = idx[i];
-    prm.use_order = 1;
+    auto chunks = [&](int sq) { return (long long)((cu_host[sq + 1] - cu_host[sq] + kC - 1) / kC); };
+    const int n = build_unit_schedule(idx, p.num_heads, grid, chunks, prm.order, kMaxOrder);
+    if (n > 0) {
+      prm.num_units = n;
+      prm.use_order = 2;
+    } else {
+      for (int i = 0; i < p.num_seqs; ++i) prm.order[i] = idx[i];
+      prm.use_order = 1;
+    }
   }
-  const int grid = grid_for(p);
   if (p.io_bf16)
     a.zhead ? chunk_bwd_kernel<__nv_bfloat16, true><<<grid, kNT, SMEM_BYTES, st>>>(prm)
             : chunk_bwd_kernel<__nv_bfloat16, false><<<grid, kNT, SMEM_BYTES, st>>>(prm);
