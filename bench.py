@@ -728,11 +728,12 @@ def bench_decode_fused(kda, d, steps, device, width=4, clk=None):
     return a.elapsed_time(b)
 
 
-def bench_e2e(kda, p, steps, device, groups=8):
+def bench_e2e(kda, p, steps, device, groups=8, warmup=3):
     """End to end through kda_chunk_fwd_host: inputs and outputs in pinned host
     memory, every step copies the batch in, computes and copies out and the
     final state back (groups of sequences overlapped), all inside the timed
-    region.  The device staging area is allocated once, outside it."""
+    region.  The device staging area is allocated once, outside it; `warmup`
+    (at least 3) untimed steps first."""
     import torch
     stream = torch.cuda.current_stream()
     hq, hk, hv, hz, hb = (getattr(p, n).cpu().pin_memory() for n in ("q", "k", "v", "z", "beta"))
@@ -750,7 +751,8 @@ def bench_e2e(kda, p, steps, device, groups=8):
         kda.chunk_fwd_host(hq, hk, hv, hz, hb, p.cu_seqlens_host, hs0, out=out_h,
                            final_state=fin_h, workspace=ws, groups=groups)
 
-    step()
+    for _ in range(max(3, warmup)):
+        step()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -1146,11 +1148,13 @@ def main():
         if p is None:
             p = workloads.prefill_workload(args.workload, device=device, seed=rank)
         groups = 16
-        ms, h2d, d2h, link = bench_e2e(kda, p, args.e2e_steps, device, groups=groups)
+        ms, h2d, d2h, link = bench_e2e(kda, p, args.e2e_steps, device, groups=groups,
+                                       warmup=args.warmup)
         ms = max_over_ranks(ms, dist, device)
         line["e2e"] = {"value": round(weak_scaling_value(T, world, ms / 1e3), 3), "unit": UNIT,
                        "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                       "warmup": max(3, args.warmup),
                        "copy_gbs_effective": round((h2d + d2h) / (ms * 1e-3) / 1e9, 1),
                        "min_ms_per_step": round(bench_e2e.min_ms, 3),
                        "link_gbs_1gib_pinned_copy": {k: round(v, 1) for k, v in link.items()},
