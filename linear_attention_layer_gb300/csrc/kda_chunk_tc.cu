@@ -1234,6 +1234,8 @@ bool make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize
 constexpr int kScanThreads = 256;
 constexpr int kMaxScanSeqs = 512;
 constexpr int kScanLd = 132;  // padded row (floats) of the scan's shared tiles
+// dynamic shared memory of the scan: Mt and Ss (padded), and M as copied in
+constexpr size_t kScanSmem = (2 * (size_t)kD * kScanLd + (size_t)kD * kD) * sizeof(float);
 
 struct ScanSeq {
   int seq, base, nseg;
@@ -1254,6 +1256,7 @@ state_scan_kernel(const __grid_constant__ ScanParams Q) {
   extern __shared__ __align__(16) float scan_smem[];
   float* Mt = scan_smem;                 // M transposed: Mt[k][c]
   float* Ss = scan_smem + kD * kScanLd;  // current state: Ss[k][j]
+  float* Mr = scan_smem + 2 * kD * kScanLd;  // M as stored, [c][k]
   const ScanSeq sq = Q.s[blockIdx.x / Q.H];
   const int h = blockIdx.x % Q.H, tid = threadIdx.x;
   const int r0 = (tid >> 4) * 8, c0 = (tid & 15) * 8;
@@ -1280,9 +1283,20 @@ state_scan_kernel(const __grid_constant__ ScanParams Q) {
     const float* M = slot(2 * Q.E + sq.base + p);
     const float* St = slot(Q.E + sq.base + p);
     __syncthreads();
+    // M into shared memory in one round trip (16-byte cp.async pieces), then
+    // transposed there
+#pragma unroll
+    for (int i = 0; i < kD * kD / 4 / kScanThreads; ++i) {
+      const int e = 4 * (tid + i * kScanThreads);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(Mr + e)),
+                   "l"(M + e)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     for (int idx = tid; idx < kD * kD; idx += kScanThreads) {
       const int c = idx >> 7, k = idx & 127;
-      Mt[k * kScanLd + c] = M[idx];
+      Mt[k * kScanLd + c] = Mr[idx];
     }
     for (int i = 0; i < 8; ++i)
       for (int j = 0; j < 8; ++j) Ss[(r0 + i) * kScanLd + c0 + j] = s[i][j];
@@ -1625,7 +1639,7 @@ struct TcLaunch {
                                    (int)SMEM_BYTES_CONV);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(state_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(2 * kD * kScanLd * sizeof(float)));
+                                 (int)kScanSmem);
       return e;
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -1753,8 +1767,7 @@ cudaError_t launch_chunk_tc(const Problem& p, const Args& a, const int32_t* cu_h
     sp.H = p.num_heads;
     sp.E = E;
     for (int n = 0; n < p.num_seqs; ++n) sp.s[n] = ScanSeq{n, plan.base[n], plan.nseg[n]};
-    state_scan_kernel<<<p.num_seqs * p.num_heads, kScanThreads,
-                        2 * kD * kScanLd * sizeof(float), st>>>(sp);
+    state_scan_kernel<<<p.num_seqs * p.num_heads, kScanThreads, kScanSmem, st>>>(sp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
