@@ -65,7 +65,9 @@ struct ConvRegs {
 
 __device__ __forceinline__ float swish(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
-__device__ __forceinline__ float conv_step(float (&h)[3], const float (&t)[4], float x) {
+// One token of a channel's convolution: taps t[0..3] (registers or shared
+// memory), history h advanced by the raw input x; returns the Swish output.
+__device__ __forceinline__ float conv_step(float (&h)[3], const float* t, float x) {
   const float u = fmaf(t[0], h[0], fmaf(t[1], h[1], fmaf(t[2], h[2], t[3] * x)));
   h[0] = h[1];
   h[1] = h[2];
@@ -388,13 +390,6 @@ __device__ __forceinline__ void win_copy(WinRaw<DK, DV, T>& x, const WinPart<T>&
 struct ConvHist {
   float hq[3], hk[3];
 };
-__device__ __forceinline__ float conv_step_s(float (&h)[3], const float* t, float x) {
-  const float u = fmaf(t[0], h[0], fmaf(t[1], h[1], fmaf(t[2], h[2], t[3] * x)));
-  h[0] = h[1];
-  h[1] = h[2];
-  h[2] = x;
-  return swish(u);
-}
 
 // Token j of the unit (whose part starts afresh when `fresh`): q, k (through
 // the fused convolution), the decay's running product gam (this channel's,
@@ -408,8 +403,8 @@ __device__ __forceinline__ void win_stage(WinSmem<DK, DV>& sm, int bf, const Win
   if (tid < DK) {
     float a = ld_raw(x.q + tid), b = ld_raw(x.k + tid);
     if (CONV && conv_on) {
-      a = conv_step_s(ch.hq, taps[tid], a);
-      b = conv_step_s(ch.hk, taps[tid] + 4, b);
+      a = conv_step(ch.hq, taps[tid], a);
+      b = conv_step(ch.hk, taps[tid] + 4, b);
     }
     const float al = __expf(log_decay(zscale * (zhead ? x.zh : x.z[tid])));
     gam = fresh ? al : gam * al;
