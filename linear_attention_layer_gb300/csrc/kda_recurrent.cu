@@ -385,11 +385,12 @@ __device__ __forceinline__ void win_copy(WinRaw<DK, DV, T>& x, const WinPart<T>&
   }
 }
 
-// The fused convolution of one channel: its history in registers, its taps
-// (q then k, right-aligned as in ConvRegs) in shared memory.
-struct ConvHist {
-  float hq[3], hk[3];
-};
+// The fused convolution of one channel, in a shared-memory row of its own
+// thread: taps of q then k (right-aligned as in ConvRegs), then the last
+// three raw inputs of q then of k (an odd row length keeps the rows of a
+// warp's threads in different banks).
+constexpr int kConvRow = 15;
+constexpr int kConvHq = 8, kConvHk = 11;
 
 // Token j of the unit (whose part starts afresh when `fresh`): q, k (through
 // the fused convolution), the decay's running product gam (this channel's,
@@ -398,13 +399,21 @@ struct ConvHist {
 template <int DK, int DV, typename T, bool CONV>
 __device__ __forceinline__ void win_stage(WinSmem<DK, DV>& sm, int bf, const WinRaw<DK, DV, T>& x,
                                           float zscale, bool zhead, bool fresh, float& gam,
-                                          ConvHist& ch, const float (*taps)[8], bool conv_on) {
+                                          float (*conv_rows)[kConvRow], bool conv_on) {
   const int tid = threadIdx.x;
   if (tid < DK) {
     float a = ld_raw(x.q + tid), b = ld_raw(x.k + tid);
     if (CONV && conv_on) {
-      a = conv_step(ch.hq, taps[tid], a);
-      b = conv_step(ch.hk, taps[tid] + 4, b);
+      float* const r = conv_rows[tid];
+      float hq[3] = {r[kConvHq], r[kConvHq + 1], r[kConvHq + 2]};
+      float hk[3] = {r[kConvHk], r[kConvHk + 1], r[kConvHk + 2]};
+      a = conv_step(hq, r, a);
+      b = conv_step(hk, r + 4, b);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        r[kConvHq + j] = hq[j];
+        r[kConvHk + j] = hk[j];
+      }
     }
     const float al = __expf(log_decay(zscale * (zhead ? x.zh : x.z[tid])));
     gam = fresh ? al : gam * al;
@@ -450,9 +459,10 @@ __global__ void __launch_bounds__(kNT, 2)
 window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int H, int zhead,
               float* __restrict__ state, T* __restrict__ out, int* err, const Fusion f) {
   using SH = WinShape<DK, DV>;
+  static_assert(!FUSED || (DK <= kNT - 32 && DV <= 128), "the last warp stages no q or k");
   __shared__ __align__(16) WinSmem<DK, DV> sm;
   __shared__ __align__(16) WinRaw<DK, DV, T> raw[kWinSlots];
-  __shared__ __align__(16) float taps[FUSED ? DK : 1][8];
+  __shared__ float conv_rows[FUSED ? DK : 1][kConvRow];
   const size_t unit = blockIdx.x;  // b * H + h
   const int b = (int)(unit / H), h = (int)(unit % H);
   int nrep = 0;
@@ -489,28 +499,29 @@ window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int
   // tokens advance it and it is stored with the state, the window's drafts
   // advance only this copy
   const bool conv = FUSED && f.W > 0;
-  ConvHist ch;
   if (conv && threadIdx.x < DK) {
     ConvRegs cr;
     conv_load<DK>(cr, f, unit, h, threadIdx.x);
+    float* const r = conv_rows[threadIdx.x];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      taps[threadIdx.x][j] = cr.tq[j];
-      taps[threadIdx.x][4 + j] = cr.tk[j];
+      r[j] = cr.tq[j];
+      r[4 + j] = cr.tk[j];
     }
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-      ch.hq[j] = cr.hq[j];
-      ch.hk[j] = cr.hk[j];
+      r[kConvHq + j] = cr.hq[j];
+      r[kConvHk + j] = cr.hk[j];
     }
   }
   auto conv_save = [&]() {  // the history after the replayed tokens
     if (conv && threadIdx.x < DK) {
       ConvRegs cr;
+      const float* const r = conv_rows[threadIdx.x];
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
-        cr.hq[j] = ch.hq[j];
-        cr.hk[j] = ch.hk[j];
+        cr.hq[j] = r[kConvHq + j];
+        cr.hk[j] = r[kConvHk + j];
       }
       conv_store<DK>(cr, f, unit, threadIdx.x);
     }
@@ -519,22 +530,24 @@ window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int
   auto fresh = [&](int j) { return j == nrep || (j < nrep ? j : j - nrep) % kWinRenorm == 0; };
   float gam = 1.f;  // (staging threads) this channel's running decay product
   const bool onorm = FUSED && f.onw != nullptr;
-  // (output norm) token i's raw outputs wait in sm.os[i & 1] for the next barrier
+  // (output norm) token i's raw outputs wait in sm.os[i & 1] for the next
+  // barrier; the last warp, which stages no q or k, scales and stores them
   auto finish = [&](int i) {
-    if (g != 0) return;
+    if (w != kNT / 32 - 1 || 4 * lane >= DV) return;
+    const int cc = 4 * lane;
     float ss = 0.f;
 #pragma unroll
     for (int ww = 0; ww < kNT / 32; ++ww) ss += sm.onorm[i & 1][ww];
     const float r = rsqrtf(ss * (1.f / DV) + f.eps);
-    const float4 o = *reinterpret_cast<const float4*>(&sm.os[i & 1][c]);
-    const float4 gm = __ldg(reinterpret_cast<const float4*>(f.onw + (size_t)h * DV + c));
-    st4_io(out + (((size_t)b * wn.W + (i - nrep)) * H + h) * DV + c,
+    const float4 o = *reinterpret_cast<const float4*>(&sm.os[i & 1][cc]);
+    const float4 gm = __ldg(reinterpret_cast<const float4*>(f.onw + (size_t)h * DV + cc));
+    st4_io(out + (((size_t)b * wn.W + (i - nrep)) * H + h) * DV + cc,
            make_float4(o.x * r * gm.x, o.y * r * gm.y, o.z * r * gm.z, o.w * r * gm.w));
   };
 
   cp_async_wait_pending<2>();  // token 0's copies (this thread's)
   __syncthreads();             // ... and every thread's
-  win_stage<DK, DV, T, FUSED>(sm, 0, raw[0], zscale, zhead, true, gam, ch, taps, conv);
+  win_stage<DK, DV, T, FUSED>(sm, 0, raw[0], zscale, zhead, true, gam, conv_rows, conv);
   if (nrep == 1) conv_save();
   cp_async_wait_pending<1>();  // token 1's
   for (int i = 0; i < ntok; ++i) {
@@ -543,7 +556,7 @@ window_kernel(WinPart<T> rp, WinPart<T> wn, const float* __restrict__ a_log, int
     if (onorm && i > nrep) finish(i - 1);  // the previous token's outputs, normalised
     if (i + 1 < ntok) {  // token i + 1 into the other buffer
       win_stage<DK, DV, T, FUSED>(sm, bf ^ 1, raw[(i + 1) % kWinSlots], zscale, zhead,
-                                  fresh(i + 1), gam, ch, taps, conv);
+                                  fresh(i + 1), gam, conv_rows, conv);
       if (i + 2 == nrep) conv_save();
     }
     fetch(i + 3);  // into the slot of token i - 1, staged before the barrier above
