@@ -338,6 +338,20 @@ def cpu_oracle_sample(budget_s=12.0, seed=0, max_seqs=64):
     return done_tok / elapsed, done_tok * 32, used, desc
 
 
+def cpu_oracle_one_core(seed=0, tokens=512):
+    """The same oracle on one host thread: one sequence of `tokens` tokens x
+    32 heads (about a second or two of CPU work).  Returns (tokens/s, description)."""
+    import oracle
+    import workloads
+    p = workloads.random_problem([tokens], 32, 128, 128, init_std=0.1, seed=seed,
+                                 name="varlen-sample")
+    t0 = time.perf_counter()
+    oracle.recurrent(p.q, p.k, p.v, p.z, p.beta, p.cu_seqlens_host, p.initial_state, threads=1)
+    dt = time.perf_counter() - t0
+    return tokens / dt, (f"one {tokens}-token sequence x 32 heads (dk=dv=128), one thread, "
+                         f"{dt:.1f} s")
+
+
 def reference_arm(args):
     """The oracle as it stands on the host cores: `--impl reference`."""
     rank, world, _ = dist_info()
@@ -1165,8 +1179,11 @@ def main():
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     if "cpu" not in skip and rank == 0 and world == 1:
         tps, htok, used, desc = cpu_oracle_sample(args.cpu_budget)
+        tps1, desc1 = cpu_oracle_one_core()
         line["cpu_baseline"] = {"value": round(tps / 1e6, 6), "unit": UNIT, "cores": used,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "one_core": {"value": round(tps1 / 1e6, 6), "unit": UNIT,
+                                             "cores": 1, "sample": desc1}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
