@@ -23,9 +23,11 @@ def _unit(x, eps):
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
 
 
-def grouped_forward(q, k, v, z, beta, s0, a_log=None, eps=1e-6, group=4):
+def grouped_forward(q, k, v, z, beta, s0, a_log=None, eps=1e-6, group=4, slip=None):
     """q, k, z [T, D], v [T, E], beta [T], s0 [D, E] (or None).  Returns
-    (o [T, E], final state [D, E])."""
+    (o [T, E], final state [D, E]).  `slip` plants one mistake (test use
+    only): 'ratio_off_by_one' (A_j / A_i taken over tokens i..j), 'no_output_term'
+    (o_j without (q_j . k_j) x_j), 'end_decay' (S' = A_2 S instead of A_3 S)."""
     T, D = q.shape
     E = v.shape[1]
     scale = np.exp(a_log) if a_log is not None else 1.0
@@ -45,7 +47,8 @@ def grouped_forward(q, k, v, z, beta, s0, a_log=None, eps=1e-6, group=4):
         A = np.cumprod(al, axis=0)  # A_j over the group's tokens 0..j
 
         def rho(j, i):  # A_j / A_i as the product of the decays in between
-            return np.prod(al[i + 1:j + 1], axis=0)
+            lo = i if slip == "ratio_off_by_one" else i + 1
+            return np.prod(al[lo:j + 1], axis=0)
 
         Kj = (A * K) @ S  # [group, E]
         Qj = (A * Qr) @ S
@@ -56,12 +59,12 @@ def grouped_forward(q, k, v, z, beta, s0, a_log=None, eps=1e-6, group=4):
                 e = e - np.dot(K[j] * rho(j, i), K[i]) * x[i]
             x[j] = b[j] * e
         for j in range(n):
-            oj = Qj[j] + np.dot(Qr[j], K[j]) * x[j]
+            oj = Qj[j] + (0.0 if slip == "no_output_term" else np.dot(Qr[j], K[j])) * x[j]
             for i in range(j):
                 oj = oj + np.dot(Qr[j] * rho(j, i), K[i]) * x[i]
             o[t0 + j] = oj
         last = group - 1
-        S = A[last][:, None] * S
+        S = A[last - 1 if slip == "end_decay" else last][:, None] * S
         for i in range(group):
             S = S + np.outer(rho(last, i) * K[i], x[i])
     return o, S
