@@ -49,9 +49,13 @@ def _block_inverse(A):
     return series @ Dinv
 
 
-def chunk_forward(q, k, v, z, beta, s0=None, a_log=0.0, eps=1e-6):
+def chunk_forward(q, k, v, z, beta, s0=None, a_log=0.0, eps=1e-6, slip=None):
     """One sequence, one head: q, k, z [T, dk], v [T, dv], beta [T].
-    Returns (out [T, dv], final state [dk, dv])."""
+    Returns (out [T, dv], final state [dk, dv]).  `slip` plants one mistake
+    (test use only): 'reference_off' (the query side of subtile a > 0 against
+    r_{a-1}), 'chain_factor' (K^(a) chained by e^{r_a} instead of
+    e^{r_a - r_{a-1}}), 'state_decay' (S carried without Diag(e^{G_C})),
+    'key_end' (Khat = k^ e^{-G} instead of k^ e^{G_C - G})."""
     q, k, v, z = (np.asarray(x, dtype=np.float64) for x in (q, k, v, z))
     beta = np.asarray(beta, dtype=np.float64)
     T, D = q.shape
@@ -72,7 +76,8 @@ def chunk_forward(q, k, v, z, beta, s0=None, a_log=0.0, eps=1e-6):
             base[j] = kh[c0 + j] * np.exp(r[0] - G[j])
         Ka.append(base)
         for a in range(1, nsub):
-            prev = Ka[-1] * np.exp(r[a] - r[a - 1])  # chain factor e^{r_a - r_{a-1}} <= 1
+            chain = r[a] if slip == "chain_factor" else r[a] - r[a - 1]
+            prev = Ka[-1] * np.exp(chain)  # chain factor e^{r_a - r_{a-1}} <= 1
             for j in range(a * SUB, min((a + 1) * SUB, n)):  # the new diagonal subtile
                 prev[j] = kh[c0 + j] * np.exp(r[a] - G[j])
             Ka.append(prev)
@@ -80,8 +85,9 @@ def chunk_forward(q, k, v, z, beta, s0=None, a_log=0.0, eps=1e-6):
         A = np.zeros((n, n))
         for t in range(n):
             a = t // SUB
-            qt = qh[c0 + t] * np.exp(G[t] - r[a])
-            kq = kh[c0 + t] * np.exp(G[t] - r[a])
+            ra = r[a - 1] if (slip == "reference_off" and a > 0) else r[a]
+            qt = qh[c0 + t] * np.exp(G[t] - ra)
+            kq = kh[c0 + t] * np.exp(G[t] - ra)
             for j in range(t + 1):
                 P[t, j] = qt @ Ka[a][j]
                 if j < t:
@@ -89,8 +95,8 @@ def chunk_forward(q, k, v, z, beta, s0=None, a_log=0.0, eps=1e-6):
         Tp = _block_inverse(A) * beta[None, c0:c1]
         Qp = qh[c0:c1] * np.exp(G)
         Kp = kh[c0:c1] * np.exp(G)
-        Kt = kh[c0:c1] * np.exp(G[-1] - G)
+        Kt = kh[c0:c1] * np.exp((0.0 if slip == "key_end" else G[-1]) - G)
         U = Tp @ (v[c0:c1] - Kp @ S)
         out[c0:c1] = Qp @ S + P @ U
-        S = np.exp(G[-1])[:, None] * S + Kt.T @ U
+        S = (S if slip == "state_decay" else np.exp(G[-1])[:, None] * S) + Kt.T @ U
     return out, S

@@ -57,3 +57,20 @@ def test_chunk_algebra_slow_decay_needs_every_series_term():
     o, f = chunk_forward(q[:, 0], k[:, 0], v[:, 0], z[:, 0], b[:, 0], None)
     assert np.linalg.norm(o - ro[:, 0]) <= 1e-10 * np.linalg.norm(ro)
     assert np.linalg.norm(f - rf[0, 0]) <= 1e-10 * np.linalg.norm(rf)
+
+
+@pytest.mark.parametrize("slip", ["reference_off", "chain_factor", "state_decay", "key_end"])
+def test_planted_slips_fail(slip):
+    rng = np.random.default_rng(41)
+    T, D, E = 150, 8, 6
+    q = rng.standard_normal((T, 1, D))
+    k = rng.standard_normal((T, 1, D))
+    v = rng.standard_normal((T, 1, E))
+    z = rng.normal(-2.0, 1.5, size=(T, 1, D))
+    b = 1 / (1 + np.exp(-rng.standard_normal((T, 1))))
+    s0 = rng.normal(0, 0.3, size=(1, 1, D, E))
+    ro, rf, _ = oracle.recurrent(q, k, v, z, b, [0, T], s0)
+    o, f = chunk_forward(q[:, 0], k[:, 0], v[:, 0], z[:, 0], b[:, 0], s0[0, 0], slip=slip)
+    err = max(np.linalg.norm(o - ro[:, 0]) / np.linalg.norm(ro),
+              np.linalg.norm(f - rf[0, 0]) / np.linalg.norm(rf))
+    assert err > 1e-3
