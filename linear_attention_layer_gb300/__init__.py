@@ -733,7 +733,9 @@ def decode_replay_window_fused(prev, accept_len, window, state, *, conv_weight_q
     drafts of ``prev`` = (q, k, v, z, beta) [B, Wp, H, .] into ``state`` and the
     convolution states (in place), then the outputs [B, W, H, dv] of ``window``
     = (q, k, v, z, beta) [B, W, H, .] through the output norm.  ``prev`` or
-    ``window`` may be None (no replay / no outputs; returns None then)."""
+    ``window`` may be None (no replay / no outputs; returns None then).
+    ``state`` and ``out_norm_weight`` must start on a 16-byte boundary (the
+    library refuses them otherwise: KDA_ERR_INVALID_ARGUMENT)."""
     lib = load()
     ref = window if window is not None else prev
     if ref is None:

@@ -384,6 +384,7 @@ kda_status_t kda_decode_replay_window_fused(
   kda::FusionArgs fa;
   s = check_fusion(fusion, fa);
   if (s != KDA_OK) return s;
+  if (fa.onw && !aligned16(fa.onw)) return KDA_ERR_INVALID_ARGUMENT;  // read as float4
   const int B = desc->num_seqs;
   if (B > 0) {
     if (!state) return KDA_ERR_INVALID_ARGUMENT;

@@ -149,6 +149,18 @@ def test_window_rejects_missing_out_and_replay_missing_accept(lib):
                                  None) == 1
 
 
+def test_fused_window_rejects_unaligned_output_norm_weight(lib):
+    """The fused window kernel reads the norm weight four floats at a time, so
+    a weight off a 16-byte boundary is refused before anything is enqueued
+    (every other argument here passes validation)."""
+    d, _ = kda.make_desc(4, 8, 2, 128, 128, kda.KDA_BF16)
+    f = kda.KdaFusion(0, None, None, None, None, ctypes.c_void_p(0x1004), 1e-6)
+    acc = ctypes.c_void_p(0x1800)
+    assert lib.kda_decode_replay_window_fused(
+        ctypes.byref(d), ctypes.byref(f), 2, FAKE, FAKE, FAKE, FAKE, FAKE, acc, 2, FAKE, FAKE,
+        FAKE, FAKE, FAKE, ctypes.c_void_p(0x3000), ctypes.c_void_p(0x2000), None) == 1
+
+
 def test_workspace_size_query(lib):
     d, keep = kda.make_desc(1, 65536, 32, 128, 128, kda.KDA_BF16, [0, 65536])
     n = ctypes.c_size_t(123)
