@@ -330,7 +330,9 @@ def recurrent_fwd(q, k, v, z, beta, cu_seqlens, initial_state=None, *, out=None,
                   final_state=None, output_final_state=True, cu_seqlens_host=None, stream=None,
                   a_log=None, checkpoint_every=0, checkpoints=None):
     """Token-by-token KDA prefill (``kda_recurrent_fwd``).  Returns (out, final_state)
-    (and the checkpoints, as ``chunk_fwd``)."""
+    (and the checkpoints, as ``chunk_fwd``).  ``initial_state``, ``final_state``
+    and ``checkpoints`` must start on a 16-byte boundary (the library refuses
+    them otherwise: KDA_ERR_INVALID_ARGUMENT)."""
     return _prefill("kda_recurrent_fwd", q, k, v, z, beta, cu_seqlens, initial_state, out,
                     final_state, output_final_state, cu_seqlens_host, None, stream, a_log,
                     checkpoint_every, checkpoints)

@@ -211,6 +211,11 @@ kda_status_t kda_recurrent_fwd(const kda_desc_t* desc, const void* q, const void
                                const void* v, const float* z, const float* beta,
                                const float* initial_state, const int32_t* cu_seqlens,
                                void* out, float* final_state, kda_stream_t stream) {
+  // the token-by-token kernel moves states and checkpoints four floats at a time
+  if (!desc || (initial_state && !aligned16(initial_state)) ||
+      (final_state && !aligned16(final_state)) ||
+      (desc->checkpoint_every > 0 && desc->checkpoints && !aligned16(desc->checkpoints)))
+    return KDA_ERR_INVALID_ARGUMENT;
   kda::Args a;
   kda_status_t s = prefill_common(desc, q, k, v, z, beta, initial_state, cu_seqlens, out,
                                   final_state, a);

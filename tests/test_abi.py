@@ -111,6 +111,22 @@ def test_prefill_rejects_bad_checkpoint_arguments(lib, fn, every, ckpt, offs):
     assert _call_chunk(lib, desc, fn=fn) == 1  # KDA_ERR_INVALID_ARGUMENT
 
 
+@pytest.mark.parametrize("which", ["initial", "final", "checkpoints"])
+def test_recurrent_prefill_rejects_unaligned_states(lib, which):
+    """kda_recurrent_fwd moves states and checkpoints four floats at a time:
+    one off a 16-byte boundary is refused before anything is enqueued."""
+    desc, keep = kda.make_desc(2, 128, 2, 128, 128, kda.KDA_BF16, [0, 64, 128])
+    odd = ctypes.c_void_p(0x3004)
+    s0 = odd if which == "initial" else None
+    fin = odd if which == "final" else None
+    if which == "checkpoints":
+        desc.checkpoint_every = 64
+        desc.checkpoints = odd
+        desc.checkpoint_offsets = ctypes.c_void_p(0x5000)
+    assert lib.kda_recurrent_fwd(ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, FAKE, s0, FAKE,
+                                 ctypes.c_void_p(0x2000), fin, None) == 1
+
+
 def test_checkpoint_offsets_count_whole_intervals():
     # lengths 63, 1, 0, 266, 1024
     assert kda.checkpoint_offsets([0, 63, 64, 64, 330, 1354], 64) == [0, 0, 0, 0, 4, 20]
